@@ -1,0 +1,180 @@
+/*
+ * latent_moe.h — C ABI of a GB300 (sm_103a) implementation of the Muse Spark
+ * Open latent mixture-of-experts decoder block:
+ *
+ *     out = x + RMSNorm_post( F( RMSNorm_pre(x) ) )
+ *
+ * with F = full-width router (softmax over all experts, top-k, weights
+ * renormalised over the k) ; pooler d_model -> d_latent and RMSNorm ; routed
+ * SwiGLU experts at width d_latent ; each selected expert's output
+ * RMS-normalised with its own gamma BEFORE it is multiplied by its routing
+ * weight ; FP32 weighted sum ; unpooler d_latent -> d_model.
+ *
+ * Sources: LMSYS "SGLang and Miles Add Day-0 Support for Muse Spark Open",
+ * section "MoE with pooler, unpooler and per-expert normalization" (router on
+ * the full-width input, pooled input normalised before the experts, per-expert
+ * RMSNorm before the weighted sum, then unpool), "Fused per-expert post-norm"
+ * (partial sums of squares of the bf16 values of each down-projection tile,
+ * one scalar per selected expert read at combine), "Reinforcement learning"
+ * (weighted sum in FP32), "NVFP4 as a third MMA type" (E2M1 data, UE4M3 scale
+ * per 16 elements, per-token FP32 input scale); vLLM "Day 0 support for Muse
+ * Spark Open", sections "Sandwich normalization" and "Latent MoE".
+ *
+ * Conventions
+ *  - Every pointer named in a signature as device memory must be a CUDA
+ *    device pointer of the current device, 16-byte aligned.  Host-memory
+ *    arguments are marked "host".
+ *  - Every weight matrix is "out x in", row-major, K (the "in" dimension)
+ *    contiguous: W_router [E, D], W_pool [L, D], W_gate/W_up [E, I, L],
+ *    W_down [E, L, I], W_unpool [D, L].
+ *  - The caller owns all memory (inputs, out, workspace).  The library
+ *    allocates no device memory in any call.
+ *  - Calls are asynchronous on `stream`; nothing synchronises the host.
+ *  - Host-detectable errors return a negative status before any launch and
+ *    leave out/workspace untouched.  A launch error maps to LMOE_ERR_CUDA.
+ *    A device-side wait that exceeds its budget sets an error word in the
+ *    workspace, which lmoe_check_status() reads back (LMOE_ERR_TIMEOUT).
+ *  - Calls that share one workspace must not overlap on the GPU.
+ */
+#ifndef LATENT_MOE_H_
+#define LATENT_MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LMOE_OK = 0,
+  LMOE_ERR_ARG = -1,          /* null pointer, bad size, top_k out of range            */
+  LMOE_ERR_UNSUPPORTED = -2,  /* a shape or dtype combination the kernels do not cover */
+  LMOE_ERR_ALIGN = -3,        /* a device pointer not 16-byte aligned                  */
+  LMOE_ERR_WORKSPACE = -4,    /* workspace null or smaller than lmoe_workspace_size()  */
+  LMOE_ERR_CUDA = -5,         /* a CUDA runtime/driver call failed                     */
+  LMOE_ERR_TIMEOUT = -6       /* a device wait ran past its budget                     */
+} lmoe_status;
+
+typedef enum { LMOE_F32 = 0, LMOE_BF16 = 1, LMOE_NVFP4 = 2 } lmoe_dtype;
+
+/* Block shape and dtypes.
+ *  T          tokens (rows of x), 0 <= T <= 1<<20 (T = 0 is a no-op)
+ *  d_model    D, multiple of 128           d_latent  L, multiple of 128
+ *  n_experts  E, 1..1024                   d_ff      I, multiple of 128
+ *  top_k      k, 1..min(E, 16)             eps       RMSNorm epsilon (all four norms)
+ *  act_dtype  dtype of x: LMOE_F32 or LMOE_BF16
+ *  weight_dtype  LMOE_F32, LMOE_BF16, or LMOE_NVFP4 (pooler, experts, unpooler packed;
+ *             the router then stays LMOE_BF16)
+ *  out_dtype  LMOE_F32 or LMOE_BF16                                                  */
+typedef struct {
+  int T, d_model, d_latent, n_experts, d_ff, top_k;
+  float eps;
+  lmoe_dtype act_dtype, weight_dtype, out_dtype;
+} lmoe_config;
+
+/* One NVFP4-packed weight (host struct holding device pointers), "out x in" [rows, K]:
+ *  data          [rows, K/2] bytes, two E2M1 codes per byte, the low nibble holds the even k
+ *  scales        [rows, K/16] E4M3 block-scale codes (one per 16 consecutive k)
+ *  tensor_scale  fp32 second-level scale: 1 value, or one per expert for expert stacks
+ *  value = e2m1(code) * e4m3(scale) * tensor_scale.                                    */
+typedef struct {
+  const uint8_t* data;
+  const uint8_t* scales;
+  const float* tensor_scale;
+} lmoe_nvfp4_weight;
+
+/* Optional extensions of one call (host struct; every member may be NULL/0).
+ *  router_bias       [E] fp32 device: added to the router logits before softmax/top-k
+ *  forced_idx        [T, k] int32 device: use these experts (distinct per row) instead of
+ *                    the top-k; weights are the softmax of the logits renormalised over them
+ *  topk_idx_out      [T, k] int32 device: selected experts, descending logit
+ *  topk_w_out        [T, k] fp32 device: their routing weights
+ *  near_tie_count_out  [1] int32 device: tokens whose k-th and (k+1)-th logits differ by < 1e-3
+ *  wait_budget_cycles  SM clock cycles a device wait may spin before it gives up (0: default) */
+typedef struct {
+  const float* router_bias;
+  const int32_t* forced_idx;
+  int32_t* topk_idx_out;
+  float* topk_w_out;
+  int32_t* near_tie_count_out;
+  long long wait_budget_cycles;
+} lmoe_ex;
+
+/* Bytes of device workspace a call with this config needs (host out-parameter). */
+lmoe_status lmoe_workspace_size(const lmoe_config* cfg, size_t* bytes);
+
+/* The block.  Device pointers:
+ *  x         [T, D]   act_dtype
+ *  W_router  [E, D]   fp32 when weight_dtype is LMOE_F32, else bf16
+ *  W_pool    [L, D]   } bf16/fp32 per weight_dtype, or, for LMOE_NVFP4, a HOST pointer to
+ *  W_gate    [E, I, L]}  an lmoe_nvfp4_weight (expert stacks: data [E, rows, K/2], scales
+ *  W_up      [E, I, L]}  [E, rows, K/16], tensor_scale [E]; W_gate and W_up may use
+ *  W_down    [E, L, I]}  different scales)
+ *  W_unpool  [D, L]   }
+ *  g_pool [L], g_expert [E, L], g_pre [D], g_post [D]   fp32 RMSNorm gammas
+ *  top_k     must equal cfg->top_k
+ *  out       [T, D]   out_dtype (may not alias x)
+ *  workspace device buffer of at least lmoe_workspace_size() bytes, 256-byte aligned  */
+lmoe_status latent_moe_forward(const lmoe_config* cfg, const void* x, const void* W_router,
+                               const void* W_pool, const float* g_pool, const void* W_gate,
+                               const void* W_up, const void* W_down, const float* g_expert,
+                               const void* W_unpool, const float* g_pre, const float* g_post,
+                               int top_k, void* out, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+
+/* latent_moe_forward with the extensions of `ex` (host pointer, may be NULL). */
+lmoe_status latent_moe_forward_ex(const lmoe_config* cfg, const void* x, const void* W_router,
+                                  const void* W_pool, const float* g_pool, const void* W_gate,
+                                  const void* W_up, const void* W_down, const float* g_expert,
+                                  const void* W_unpool, const float* g_pre, const float* g_post,
+                                  int top_k, void* out, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream, const lmoe_ex* ex);
+
+/* latent_moe_forward with x and out in HOST memory (pinned for asynchronous copies):
+ * copies x to the workspace, runs the block, copies out back, all on `stream`.
+ * The weights stay device pointers.  workspace must hold lmoe_workspace_size() plus
+ * the x and out staging bytes reported by lmoe_workspace_size_host_io().             */
+lmoe_status lmoe_workspace_size_host_io(const lmoe_config* cfg, size_t* bytes);
+lmoe_status latent_moe_forward_host_io(const lmoe_config* cfg, const void* x_host,
+                                       const void* W_router, const void* W_pool,
+                                       const float* g_pool, const void* W_gate, const void* W_up,
+                                       const void* W_down, const float* g_expert,
+                                       const void* W_unpool, const float* g_pre,
+                                       const float* g_post, int top_k, void* out_host,
+                                       void* workspace, size_t workspace_bytes,
+                                       cudaStream_t stream);
+
+/* Reads (synchronising `stream`) and clears the device error word of `workspace`.
+ * Returns LMOE_OK or LMOE_ERR_TIMEOUT; *detail (host, may be NULL) receives the raw word. */
+lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStream_t stream,
+                              uint32_t* detail);
+
+/* Byte offsets of the intermediates inside the workspace, for inspection:
+ *  xa (router/pooler input rows), logits [T,E] f32, topk_idx [T,k] i32, topk_w [T,k] f32,
+ *  counts [E] i32, offsets [E+1] i32, row_of [T,k] i32, tok_of [T*k] i32,
+ *  p [T,L] bf16, xe [T*k, L] (expert-contiguous expert inputs), h [T*k, I], y [T*k, L] bf16,
+ *  ss_y [T*k, L/128] f32, c [T,L] bf16, u [T,D] bf16, err (u32).  Unused fields are -1. */
+typedef struct {
+  long long xa, logits, topk_idx, topk_w, counts, offsets, row_of, tok_of, tiles, n_tiles,
+      p, ss_p, xe, xe_scale, h, y, ss_y, c, u, ss_u, err, total;
+  int xa_cols; /* columns of one xa row (2*D: xn_hi | xn_lo, or 3*D for fp32 weights) */
+} lmoe_workspace_layout;
+lmoe_status lmoe_get_workspace_layout(const lmoe_config* cfg, lmoe_workspace_layout* layout);
+
+/* Diagnostic of the device wait-timeout path: launches one CTA that waits on an
+ * mbarrier nothing ever arrives on, with a budget of `budget_cycles` SM cycles
+ * (clamped to 1..4e9).  The wait gives up, sets the workspace error word, and the
+ * kernel returns; lmoe_check_status() then reports LMOE_ERR_TIMEOUT.  workspace as for
+ * latent_moe_forward (only its error word is touched).                               */
+lmoe_status lmoe_wait_selftest(const lmoe_config* cfg, void* workspace, long long budget_cycles,
+                               cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* lmoe_status_string(lmoe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LATENT_MOE_H_ */

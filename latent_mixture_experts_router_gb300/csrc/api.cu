@@ -1,0 +1,436 @@
+// api.cu — the C ABI of include/latent_moe.h: argument checks, workspace layout,
+// TMA tensor maps, and the launch sequence of one latent-MoE block call.
+//
+// Launch sequence (one stream, no host synchronisation):
+//   prenorm -> router GEMM (fp32 logits) -> top-k/softmax -> expert histogram +
+//   stable scatter (expert-contiguous rows, M-tile table) -> pooler GEMM (+ row
+//   sums of squares) -> pool norm, copied to the k expert rows -> grouped gate/up
+//   GEMM with SwiGLU epilogue -> grouped down GEMM (+ per-expert row sums of
+//   squares) -> combine (per-expert RMSNorm, routing weight, fp32 sum in slot
+//   order) -> unpooler GEMM (+ row sums of squares) -> post-norm + residual.
+// Grouped GEMMs read their tile table on the device, so per-expert row counts
+// never travel to the host.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "../../include/latent_moe.h"
+#include "internal.h"
+
+using namespace lmoe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+struct Layout {
+  lmoe_workspace_layout pub;
+  long long near_tie;
+  // fp32-weight mode: bf16 copies of the weights
+  long long w_router, w_pool, w_gate, w_up, w_down, w_unpool;
+  long long x_stage, out_stage, host_io_total;
+  int ld_logits, ld_ss_p, ld_ss_y, ld_ss_u, max_tiles;
+};
+
+lmoe_status check_config(const lmoe_config* c) {
+  if (c == nullptr) return LMOE_ERR_ARG;
+  if (c->T < 0 || c->T > (1 << 20)) return LMOE_ERR_ARG;
+  if (c->d_model <= 0 || c->d_latent <= 0 || c->d_ff <= 0 || c->n_experts <= 0)
+    return LMOE_ERR_ARG;
+  if (c->top_k < 1 || c->top_k > 16 || c->top_k > c->n_experts) return LMOE_ERR_ARG;
+  if (c->n_experts > 1024) return LMOE_ERR_UNSUPPORTED;
+  if (c->d_model % 128 || c->d_latent % 128 || c->d_ff % 128) return LMOE_ERR_UNSUPPORTED;
+  if (c->d_model > 65536 || c->d_latent > 65536 || c->d_ff > 65536) return LMOE_ERR_UNSUPPORTED;
+  if (!(c->eps >= 0.f)) return LMOE_ERR_ARG;
+  if (c->act_dtype != LMOE_F32 && c->act_dtype != LMOE_BF16) return LMOE_ERR_UNSUPPORTED;
+  if (c->out_dtype != LMOE_F32 && c->out_dtype != LMOE_BF16) return LMOE_ERR_UNSUPPORTED;
+  if (c->weight_dtype != LMOE_F32 && c->weight_dtype != LMOE_BF16) return LMOE_ERR_UNSUPPORTED;
+  return LMOE_OK;
+}
+
+void make_layout(const lmoe_config* c, Layout* L) {
+  const long long T = c->T, D = c->d_model, Ld = c->d_latent, E = c->n_experts, I = c->d_ff,
+                  k = c->top_k, R = T * k;
+  const bool f32w = c->weight_dtype == LMOE_F32;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> long long {
+    const long long o = static_cast<long long>(off);
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  memset(L, 0xff, sizeof(*L));
+  lmoe_workspace_layout& P = L->pub;
+  P.xa_cols = static_cast<int>((f32w ? 3 : 2) * D);
+  L->ld_logits = static_cast<int>(align_up(E, 32));
+  L->ld_ss_p = cdiv(Ld, kBNWide);
+  L->ld_ss_y = cdiv(Ld, kBNWide);
+  L->ld_ss_u = cdiv(D, kBNWide);
+  L->max_tiles = cdiv(R, kBM) + static_cast<int>(E < R ? E : R);
+  P.err = take(kAlign);  // error word; the near-tie counter shares this line
+  L->near_tie = P.err + 4;
+  P.xa = take(T * P.xa_cols * 2);
+  P.logits = take(T * L->ld_logits * 4);
+  P.topk_idx = take(R * 4);
+  P.topk_w = take(R * 4);
+  P.counts = take(E * 4);
+  P.offsets = take((E + 1) * 4);
+  P.row_of = take(R * 4);
+  P.tok_of = take(R * 4);
+  P.tiles = take(static_cast<size_t>(L->max_tiles) * sizeof(Tile));
+  P.n_tiles = take(4);
+  P.p = take(T * Ld * 2);
+  P.ss_p = take(T * L->ld_ss_p * 4);
+  P.xe = take(R * Ld * 2);
+  P.xe_scale = -1;
+  P.h = take(R * I * 2);
+  P.y = take(R * Ld * 2);
+  P.ss_y = take(R * L->ld_ss_y * 4);
+  P.c = take(T * Ld * 2);
+  P.u = take(T * D * 2);
+  P.ss_u = take(T * L->ld_ss_u * 4);
+  if (f32w) {
+    L->w_router = take(E * 3 * D * 2);
+    L->w_pool = take(Ld * D * 2);
+    L->w_gate = take(E * I * Ld * 2);
+    L->w_up = take(E * I * Ld * 2);
+    L->w_down = take(E * Ld * I * 2);
+    L->w_unpool = take(D * Ld * 2);
+  }
+  P.total = static_cast<long long>(off);
+  L->x_stage = take(T * D * (c->act_dtype == LMOE_F32 ? 4 : 2));
+  L->out_stage = take(T * D * (c->out_dtype == LMOE_F32 ? 4 : 2));
+  L->host_io_total = static_cast<long long>(off);
+}
+
+// ------------------------------------------------------------------ tensor maps
+// cuTensorMapEncodeTiled is a driver entry point; it is resolved through the runtime
+// once per process so the library does not link libcuda directly.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool encode_bf16_2d(CUtensorMap* m, const void* base, unsigned long long cols,
+                    unsigned long long rows, unsigned long long row_stride_bytes,
+                    unsigned box_cols, unsigned box_rows) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const CUresult r = enc(
+      m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define LMOE_CUDA(call)                       \
+  do {                                        \
+    if ((call) != cudaSuccess) return LMOE_ERR_CUDA; \
+  } while (0)
+
+lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_cols_used,
+                     long long a_row_stride_elems, const void* B, long long b_rows,
+                     long long b_cols, const void* B2, int N, int num_kb, int kb_period,
+                     const Tile* tiles, const int* n_tiles, int m_tiles, void* out,
+                     long long ldo, float* ss, int ld_ss, unsigned* err, long long budget,
+                     cudaStream_t s) {
+  const unsigned bn = epi == kEpiSwiGLU ? kBNSwiGLU : kBNWide;
+  CUtensorMap ta, tb, tb2;
+  if (!encode_bf16_2d(&ta, A, a_cols_used, a_rows, a_row_stride_elems * 2, kBK, kBM))
+    return LMOE_ERR_CUDA;
+  if (!encode_bf16_2d(&tb, B, b_cols, b_rows, b_cols * 2, kBK, bn)) return LMOE_ERR_CUDA;
+  tb2 = tb;
+  if (B2 && !encode_bf16_2d(&tb2, B2, b_cols, b_rows, b_cols * 2, kBK, bn)) return LMOE_ERR_CUDA;
+  GemmArgs a{};
+  a.M = static_cast<int>(a_rows);
+  a.N = N;
+  a.num_kb = num_kb;
+  a.kb_period = kb_period;
+  a.tiles = tiles;
+  a.n_tiles = n_tiles;
+  a.out = out;
+  a.ldo = ldo;
+  a.ss = ss;
+  a.ld_ss = ld_ss;
+  a.err = err;
+  a.budget = budget;
+  LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s));
+  return LMOE_OK;
+}
+
+lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_router,
+                         const void* W_pool, const float* g_pool, const void* W_gate,
+                         const void* W_up, const void* W_down, const float* g_expert,
+                         const void* W_unpool, const float* g_pre, const float* g_post,
+                         int top_k, void* out, void* workspace, size_t ws_bytes, cudaStream_t s,
+                         const lmoe_ex* ex) {
+  lmoe_status st = check_config(cfg);
+  if (st != LMOE_OK) return st;
+  if (top_k != cfg->top_k) return LMOE_ERR_ARG;
+  const void* ptrs[] = {x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert,
+                        W_unpool, g_pre, g_post, out};
+  for (const void* p : ptrs)
+    if (p == nullptr) return LMOE_ERR_ARG;
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return LMOE_ERR_ALIGN;
+  if (x == out) return LMOE_ERR_ARG;
+  Layout L;
+  make_layout(cfg, &L);
+  if (workspace == nullptr || ws_bytes < static_cast<size_t>(L.pub.total)) return LMOE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return LMOE_ERR_ALIGN;
+  if (ex && ex->router_bias && !aligned16(ex->router_bias)) return LMOE_ERR_ALIGN;
+  if (cfg->T == 0) return LMOE_OK;
+
+  const int T = cfg->T, D = cfg->d_model, Ld = cfg->d_latent, E = cfg->n_experts,
+            I = cfg->d_ff, k = cfg->top_k;
+  const long long R = static_cast<long long>(T) * k;
+  const float eps = cfg->eps;
+  const bool x_f32 = cfg->act_dtype == LMOE_F32, f32w = cfg->weight_dtype == LMOE_F32;
+  const long long budget =
+      (ex && ex->wait_budget_cycles > 0) ? ex->wait_budget_cycles : kDefaultWaitBudget;
+  char* ws = static_cast<char*>(workspace);
+  auto at = [&](long long o) { return static_cast<void*>(ws + o); };
+  unsigned* err = static_cast<unsigned*>(at(L.pub.err));
+  int32_t* near_tie = static_cast<int32_t*>(at(L.near_tie));
+  __nv_bfloat16* xa = static_cast<__nv_bfloat16*>(at(L.pub.xa));
+  float* logits = static_cast<float*>(at(L.pub.logits));
+  int32_t* tk_idx = static_cast<int32_t*>(at(L.pub.topk_idx));
+  float* tk_w = static_cast<float*>(at(L.pub.topk_w));
+  int32_t* counts = static_cast<int32_t*>(at(L.pub.counts));
+  int32_t* offsets = static_cast<int32_t*>(at(L.pub.offsets));
+  int32_t* row_of = static_cast<int32_t*>(at(L.pub.row_of));
+  int32_t* tok_of = static_cast<int32_t*>(at(L.pub.tok_of));
+  Tile* tiles = static_cast<Tile*>(at(L.pub.tiles));
+  int32_t* n_tiles = static_cast<int32_t*>(at(L.pub.n_tiles));
+  __nv_bfloat16* p = static_cast<__nv_bfloat16*>(at(L.pub.p));
+  float* ss_p = static_cast<float*>(at(L.pub.ss_p));
+  __nv_bfloat16* xe = static_cast<__nv_bfloat16*>(at(L.pub.xe));
+  __nv_bfloat16* h = static_cast<__nv_bfloat16*>(at(L.pub.h));
+  __nv_bfloat16* y = static_cast<__nv_bfloat16*>(at(L.pub.y));
+  float* ss_y = static_cast<float*>(at(L.pub.ss_y));
+  __nv_bfloat16* c = static_cast<__nv_bfloat16*>(at(L.pub.c));
+  __nv_bfloat16* u = static_cast<__nv_bfloat16*>(at(L.pub.u));
+  float* ss_u = static_cast<float*>(at(L.pub.ss_u));
+
+  // error word and near-tie counter start at zero on every call
+  LMOE_CUDA(cudaMemsetAsync(err, 0, 8, s));
+
+  // weights as bf16 K-major operands (fp32 weights are rounded here, the router split hi/lo)
+  const void *wr = W_router, *wp = W_pool, *wg = W_gate, *wu = W_up, *wd = W_down,
+             *wun = W_unpool;
+  if (f32w) {
+    __nv_bfloat16* d_wr = static_cast<__nv_bfloat16*>(at(L.w_router));
+    LMOE_CUDA(launch_router_split(static_cast<const float*>(W_router), E, D, d_wr, s));
+    const struct { const void* src; long long dst; long long n; } conv[] = {
+        {W_pool, L.w_pool, 1LL * Ld * D},        {W_gate, L.w_gate, 1LL * E * I * Ld},
+        {W_up, L.w_up, 1LL * E * I * Ld},        {W_down, L.w_down, 1LL * E * Ld * I},
+        {W_unpool, L.w_unpool, 1LL * D * Ld}};
+    for (const auto& cv : conv)
+      LMOE_CUDA(launch_f32_to_bf16(static_cast<const float*>(cv.src),
+                                   static_cast<__nv_bfloat16*>(at(cv.dst)), cv.n, s));
+    wr = d_wr;
+    wp = at(L.w_pool);
+    wg = at(L.w_gate);
+    wu = at(L.w_up);
+    wd = at(L.w_down);
+    wun = at(L.w_unpool);
+  }
+  const int xa_cols = L.pub.xa_cols;
+
+  // S1 pre-norm
+  LMOE_CUDA(launch_prenorm(x, x_f32, g_pre, T, D, eps, xa, xa_cols, s));
+  // S2 router logits = [xn_hi | xn_lo (| xn_hi)] . [W | W (| W_lo)]^T
+  const int m_tiles_T = cdiv(T, kBM);
+  st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
+                xa_cols / kBK, (f32w ? 3 * D : D) / kBK, nullptr, nullptr, m_tiles_T, logits,
+                L.ld_logits, nullptr, 0, err, budget, s);
+  if (st != LMOE_OK) return st;
+  // S3 top-k + softmax
+  LMOE_CUDA(launch_topk(logits, L.ld_logits, ex ? ex->router_bias : nullptr,
+                        ex ? ex->forced_idx : nullptr, T, E, k, tk_idx, tk_w, near_tie,
+                        ex ? ex->topk_idx_out : nullptr, ex ? ex->topk_w_out : nullptr, err, s));
+  if (ex && ex->near_tie_count_out)
+    LMOE_CUDA(cudaMemcpyAsync(ex->near_tie_count_out, near_tie, 4, cudaMemcpyDeviceToDevice, s));
+  // S4 permutation
+  LMOE_CUDA(launch_permute(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, s));
+  // S5 pooler p = xn_hi . W_pool^T, with row partial sums of squares
+  st = run_gemm(kEpiBf16Ss, xa, T, D, xa_cols, wp, Ld, D, nullptr, Ld, D / kBK, D / kBK, nullptr,
+                nullptr, m_tiles_T, p, Ld, ss_p, L.ld_ss_p, err, budget, s);
+  if (st != LMOE_OK) return st;
+  // S6 pool norm, scattered to the k expert-contiguous rows of each token
+  LMOE_CUDA(launch_poolnorm_scatter(p, ss_p, L.ld_ss_p, g_pool, row_of, T, Ld, k, eps, xe, s));
+  // S7 grouped gate/up + SwiGLU
+  st = run_gemm(kEpiSwiGLU, xe, R, Ld, Ld, wg, 1LL * E * I, Ld, wu, I, Ld / kBK, Ld / kBK, tiles,
+                n_tiles, L.max_tiles, h, I, nullptr, 0, err, budget, s);
+  if (st != LMOE_OK) return st;
+  // S8 grouped down, with per-row partial sums of squares of the bf16 outputs
+  st = run_gemm(kEpiBf16Ss, h, R, I, I, wd, 1LL * E * Ld, I, nullptr, Ld, I / kBK, I / kBK, tiles,
+                n_tiles, L.max_tiles, y, Ld, ss_y, L.ld_ss_y, err, budget, s);
+  if (st != LMOE_OK) return st;
+  // S9 combine: per-expert RMSNorm, routing weight, fp32 sum in slot order
+  LMOE_CUDA(launch_combine(y, ss_y, L.ld_ss_y, row_of, tk_idx, tk_w, g_expert, T, Ld, k, eps, c, s));
+  // S10 unpooler u = c . W_unpool^T with row partial sums of squares
+  st = run_gemm(kEpiBf16Ss, c, T, Ld, Ld, wun, D, Ld, nullptr, D, Ld / kBK, Ld / kBK, nullptr,
+                nullptr, m_tiles_T, u, D, ss_u, L.ld_ss_u, err, budget, s);
+  if (st != LMOE_OK) return st;
+  // S11 post-norm + residual
+  LMOE_CUDA(launch_postnorm_residual(x, x_f32, u, ss_u, L.ld_ss_u, g_post, T, D, eps, out,
+                                     cfg->out_dtype == LMOE_F32, s));
+  return LMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lmoe_status lmoe_workspace_size(const lmoe_config* cfg, size_t* bytes) {
+  const lmoe_status st = check_config(cfg);
+  if (st != LMOE_OK) return st;
+  if (bytes == nullptr) return LMOE_ERR_ARG;
+  Layout L;
+  make_layout(cfg, &L);
+  *bytes = static_cast<size_t>(L.pub.total);
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_workspace_size_host_io(const lmoe_config* cfg, size_t* bytes) {
+  const lmoe_status st = check_config(cfg);
+  if (st != LMOE_OK) return st;
+  if (bytes == nullptr) return LMOE_ERR_ARG;
+  Layout L;
+  make_layout(cfg, &L);
+  *bytes = static_cast<size_t>(L.host_io_total);
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_get_workspace_layout(const lmoe_config* cfg, lmoe_workspace_layout* layout) {
+  const lmoe_status st = check_config(cfg);
+  if (st != LMOE_OK) return st;
+  if (layout == nullptr) return LMOE_ERR_ARG;
+  Layout L;
+  make_layout(cfg, &L);
+  *layout = L.pub;
+  return LMOE_OK;
+}
+
+lmoe_status latent_moe_forward(const lmoe_config* cfg, const void* x, const void* W_router,
+                               const void* W_pool, const float* g_pool, const void* W_gate,
+                               const void* W_up, const void* W_down, const float* g_expert,
+                               const void* W_unpool, const float* g_pre, const float* g_post,
+                               int top_k, void* out, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+  return forward_impl(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool,
+                      g_pre, g_post, top_k, out, workspace, workspace_bytes, stream, nullptr);
+}
+
+lmoe_status latent_moe_forward_ex(const lmoe_config* cfg, const void* x, const void* W_router,
+                                  const void* W_pool, const float* g_pool, const void* W_gate,
+                                  const void* W_up, const void* W_down, const float* g_expert,
+                                  const void* W_unpool, const float* g_pre, const float* g_post,
+                                  int top_k, void* out, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream, const lmoe_ex* ex) {
+  return forward_impl(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool,
+                      g_pre, g_post, top_k, out, workspace, workspace_bytes, stream, ex);
+}
+
+lmoe_status latent_moe_forward_host_io(const lmoe_config* cfg, const void* x_host,
+                                       const void* W_router, const void* W_pool,
+                                       const float* g_pool, const void* W_gate, const void* W_up,
+                                       const void* W_down, const float* g_expert,
+                                       const void* W_unpool, const float* g_pre,
+                                       const float* g_post, int top_k, void* out_host,
+                                       void* workspace, size_t workspace_bytes,
+                                       cudaStream_t stream) {
+  const lmoe_status st = check_config(cfg);
+  if (st != LMOE_OK) return st;
+  if (x_host == nullptr || out_host == nullptr) return LMOE_ERR_ARG;
+  Layout L;
+  make_layout(cfg, &L);
+  if (workspace == nullptr || workspace_bytes < static_cast<size_t>(L.host_io_total))
+    return LMOE_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  const size_t xb = static_cast<size_t>(cfg->T) * cfg->d_model * (cfg->act_dtype == LMOE_F32 ? 4 : 2);
+  const size_t ob = static_cast<size_t>(cfg->T) * cfg->d_model * (cfg->out_dtype == LMOE_F32 ? 4 : 2);
+  if (cfg->T == 0) return LMOE_OK;
+  if (cudaMemcpyAsync(ws + L.x_stage, x_host, xb, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  const lmoe_status s2 =
+      forward_impl(cfg, ws + L.x_stage, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert,
+                   W_unpool, g_pre, g_post, top_k, ws + L.out_stage, workspace,
+                   static_cast<size_t>(L.pub.total), stream, nullptr);
+  if (s2 != LMOE_OK) return s2;
+  if (cudaMemcpyAsync(out_host, ws + L.out_stage, ob, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStream_t stream,
+                              uint32_t* detail) {
+  const lmoe_status st = check_config(cfg);
+  if (st != LMOE_OK) return st;
+  if (workspace == nullptr) return LMOE_ERR_WORKSPACE;
+  Layout L;
+  make_layout(cfg, &L);
+  uint32_t word = 0;
+  unsigned* err = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + L.pub.err);
+  if (cudaMemcpyAsync(&word, err, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (detail) *detail = word;
+  if (word & (kErrWaitProducer | kErrWaitMma | kErrWaitEpilogue | kErrDrain)) return LMOE_ERR_TIMEOUT;
+  if (word & kErrBadIndex) return LMOE_ERR_ARG;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_wait_selftest(const lmoe_config* cfg, void* workspace, long long budget_cycles,
+                               cudaStream_t stream) {
+  const lmoe_status st = check_config(cfg);
+  if (st != LMOE_OK) return st;
+  if (workspace == nullptr) return LMOE_ERR_WORKSPACE;
+  Layout L;
+  make_layout(cfg, &L);
+  const long long b = budget_cycles < 1 ? 1 : (budget_cycles > 4000000000LL ? 4000000000LL : budget_cycles);
+  unsigned* err = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + L.pub.err);
+  if (launch_wait_selftest(b, err, stream) != cudaSuccess) return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+const char* lmoe_status_string(lmoe_status s) {
+  switch (s) {
+    case LMOE_OK: return "ok";
+    case LMOE_ERR_ARG: return "invalid argument";
+    case LMOE_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case LMOE_ERR_ALIGN: return "pointer not aligned (16 B for tensors, 256 B for workspace)";
+    case LMOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case LMOE_ERR_CUDA: return "CUDA call failed";
+    case LMOE_ERR_TIMEOUT: return "a device wait exceeded its budget";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

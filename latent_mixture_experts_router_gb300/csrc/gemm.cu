@@ -1,0 +1,279 @@
+// gemm.cu — grouped BF16 GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// out[r, n] = sum_k A[r, k] * B[e*N + n, k]  for the rows r of each M tile, where
+// e is the tile's expert (0 for a plain GEMM).  A and B are K-major bf16 and are
+// staged in shared memory by TMA (128-byte swizzle); the fp32 accumulator lives
+// in tensor memory.  One CTA computes one 128 x BN output tile with three roles:
+//   warp 0, lane 0   TMA producer over a STAGES-deep ring of smem slots
+//   warp 1, lane 0   tcgen05.mma issuer (warp 1 also owns the TMEM allocation)
+//   warps 2..5       epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (one row each)
+// Epilogues (one per use in the latent-MoE block):
+//   kEpiF32     fp32 logits (router)
+//   kEpiBf16Ss  bf16 output plus, per row, the partial sum of squares of the
+//               bf16-rounded values of this tile's columns.  The row's RMS is
+//               finished later from these partials, so no kernel re-reads the row to
+//               normalise it (the "fused per-expert post-norm" of the LMSYS Muse Spark
+//               Open post: each second-GEMM tile accumulates the sum of squares of the
+//               BF16 values it holds; here partials go to [rows, N/BN] without atomics,
+//               so the result is deterministic).
+//   kEpiSwiGLU  gate and up tiles of the same columns in one CTA (two B loads per
+//               stage, two accumulators), output bf16 silu(a) * b.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lmoe {
+
+template <int BN, int EPI>
+struct GemmCfg {
+  static constexpr bool kDual = (EPI == kEpiSwiGLU);
+  static constexpr int kStages = 4;
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes * (kDual ? 2 : 1);
+  static constexpr int kAccCols = kDual ? 2 * BN : BN;
+  static constexpr uint32_t kTmemCols = kAccCols <= 32    ? 32
+                                        : kAccCols <= 64  ? 64
+                                        : kAccCols <= 128 ? 128
+                                        : kAccCols <= 256 ? 256
+                                                          : 512;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
+};
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
+  using C = GemmCfg<BN, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* accum = empty + C::kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  // ---- which tile
+  int expert = 0, row0, nrows;
+  if (args.tiles != nullptr) {
+    if (static_cast<int>(blockIdx.y) >= *args.n_tiles) return;
+    const Tile t = args.tiles[blockIdx.y];
+    expert = t.expert;
+    row0 = t.row0;
+    nrows = t.nrows;
+  } else {
+    row0 = blockIdx.y * kBM;
+    nrows = min(kBM, args.M - row0);
+  }
+  if (nrows <= 0) return;
+  const int n0 = blockIdx.x * BN;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- setup
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (C::kDual) prefetch_tmap(&tmB2);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const long long budget = args.budget;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer
+      const int brow = expert * args.N + n0;
+      const uint64_t pol_b = policy_evict_first();  // weights: streamed once per tile
+      int issued = 0;
+      for (int kb = 0; kb < args.num_kb; ++kb) {
+        const int s = kb % C::kStages;
+        const uint32_t ph = (kb / C::kStages) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, budget)) {
+          atomicOr(args.err, kErrWaitProducer);
+          atomicExch(abort_flag, 1);
+          break;
+        }
+        uint8_t* sa = smem + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+        tma_load_2d(sa, &tmA, &full[s], kb * kBK, row0);
+        const int kbb = (kb % args.kb_period) * kBK;
+        tma_load_2d_hint(sa + C::kABytes, &tmB, &full[s], kbb, brow, pol_b);
+        if (C::kDual) tma_load_2d_hint(sa + C::kABytes + C::kBBytes, &tmB2, &full[s], kbb, brow, pol_b);
+        issued = kb + 1;
+      }
+      // before leaving, let every copy this thread issued land (drain budget, independent
+      // of the caller's: the CTA must not exit with a copy still writing its smem)
+      for (int kb = max(0, issued - C::kStages); kb < issued; ++kb)
+        if (!mbar_wait(&full[kb % C::kStages], (kb / C::kStages) & 1, kDrainBudget))
+          atomicOr(args.err, kErrDrain);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      for (int kb = 0; kb < args.num_kb; ++kb) {
+        const int s = kb % C::kStages;
+        const uint32_t ph = (kb / C::kStages) & 1;
+        if (!mbar_wait(&full[s], ph, budget)) {
+          atomicOr(args.err, kErrWaitMma);
+          atomicExch(abort_flag, 1);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(smem + s * C::kStageBytes);
+        const uint32_t b0 = a0 + C::kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t ad = sw128_kmajor_desc(a0 + kk * 32);
+          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+          mma_bf16(tmem, ad, sw128_kmajor_desc(b0 + kk * 32), idesc, acc);
+          if (C::kDual)
+            mma_bf16(tmem + BN, ad, sw128_kmajor_desc(b0 + C::kBBytes + kk * 32), idesc, acc);
+        }
+        mma_commit(&empty[s]);  // the slot is free once these MMAs have read it
+      }
+      mma_commit(accum);        // accumulator complete
+    }
+  } else {
+    // ---- epilogue: warps 2..5 ; TMEM lane quadrant = warp % 4
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const bool row_ok = r < nrows;
+    const long long grow = static_cast<long long>(row0) + r;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const bool ok = mbar_wait(accum, 0, budget);
+    if (!ok) {
+      atomicOr(args.err, kErrWaitEpilogue);
+      // the MMAs already issued must finish before TMEM is released
+      if (!mbar_wait(accum, 0, kDrainBudget)) atomicOr(args.err, kErrDrain);
+    }
+    tc_fence_after();
+    if (ok) {
+      if constexpr (EPI == kEpiF32) {
+        float* orow = static_cast<float*>(args.out) + grow * args.ldo;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32cols(tq + c0, v);
+          tmem_ld_wait();
+          const int col = n0 + c0;
+          if (row_ok && col + 32 <= args.N) {
+            float4* o = reinterpret_cast<float4*>(orow + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          } else if (row_ok && col < args.N) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col + i < args.N) orow[col + i] = __uint_as_float(v[i]);
+          }
+        }
+      } else if constexpr (EPI == kEpiBf16Ss) {
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo;
+        float ss = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32cols(tq + c0, v);
+          tmem_ld_wait();
+          const int col = n0 + c0;
+          if (row_ok && col + 32 <= args.N) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float a = bf16_round(__uint_as_float(v[2 * i]));
+              const float b = bf16_round(__uint_as_float(v[2 * i + 1]));
+              ss = fmaf(a, a, ss);
+              ss = fmaf(b, b, ss);
+              pk[i] = pack_bf16x2(a, b);
+            }
+            uint4* o = reinterpret_cast<uint4*>(orow + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (row_ok) args.ss[grow * args.ld_ss + blockIdx.x] = ss;
+      } else {  // kEpiSwiGLU
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld_32cols(tq + c0, g);
+          tmem_ld_32cols(tq + BN + c0, u);
+          tmem_ld_wait();
+          const int col = n0 + c0;
+          if (row_ok && col + 32 <= args.N) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float a0 = __uint_as_float(g[2 * i]), a1 = __uint_as_float(g[2 * i + 1]);
+              const float h0 = a0 / (1.f + __expf(-a0)) * __uint_as_float(u[2 * i]);
+              const float h1 = a1 / (1.f + __expf(-a1)) * __uint_as_float(u[2 * i + 1]);
+              pk[i] = pack_bf16x2(h0, h1);
+            }
+            uint4* o = reinterpret_cast<uint4*>(orow + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  // ---- teardown: every TMEM read is complete before the columns are released
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int BN, int EPI>
+static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const CUtensorMap& tmB2, const GemmArgs& a, int m_tiles,
+                              cudaStream_t s) {
+  using C = GemmCfg<BN, EPI>;
+  auto kern = gemm_tcgen05_kernel<BN, EPI>;
+  static bool attr_set = false;  // per process; the attribute is per function
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid((a.N + BN - 1) / BN, m_tiles);
+  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  kern<<<grid, 192, C::kSmemBytes, s>>>(tmA, tmB, tmB2, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        const CUtensorMap& tmB2, const GemmArgs& a, int m_tiles,
+                        cudaStream_t s) {
+  switch (epi) {
+    case kEpiF32: return launch_one<kBNWide, kEpiF32>(tmA, tmB, tmB2, a, m_tiles, s);
+    case kEpiBf16Ss: return launch_one<kBNWide, kEpiBf16Ss>(tmA, tmB, tmB2, a, m_tiles, s);
+    case kEpiSwiGLU: return launch_one<kBNSwiGLU, kEpiSwiGLU>(tmA, tmB, tmB2, a, m_tiles, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lmoe

@@ -1,0 +1,81 @@
+// internal.h — declarations shared by the library's translation units (not public).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lmoe {
+
+constexpr int kBM = 128;            // rows of one GEMM tile (tcgen05 M)
+constexpr int kBK = 64;             // K elements of one pipeline stage (128 B of bf16)
+constexpr int kBNWide = 256;        // N of the single-B GEMM tiles
+constexpr int kBNSwiGLU = 128;      // N of each of the gate and up tiles
+constexpr long long kDefaultWaitBudget = 4000000000LL;  // ~2 s of SM clock
+constexpr long long kDrainBudget = 4000000000LL;        // waits for a CTA's own async work
+
+// error-word bits written by device code
+enum : uint32_t {
+  kErrWaitProducer = 1u << 0,
+  kErrWaitMma = 1u << 1,
+  kErrWaitEpilogue = 1u << 2,
+  kErrBadIndex = 1u << 3,
+  kErrDrain = 1u << 4,
+};
+
+enum EpiKind : int {
+  kEpiF32 = 0,      // fp32 store (router logits)
+  kEpiBf16Ss = 1,   // bf16 store + per-row partial sum of squares of the bf16 values
+  kEpiSwiGLU = 2,   // two accumulators a, b -> bf16 silu(a) * b
+};
+
+// One M tile of a grouped GEMM: rows [row0, row0 + nrows) of A, all of expert `expert`.
+struct Tile {
+  int expert, row0, nrows, pad;
+};
+
+struct GemmArgs {
+  int M;                   // rows of A when tiles == nullptr (dense tiling)
+  int N;                   // output columns (rows of one expert's B)
+  int num_kb;              // K / kBK
+  int kb_period;           // B's k-blocks before its coordinate wraps (K of B / kBK)
+  const Tile* tiles;       // grouped tiles, or nullptr
+  const int* n_tiles;      // number of valid grouped tiles (device)
+  void* out;               // [rows, ldo] fp32 or bf16
+  long long ldo;           // elements
+  float* ss;               // [rows, ld_ss] partial sums of squares (kEpiBf16Ss)
+  int ld_ss;
+  unsigned* err;           // device error word
+  long long budget;        // wait budget, SM cycles
+};
+
+// Launches one tcgen05 GEMM: out = A * B^T over grid (ceil(N/BN), m_tiles).
+cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                        const CUtensorMap& tmB2, const GemmArgs& a, int m_tiles,
+                        cudaStream_t s);
+
+// Row kernels (rowops.cu)
+cudaError_t launch_prenorm(const void* x, bool x_f32, const float* g_pre, int T, int D, float eps,
+                           __nv_bfloat16* xa, int xa_cols, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, int ld, const float* bias, const int32_t* forced,
+                        int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
+                        int32_t* idx_copy, float* w_copy, unsigned* err, cudaStream_t s);
+cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
+                           int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
+                           int32_t* n_tiles, cudaStream_t s);
+cudaError_t launch_poolnorm_scatter(const __nv_bfloat16* p, const float* ss_p, int ld_ss,
+                                    const float* g_pool, const int32_t* row_of, int T, int L,
+                                    int k, float eps, __nv_bfloat16* xe, cudaStream_t s);
+cudaError_t launch_combine(const __nv_bfloat16* y, const float* ss_y, int ld_ss,
+                           const int32_t* row_of, const int32_t* idx, const float* w,
+                           const float* g_expert, int T, int L, int k, float eps,
+                           __nv_bfloat16* c, cudaStream_t s);
+cudaError_t launch_postnorm_residual(const void* x, bool x_f32, const __nv_bfloat16* u,
+                                     const float* ss_u, int ld_ss, const float* g_post, int T,
+                                     int D, float eps, void* out, bool out_f32, cudaStream_t s);
+cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s);
+cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, long long n, cudaStream_t s);
+cudaError_t launch_router_split(const float* W, int E, int D, __nv_bfloat16* dst,
+                                cudaStream_t s);
+
+}  // namespace lmoe

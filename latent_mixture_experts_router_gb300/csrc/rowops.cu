@@ -1,0 +1,503 @@
+// rowops.cu — memory-bound kernels of the latent-MoE block: one row (token) per
+// CTA or per warp, 16-byte vector loads and stores, fp32 arithmetic, fixed
+// reduction orders (results do not depend on scheduling).
+//
+// Block structure they implement (LMSYS "SGLang and Miles Add Day-0 Support for
+// Muse Spark Open", section "MoE with pooler, unpooler and per-expert
+// normalization"; vLLM "Day 0 support for Muse Spark Open", "Sandwich
+// normalization"):
+//   prenorm            xn = x / sqrt(mean(x^2) + eps) * g_pre, written as a bf16
+//                      hi/lo pair so that the router sees xn to ~fp32 accuracy
+//   topk               softmax over all experts, top-k (ties -> lower index),
+//                      weights renormalised over the k
+//   permute            expert-contiguous order of the (token, slot) pairs:
+//                      per-expert histogram, exclusive scan, stable scatter
+//   poolnorm_scatter   h0 = p / sqrt(mean(p^2) + eps) * g_pool, copied to the
+//                      k expert-contiguous rows of the token
+//   combine            c = sum_j w_j * g_expert[e_j] * y_j / sqrt(mean(y_j^2) + eps)
+//                      in fp32, slot order (per-expert norm BEFORE weighting)
+//   postnorm_residual  out = x + u / sqrt(mean(u^2) + eps) * g_post
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lmoe {
+
+namespace {
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  // fixed-order reduction: warp butterfly, then warp 0 over the warp partials
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (w == 0) {
+    t = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (l == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+__device__ __forceinline__ int block_sum_int(int v, int* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int t = (l < (int)(blockDim.x >> 5)) ? red[l] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (l == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+// 8 consecutive elements of a row as fp32
+__device__ __forceinline__ void load8(const void* base, bool f32, long long i, float (&v)[8]) {
+  if (f32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+    const float4 a = p[0], b = p[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + i);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      v[2 * j] = f.x;
+      v[2 * j + 1] = f.y;
+    }
+  }
+}
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float (&v)[8]) {
+  load8(p, false, 0, v);
+}
+__device__ __forceinline__ void store8_bf16(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 q;
+  q.x = pack_bf16x2(v[0], v[1]);
+  q.y = pack_bf16x2(v[2], v[3]);
+  q.z = pack_bf16x2(v[4], v[5]);
+  q.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = q;
+}
+__device__ __forceinline__ void load8_f32(const float* p, float (&v)[8]) { load8(p, true, 0, v); }
+
+// ------------------------------------------------------------------ prenorm
+// One CTA per token.  xa row = [xn_hi | xn_lo] (or [hi | lo | hi] when xa_cols = 3D,
+// to pair with router weights split as [W_hi | W_hi | W_lo]).
+__global__ void __launch_bounds__(kRowThreads) prenorm_kernel(const void* __restrict__ x, int x_f32,
+                                                              const float* __restrict__ g,
+                                                              int D, float eps,
+                                                              __nv_bfloat16* __restrict__ xa,
+                                                              int xa_cols) {
+  __shared__ float red[33];
+  const long long t = blockIdx.x;
+  const long long xoff = t * D;
+  float ss = 0.f;
+  for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
+    float v[8];
+    load8(x, x_f32, xoff + i, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
+  }
+  const float rs = rsqrtf(block_sum(ss, red) / static_cast<float>(D) + eps);
+  __nv_bfloat16* row = xa + t * xa_cols;
+  for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
+    float v[8], gg[8], hi[8], lo[8];
+    load8(x, x_f32, xoff + i, v);
+    load8_f32(g + i, gg);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float xn = v[j] * rs * gg[j];
+      hi[j] = bf16_round(xn);
+      lo[j] = xn - hi[j];
+    }
+    store8_bf16(row + i, hi);
+    store8_bf16(row + D + i, lo);
+    if (xa_cols == 3 * D) store8_bf16(row + 2 * D + i, hi);
+  }
+}
+
+// ------------------------------------------------------------------ top-k + softmax
+// One warp per token.  Selection: k rounds of a warp arg-max over (value desc,
+// index asc); the (k+1)-th round gives the margin for the near-tie count.
+constexpr int kTopkWarps = 4;
+
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
+    const float* __restrict__ logits, int ld, const float* __restrict__ bias,
+    const int32_t* __restrict__ forced, int T, int E, int k, int32_t* __restrict__ idx_out,
+    float* __restrict__ w_out, int32_t* __restrict__ near_tie, int32_t* __restrict__ idx_copy,
+    float* __restrict__ w_copy, unsigned* __restrict__ err) {
+  extern __shared__ float vals_all[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * kTopkWarps + warp;
+  if (t >= T) return;
+  float* vals = vals_all + warp * E;
+  for (int i = lane; i < E; i += 32) vals[i] = logits[t * ld + i] + (bias ? bias[i] : 0.f);
+  __syncwarp();
+  int sel[16];
+  float sval[16];
+  if (forced != nullptr) {
+    for (int j = 0; j < k; ++j) {
+      int e = forced[t * k + j];
+      if (e < 0 || e >= E) {  // an id outside [0, E) would index out of bounds downstream
+        if (lane == 0) atomicOr(err, kErrBadIndex);
+        e = 0;
+      }
+      sel[j] = e;
+      sval[j] = vals[e];
+    }
+  } else {
+    const int rounds = (k < E) ? k + 1 : k;
+    for (int j = 0; j < rounds; ++j) {
+      float best = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int i = lane; i < E; i += 32) {
+        const float v = vals[i];
+        if (v > best || (v == best && i < bi)) {
+          best = v;
+          bi = i;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > best || (ov == best && oi < bi)) {
+          best = ov;
+          bi = oi;
+        }
+      }
+      if (j < k) {
+        sel[j] = bi;
+        sval[j] = best;
+        if (lane == 0) vals[bi] = -INFINITY;
+        __syncwarp();
+      } else if (lane == 0 && near_tie != nullptr && (sval[k - 1] - best) < 1e-3f) {
+        atomicAdd(near_tie, 1);
+      }
+    }
+  }
+  if (lane == 0) {
+    float m = sval[0];
+    for (int j = 1; j < k; ++j) m = fmaxf(m, sval[j]);
+    float ex[16], sum = 0.f;
+    for (int j = 0; j < k; ++j) {
+      ex[j] = expf(sval[j] - m);
+      sum += ex[j];
+    }
+    const float inv = 1.f / sum;
+    for (int j = 0; j < k; ++j) {
+      idx_out[t * k + j] = sel[j];
+      w_out[t * k + j] = ex[j] * inv;
+      if (idx_copy) idx_copy[t * k + j] = sel[j];
+      if (w_copy) w_copy[t * k + j] = ex[j] * inv;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ permutation
+// Pairs (t, j) are numbered i = t*k + j.  Expert e owns rows [off[e], off[e] + cnt[e])
+// of the expert-contiguous matrices, in increasing i (stable, so deterministic).
+constexpr int kPermThreads = 256;
+constexpr int kPermPerThread = 16;
+
+__global__ void __launch_bounds__(kPermThreads) expert_count_kernel(const int32_t* __restrict__ idx,
+                                                                    int n, int32_t* counts) {
+  __shared__ int red[33];
+  const int e = blockIdx.x;
+  int c = 0;
+  for (int i = threadIdx.x; i < n; i += kPermThreads) c += (idx[i] == e);
+  const int tot = block_sum_int(c, red);
+  if (threadIdx.x == 0) counts[e] = tot;
+}
+
+__global__ void __launch_bounds__(kPermThreads) expert_scatter_kernel(
+    const int32_t* __restrict__ idx, int n, int k, int E, const int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of,
+    Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles) {
+  __shared__ int wsum[kPermThreads / 32];
+  __shared__ int red[33];
+  const int e = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int my_off = 0, my_t0 = 0;
+  for (int q = threadIdx.x; q < e; q += kPermThreads) {
+    my_off += counts[q];
+    my_t0 += (counts[q] + kBM - 1) / kBM;
+  }
+  const int off = block_sum_int(my_off, red);
+  const int tile0 = block_sum_int(my_t0, red);
+  const int cnt = counts[e];
+  if (threadIdx.x == 0) {
+    offsets[e] = off;
+    if (e == E - 1) {
+      offsets[E] = off + cnt;
+      *n_tiles = tile0 + (cnt + kBM - 1) / kBM;
+    }
+  }
+  const int ntile = (cnt + kBM - 1) / kBM;
+  for (int m = threadIdx.x; m < ntile; m += kPermThreads)
+    tiles[tile0 + m] = Tile{e, off + m * kBM, min(kBM, cnt - m * kBM), 0};
+  if (cnt == 0) return;
+  int running = 0;
+  for (int base = 0; base < n; base += kPermThreads * kPermPerThread) {
+    const int i0 = base + threadIdx.x * kPermPerThread;
+    uint32_t mask = 0;
+#pragma unroll
+    for (int q = 0; q < kPermPerThread; ++q) {
+      const int i = i0 + q;
+      if (i < n && idx[i] == e) mask |= 1u << q;
+    }
+    const int mine = __popc(mask);
+    int incl = mine;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int q = 0; q < kPermThreads / 32; ++q) {
+      before += (q < warp) ? wsum[q] : 0;
+      total += wsum[q];
+    }
+    int r = off + running + before + incl - mine;
+    while (mask) {
+      const int q = __ffs(mask) - 1;
+      mask &= mask - 1;
+      const int i = i0 + q;
+      row_of[i] = r;
+      tok_of[r] = i / k;
+      ++r;
+    }
+    running += total;
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ pool norm + scatter
+__global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
+    const __nv_bfloat16* __restrict__ p, const float* __restrict__ ss_p, int ld_ss,
+    const float* __restrict__ g, const int32_t* __restrict__ row_of, int L, int k, float eps,
+    __nv_bfloat16* __restrict__ xe) {
+  __shared__ float s_rs;
+  __shared__ int s_rows[16];
+  const long long t = blockIdx.x;
+  if (threadIdx.x == 0) {
+    float ss = 0.f;
+    for (int q = 0; q < ld_ss; ++q) ss += ss_p[t * ld_ss + q];
+    s_rs = rsqrtf(ss / static_cast<float>(L) + eps);
+  }
+  if (threadIdx.x < k) s_rows[threadIdx.x] = row_of[t * k + threadIdx.x];
+  __syncthreads();
+  const float rs = s_rs;
+  for (int i = threadIdx.x * 8; i < L; i += kRowThreads * 8) {
+    float v[8], gg[8];
+    load8_bf16(p + t * L + i, v);
+    load8_f32(g + i, gg);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = v[j] * rs * gg[j];
+    for (int j = 0; j < k; ++j) store8_bf16(xe + static_cast<long long>(s_rows[j]) * L + i, v);
+  }
+}
+
+// ------------------------------------------------------------------ combine
+__global__ void __launch_bounds__(kRowThreads) combine_kernel(
+    const __nv_bfloat16* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
+    const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx,
+    const float* __restrict__ w, const float* __restrict__ g_expert, int L, int k, float eps,
+    __nv_bfloat16* __restrict__ c) {
+  __shared__ float s_coef[16];
+  __shared__ int s_row[16], s_e[16];
+  const long long t = blockIdx.x;
+  if (threadIdx.x < k) {
+    const int j = threadIdx.x;
+    const int row = row_of[t * k + j];
+    float ss = 0.f;
+    for (int q = 0; q < ld_ss; ++q) ss += ss_y[static_cast<long long>(row) * ld_ss + q];
+    s_coef[j] = w[t * k + j] * rsqrtf(ss / static_cast<float>(L) + eps);
+    s_row[j] = row;
+    s_e[j] = idx[t * k + j];
+  }
+  __syncthreads();
+  for (int i = threadIdx.x * 8; i < L; i += kRowThreads * 8) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {  // slot order
+      float v[8], gg[8];
+      load8_bf16(y + static_cast<long long>(s_row[j]) * L + i, v);
+      load8_f32(g_expert + static_cast<long long>(s_e[j]) * L + i, gg);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_coef[j], v[q] * gg[q], acc[q]);
+    }
+    store8_bf16(c + t * L + i, acc);
+  }
+}
+
+// ------------------------------------------------------------------ post-norm + residual
+__global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
+    const void* __restrict__ x, int x_f32, const __nv_bfloat16* __restrict__ u,
+    const float* __restrict__ ss_u, int ld_ss, const float* __restrict__ g, int D, float eps,
+    void* __restrict__ out, int out_f32) {
+  __shared__ float s_rs;
+  const long long t = blockIdx.x;
+  if (threadIdx.x == 0) {
+    float ss = 0.f;
+    for (int q = 0; q < ld_ss; ++q) ss += ss_u[t * ld_ss + q];
+    s_rs = rsqrtf(ss / static_cast<float>(D) + eps);
+  }
+  __syncthreads();
+  const float rs = s_rs;
+  for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
+    float xv[8], uv[8], gg[8];
+    load8(x, x_f32, t * D + i, xv);
+    load8_bf16(u + t * D + i, uv);
+    load8_f32(g + i, gg);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) xv[j] = xv[j] + uv[j] * rs * gg[j];
+    if (out_f32) {
+      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + t * D + i);
+      o[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
+      o[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+    } else {
+      store8_bf16(static_cast<__nv_bfloat16*>(out) + t * D + i, xv);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ fp32 weights -> bf16
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                                   long long n) {
+  for (long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x * 8) {
+    float v[8];
+    load8_f32(src + i, v);
+    store8_bf16(dst + i, v);
+  }
+}
+
+// W [E, D] fp32 -> [E, 3D] bf16 as [W_hi | W_hi | W_lo], W_lo = bf16(W - W_hi)
+__global__ void router_split_kernel(const float* __restrict__ W, int D,
+                                    __nv_bfloat16* __restrict__ dst) {
+  const long long e = blockIdx.x;
+  for (int i = threadIdx.x * 8; i < D; i += blockDim.x * 8) {
+    float v[8], hi[8], lo[8];
+    load8_f32(W + e * D + i, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      hi[j] = bf16_round(v[j]);
+      lo[j] = v[j] - hi[j];
+    }
+    __nv_bfloat16* row = dst + e * 3 * D;
+    store8_bf16(row + i, hi);
+    store8_bf16(row + D + i, hi);
+    store8_bf16(row + 2 * D + i, lo);
+  }
+}
+
+// ------------------------------------------------------------------ wait self-test
+// One thread waits on a barrier that is initialised for one arrival that never comes.
+__global__ void wait_selftest_kernel(long long budget, unsigned* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, budget)) atomicOr(err, kErrWaitEpilogue);
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(budget, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prenorm(const void* x, bool x_f32, const float* g_pre, int T, int D, float eps,
+                           __nv_bfloat16* xa, int xa_cols, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  prenorm_kernel<<<T, kRowThreads, 0, s>>>(x, x_f32 ? 1 : 0, g_pre, D, eps, xa, xa_cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float* logits, int ld, const float* bias, const int32_t* forced,
+                        int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
+                        int32_t* idx_copy, float* w_copy, unsigned* err, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int blocks = (T + kTopkWarps - 1) / kTopkWarps;
+  const size_t smem = static_cast<size_t>(kTopkWarps) * E * sizeof(float);
+  topk_kernel<<<blocks, kTopkWarps * 32, smem, s>>>(logits, ld, bias, forced, T, E, k, idx, w,
+                                                    near_tie, idx_copy, w_copy, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
+                           int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
+                           int32_t* n_tiles, cudaStream_t s) {
+  const int n = T * k;
+  expert_count_kernel<<<E, kPermThreads, 0, s>>>(idx, n, counts);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  expert_scatter_kernel<<<E, kPermThreads, 0, s>>>(idx, n, k, E, counts, offsets, row_of, tok_of,
+                                                   tiles, n_tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_poolnorm_scatter(const __nv_bfloat16* p, const float* ss_p, int ld_ss,
+                                    const float* g_pool, const int32_t* row_of, int T, int L,
+                                    int k, float eps, __nv_bfloat16* xe, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  poolnorm_scatter_kernel<<<T, kRowThreads, 0, s>>>(p, ss_p, ld_ss, g_pool, row_of, L, k, eps, xe);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const __nv_bfloat16* y, const float* ss_y, int ld_ss,
+                           const int32_t* row_of, const int32_t* idx, const float* w,
+                           const float* g_expert, int T, int L, int k, float eps,
+                           __nv_bfloat16* c, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  combine_kernel<<<T, kRowThreads, 0, s>>>(y, ss_y, ld_ss, row_of, idx, w, g_expert, L, k, eps, c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_postnorm_residual(const void* x, bool x_f32, const __nv_bfloat16* u,
+                                     const float* ss_u, int ld_ss, const float* g_post, int T,
+                                     int D, float eps, void* out, bool out_f32, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  postnorm_residual_kernel<<<T, kRowThreads, 0, s>>>(x, x_f32 ? 1 : 0, u, ss_u, ld_ss, g_post, D,
+                                                     eps, out, out_f32 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, long long n,
+                               cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  const long long chunks = (n + 7) / 8;
+  const int blocks = static_cast<int>(std::min<long long>((chunks + 255) / 256, 152 * 16));
+  f32_to_bf16_kernel<<<blocks, 256, 0, s>>>(src, dst, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_split(const float* W, int E, int D, __nv_bfloat16* dst,
+                                cudaStream_t s) {
+  router_split_kernel<<<E, 256, 0, s>>>(W, D, dst);
+  return cudaGetLastError();
+}
+
+}  // namespace lmoe

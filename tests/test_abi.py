@@ -1,0 +1,88 @@
+"""The C ABI loads and exports every function include/latent_moe.h declares, and rejects
+bad arguments on the host before any launch (no GPU needed for these paths)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lm():
+    from latent_mixture_experts_router_gb300 import build
+    build.build()
+    import latent_mixture_experts_router_gb300 as lm
+    return lm
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:lmoe_status|const char\*)\s+(\w+)\s*\(", src, flags=re.M)
+    return names
+
+
+def test_exports_every_declared_symbol(lm):
+    names = declared_functions()
+    assert "latent_moe_forward" in names and len(names) >= 8
+    lib = ctypes.CDLL(lm.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lm):
+    lib = lm.load()
+    for s in range(-6, 1):
+        assert lib.lmoe_status_string(s)
+
+
+def test_workspace_sizes_and_layout(lm):
+    c = lm.Config(128, 8192, 4096, 256, 4096, 8)
+    n = lm.lmoe_workspace_size(c)
+    lay = lm.lmoe_get_workspace_layout(c)
+    assert lay["total"] == n and lay["xa_cols"] == 2 * 8192
+    offs = sorted(v for k, v in lay.items() if k not in ("total", "xa_cols") and v >= 0)
+    assert all(o % 256 == 0 for o in offs)
+    assert lm.lmoe_workspace_size_host_io(c) > n
+    # f32 weights need the bf16 copies and the 3-way router split
+    c32 = lm.Config(64, 512, 256, 16, 512, 2, act_dtype="f32", weight_dtype="f32")
+    assert lm.lmoe_get_workspace_layout(c32)["xa_cols"] == 3 * 512
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(top_k=0), -1), (dict(top_k=17), -1), (dict(n_experts=4, top_k=5), -1),
+    (dict(d_model=200), -2), (dict(d_latent=96), -2), (dict(n_experts=2048), -2),
+    (dict(T=-1), -1), (dict(eps=-1.0), -1),
+])
+def test_config_rejected(lm, kw, status):
+    base = dict(T=8, d_model=256, d_latent=128, n_experts=8, d_ff=128, top_k=2)
+    base.update(kw)
+    with pytest.raises(lm.LmoeError) as ei:
+        lm.lmoe_workspace_size(lm.Config(**base))
+    assert ei.value.status == status
+
+
+def test_forward_rejects_bad_pointers_without_launching(lm):
+    lib = lm.load()
+    from latent_mixture_experts_router_gb300._lib import lmoe_config
+    c = lm.Config(8, 256, 128, 8, 128, 2).c()
+    fake = 1 << 20   # never dereferenced: validation fails first
+    args = [ctypes.byref(c)] + [fake] * 11
+    # NULL x
+    st = lib.latent_moe_forward(ctypes.byref(c), None, *[fake] * 10, 2, fake, fake, 1 << 30, None)
+    assert st == -1
+    # top_k argument disagreeing with the config
+    st = lib.latent_moe_forward(*args, 3, fake, fake, 1 << 30, None)
+    assert st == -1
+    # misaligned pointer
+    st = lib.latent_moe_forward(ctypes.byref(c), fake + 2, *[fake] * 10, 2, fake, fake, 1 << 30, None)
+    assert st == -3
+    # workspace too small
+    st = lib.latent_moe_forward(*args, 2, fake + 4096, fake, 16, None)
+    assert st == -4
+    assert isinstance(lmoe_config, type)

@@ -1,0 +1,196 @@
+"""GPU parity of the latent-MoE block against the fp64 oracle, through the C ABI.
+
+Bars: top-k indices exact (near-tie tokens counted, compared against the oracle re-run
+with the GPU's selection); permutation bit-exact; every stage and the output within
+2e-2 x RMS of the oracle's value (BF16 compute)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from oracle.compare import TOL_BF16, compare_block
+
+from gpu_util import expected_permutation, make_block, rel_err, run, views
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from latent_mixture_experts_router_gb300 import build
+    build.build()
+    return torch.device("cuda:0")
+
+
+def _oracle(inp, rows=None):
+    P = oracle.params_from_inputs(inp)
+    x = inp.x.double().cpu().numpy()
+    forced = None if inp.forced_idx is None else inp.forced_idx.cpu().numpy()
+    tr = oracle.Trace()
+    ref = oracle.forward_batched(x, P, inp.w.k, forced_idx=forced, trace=tr)
+    return P, x, tr, ref
+
+
+def _check_permutation(v, idx, E):
+    counts, offsets, row_of, tok_of = expected_permutation(idx, E)
+    assert np.array_equal(v["counts"], counts)
+    assert np.array_equal(v["offsets"], offsets)
+    assert np.array_equal(v["row_of"], row_of)
+    assert np.array_equal(v["tok_of"], tok_of)
+    assert int(v["n_tiles"][0]) == int(np.sum((counts + 127) // 128))
+
+
+def test_tiny_fp32_stage_by_stage(cuda):
+    w = workloads.WORKLOADS["tiny_fp32"]
+    inp = workloads.make_inputs(w, cuda)
+    out, idx, blk, cfg = run(inp)
+    P, x, tr, ref = _oracle(inp)
+    v = views(blk, cfg)
+    D = w.D
+    # S1: xn_hi + xn_lo carries xn to ~2^-16 relative
+    assert np.max(np.abs(v["xa"][:, :D] + v["xa"][:, D:2 * D] - tr.xn)) < 1e-5
+    # S2: router logits to fp32-level accuracy (well inside the 1e-3 tie band)
+    assert np.max(np.abs(v["logits"] - tr.logits)) < 2e-4
+    # S3: top-k
+    rep = compare_block(out.cpu().numpy(), idx.cpu().numpy(), x, P, w.k, TOL_BF16, tr=tr, ref=ref)
+    assert not rep.bad_idx_tokens, str(rep)
+    ex = np.all(v["topk_idx"] == tr.idx, axis=1)
+    assert np.max(np.abs(v["topk_w"][ex] - tr.w[ex])) < 1e-5
+    # S4: permutation, bit-exact against numpy's stable sort of the GPU's own ids
+    _check_permutation(v, v["topk_idx"], w.E)
+    # S5: pooler (from xn_hi, bf16 weights)
+    assert rel_err(v["p"], tr.p) < 2e-2
+    # S6: h0 rows in expert-contiguous order
+    ok_tok = np.all(v["topk_idx"] == tr.idx, axis=1)
+    rows = v["row_of"][ok_tok].reshape(-1)
+    toks = np.repeat(np.nonzero(ok_tok)[0], w.k)
+    assert rel_err(v["xe"][rows], tr.h0[toks]) < 2e-2
+    # S8: per-expert outputs before their norm
+    for (t, j), y in list(tr.y.items())[:64]:
+        if ok_tok[t]:
+            assert rel_err(v["y"][v["row_of"][t, j]], y) < 3e-2
+    # S9, S10
+    assert rel_err(v["c"][ok_tok], tr.c[ok_tok]) < 2e-2
+    assert rel_err(v["u"][ok_tok], tr.u[ok_tok]) < 2e-2
+    # output
+    assert rep.ok, str(rep)
+
+
+SHAPES = [  # (T, D, L, E, I, k): ragged T, N tails of the 256-wide tiles, k = 1 and k = E
+    (1, 256, 128, 4, 128, 1),
+    (3, 384, 256, 8, 384, 2),
+    (130, 256, 384, 20, 256, 3),
+    (257, 512, 256, 6, 128, 6),
+    (200, 256, 128, 1, 256, 1),
+    (64, 1024, 512, 64, 768, 8),
+]
+
+
+@pytest.mark.parametrize("T,D,L,E,I,k", SHAPES)
+def test_random_shapes_bf16(cuda, T, D, L, E, I, k):
+    w = workloads.Workload(f"shape{T}_{D}_{L}_{E}_{I}_{k}", T=T, D=D, L=L, E=E, I=I, k=k, seed=T % 7)
+    inp = workloads.make_inputs(w, cuda)
+    out, idx, blk, cfg = run(inp)
+    P, x, tr, ref = _oracle(inp)
+    rep = compare_block(out.cpu().numpy(), idx.cpu().numpy(), x, P, k, TOL_BF16, tr=tr, ref=ref)
+    assert rep.ok, str(rep)
+    _check_permutation(views(blk, cfg), idx.cpu().numpy(), E)
+
+
+def test_zero_tokens(cuda):
+    import latent_mixture_experts_router_gb300 as lm
+    w = workloads.Workload("t0", T=4, D=256, L=128, E=4, I=128, k=2)
+    inp = workloads.make_inputs(w, cuda)
+    blk = make_block(inp)
+    x0 = inp.x[:0]
+    out = blk.forward(x0)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 256)
+    assert lm.lmoe_check_status(blk.config(0), blk._ws)[0] == 0
+
+
+def test_deterministic_and_token_order_equivariant(cuda):
+    w = workloads.Workload("det", T=300, D=512, L=256, E=16, I=256, k=4)
+    inp = workloads.make_inputs(w, cuda)
+    blk = make_block(inp)
+    a, ia, _, _ = run(inp, blk=blk)
+    a = a.clone()
+    b, ib, _, _ = run(inp, blk=blk)
+    assert torch.equal(a, b) and torch.equal(ia, ib)
+    perm = torch.randperm(w.T, generator=torch.Generator().manual_seed(0)).to(cuda)
+    c, ic, _, _ = run(inp, blk=blk, x=inp.x[perm].contiguous())
+    assert torch.equal(c, a[perm]) and torch.equal(ic, ia[perm])
+
+
+def test_router_bias_and_forced_routing(cuda):
+    w = workloads.Workload("bias", T=96, D=256, L=128, E=32, I=256, k=4, routing="zipf")
+    inp = workloads.make_inputs(w, cuda)
+    out, idx, _, _ = run(inp)
+    P, x, tr, ref = _oracle(inp)
+    rep = compare_block(out.cpu().numpy(), idx.cpu().numpy(), x, P, w.k, TOL_BF16, tr=tr, ref=ref)
+    assert rep.ok, str(rep)
+    w2 = workloads.Workload("forced", T=33, D=256, L=128, E=32, I=256, k=8, routing="hot4")
+    inp2 = workloads.make_inputs(w2, cuda)
+    out2, idx2, _, _ = run(inp2)
+    assert torch.equal(idx2.cpu(), inp2.forced_idx.cpu())
+    P2, x2, tr2, ref2 = _oracle(inp2)
+    rep2 = compare_block(out2.cpu().numpy(), idx2.cpu().numpy(), x2, P2, w2.k, TOL_BF16, tr=tr2, ref=ref2)
+    assert rep2.ok, str(rep2)
+
+
+def test_bf16_output_and_host_io(cuda):
+    import latent_mixture_experts_router_gb300 as lm
+    w = workloads.Workload("io", T=70, D=256, L=256, E=8, I=128, k=2)
+    inp = workloads.make_inputs(w, cuda)
+    out32, _, blk, _ = run(inp)
+    out16, _, _, _ = run(inp, out_dtype="bf16", blk=blk)
+    assert out16.dtype == torch.bfloat16
+    assert torch.equal(out16.float(), out32.to(torch.bfloat16).float())
+    cfg = blk.config(w.T, "bf16", "f32")
+    ws = torch.empty(lm.lmoe_workspace_size_host_io(cfg), dtype=torch.uint8, device=cuda)
+    xh = inp.x.cpu().pin_memory()
+    oh = torch.empty(w.T, w.D, dtype=torch.float32).pin_memory()
+    W = blk.W
+    lm.latent_moe_forward_host_io(cfg, xh, W["W_router"], W["W_pool"], W["g_pool"], W["W_gate"], W["W_up"],
+                                  W["W_down"], W["g_expert"], W["W_unpool"], W["g_pre"], W["g_post"], w.k,
+                                  oh, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, out32.cpu())
+
+
+def test_out_of_range_forced_id_is_flagged(cuda):
+    import latent_mixture_experts_router_gb300 as lm
+    w = workloads.Workload("badidx", T=8, D=256, L=128, E=8, I=128, k=2)
+    inp = workloads.make_inputs(w, cuda)
+    blk = make_block(inp)
+    forced = torch.tensor([[0, 1]] * 7 + [[3, 99]], dtype=torch.int32, device=cuda)
+    blk.forward(inp.x, forced_idx=forced)
+    st, word = lm.lmoe_check_status(blk.config(w.T), blk._ws)
+    assert st == -1 and word & (1 << 3)
+    # the context stays usable
+    out, idx, _, _ = run(inp, blk=blk)
+    assert torch.isfinite(out).all()
+
+
+def test_wait_budget_runs_out_and_reports(cuda):
+    import latent_mixture_experts_router_gb300 as lm
+    w = workloads.Workload("tmo", T=8, D=256, L=128, E=8, I=128, k=2)
+    inp = workloads.make_inputs(w, cuda)
+    blk = make_block(inp)
+    cfg = blk.config(w.T)
+    blk.workspace(cfg)
+    # a barrier nothing arrives on: the wait gives up after ~1e6 cycles and says so
+    lm.lmoe_wait_selftest(cfg, blk._ws, 1_000_000)
+    st, word = lm.lmoe_check_status(cfg, blk._ws)
+    assert st == -6 and word != 0
+    # the block itself under a 1-cycle budget: either finishes or reports the timeout,
+    # and the context stays usable afterwards
+    blk.forward(inp.x, wait_budget_cycles=1)
+    st, _ = lm.lmoe_check_status(cfg, blk._ws)
+    assert st in (0, -6)
+    out, idx, _, _ = run(inp, blk=blk)
+    P, x, tr, ref = _oracle(inp)
+    assert compare_block(out.cpu().numpy(), idx.cpu().numpy(), x, P, w.k, TOL_BF16, tr=tr, ref=ref).ok
