@@ -1,0 +1,387 @@
+#!/usr/bin/env python
+"""Benchmark of the latent-MoE block on GB300: one JSON line on stdout (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one full block call (pre-norm, router, top-k, permutation, pooler,
+pool norm, gate/up + SwiGLU, down, combine, unpooler, post-norm + residual)
+over one batch of T synthetic tokens with the weights resident in HBM.  With
+N > 1 (torchrun) every rank runs an independent replica on its own tokens
+(the block is token-independent: no exchange on the data path); the time is
+the max over ranks and ``value`` counts the tokens of all ranks.
+
+``--impl reference`` times the fp64 CPU oracle (test infrastructure, a
+deliberately slow reference) on the host cores over a bounded token sample of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "latent-MoE block tokens/s (BF16) at Muse shape"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ------------------------------------------------------------------ distributed
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            f = [c.strip() for c in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows if r[3].replace(".", "").isdigit()), default=None)}
+
+
+# ------------------------------------------------------------------ roofline
+def stage_costs(w: workloads.Workload, counts: np.ndarray):
+    """Algorithmic bytes and FLOPs of each stage of one call (weights counted once per
+    expert that receives at least one row; activations read/written once)."""
+    T, D, L, E, I, k = w.T, w.D, w.L, w.E, w.I, w.k
+    R = T * k
+    used = int(np.count_nonzero(counts))
+    bf, f4 = 2, 4
+    xb = 4 if w.act == "f32" else 2
+    c = {
+        "prenorm": (T * D * xb + T * 2 * D * bf, 0),
+        "router": (E * D * bf + T * 2 * D * bf + T * E * f4, 2 * T * E * 2 * D),
+        "pooler": (L * D * bf + T * D * bf + T * L * f4, 2 * T * L * D),
+        "gate_up": (used * 2 * I * L * bf + R * L * bf + R * I * bf, 2 * R * L * 2 * I),
+        "down": (used * L * I * bf + R * I * bf + R * L * f4, 2 * R * I * L),
+        "unpooler": (D * L * bf + T * L * bf + T * D * f4, 2 * T * D * L),
+        "combine": (R * L * f4 + T * L * bf, 0),
+        "postnorm": (T * D * (xb + f4 + 4), 0),
+    }
+    return c, used
+
+
+def roofline(stage: str, dur_ms: float, costs: dict, pk: dict, pk_kind: str, sustained: bool):
+    nbytes, flops = costs[stage]
+    hbm = pk["hbm_gbs"]
+    tf = pk["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    t_hbm = nbytes / (hbm * 1e9)
+    t_tc = flops / (tf * 1e12) if flops else 0.0
+    if t_tc > t_hbm:
+        ach = flops / (dur_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "kernel": stage, "achieved": round(ach, 2), "peak": tf, "unit": "TFLOP/s",
+                "frac": round(ach / tf, 4), "peak_source": f"{pk_kind} bf16_tflops{'_sustained' if sustained else ''}",
+                "algorithmic_flop": flops, "traffic": None}
+    ach = nbytes / (dur_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": stage, "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(ach / hbm, 4), "peak_source": f"{pk_kind} hbm_gbs",
+            "algorithmic_bytes": nbytes, "traffic": None}
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_sample_params(w: workloads.Workload, tokens, inp=None):
+    """Oracle parameters holding, as fp64 arrays, only the experts the sampled tokens
+    route to.  Weights come from the seeded generator (copied from ``inp`` when given,
+    else regenerated on the host); the expert set comes from the oracle's own router
+    (or the forced routing of the workload)."""
+    import oracle
+    P = oracle.params_from_inputs(inp) if inp is not None else oracle.params_for_workload(w)
+    x = workloads.x_tensor(w, rows=tokens).double().numpy()
+    if w.routing == "hot4":
+        sel = workloads.forced_routing(w)[tokens].numpy()
+    else:
+        lg = oracle.rms_norm(x, P.g_pre, P.eps) @ P.W_router.T
+        if P.router_bias is not None:
+            lg = lg + P.router_bias
+        sel = oracle.top_k(lg, w.k)
+    experts = sorted({int(e) for e in sel.reshape(-1)})
+    stacks = {}
+    for name in ("W_gate", "W_up", "W_down"):
+        mats = {e: np.array(getattr(P, name)[e]) for e in experts}
+        stacks[name] = oracle.ExpertStack(lambda e, m=mats: m[int(e)], w.E)
+    return oracle.BlockParams(**{**P.__dict__, **stacks}), x
+
+
+def time_oracle(w: workloads.Workload, n_tokens: int, inp=None, repeats: int = 1):
+    import oracle
+    tokens = list(range(n_tokens))
+    P, x = oracle_sample_params(w, tokens, inp=inp)
+    forced = None
+    if w.routing == "hot4":
+        forced = workloads.forced_routing(w)[:n_tokens].numpy()
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle.forward_batched(x, P, w.k, forced_idx=forced)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, ws, rank, local):
+    import latent_mixture_experts_router_gb300 as lm
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[args.workload]
+    if args.tokens:
+        w = w.with_tokens(args.tokens)
+    T = w.T
+    inp = workloads.make_inputs(w, dev)
+    if ws > 1:   # each replica gets its own tokens: rows [rank*T, (rank+1)*T) of one long batch
+        inp.x = workloads.configs.normal_tensor(w, workloads.configs.S_X, (T, w.D), 1.0, w.act, dev,
+                                                start=rank * T * w.D)
+    blk = lm.LatentMoEBlock(inp.W_router, inp.W_pool, inp.g_pool, inp.W_gate, inp.W_up, inp.W_down,
+                            inp.g_expert, inp.W_unpool, inp.g_pre, inp.g_post, w.k, w.eps, weight_dtype=w.weights)
+    cfg = blk.config(T, w.act, "f32")
+    blk.workspace(cfg)
+    out = torch.empty(T, w.D, dtype=torch.float32, device=dev)
+    ex = {}
+    if inp.router_bias is not None:
+        ex["router_bias"] = inp.router_bias
+    if inp.forced_idx is not None:
+        ex["forced_idx"] = inp.forced_idx
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs is not None:
+            blk.forward(inp.x, out=out, stage_events=evs, **ex)
+        else:
+            blk.forward(inp.x, out=out, **ex)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, word = lm.lmoe_check_status(cfg, blk._ws)
+    assert st == 0, f"device status {st} ({word:#x})"
+    lay = lm.lmoe_get_workspace_layout(cfg)
+    counts = blk._ws[lay["counts"]:lay["counts"] + 4 * w.E].view(torch.int32).cpu().numpy()
+
+    # ---- timed region (device), stage events recorded by the library on the stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(lm.NUM_STAGE_EVENTS)] for _ in range(args.steps)]
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    n0 = lm.lmoe_kernel_launches()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    launches = lm.lmoe_kernel_launches() - n0
+    clk = clocks.stop() if clocks else None
+    ms = t_start.elapsed_time(t_end)
+    ms_max = allreduce_max(ms, ws)
+    stage_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i, name in enumerate(lm.STAGES)}
+
+    # ---- end to end through the host-I/O entry point: pinned x in, pinned out back
+    x_host = inp.x.cpu().pin_memory()
+    out_host = torch.empty(T, w.D, dtype=torch.float32).pin_memory()
+    ws_io = torch.zeros(lm.lmoe_workspace_size_host_io(cfg), dtype=torch.uint8, device=dev)
+    W = blk.W
+
+    def step_io():
+        lm.latent_moe_forward_host_io(cfg, x_host, W["W_router"], W["W_pool"], W["g_pool"], W["W_gate"],
+                                      W["W_up"], W["W_down"], W["g_expert"], W["W_unpool"], W["g_pre"],
+                                      W["g_post"], w.k, out_host, ws_io)
+
+    e2e = None
+    if inp.router_bias is None and inp.forced_idx is None:
+        for _ in range(max(2, args.warmup // 2)):
+            step_io()
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step_io()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(ws)
+        ms_io = allreduce_max(e0.elapsed_time(e1), ws)
+        e2e = {"value": round(ws * T * args.steps / (ms_io * 1e-3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
+               "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()),
+               "ms_per_step": round(ms_io / args.steps, 4), "path": "latent_moe_forward_host_io"}
+
+    if rank != 0:
+        return None
+    pk, pk_kind = peaks()
+    costs, used = stage_costs(w, counts)
+    dom = max((s for s in costs if s in stage_ms), key=lambda s: stage_ms[s])
+    total_flops = sum(f for _, f in costs.values())
+    ms_step = ms_max / args.steps
+    line = {
+        "metric": METRIC, "value": round(ws * T * args.steps / (ms_max * 1e-3), 1), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; random-init weights of the Muse layer shapes)",
+        "config": {"workload": w.name, "T_per_gpu": T, "d_model": w.D, "d_latent": w.L, "n_experts": w.E,
+                   "d_ff": w.I, "top_k": w.k, "routing": w.routing, "weights": w.weights,
+                   "experts_touched": used, "parallelism": f"replicas x{ws} (token-independent, no exchange)",
+                   "l2": "inputs larger than L2: each step streams "
+                         f"{sum(b for b, _ in costs.values()) / 1e9:.1f} GB (129 MB L2)"},
+        "tflops": round(total_flops / (ms_step * 1e-3) / 1e12, 2),
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "roofline": roofline(dom, stage_ms[dom], costs, pk, pk_kind, sustained=False),
+        "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        n_tok = max(1, args.cpu_tokens)
+        t = time_oracle(w, n_tok, inp=inp)[0]
+        line["cpu_baseline"] = {"value": round(n_tok / t, 3), "unit": "tokens/s", "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"first {n_tok} tokens of {w.name} through the fp64 oracle "
+                                          f"(numpy BLAS), {t:.1f} s"}
+    return line
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    w = workloads.WORKLOADS[args.workload]
+    if args.tokens:
+        w = w.with_tokens(args.tokens)
+    n_tok = max(1, args.cpu_tokens)
+    import oracle
+    tokens = list(range(n_tok))
+    P, x = oracle_sample_params(w, tokens)
+    forced = workloads.forced_routing(w)[:n_tok].numpy() if w.routing == "hot4" else None
+    for _ in range(args.warmup):
+        oracle.forward_batched(x, P, w.k, forced_idx=forced)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward_batched(x, P, w.k, forced_idx=forced)
+    dt = time.perf_counter() - t0
+    v = round(n_tok * args.steps / dt, 3)
+    sample = (f"each step: {n_tok} tokens of {w.name} through the fp64 oracle (numpy BLAS on the host "
+              f"cores); weights of the experts they route to prepared before timing")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "T": w.T, "sample_tokens": n_tok},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_bf16", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=0, help="override T of the workload")
+    ap.add_argument("--cpu-tokens", type=int, default=4, help="oracle sample size (tokens)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        args.steps = 3 if args.steps is None else args.steps
+        args.warmup = 1 if args.warmup is None else args.warmup
+        line = run_reference(args, ws, rank)
+    else:
+        args.steps = 200 if args.steps is None else args.steps
+        args.warmup = 10 if args.warmup is None else args.warmup
+        line = run_ours(args, ws, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

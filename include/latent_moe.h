@@ -85,6 +85,24 @@ typedef struct {
   const float* tensor_scale;
 } lmoe_nvfp4_weight;
 
+/* Stage boundaries of one call, for stage_events (see lmoe_ex).  Event i is recorded on
+ * the call's stream just before stage i is enqueued; event LMOE_STAGE_END after the last. */
+enum {
+  LMOE_STAGE_PRENORM = 0,   /* pre-norm (and fp32 weight splits)              */
+  LMOE_STAGE_ROUTER = 1,    /* router GEMM                                     */
+  LMOE_STAGE_TOPK = 2,      /* softmax + top-k                                 */
+  LMOE_STAGE_PERMUTE = 3,   /* expert histogram + stable scatter               */
+  LMOE_STAGE_POOLER = 4,    /* pooler GEMM                                     */
+  LMOE_STAGE_POOLNORM = 5,  /* pool norm, copied to expert rows                */
+  LMOE_STAGE_GATE_UP = 6,   /* grouped gate/up GEMM + SwiGLU                   */
+  LMOE_STAGE_DOWN = 7,      /* grouped down GEMM                               */
+  LMOE_STAGE_COMBINE = 8,   /* per-expert norm, routing weight, weighted sum   */
+  LMOE_STAGE_UNPOOLER = 9,  /* unpooler GEMM                                   */
+  LMOE_STAGE_POSTNORM = 10, /* post-norm + residual                            */
+  LMOE_STAGE_END = 11,
+  LMOE_NUM_STAGE_EVENTS = 12
+};
+
 /* Optional extensions of one call (host struct; every member may be NULL/0).
  *  router_bias       [E] fp32 device: added to the router logits before softmax/top-k
  *  forced_idx        [T, k] int32 device: use these experts (distinct per row) instead of
@@ -92,7 +110,9 @@ typedef struct {
  *  topk_idx_out      [T, k] int32 device: selected experts, descending logit
  *  topk_w_out        [T, k] fp32 device: their routing weights
  *  near_tie_count_out  [1] int32 device: tokens whose k-th and (k+1)-th logits differ by < 1e-3
- *  wait_budget_cycles  SM clock cycles a device wait may spin before it gives up (0: default) */
+ *  wait_budget_cycles  SM clock cycles a device wait may spin before it gives up (0: default)
+ *  stage_events      host array of LMOE_NUM_STAGE_EVENTS caller-created cudaEvent_t, or NULL:
+ *                    recorded on the stream at the stage boundaries above (timing only) */
 typedef struct {
   const float* router_bias;
   const int32_t* forced_idx;
@@ -100,6 +120,7 @@ typedef struct {
   float* topk_w_out;
   int32_t* near_tie_count_out;
   long long wait_budget_cycles;
+  cudaEvent_t* stage_events;
 } lmoe_ex;
 
 /* Bytes of device workspace a call with this config needs (host out-parameter). */
@@ -170,6 +191,9 @@ lmoe_status lmoe_get_workspace_layout(const lmoe_config* cfg, lmoe_workspace_lay
  * latent_moe_forward (only its error word is touched).                               */
 lmoe_status lmoe_wait_selftest(const lmoe_config* cfg, void* workspace, long long budget_cycles,
                                cudaStream_t stream);
+
+/* Number of kernels this library has launched in this process (all devices, all calls). */
+unsigned long long lmoe_kernel_launches(void);
 
 /* Human-readable name of a status code (static string). */
 const char* lmoe_status_string(lmoe_status s);

@@ -21,7 +21,7 @@ import torch
 from ._lib import (Config, LmoeError, lmoe_workspace_size, lmoe_workspace_size_host_io,  # noqa: F401
                    lmoe_get_workspace_layout, latent_moe_forward, latent_moe_forward_ex,
                    latent_moe_forward_host_io, lmoe_check_status, lmoe_wait_selftest, load,
-                   LIB_PATH)
+                   LIB_PATH, STAGES, NUM_STAGE_EVENTS, lmoe_kernel_launches)
 
 load()
 
@@ -50,7 +50,7 @@ class LatentMoEBlock:
     def workspace(self, cfg: Config, host_io: bool = False) -> torch.Tensor:
         n = lmoe_workspace_size_host_io(cfg) if host_io else lmoe_workspace_size(cfg)
         if self._ws is None or self._ws.numel() < n:
-            self._ws = torch.empty(max(n, 256), dtype=torch.uint8, device=self.W["g_pre"].device)
+            self._ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=self.W["g_pre"].device)
         return self._ws
 
     def forward(self, x: torch.Tensor, out_dtype="f32", out=None, stream=None, **ex) -> torch.Tensor:

@@ -43,7 +43,12 @@ class lmoe_nvfp4_weight(ctypes.Structure):
 class lmoe_ex(ctypes.Structure):
     _fields_ = [("router_bias", ctypes.c_void_p), ("forced_idx", ctypes.c_void_p),
                 ("topk_idx_out", ctypes.c_void_p), ("topk_w_out", ctypes.c_void_p),
-                ("near_tie_count_out", ctypes.c_void_p), ("wait_budget_cycles", ctypes.c_longlong)]
+                ("near_tie_count_out", ctypes.c_void_p), ("wait_budget_cycles", ctypes.c_longlong),
+                ("stage_events", ctypes.c_void_p)]
+
+STAGES = ["prenorm", "router", "topk", "permute", "pooler", "poolnorm", "gate_up", "down", "combine",
+          "unpooler", "postnorm"]
+NUM_STAGE_EVENTS = len(STAGES) + 1
 
 
 _LAYOUT_FIELDS = ["xa", "logits", "topk_idx", "topk_w", "counts", "offsets", "row_of", "tok_of",
@@ -84,6 +89,8 @@ def _lib():
         L.lmoe_check_status.restype = ctypes.c_int
         L.lmoe_wait_selftest.argtypes = [ctypes.POINTER(lmoe_config), _P, ctypes.c_longlong, _P]
         L.lmoe_wait_selftest.restype = ctypes.c_int
+        L.lmoe_kernel_launches.restype = ctypes.c_ulonglong
+        L.lmoe_kernel_launches.argtypes = []
         _lib_handle = L
     return _lib_handle
 
@@ -187,12 +194,23 @@ def latent_moe_forward(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g
 def latent_moe_forward_ex(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool,
                           g_pre, g_post, top_k, out, workspace, stream=None, router_bias=None,
                           forced_idx=None, topk_idx_out=None, topk_w_out=None, near_tie_count_out=None,
-                          wait_budget_cycles=0):
+                          wait_budget_cycles=0, stage_events=None):
+    """``stage_events``: a list of NUM_STAGE_EVENTS torch.cuda.Event(enable_timing=True), recorded
+    by the library at the stage boundaries (for per-stage timing)."""
     keep = []
     args = _fwd_args(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool, g_pre,
                      g_post, top_k, out, workspace, stream, keep)
+    evs = None
+    if stage_events is not None:
+        assert len(stage_events) == NUM_STAGE_EVENTS
+        for e in stage_events:   # torch creates the CUDA event lazily
+            if e.cuda_event == 0:
+                e.record()
+        evs = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
+        keep.append(evs)
     ex = lmoe_ex(_ptr(router_bias), _ptr(forced_idx), _ptr(topk_idx_out), _ptr(topk_w_out),
-                 _ptr(near_tie_count_out), int(wait_budget_cycles))
+                 _ptr(near_tie_count_out), int(wait_budget_cycles),
+                 ctypes.cast(evs, ctypes.c_void_p) if evs is not None else None)
     _check(_lib().latent_moe_forward_ex(*args, ctypes.byref(ex)), "latent_moe_forward_ex")
 
 
@@ -217,3 +235,8 @@ def lmoe_wait_selftest(cfg, workspace, budget_cycles: int, stream=None):
     c = cfg.c()
     _check(_lib().lmoe_wait_selftest(ctypes.byref(c), _ptr(workspace), int(budget_cycles), _stream(stream)),
            "lmoe_wait_selftest")
+
+
+def lmoe_kernel_launches() -> int:
+    """Kernels the library has launched in this process."""
+    return int(_lib().lmoe_kernel_launches())

@@ -14,12 +14,18 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/latent_moe.h"
 #include "internal.h"
 
 using namespace lmoe;
+
+namespace lmoe {
+static std::atomic<unsigned long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace lmoe
 
 namespace {
 
@@ -83,23 +89,23 @@ void make_layout(const lmoe_config* c, Layout* L) {
   P.tok_of = take(R * 4);
   P.tiles = take(static_cast<size_t>(L->max_tiles) * sizeof(Tile));
   P.n_tiles = take(4);
-  P.p = take(T * Ld * 2);
+  P.p = take(T * Ld * 4);
   P.ss_p = take(T * L->ld_ss_p * 4);
   P.xe = take(R * Ld * 2);
   P.xe_scale = -1;
   P.h = take(R * I * 2);
-  P.y = take(R * Ld * 2);
+  P.y = take(R * Ld * 4);
   P.ss_y = take(R * L->ld_ss_y * 4);
   P.c = take(T * Ld * 2);
-  P.u = take(T * D * 2);
+  P.u = take(T * D * 4);
   P.ss_u = take(T * L->ld_ss_u * 4);
-  if (f32w) {
+  if (f32w) {  // bf16 hi/lo splits of fp32 weights: [hi|hi|lo] (router, pooler), [hi|lo] (rest)
     L->w_router = take(E * 3 * D * 2);
-    L->w_pool = take(Ld * D * 2);
-    L->w_gate = take(E * I * Ld * 2);
-    L->w_up = take(E * I * Ld * 2);
-    L->w_down = take(E * Ld * I * 2);
-    L->w_unpool = take(D * Ld * 2);
+    L->w_pool = take(Ld * 3 * D * 2);
+    L->w_gate = take(E * I * 2 * Ld * 2);
+    L->w_up = take(E * I * 2 * Ld * 2);
+    L->w_down = take(E * Ld * 2 * I * 2);
+    L->w_unpool = take(D * 2 * Ld * 2);
   }
   P.total = static_cast<long long>(off);
   L->x_stage = take(T * D * (c->act_dtype == LMOE_F32 ? 4 : 2));
@@ -154,7 +160,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_cols_used,
                      long long a_row_stride_elems, const void* B, long long b_rows,
-                     long long b_cols, const void* B2, int N, int num_kb, int kb_period,
+                     long long b_cols, const void* B2, int N, int num_kb,
                      const Tile* tiles, const int* n_tiles, int m_tiles, void* out,
                      long long ldo, float* ss, int ld_ss, unsigned* err, long long budget,
                      cudaStream_t s) {
@@ -169,7 +175,8 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   a.M = static_cast<int>(a_rows);
   a.N = N;
   a.num_kb = num_kb;
-  a.kb_period = kb_period;
+  a.kb_period_a = static_cast<int>(a_cols_used / kBK);
+  a.kb_period_b = static_cast<int>(b_cols / kBK);
   a.tiles = tiles;
   a.n_tiles = n_tiles;
   a.out = out;
@@ -191,6 +198,13 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   lmoe_status st = check_config(cfg);
   if (st != LMOE_OK) return st;
   if (top_k != cfg->top_k) return LMOE_ERR_ARG;
+  if (cfg->T == 0) {  // no rows: nothing is read; only the error word is cleared
+    Layout L0;
+    make_layout(cfg, &L0);
+    if (workspace != nullptr && ws_bytes >= static_cast<size_t>(L0.pub.total))
+      LMOE_CUDA(cudaMemsetAsync(static_cast<char*>(workspace) + L0.pub.err, 0, 8, s));
+    return LMOE_OK;
+  }
   const void* ptrs[] = {x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert,
                         W_unpool, g_pre, g_post, out};
   for (const void* p : ptrs)
@@ -203,7 +217,6 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   if (workspace == nullptr || ws_bytes < static_cast<size_t>(L.pub.total)) return LMOE_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return LMOE_ERR_ALIGN;
   if (ex && ex->router_bias && !aligned16(ex->router_bias)) return LMOE_ERR_ALIGN;
-  if (cfg->T == 0) return LMOE_OK;
 
   const int T = cfg->T, D = cfg->d_model, Ld = cfg->d_latent, E = cfg->n_experts,
             I = cfg->d_ff, k = cfg->top_k;
@@ -226,33 +239,39 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   int32_t* tok_of = static_cast<int32_t*>(at(L.pub.tok_of));
   Tile* tiles = static_cast<Tile*>(at(L.pub.tiles));
   int32_t* n_tiles = static_cast<int32_t*>(at(L.pub.n_tiles));
-  __nv_bfloat16* p = static_cast<__nv_bfloat16*>(at(L.pub.p));
+  float* p = static_cast<float*>(at(L.pub.p));
   float* ss_p = static_cast<float*>(at(L.pub.ss_p));
   __nv_bfloat16* xe = static_cast<__nv_bfloat16*>(at(L.pub.xe));
   __nv_bfloat16* h = static_cast<__nv_bfloat16*>(at(L.pub.h));
-  __nv_bfloat16* y = static_cast<__nv_bfloat16*>(at(L.pub.y));
+  float* y = static_cast<float*>(at(L.pub.y));
   float* ss_y = static_cast<float*>(at(L.pub.ss_y));
   __nv_bfloat16* c = static_cast<__nv_bfloat16*>(at(L.pub.c));
-  __nv_bfloat16* u = static_cast<__nv_bfloat16*>(at(L.pub.u));
+  float* u = static_cast<float*>(at(L.pub.u));
   float* ss_u = static_cast<float*>(at(L.pub.ss_u));
 
+  cudaEvent_t* ev = ex ? ex->stage_events : nullptr;
+  auto mark = [&](int i) -> bool { return ev == nullptr || cudaEventRecord(ev[i], s) == cudaSuccess; };
+#define LMOE_MARK(i) \
+  if (!mark(i)) return LMOE_ERR_CUDA;
+
+  LMOE_MARK(LMOE_STAGE_PRENORM);
   // error word and near-tie counter start at zero on every call
   LMOE_CUDA(cudaMemsetAsync(err, 0, 8, s));
 
-  // weights as bf16 K-major operands (fp32 weights are rounded here, the router split hi/lo)
+  // weights as bf16 K-major operands; fp32 weights become hi/lo bf16 pairs laid side by
+  // side along K, so every product keeps ~16 significant bits of the weight
   const void *wr = W_router, *wp = W_pool, *wg = W_gate, *wu = W_up, *wd = W_down,
              *wun = W_unpool;
+  const int wsplit = f32w ? 2 : 1;  // K multiplier of expert/unpooler weights
   if (f32w) {
-    __nv_bfloat16* d_wr = static_cast<__nv_bfloat16*>(at(L.w_router));
-    LMOE_CUDA(launch_router_split(static_cast<const float*>(W_router), E, D, d_wr, s));
-    const struct { const void* src; long long dst; long long n; } conv[] = {
-        {W_pool, L.w_pool, 1LL * Ld * D},        {W_gate, L.w_gate, 1LL * E * I * Ld},
-        {W_up, L.w_up, 1LL * E * I * Ld},        {W_down, L.w_down, 1LL * E * Ld * I},
-        {W_unpool, L.w_unpool, 1LL * D * Ld}};
-    for (const auto& cv : conv)
-      LMOE_CUDA(launch_f32_to_bf16(static_cast<const float*>(cv.src),
-                                   static_cast<__nv_bfloat16*>(at(cv.dst)), cv.n, s));
-    wr = d_wr;
+    const struct { const void* src; long long dst; long long rows; int K; int parts; unsigned lo; } cv[] = {
+        {W_router, L.w_router, E, D, 3, 4u},      {W_pool, L.w_pool, Ld, D, 3, 4u},
+        {W_gate, L.w_gate, 1LL * E * I, Ld, 2, 2u}, {W_up, L.w_up, 1LL * E * I, Ld, 2, 2u},
+        {W_down, L.w_down, 1LL * E * Ld, I, 2, 2u}, {W_unpool, L.w_unpool, D, Ld, 2, 2u}};
+    for (const auto& c : cv)
+      LMOE_CUDA(launch_weight_split(static_cast<const float*>(c.src), c.rows, c.K, c.parts, c.lo,
+                                    static_cast<__nv_bfloat16*>(at(c.dst)), s));
+    wr = at(L.w_router);
     wp = at(L.w_pool);
     wg = at(L.w_gate);
     wu = at(L.w_up);
@@ -263,43 +282,56 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
 
   // S1 pre-norm
   LMOE_CUDA(launch_prenorm(x, x_f32, g_pre, T, D, eps, xa, xa_cols, s));
+  LMOE_MARK(LMOE_STAGE_ROUTER);
   // S2 router logits = [xn_hi | xn_lo (| xn_hi)] . [W | W (| W_lo)]^T
   const int m_tiles_T = cdiv(T, kBM);
   st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
-                xa_cols / kBK, (f32w ? 3 * D : D) / kBK, nullptr, nullptr, m_tiles_T, logits,
-                L.ld_logits, nullptr, 0, err, budget, s);
+                xa_cols / kBK, nullptr, nullptr, m_tiles_T, logits, L.ld_logits, nullptr, 0, err,
+                budget, s);
   if (st != LMOE_OK) return st;
+  LMOE_MARK(LMOE_STAGE_TOPK);
   // S3 top-k + softmax
   LMOE_CUDA(launch_topk(logits, L.ld_logits, ex ? ex->router_bias : nullptr,
                         ex ? ex->forced_idx : nullptr, T, E, k, tk_idx, tk_w, near_tie,
                         ex ? ex->topk_idx_out : nullptr, ex ? ex->topk_w_out : nullptr, err, s));
   if (ex && ex->near_tie_count_out)
     LMOE_CUDA(cudaMemcpyAsync(ex->near_tie_count_out, near_tie, 4, cudaMemcpyDeviceToDevice, s));
+  LMOE_MARK(LMOE_STAGE_PERMUTE);
   // S4 permutation
   LMOE_CUDA(launch_permute(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, s));
+  LMOE_MARK(LMOE_STAGE_POOLER);
   // S5 pooler p = xn_hi . W_pool^T, with row partial sums of squares
-  st = run_gemm(kEpiBf16Ss, xa, T, D, xa_cols, wp, Ld, D, nullptr, Ld, D / kBK, D / kBK, nullptr,
-                nullptr, m_tiles_T, p, Ld, ss_p, L.ld_ss_p, err, budget, s);
+  const int pool_k = f32w ? 3 * D : D;
+  st = run_gemm(kEpiF32Ss, xa, T, pool_k, xa_cols, wp, Ld, pool_k, nullptr, Ld, pool_k / kBK,
+                nullptr, nullptr, m_tiles_T, p, Ld, ss_p, L.ld_ss_p, err, budget, s);
   if (st != LMOE_OK) return st;
+  LMOE_MARK(LMOE_STAGE_POOLNORM);
   // S6 pool norm, scattered to the k expert-contiguous rows of each token
   LMOE_CUDA(launch_poolnorm_scatter(p, ss_p, L.ld_ss_p, g_pool, row_of, T, Ld, k, eps, xe, s));
+  LMOE_MARK(LMOE_STAGE_GATE_UP);
   // S7 grouped gate/up + SwiGLU
-  st = run_gemm(kEpiSwiGLU, xe, R, Ld, Ld, wg, 1LL * E * I, Ld, wu, I, Ld / kBK, Ld / kBK, tiles,
-                n_tiles, L.max_tiles, h, I, nullptr, 0, err, budget, s);
+  st = run_gemm(kEpiSwiGLU, xe, R, Ld, Ld, wg, 1LL * E * I, 1LL * wsplit * Ld, wu, I,
+                wsplit * Ld / kBK, tiles, n_tiles, L.max_tiles, h, I, nullptr, 0, err, budget, s);
   if (st != LMOE_OK) return st;
-  // S8 grouped down, with per-row partial sums of squares of the bf16 outputs
-  st = run_gemm(kEpiBf16Ss, h, R, I, I, wd, 1LL * E * Ld, I, nullptr, Ld, I / kBK, I / kBK, tiles,
-                n_tiles, L.max_tiles, y, Ld, ss_y, L.ld_ss_y, err, budget, s);
+  LMOE_MARK(LMOE_STAGE_DOWN);
+  // S8 grouped down (fp32 y), with per-row partial sums of squares
+  st = run_gemm(kEpiF32Ss, h, R, I, I, wd, 1LL * E * Ld, 1LL * wsplit * I, nullptr, Ld,
+                wsplit * I / kBK, tiles, n_tiles, L.max_tiles, y, Ld, ss_y, L.ld_ss_y, err, budget, s);
   if (st != LMOE_OK) return st;
+  LMOE_MARK(LMOE_STAGE_COMBINE);
   // S9 combine: per-expert RMSNorm, routing weight, fp32 sum in slot order
   LMOE_CUDA(launch_combine(y, ss_y, L.ld_ss_y, row_of, tk_idx, tk_w, g_expert, T, Ld, k, eps, c, s));
+  LMOE_MARK(LMOE_STAGE_UNPOOLER);
   // S10 unpooler u = c . W_unpool^T with row partial sums of squares
-  st = run_gemm(kEpiBf16Ss, c, T, Ld, Ld, wun, D, Ld, nullptr, D, Ld / kBK, Ld / kBK, nullptr,
-                nullptr, m_tiles_T, u, D, ss_u, L.ld_ss_u, err, budget, s);
+  st = run_gemm(kEpiF32Ss, c, T, Ld, Ld, wun, D, 1LL * wsplit * Ld, nullptr, D, wsplit * Ld / kBK,
+                nullptr, nullptr, m_tiles_T, u, D, ss_u, L.ld_ss_u, err, budget, s);
   if (st != LMOE_OK) return st;
+  LMOE_MARK(LMOE_STAGE_POSTNORM);
   // S11 post-norm + residual
   LMOE_CUDA(launch_postnorm_residual(x, x_f32, u, ss_u, L.ld_ss_u, g_post, T, D, eps, out,
                                      cfg->out_dtype == LMOE_F32, s));
+  LMOE_MARK(LMOE_STAGE_END);
+#undef LMOE_MARK
   return LMOE_OK;
 }
 
@@ -419,6 +451,8 @@ lmoe_status lmoe_wait_selftest(const lmoe_config* cfg, void* workspace, long lon
   if (launch_wait_selftest(b, err, stream) != cudaSuccess) return LMOE_ERR_CUDA;
   return LMOE_OK;
 }
+
+unsigned long long lmoe_kernel_launches(void) { return g_launches.load(); }
 
 const char* lmoe_status_string(lmoe_status s) {
   switch (s) {

@@ -1,7 +1,9 @@
 // gemm.cu — grouped BF16 GEMM on the 5th-generation tensor cores (tcgen05).
 //
-// out[r, n] = sum_k A[r, k] * B[e*N + n, k]  for the rows r of each M tile, where
-// e is the tile's expert (0 for a plain GEMM).  A and B are K-major bf16 and are
+// out[r, n] = sum_kb A[r, kA(kb)] * B[e*N + n, kB(kb)]  for the rows r of each M tile,
+// where e is the tile's expert (0 for a plain GEMM) and the k coordinates of A and B
+// wrap at their own periods, so that one operand can be paired with a hi/lo split of
+// the other (K-concatenation without copying).  A and B are K-major bf16 and are
 // staged in shared memory by TMA (128-byte swizzle); the fp32 accumulator lives
 // in tensor memory.  One CTA computes one 128 x BN output tile with three roles:
 //   warp 0, lane 0   TMA producer over a STAGES-deep ring of smem slots
@@ -9,13 +11,14 @@
 //   warps 2..5       epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (one row each)
 // Epilogues (one per use in the latent-MoE block):
 //   kEpiF32     fp32 logits (router)
-//   kEpiBf16Ss  bf16 output plus, per row, the partial sum of squares of the
-//               bf16-rounded values of this tile's columns.  The row's RMS is
-//               finished later from these partials, so no kernel re-reads the row to
-//               normalise it (the "fused per-expert post-norm" of the LMSYS Muse Spark
-//               Open post: each second-GEMM tile accumulates the sum of squares of the
-//               BF16 values it holds; here partials go to [rows, N/BN] without atomics,
-//               so the result is deterministic).
+//   kEpiF32Ss   fp32 output plus, per row, the partial sum of squares of the
+//               values of this tile's columns.  The row's RMS is finished later from
+//               these partials, so no kernel re-reads the row to normalise it (the
+//               "fused per-expert post-norm" of the LMSYS Muse Spark Open post: each
+//               second-GEMM tile accumulates a partial sum of squares of the values it
+//               holds in registers; here partials go to [rows, N/BN] without atomics, so
+//               the result is deterministic).  The outputs stay fp32 because they are
+//               not tensor-core operands: rounding them would only add error.
 //   kEpiSwiGLU  gate and up tiles of the same columns in one CTA (two B loads per
 //               stage, two accumulators), output bf16 silu(a) * b.
 #include "internal.h"
@@ -111,8 +114,8 @@ __global__ void __launch_bounds__(192, 1)
         }
         uint8_t* sa = smem + s * C::kStageBytes;
         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-        tma_load_2d(sa, &tmA, &full[s], kb * kBK, row0);
-        const int kbb = (kb % args.kb_period) * kBK;
+        tma_load_2d(sa, &tmA, &full[s], (kb % args.kb_period_a) * kBK, row0);
+        const int kbb = (kb % args.kb_period_b) * kBK;
         tma_load_2d_hint(sa + C::kABytes, &tmB, &full[s], kbb, brow, pol_b);
         if (C::kDual) tma_load_2d_hint(sa + C::kABytes + C::kBBytes, &tmB2, &full[s], kbb, brow, pol_b);
         issued = kb + 1;
@@ -185,8 +188,8 @@ __global__ void __launch_bounds__(192, 1)
               if (col + i < args.N) orow[col + i] = __uint_as_float(v[i]);
           }
         }
-      } else if constexpr (EPI == kEpiBf16Ss) {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo;
+      } else if constexpr (EPI == kEpiF32Ss) {
+        float* orow = static_cast<float*>(args.out) + grow * args.ldo;
         float ss = 0.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -195,18 +198,17 @@ __global__ void __launch_bounds__(192, 1)
           tmem_ld_wait();
           const int col = n0 + c0;
           if (row_ok && col + 32 <= args.N) {
-            uint32_t pk[16];
+            float4* o = reinterpret_cast<float4*>(orow + col);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float a = bf16_round(__uint_as_float(v[2 * i]));
-              const float b = bf16_round(__uint_as_float(v[2 * i + 1]));
-              ss = fmaf(a, a, ss);
-              ss = fmaf(b, b, ss);
-              pk[i] = pack_bf16x2(a, b);
+            for (int i = 0; i < 8; ++i) {
+              const float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                           __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+              ss = fmaf(f.x, f.x, ss);
+              ss = fmaf(f.y, f.y, ss);
+              ss = fmaf(f.z, f.z, ss);
+              ss = fmaf(f.w, f.w, ss);
+              o[i] = f;
             }
-            uint4* o = reinterpret_cast<uint4*>(orow + col);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
         }
         if (row_ok) args.ss[grow * args.ld_ss + blockIdx.x] = ss;
@@ -261,6 +263,7 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
   }
   dim3 grid((a.N + BN - 1) / BN, m_tiles);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  count_launch();
   kern<<<grid, 192, C::kSmemBytes, s>>>(tmA, tmB, tmB2, a);
   return cudaGetLastError();
 }
@@ -270,7 +273,7 @@ cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& 
                         cudaStream_t s) {
   switch (epi) {
     case kEpiF32: return launch_one<kBNWide, kEpiF32>(tmA, tmB, tmB2, a, m_tiles, s);
-    case kEpiBf16Ss: return launch_one<kBNWide, kEpiBf16Ss>(tmA, tmB, tmB2, a, m_tiles, s);
+    case kEpiF32Ss: return launch_one<kBNWide, kEpiF32Ss>(tmA, tmB, tmB2, a, m_tiles, s);
     case kEpiSwiGLU: return launch_one<kBNSwiGLU, kEpiSwiGLU>(tmA, tmB, tmB2, a, m_tiles, s);
   }
   return cudaErrorInvalidValue;

@@ -25,7 +25,7 @@ enum : uint32_t {
 
 enum EpiKind : int {
   kEpiF32 = 0,      // fp32 store (router logits)
-  kEpiBf16Ss = 1,   // bf16 store + per-row partial sum of squares of the bf16 values
+  kEpiF32Ss = 1,    // fp32 store + per-row partial sum of squares of the stored values
   kEpiSwiGLU = 2,   // two accumulators a, b -> bf16 silu(a) * b
 };
 
@@ -37,17 +37,21 @@ struct Tile {
 struct GemmArgs {
   int M;                   // rows of A when tiles == nullptr (dense tiling)
   int N;                   // output columns (rows of one expert's B)
-  int num_kb;              // K / kBK
-  int kb_period;           // B's k-blocks before its coordinate wraps (K of B / kBK)
+  int num_kb;              // k-blocks of the reduction (K / kBK)
+  int kb_period_a;         // A's k coordinate is (kb % kb_period_a) * kBK
+  int kb_period_b;         // B's k coordinate is (kb % kb_period_b) * kBK
   const Tile* tiles;       // grouped tiles, or nullptr
   const int* n_tiles;      // number of valid grouped tiles (device)
   void* out;               // [rows, ldo] fp32 or bf16
   long long ldo;           // elements
-  float* ss;               // [rows, ld_ss] partial sums of squares (kEpiBf16Ss)
+  float* ss;               // [rows, ld_ss] partial sums of squares (kEpiF32Ss)
   int ld_ss;
   unsigned* err;           // device error word
   long long budget;        // wait budget, SM cycles
 };
+
+// Counts every kernel launch of the library (lmoe_kernel_launches).
+void count_launch();
 
 // Launches one tcgen05 GEMM: out = A * B^T over grid (ceil(N/BN), m_tiles).
 cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
@@ -63,19 +67,21 @@ cudaError_t launch_topk(const float* logits, int ld, const float* bias, const in
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
                            int32_t* n_tiles, cudaStream_t s);
-cudaError_t launch_poolnorm_scatter(const __nv_bfloat16* p, const float* ss_p, int ld_ss,
+cudaError_t launch_poolnorm_scatter(const float* p, const float* ss_p, int ld_ss,
                                     const float* g_pool, const int32_t* row_of, int T, int L,
                                     int k, float eps, __nv_bfloat16* xe, cudaStream_t s);
-cudaError_t launch_combine(const __nv_bfloat16* y, const float* ss_y, int ld_ss,
+cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
                            const int32_t* row_of, const int32_t* idx, const float* w,
                            const float* g_expert, int T, int L, int k, float eps,
                            __nv_bfloat16* c, cudaStream_t s);
-cudaError_t launch_postnorm_residual(const void* x, bool x_f32, const __nv_bfloat16* u,
+cudaError_t launch_postnorm_residual(const void* x, bool x_f32, const float* u,
                                      const float* ss_u, int ld_ss, const float* g_post, int T,
                                      int D, float eps, void* out, bool out_f32, cudaStream_t s);
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s);
-cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, long long n, cudaStream_t s);
-cudaError_t launch_router_split(const float* W, int E, int D, __nv_bfloat16* dst,
-                                cudaStream_t s);
+// fp32 weight [rows, K] -> bf16 [rows, parts*K]: part q is W_hi when bit q of lo_mask is 0,
+// else W_lo = bf16(W - W_hi).  [hi | hi | lo] pairs with activations [x_hi | x_lo | x_hi];
+// [hi | lo] pairs with one activation read twice.
+cudaError_t launch_weight_split(const float* W, long long rows, int K, int parts,
+                                unsigned lo_mask, __nv_bfloat16* dst, cudaStream_t s);
 
 }  // namespace lmoe

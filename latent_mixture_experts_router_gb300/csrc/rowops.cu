@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kPermThreads) expert_scatter_kernel(
 
 // ------------------------------------------------------------------ pool norm + scatter
 __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
-    const __nv_bfloat16* __restrict__ p, const float* __restrict__ ss_p, int ld_ss,
+    const float* __restrict__ p, const float* __restrict__ ss_p, int ld_ss,
     const float* __restrict__ g, const int32_t* __restrict__ row_of, int L, int k, float eps,
     __nv_bfloat16* __restrict__ xe) {
   __shared__ float s_rs;
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
   const float rs = s_rs;
   for (int i = threadIdx.x * 8; i < L; i += kRowThreads * 8) {
     float v[8], gg[8];
-    load8_bf16(p + t * L + i, v);
+    load8_f32(p + t * L + i, v);
     load8_f32(g + i, gg);
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = v[j] * rs * gg[j];
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
 
 // ------------------------------------------------------------------ combine
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(
-    const __nv_bfloat16* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
+    const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx,
     const float* __restrict__ w, const float* __restrict__ g_expert, int L, int k, float eps,
     __nv_bfloat16* __restrict__ c) {
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {  // slot order
       float v[8], gg[8];
-      load8_bf16(y + static_cast<long long>(s_row[j]) * L + i, v);
+      load8_f32(y + static_cast<long long>(s_row[j]) * L + i, v);
       load8_f32(g_expert + static_cast<long long>(s_e[j]) * L + i, gg);
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_coef[j], v[q] * gg[q], acc[q]);
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
 
 // ------------------------------------------------------------------ post-norm + residual
 __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
-    const void* __restrict__ x, int x_f32, const __nv_bfloat16* __restrict__ u,
+    const void* __restrict__ x, int x_f32, const float* __restrict__ u,
     const float* __restrict__ ss_u, int ld_ss, const float* __restrict__ g, int D, float eps,
     void* __restrict__ out, int out_f32) {
   __shared__ float s_rs;
@@ -366,7 +366,7 @@ __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
   for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
     float xv[8], uv[8], gg[8];
     load8(x, x_f32, t * D + i, xv);
-    load8_bf16(u + t * D + i, uv);
+    load8_f32(u + t * D + i, uv);
     load8_f32(g + i, gg);
 #pragma unroll
     for (int j = 0; j < 8; ++j) xv[j] = xv[j] + uv[j] * rs * gg[j];
@@ -380,33 +380,24 @@ __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
   }
 }
 
-// ------------------------------------------------------------------ fp32 weights -> bf16
-__global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
-                                   long long n) {
-  for (long long i = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x * 8) {
-    float v[8];
-    load8_f32(src + i, v);
-    store8_bf16(dst + i, v);
-  }
-}
-
-// W [E, D] fp32 -> [E, 3D] bf16 as [W_hi | W_hi | W_lo], W_lo = bf16(W - W_hi)
-__global__ void router_split_kernel(const float* __restrict__ W, int D,
-                                    __nv_bfloat16* __restrict__ dst) {
-  const long long e = blockIdx.x;
-  for (int i = threadIdx.x * 8; i < D; i += blockDim.x * 8) {
+// ------------------------------------------------------------------ fp32 weights -> bf16 hi/lo
+// W [rows, K] fp32 -> [rows, parts*K] bf16; part q = W_lo if bit q of lo_mask else W_hi
+__global__ void weight_split_kernel(const float* __restrict__ W, long long rows, int K, int parts,
+                                    unsigned lo_mask, __nv_bfloat16* __restrict__ dst) {
+  const long long chunks = rows * (K / 8);
+  for (long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
+       c += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = c / (K / 8);
+    const int i = static_cast<int>(c % (K / 8)) * 8;
     float v[8], hi[8], lo[8];
-    load8_f32(W + e * D + i, v);
+    load8_f32(W + r * K + i, v);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       hi[j] = bf16_round(v[j]);
       lo[j] = v[j] - hi[j];
     }
-    __nv_bfloat16* row = dst + e * 3 * D;
-    store8_bf16(row + i, hi);
-    store8_bf16(row + D + i, hi);
-    store8_bf16(row + 2 * D + i, lo);
+    __nv_bfloat16* row = dst + r * parts * K;
+    for (int q = 0; q < parts; ++q) store8_bf16(row + static_cast<long long>(q) * K + i, ((lo_mask >> q) & 1) ? lo : hi);
   }
 }
 
@@ -425,6 +416,7 @@ __global__ void wait_selftest_kernel(long long budget, unsigned* err) {
 
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s) {
+  count_launch();
   wait_selftest_kernel<<<1, 32, 0, s>>>(budget, err);
   return cudaGetLastError();
 }
@@ -432,6 +424,7 @@ cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s
 cudaError_t launch_prenorm(const void* x, bool x_f32, const float* g_pre, int T, int D, float eps,
                            __nv_bfloat16* xa, int xa_cols, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  count_launch();
   prenorm_kernel<<<T, kRowThreads, 0, s>>>(x, x_f32 ? 1 : 0, g_pre, D, eps, xa, xa_cols);
   return cudaGetLastError();
 }
@@ -442,6 +435,7 @@ cudaError_t launch_topk(const float* logits, int ld, const float* bias, const in
   if (T == 0) return cudaSuccess;
   const int blocks = (T + kTopkWarps - 1) / kTopkWarps;
   const size_t smem = static_cast<size_t>(kTopkWarps) * E * sizeof(float);
+  count_launch();
   topk_kernel<<<blocks, kTopkWarps * 32, smem, s>>>(logits, ld, bias, forced, T, E, k, idx, w,
                                                     near_tie, idx_copy, w_copy, err);
   return cudaGetLastError();
@@ -451,52 +445,52 @@ cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* cou
                            int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
                            int32_t* n_tiles, cudaStream_t s) {
   const int n = T * k;
+  count_launch();
   expert_count_kernel<<<E, kPermThreads, 0, s>>>(idx, n, counts);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  count_launch();
   expert_scatter_kernel<<<E, kPermThreads, 0, s>>>(idx, n, k, E, counts, offsets, row_of, tok_of,
                                                    tiles, n_tiles);
   return cudaGetLastError();
 }
 
-cudaError_t launch_poolnorm_scatter(const __nv_bfloat16* p, const float* ss_p, int ld_ss,
+cudaError_t launch_poolnorm_scatter(const float* p, const float* ss_p, int ld_ss,
                                     const float* g_pool, const int32_t* row_of, int T, int L,
                                     int k, float eps, __nv_bfloat16* xe, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  count_launch();
   poolnorm_scatter_kernel<<<T, kRowThreads, 0, s>>>(p, ss_p, ld_ss, g_pool, row_of, L, k, eps, xe);
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const __nv_bfloat16* y, const float* ss_y, int ld_ss,
+cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
                            const int32_t* row_of, const int32_t* idx, const float* w,
                            const float* g_expert, int T, int L, int k, float eps,
                            __nv_bfloat16* c, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  count_launch();
   combine_kernel<<<T, kRowThreads, 0, s>>>(y, ss_y, ld_ss, row_of, idx, w, g_expert, L, k, eps, c);
   return cudaGetLastError();
 }
 
-cudaError_t launch_postnorm_residual(const void* x, bool x_f32, const __nv_bfloat16* u,
+cudaError_t launch_postnorm_residual(const void* x, bool x_f32, const float* u,
                                      const float* ss_u, int ld_ss, const float* g_post, int T,
                                      int D, float eps, void* out, bool out_f32, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  count_launch();
   postnorm_residual_kernel<<<T, kRowThreads, 0, s>>>(x, x_f32 ? 1 : 0, u, ss_u, ld_ss, g_post, D,
                                                      eps, out, out_f32 ? 1 : 0);
   return cudaGetLastError();
 }
 
-cudaError_t launch_f32_to_bf16(const float* src, __nv_bfloat16* dst, long long n,
-                               cudaStream_t s) {
-  if (n == 0) return cudaSuccess;
-  const long long chunks = (n + 7) / 8;
+cudaError_t launch_weight_split(const float* W, long long rows, int K, int parts,
+                                unsigned lo_mask, __nv_bfloat16* dst, cudaStream_t s) {
+  const long long chunks = rows * (K / 8);
+  if (chunks == 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<long long>((chunks + 255) / 256, 152 * 16));
-  f32_to_bf16_kernel<<<blocks, 256, 0, s>>>(src, dst, n);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_router_split(const float* W, int E, int D, __nv_bfloat16* dst,
-                                cudaStream_t s) {
-  router_split_kernel<<<E, 256, 0, s>>>(W, D, dst);
+  count_launch();
+  weight_split_kernel<<<blocks, 256, 0, s>>>(W, rows, K, parts, lo_mask, dst);
   return cudaGetLastError();
 }
 

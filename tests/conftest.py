@@ -11,3 +11,9 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: takes more than a few seconds")
+
+
+def build_library():
+    """Compile the CUDA library in-tree (no-op when up to date)."""
+    import __graft_entry__
+    __graft_entry__.build()

@@ -67,12 +67,12 @@ def views(blk, cfg) -> dict:
         "row_of": get("row_of", R, torch.int32).view(T, k),
         "tok_of": get("tok_of", R, torch.int32),
         "n_tiles": get("n_tiles", 1, torch.int32),
-        "p": get("p", T * L, bf).view(T, L),
+        "p": get("p", T * L, torch.float32).view(T, L),
         "xe": get("xe", R * L, bf).view(R, L),
         "h": get("h", R * I, bf).view(R, I),
-        "y": get("y", R * L, bf).view(R, L),
+        "y": get("y", R * L, torch.float32).view(R, L),
         "c": get("c", T * L, bf).view(T, L),
-        "u": get("u", T * D, bf).view(T, D),
+        "u": get("u", T * D, torch.float32).view(T, D),
     }
     return {name: t.to(torch.float64 if t.dtype in (bf, torch.float32) else torch.int64).cpu().numpy()
             for name, t in v.items()}

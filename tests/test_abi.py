@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lm():
-    from latent_mixture_experts_router_gb300 import build
-    build.build()
+    from conftest import build_library
+    build_library()
     import latent_mixture_experts_router_gb300 as lm
     return lm
 
