@@ -163,38 +163,78 @@ def roofline(stage: str, dur_ms: float, costs: dict, pk: dict, pk_kind: str, sus
 
 
 # ------------------------------------------------------------------ oracle timing
-def oracle_sample_params(w: workloads.Workload, tokens, inp=None):
-    """Oracle parameters holding, as fp64 arrays, only the experts the sampled tokens
-    route to.  Weights come from the seeded generator (copied from ``inp`` when given,
-    else regenerated on the host); the expert set comes from the oracle's own router
-    (or the forced routing of the workload)."""
+def oracle_sample_inputs(w: workloads.Workload, tokens, inp=None) -> workloads.BlockInputs:
+    """Host-resident inputs for the sampled tokens: their x rows, the dense weights, and
+    only the experts these tokens route to (expert stacks as dicts keyed by expert id).
+    Values come from the seeded generator: copied from ``inp`` (device) when given, else
+    regenerated on the host."""
     import oracle
-    P = oracle.params_from_inputs(inp) if inp is not None else oracle.params_for_workload(w)
-    x = workloads.x_tensor(w, rows=tokens).double().numpy()
+    cpu = lambda t: tuple(u.cpu() for u in t) if isinstance(t, tuple) else t.cpu()  # noqa: E731
+    if inp is not None:
+        g = {n: getattr(inp, n).cpu() for n in ("g_pre", "g_pool", "g_expert", "g_post")}
+        dense = {n: cpu(getattr(inp, n)) for n in ("W_router", "W_pool", "W_unpool")}
+        bias = None if inp.router_bias is None else inp.router_bias.cpu()
+    else:
+        g = workloads.gammas(w)
+        nv = w.weights == "nvfp4"
+        dense = {"W_router": workloads.dense_weight(w, "W_router")}
+        for n in ("W_pool", "W_unpool"):
+            dense[n] = workloads.nvfp4_weight(w, n) if nv else workloads.dense_weight(w, n)
+        bias = workloads.zipf_bias(w) if w.routing == "zipf" else None
+    x = workloads.x_tensor(w, rows=tokens)
     if w.routing == "hot4":
         sel = workloads.forced_routing(w)[tokens].numpy()
     else:
-        lg = oracle.rms_norm(x, P.g_pre, P.eps) @ P.W_router.T
-        if P.router_bias is not None:
-            lg = lg + P.router_bias
+        xn = oracle.rms_norm(x.double().numpy(), g["g_pre"].double().numpy(), w.eps)
+        lg = xn @ dense["W_router"].double().numpy().T
+        if bias is not None:
+            lg = lg + bias.double().numpy()
         sel = oracle.top_k(lg, w.k)
     experts = sorted({int(e) for e in sel.reshape(-1)})
     stacks = {}
-    for name in ("W_gate", "W_up", "W_down"):
-        mats = {e: np.array(getattr(P, name)[e]) for e in experts}
-        stacks[name] = oracle.ExpertStack(lambda e, m=mats: m[int(e)], w.E)
-    return oracle.BlockParams(**{**P.__dict__, **stacks}), x
+    for n in ("W_gate", "W_up", "W_down"):
+        if inp is not None:
+            src = getattr(inp, n)
+            if isinstance(src, tuple):
+                stacks[n] = ({e: src[0][e].cpu() for e in experts}, {e: src[1][e].cpu() for e in experts},
+                             src[2].cpu())
+            else:
+                stacks[n] = {e: src[e].cpu() for e in experts}
+        elif w.weights == "nvfp4":
+            parts = {e: workloads.nvfp4_weight(w, n, expert=e) for e in experts}
+            s = torch.full((w.E,), float(next(iter(parts.values()))[2][0]), dtype=torch.float32)
+            stacks[n] = ({e: p[0] for e, p in parts.items()}, {e: p[1] for e, p in parts.items()}, s)
+        else:
+            stacks[n] = {e: workloads.dense_weight(w, n, expert=e) for e in experts}
+    forced = workloads.forced_routing(w)[tokens] if w.routing == "hot4" else None
+    return workloads.BlockInputs(w=w, x=x, **dense, **stacks, **g, router_bias=bias, forced_idx=forced)
 
 
-def time_oracle(w: workloads.Workload, n_tokens: int, inp=None, repeats: int = 1):
+def oracle_resident(w: workloads.Workload, n_tokens: int, inp=None):
+    """(params, x, forced) for the first n_tokens of w with every routed expert already
+    widened to fp64: the oracle's inputs resident in its own format, as the GPU arm's
+    weights are resident in HBM before its timed region."""
     import oracle
     tokens = list(range(n_tokens))
-    P, x = oracle_sample_params(w, tokens, inp=inp)
-    forced = None
-    if w.routing == "hot4":
-        forced = workloads.forced_routing(w)[:n_tokens].numpy()
+    sample = oracle_sample_inputs(w, tokens, inp=inp)
+    P = oracle.params_from_inputs(sample)
+    for n in ("W_gate", "W_up", "W_down"):
+        keys = getattr(sample, n)[0].keys() if isinstance(getattr(sample, n), tuple) else getattr(sample, n).keys()
+        mats = {e: np.array(getattr(P, n)[e]) for e in keys}
+        setattr(P, n, oracle.ExpertStack(lambda e, m=mats: m[int(e)], w.E))
+    x = sample.x.double().numpy()
+    forced = None if sample.forced_idx is None else sample.forced_idx.numpy()
+    return P, x, forced
+
+
+def time_oracle(w: workloads.Workload, n_tokens: int, inp=None, min_seconds: float = 0.0,
+                repeats: int = 1):
+    """Per-call seconds of the fp64 oracle on the first n_tokens of w; repeats the call
+    at least ``repeats`` times and until ``min_seconds`` of oracle time have passed."""
+    import oracle
+    P, x, forced = oracle_resident(w, n_tokens, inp=inp)
     times = []
-    for _ in range(repeats):
+    while len(times) < repeats or sum(times) < min_seconds:
         t0 = time.perf_counter()
         oracle.forward_batched(x, P, w.k, forced_idx=forced)
         times.append(time.perf_counter() - t0)
@@ -318,11 +358,13 @@ def run_ours(args, ws, rank, local):
     }
     if not args.no_cpu_baseline:
         n_tok = max(1, args.cpu_tokens)
-        t = time_oracle(w, n_tok, inp=inp)[0]
-        line["cpu_baseline"] = {"value": round(n_tok / t, 3), "unit": "tokens/s", "cores": os.cpu_count(),
-                                "kind": "oracle",
-                                "sample": f"first {n_tok} tokens of {w.name} through the fp64 oracle "
-                                          f"(numpy BLAS), {t:.1f} s"}
+        times = time_oracle(w, n_tok, inp=inp, min_seconds=10.0)
+        t = sum(times)
+        line["cpu_baseline"] = {"value": round(n_tok * len(times) / t, 3), "unit": "tokens/s",
+                                "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"first {n_tok} tokens of {w.name} through the fp64 oracle (numpy "
+                                          f"BLAS, routed experts pre-widened to fp64), {len(times)} calls, "
+                                          f"{t:.1f} s"}
     return line
 
 
@@ -334,19 +376,12 @@ def run_reference(args, ws, rank):
     if args.tokens:
         w = w.with_tokens(args.tokens)
     n_tok = max(1, args.cpu_tokens)
-    import oracle
-    tokens = list(range(n_tok))
-    P, x = oracle_sample_params(w, tokens)
-    forced = workloads.forced_routing(w)[:n_tok].numpy() if w.routing == "hot4" else None
-    for _ in range(args.warmup):
-        oracle.forward_batched(x, P, w.k, forced_idx=forced)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.forward_batched(x, P, w.k, forced_idx=forced)
-    dt = time.perf_counter() - t0
+    times = time_oracle(w, n_tok, repeats=args.warmup + args.steps)[args.warmup:]
+    dt = sum(times)
     v = round(n_tok * args.steps / dt, 3)
-    sample = (f"each step: {n_tok} tokens of {w.name} through the fp64 oracle (numpy BLAS on the host "
-              f"cores); weights of the experts they route to prepared before timing")
+    sample = (f"each step: the first {n_tok} tokens of {w.name} through the fp64 oracle (numpy BLAS "
+              f"on the host cores); weights of the routed experts generated on the host and widened "
+              f"to fp64 before timing")
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -364,10 +399,13 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_bf16", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--tokens", type=int, default=0, help="override T of the workload")
-    ap.add_argument("--cpu-tokens", type=int, default=4, help="oracle sample size (tokens)")
+    ap.add_argument("--cpu-tokens", type=int, default=None,
+                    help="oracle sample size in tokens (default: ~10-30 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     ws, rank, local = dist_init()
+    if args.cpu_tokens is None:   # bounded host memory: <= 8*k routed experts held in fp64
+        args.cpu_tokens = {"tiny_fp32": 64}.get(args.workload, 4 if args.impl == "reference" else 8)
     if args.impl == "reference":
         args.steps = 3 if args.steps is None else args.steps
         args.warmup = 1 if args.warmup is None else args.warmup

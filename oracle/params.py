@@ -18,13 +18,18 @@ def _np(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu").to(torch.float64).numpy()
 
 
+def _host_u8(t) -> np.ndarray:
+    return t.detach().to("cpu").numpy()
+
+
 def _dense_or_nvfp4(v, per_expert: bool):
-    """Tensor, or (codes, scales, s) triple -> fp64 array or per-expert callable."""
+    """Tensor, or (codes, scales, s) triple -> fp64 array, or for expert stacks a callable
+    that widens one expert on demand (stacks may be tensors or dicts keyed by expert)."""
     if isinstance(v, tuple):
-        codes, scales, s = (t.detach().cpu() for t in v)
+        codes, scales, s = v
         if per_expert:
-            return lambda e: formats.nvfp4_dequantize(codes[e].numpy(), scales[e].numpy(), float(s[e]))
-        return formats.nvfp4_dequantize(codes.numpy(), scales.numpy(), float(s[0]))
+            return lambda e: formats.nvfp4_dequantize(_host_u8(codes[e]), _host_u8(scales[e]), float(s[e]))
+        return formats.nvfp4_dequantize(_host_u8(codes), _host_u8(scales), float(s[0]))
     if per_expert:
         return lambda e: _np(v[e])
     return _np(v)

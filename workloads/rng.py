@@ -71,18 +71,33 @@ def _irwin_hall4(h: torch.Tensor) -> torch.Tensor:
     return u
 
 
+def _chunk(device) -> int:
+    # host: cache-sized pieces (the int64 temporaries then stay in cache); device: large
+    return 1 << 18 if torch.device(device).type == "cpu" else 1 << 26
+
+
 def normal(seed: int, stream: int, start: int, count: int, std: float,
            device="cpu") -> torch.Tensor:
     """fp64 deviates with mean 0 and standard deviation ``std`` for indices [start, start+count)."""
-    idx = torch.arange(start, start + count, dtype=torch.int64, device=device)
-    u = _irwin_hall4(hash64(seed, stream, idx))
-    return u * (math.sqrt(3.0) * std)  # one correctly rounded multiply
+    out = torch.empty(count, dtype=torch.float64, device=device)
+    c = _chunk(device)
+    for s0 in range(0, count, c):
+        n = min(c, count - s0)
+        idx = torch.arange(start + s0, start + s0 + n, dtype=torch.int64, device=device)
+        u = _irwin_hall4(hash64(seed, stream, idx))
+        out[s0:s0 + n] = u * (math.sqrt(3.0) * std)  # one correctly rounded multiply
+    return out
 
 
 def uniform_bits(seed: int, stream: int, start: int, count: int, device="cpu") -> torch.Tensor:
     """Raw int64 hash values for indices [start, start+count)."""
-    idx = torch.arange(start, start + count, dtype=torch.int64, device=device)
-    return hash64(seed, stream, idx)
+    out = torch.empty(count, dtype=torch.int64, device=device)
+    c = _chunk(device)
+    for s0 in range(0, count, c):
+        n = min(c, count - s0)
+        idx = torch.arange(start + s0, start + s0 + n, dtype=torch.int64, device=device)
+        out[s0:s0 + n] = hash64(seed, stream, idx)
+    return out
 
 
 def permutation(seed: int, stream: int, n: int) -> torch.Tensor:
