@@ -192,6 +192,28 @@ lmoe_status lmoe_get_workspace_layout(const lmoe_config* cfg, lmoe_workspace_lay
 lmoe_status lmoe_wait_selftest(const lmoe_config* cfg, void* workspace, long long budget_cycles,
                                cudaStream_t stream);
 
+/* Token permutation (expert histogram + stable scatter) that allocates nothing, for callers
+ * that cannot allocate device memory: code whose memory is planned up front by a framework
+ * that cannot hand out one more buffer, plug-ins that may not allocate after start-up, and
+ * loops that cannot afford an allocation's implicit synchronisation.  The pages have no
+ * counterpart of this entry point; it is a packaging of the block's permutation step.
+ * Device pointers:
+ *  topk_idx  [T, k] int32   expert id of each (token, slot), every id in [0, E)
+ *  offsets   [E + 1] int32  out: first row of each expert in expert-contiguous order;
+ *                           offsets[E] = T*k
+ *  row_of    [T, k] int32   out: row of pair (t, j); pairs of one expert keep (t, j) order
+ *  tok_of    [T*k] int32    out: token of each row
+ * The scratch (per-expert counts, M-tile table) is a fixed 64 KiB __device__ array inside
+ * the library, held by every GPU that loads the library until the process exits.  Limits:
+ * E <= 1024 and T*k <= 65536; larger sizes return LMOE_ERR_UNSUPPORTED before any launch.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * the current device, which must be the stream's device; make that first call before any
+ * stream capture.  All calls on a device share the one array and nothing in it needs to
+ * start at zero (each call overwrites what it reads), but calls that overlap on the GPU
+ * (unordered streams) race on it: order them. */
+lmoe_status lmoe_permute_noalloc(const int32_t* topk_idx, int T, int k, int E, int32_t* offsets,
+                                 int32_t* row_of, int32_t* tok_of, cudaStream_t stream);
+
 /* Number of kernels this library has launched in this process (all devices, all calls). */
 unsigned long long lmoe_kernel_launches(void);
 

@@ -240,3 +240,16 @@ def lmoe_wait_selftest(cfg, workspace, budget_cycles: int, stream=None):
 def lmoe_kernel_launches() -> int:
     """Kernels the library has launched in this process."""
     return int(_lib().lmoe_kernel_launches())
+
+
+def lmoe_permute_noalloc(topk_idx, E: int, offsets, row_of, tok_of, stream=None):
+    """Expert-contiguous permutation of ``topk_idx`` [T, k] (int32, device) into ``offsets``
+    [E+1], ``row_of`` [T, k] and ``tok_of`` [T*k] without any device allocation: the library's
+    fixed scratch array is used instead of a workspace (E <= 1024, T*k <= 65536)."""
+    L = _lib()
+    fn = L.lmoe_permute_noalloc
+    fn.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P]
+    fn.restype = ctypes.c_int
+    T, k = topk_idx.shape
+    _check(fn(_ptr(topk_idx), T, k, int(E), _ptr(offsets), _ptr(row_of), _ptr(tok_of), _stream(stream)),
+           "lmoe_permute_noalloc")

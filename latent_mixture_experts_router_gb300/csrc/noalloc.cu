@@ -1,0 +1,79 @@
+// noalloc.cu — the token permutation with its scratch in a fixed device array, for
+// callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc: code whose device memory is planned up front by a
+// host framework or runtime and that has no way to ask it for one more buffer, plug-ins
+// loaded into a process that forbids allocation after start-up, and latency-critical loops
+// where the implicit synchronisation of an allocation is not acceptable.  For them,
+// lmoe_permute_noalloc runs the same histogram + stable-scatter kernels as the block's
+// permutation step, with their scratch (per-expert counts, the M-tile table and its length)
+// placed in g_noalloc_scratch below instead of in a caller-provided workspace.
+//
+// The array is a file-scope __device__ object: every GPU that loads this library holds its
+// 64 KiB until the process exits.  Host code cannot use the symbol as a device address, so
+// the first call on each device looks the address up with cudaGetSymbolAddress (that
+// device current) and caches it; later calls reuse it.
+#include <mutex>
+
+#include "../../include/latent_moe.h"
+#include "internal.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+constexpr int kNoAllocMaxExperts = 1024;
+constexpr long long kNoAllocMaxPairs = 65536;  // T * k
+constexpr size_t kCountsOffset = 0;            // int32 [E]
+constexpr size_t kNTilesOffset = 4096;         // int32
+constexpr size_t kTilesOffset = 4352;          // Tile [ceil(T*k/128) + min(E, T*k)]
+
+static_assert(kCountsOffset + kNoAllocMaxExperts * sizeof(int32_t) <= kNTilesOffset, "layout");
+static_assert(kTilesOffset + (kNoAllocMaxPairs / lmoe::kBM + kNoAllocMaxExperts) * sizeof(lmoe::Tile) <=
+                  kNoAllocScratchBytes,
+              "layout");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up once per device).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" lmoe_status lmoe_permute_noalloc(const int32_t* topk_idx, int T, int k, int E,
+                                            int32_t* offsets, int32_t* row_of, int32_t* tok_of,
+                                            cudaStream_t stream) {
+  if (T < 0 || k < 1 || k > 16 || E < 1 || k > E) return LMOE_ERR_ARG;
+  if (E > kNoAllocMaxExperts || static_cast<long long>(T) * k > kNoAllocMaxPairs)
+    return LMOE_ERR_UNSUPPORTED;  // beyond the fixed scratch array
+  if (offsets == nullptr || (T > 0 && (topk_idx == nullptr || row_of == nullptr || tok_of == nullptr)))
+    return LMOE_ERR_ARG;
+  void* base = nullptr;
+  if (scratch_address(&base) != cudaSuccess) return LMOE_ERR_CUDA;
+  unsigned char* s = static_cast<unsigned char*>(base);
+  // Nothing here must start at zero: the count kernel overwrites counts[e] for every e, the
+  // scatter overwrites every tile it reports and the tile count, and offsets/row_of/tok_of
+  // are outputs.  So no clearing pass is needed between calls.
+  if (lmoe::launch_permute(topk_idx, T, k, E, reinterpret_cast<int32_t*>(s + kCountsOffset), offsets,
+                           row_of, tok_of, reinterpret_cast<lmoe::Tile*>(s + kTilesOffset),
+                           reinterpret_cast<int32_t*>(s + kNTilesOffset), stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
