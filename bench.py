@@ -162,6 +162,23 @@ def roofline(stage: str, dur_ms: float, costs: dict, pk: dict, pk_kind: str, sus
             "algorithmic_bytes": nbytes, "traffic": None}
 
 
+def measured_traffic(stage: str, w: workloads.Workload, units: int):
+    """DRAM bytes (read + write) per launch of the dominant kernel, scaled from the ncu capture
+    recorded in profiles/traffic.json by the units this launch processes; None when no capture
+    covers this kernel in this regime or the kernel source changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(stage)
+    src = os.path.join(ROOT, "latent_mixture_experts_router_gb300", "csrc", "gemm.cu")
+    if rec is None or hashlib.md5(open(src, "rb").read()).hexdigest() != rec["kernel_source_md5"]:
+        return None
+    if w.weights != "bf16" or w.T > 512:   # captured in the decode regime (few rows per expert)
+        return None
+    return int(rec["traffic_per_unit"] * units)
+
+
 # ------------------------------------------------------------------ oracle timing
 def oracle_sample_inputs(w: workloads.Workload, tokens, inp=None) -> workloads.BlockInputs:
     """Host-resident inputs for the sampled tokens: their x rows, the dense weights, and
@@ -241,14 +258,22 @@ def time_oracle(w: workloads.Workload, n_tokens: int, inp=None, min_seconds: flo
     return times
 
 
+def pick_workload(args) -> workloads.Workload:
+    import dataclasses
+    w = workloads.WORKLOADS[args.workload]
+    if args.tokens:
+        w = w.with_tokens(args.tokens)
+    if args.experts:
+        w = dataclasses.replace(w, E=args.experts, name=f"{w.name}@E{args.experts}")
+    return w
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, ws, rank, local):
     import latent_mixture_experts_router_gb300 as lm
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    w = workloads.WORKLOADS[args.workload]
-    if args.tokens:
-        w = w.with_tokens(args.tokens)
+    w = pick_workload(args)
     T = w.T
     inp = workloads.make_inputs(w, dev)
     if ws > 1:   # each replica gets its own tokens: rows [rank*T, (rank+1)*T) of one long batch
@@ -353,7 +378,8 @@ def run_ours(args, ws, rank, local):
                          f"{sum(b for b, _ in costs.values()) / 1e9:.1f} GB (129 MB L2)"},
         "tflops": round(total_flops / (ms_step * 1e-3) / 1e12, 2),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-        "roofline": roofline(dom, stage_ms[dom], costs, pk, pk_kind, sustained=False),
+        "roofline": {**roofline(dom, stage_ms[dom], costs, pk, pk_kind, sustained=False),
+                     "traffic": measured_traffic(dom, w, used)},
         "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
     }
     if not args.no_cpu_baseline:
@@ -372,9 +398,7 @@ def run_ours(args, ws, rank, local):
 def run_reference(args, ws, rank):
     if rank != 0:
         return None
-    w = workloads.WORKLOADS[args.workload]
-    if args.tokens:
-        w = w.with_tokens(args.tokens)
+    w = pick_workload(args)
     n_tok = max(1, args.cpu_tokens)
     times = time_oracle(w, n_tok, repeats=args.warmup + args.steps)[args.warmup:]
     dt = sum(times)
@@ -399,6 +423,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_bf16", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--tokens", type=int, default=0, help="override T of the workload")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override E (smaller profiling cases; the benchmark line uses the workload's E)")
     ap.add_argument("--cpu-tokens", type=int, default=None,
                     help="oracle sample size in tokens (default: ~10-30 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
