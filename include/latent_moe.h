@@ -64,6 +64,7 @@ typedef enum { LMOE_F32 = 0, LMOE_BF16 = 1, LMOE_NVFP4 = 2 } lmoe_dtype;
  *  d_model    D, multiple of 128           d_latent  L, multiple of 128
  *  n_experts  E, 1..1024                   d_ff      I, multiple of 128
  *  top_k      k, 1..min(E, 16)             eps       RMSNorm epsilon (all four norms)
+ *             (NVFP4 weights: D, L, I multiples of 256 and at most 32768)
  *  act_dtype  dtype of x: LMOE_F32 or LMOE_BF16
  *  weight_dtype  LMOE_F32, LMOE_BF16, or LMOE_NVFP4 (pooler, experts, unpooler packed;
  *             the router then stays LMOE_BF16)
@@ -180,9 +181,25 @@ lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStrea
 typedef struct {
   long long xa, logits, topk_idx, topk_w, counts, offsets, row_of, tok_of, tiles, n_tiles,
       p, ss_p, xe, xe_scale, h, y, ss_y, c, u, ss_u, err, total;
+  /* NVFP4 weights only (else -1): xn quantised for the pooler (codes [T, D/2], block scales
+   * [T, D/16], row scales [T] f32); row scales of xe [T*k] f32 (xe then holds codes
+   * [T*k, L/2] and xe_scale block scales [T*k, L/16]); h block scales [T*k, I/16] (h holds
+   * codes [T*k, I/2]); c block scales [T, L/16] and row scales [T] (c holds codes [T, L/2]). */
+  long long xq, xq_scale, xq_rowscale, xe_rowscale, h_scale, c_scale, c_rowscale;
   int xa_cols; /* columns of one xa row (2*D: xn_hi | xn_lo, or 3*D for fp32 weights) */
 } lmoe_workspace_layout;
 lmoe_status lmoe_get_workspace_layout(const lmoe_config* cfg, lmoe_workspace_layout* layout);
+
+/* NVFP4 quantisation of fp32 rows with the activation rule the block applies (one fp32
+ * scale per row s = amax/(6*448) when row_scale != 0, else s = 1; one E4M3 scale per 16
+ * elements sc = E4M3(amax_16/(6 s)); codes E2M1((v * (1/sc)) * (1/s)); each rounding in fp32,
+ * round to nearest even, saturating).  Format: LMSYS post, "NVFP4 as a third MMA type".
+ * Device pointers: src [rows, K] f32 (K a multiple of 16, at most 32768); codes [rows, K/2]
+ * (even element in the low nibble); scales [rows, K/16] E4M3 codes; s_row [rows] f32 (may
+ * be NULL).  Also a way to pack weights: with row_scale = 0 the tensor scale is 1.        */
+lmoe_status lmoe_quantize_nvfp4(const float* src, long long rows, int K, int row_scale,
+                                uint8_t* codes, uint8_t* scales, float* s_row,
+                                cudaStream_t stream);
 
 /* Diagnostic of the device wait-timeout path: launches one CTA that waits on an
  * mbarrier nothing ever arrives on, with a budget of `budget_cycles` SM cycles

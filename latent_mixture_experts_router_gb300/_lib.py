@@ -56,8 +56,12 @@ _LAYOUT_FIELDS = ["xa", "logits", "topk_idx", "topk_w", "counts", "offsets", "ro
                   "ss_u", "err", "total"]
 
 
+_LAYOUT_FIELDS_NVFP4 = ["xq", "xq_scale", "xq_rowscale", "xe_rowscale", "h_scale", "c_scale", "c_rowscale"]
+
+
 class lmoe_workspace_layout(ctypes.Structure):
-    _fields_ = [(f, ctypes.c_longlong) for f in _LAYOUT_FIELDS] + [("xa_cols", ctypes.c_int)]
+    _fields_ = ([(f, ctypes.c_longlong) for f in _LAYOUT_FIELDS + _LAYOUT_FIELDS_NVFP4]
+                + [("xa_cols", ctypes.c_int)])
 
 
 _P = ctypes.c_void_p
@@ -168,7 +172,7 @@ def lmoe_get_workspace_layout(cfg: Config) -> dict:
     lay = lmoe_workspace_layout()
     c = cfg.c()
     _check(_lib().lmoe_get_workspace_layout(ctypes.byref(c), ctypes.byref(lay)), "lmoe_get_workspace_layout")
-    d = {f: getattr(lay, f) for f in _LAYOUT_FIELDS}
+    d = {f: getattr(lay, f) for f in _LAYOUT_FIELDS + _LAYOUT_FIELDS_NVFP4}
     d["xa_cols"] = lay.xa_cols
     return d
 
@@ -253,3 +257,14 @@ def lmoe_permute_noalloc(topk_idx, E: int, offsets, row_of, tok_of, stream=None)
     T, k = topk_idx.shape
     _check(fn(_ptr(topk_idx), T, k, int(E), _ptr(offsets), _ptr(row_of), _ptr(tok_of), _stream(stream)),
            "lmoe_permute_noalloc")
+
+
+def lmoe_quantize_nvfp4(src, codes, scales, s_row=None, row_scale=True, stream=None):
+    """NVFP4-quantise the fp32 rows of ``src`` [rows, K] (device) with the block's activation rule."""
+    L = _lib()
+    fn = L.lmoe_quantize_nvfp4
+    fn.argtypes = [_P, ctypes.c_longlong, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P]
+    fn.restype = ctypes.c_int
+    rows, K = src.shape
+    _check(fn(_ptr(src), rows, K, 1 if row_scale else 0, _ptr(codes), _ptr(scales), _ptr(s_row),
+              _stream(stream)), "lmoe_quantize_nvfp4")

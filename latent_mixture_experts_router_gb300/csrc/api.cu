@@ -55,7 +55,13 @@ lmoe_status check_config(const lmoe_config* c) {
   if (!(c->eps >= 0.f)) return LMOE_ERR_ARG;
   if (c->act_dtype != LMOE_F32 && c->act_dtype != LMOE_BF16) return LMOE_ERR_UNSUPPORTED;
   if (c->out_dtype != LMOE_F32 && c->out_dtype != LMOE_BF16) return LMOE_ERR_UNSUPPORTED;
-  if (c->weight_dtype != LMOE_F32 && c->weight_dtype != LMOE_BF16) return LMOE_ERR_UNSUPPORTED;
+  if (c->weight_dtype != LMOE_F32 && c->weight_dtype != LMOE_BF16 && c->weight_dtype != LMOE_NVFP4)
+    return LMOE_ERR_UNSUPPORTED;
+  if (c->weight_dtype == LMOE_NVFP4) {
+    // NVFP4 GEMM stages cover K = 256; the quantising row kernels hold one row in smem
+    if (c->d_model % 256 || c->d_latent % 256 || c->d_ff % 256) return LMOE_ERR_UNSUPPORTED;
+    if (c->d_model > 32768 || c->d_latent > 32768 || c->d_ff > 32768) return LMOE_ERR_UNSUPPORTED;
+  }
   return LMOE_OK;
 }
 
@@ -91,12 +97,29 @@ void make_layout(const lmoe_config* c, Layout* L) {
   P.n_tiles = take(4);
   P.p = take(T * Ld * 4);
   P.ss_p = take(T * L->ld_ss_p * 4);
-  P.xe = take(R * Ld * 2);
-  P.xe_scale = -1;
-  P.h = take(R * I * 2);
+  const bool fp4 = c->weight_dtype == LMOE_NVFP4;
+  if (fp4) {  // quantised GEMM inputs: codes (2 per byte), E4M3 block scales, fp32 row scales
+    P.xq = take(T * D / 2);
+    P.xq_scale = take(T * D / 16);
+    P.xq_rowscale = take(T * 4);
+    P.xe = take(R * Ld / 2);
+    P.xe_scale = take(R * Ld / 16);
+    P.xe_rowscale = take(R * 4);
+    P.h = take(R * I / 2);
+    P.h_scale = take(R * I / 16);
+  } else {
+    P.xe = take(R * Ld * 2);
+    P.h = take(R * I * 2);
+  }
   P.y = take(R * Ld * 4);
   P.ss_y = take(R * L->ld_ss_y * 4);
-  P.c = take(T * Ld * 2);
+  if (fp4) {
+    P.c = take(T * Ld / 2);
+    P.c_scale = take(T * Ld / 16);
+    P.c_rowscale = take(T * 4);
+  } else {
+    P.c = take(T * Ld * 2);
+  }
   P.u = take(T * D * 4);
   P.ss_u = take(T * L->ld_ss_u * 4);
   if (f32w) {  // bf16 hi/lo splits of fp32 weights: [hi|hi|lo] (router, pooler), [hi|lo] (rest)
@@ -151,6 +174,21 @@ bool encode_bf16_2d(CUtensorMap* m, const void* base, unsigned long long cols,
   return r == CUDA_SUCCESS;
 }
 
+// 2-D uint8 map (NVFP4 codes or block scales): [rows, cols] bytes, rows `row_stride` apart.
+bool encode_u8_2d(CUtensorMap* m, const void* base, unsigned long long cols, unsigned long long rows,
+                  unsigned long long row_stride, unsigned box_cols, unsigned box_rows, bool swizzle) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_stride};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 #define LMOE_CUDA(call)                       \
@@ -189,6 +227,51 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   return LMOE_OK;
 }
 
+// One NVFP4 operand: codes [rows, K/2] and block scales [rows, K/16], both K contiguous.
+struct Fp4Operand {
+  const uint8_t* codes;
+  const uint8_t* scales;
+};
+
+lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, Fp4Operand B,
+                         long long b_rows, const Fp4Operand* B2, int N, const Tile* tiles,
+                         const int* n_tiles, int m_tiles, void* out, long long ldo,
+                         uint8_t* out_scales, float* ss, int ld_ss, const float* row_scale,
+                         const float* ts, const float* ts2, unsigned* err, long long budget,
+                         cudaStream_t s) {
+  const unsigned bn = epi == kFp4EpiSwiGLUQuant ? kBNSwiGLU : kBNWide;
+  CUtensorMap maps[6];
+  const unsigned long long kc = K / 2, ks = K / 16;
+  if (!encode_u8_2d(&maps[0], A.codes, kc, a_rows, kc, 128, kBM, true) ||
+      !encode_u8_2d(&maps[1], A.scales, ks, a_rows, ks, 16, kBM, false) ||
+      !encode_u8_2d(&maps[2], B.codes, kc, b_rows, kc, 128, bn, true) ||
+      !encode_u8_2d(&maps[3], B.scales, ks, b_rows, ks, 16, bn, false))
+    return LMOE_ERR_CUDA;
+  maps[4] = maps[2];
+  maps[5] = maps[3];
+  if (B2 && (!encode_u8_2d(&maps[4], B2->codes, kc, b_rows, kc, 128, bn, true) ||
+             !encode_u8_2d(&maps[5], B2->scales, ks, b_rows, ks, 16, bn, false)))
+    return LMOE_ERR_CUDA;
+  Fp4Args a{};
+  a.M = static_cast<int>(a_rows);
+  a.N = N;
+  a.num_kb = K / 256;
+  a.tiles = tiles;
+  a.n_tiles = n_tiles;
+  a.out = out;
+  a.ldo = ldo;
+  a.out_scales = out_scales;
+  a.ss = ss;
+  a.ld_ss = ld_ss;
+  a.row_scale = row_scale;
+  a.tensor_scale = ts;
+  a.tensor_scale2 = ts2;
+  a.err = err;
+  a.budget = budget;
+  LMOE_CUDA(launch_gemm_fp4(epi, maps, a, m_tiles, s));
+  return LMOE_OK;
+}
+
 lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_router,
                          const void* W_pool, const float* g_pool, const void* W_gate,
                          const void* W_up, const void* W_down, const float* g_expert,
@@ -209,8 +292,23 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                         W_unpool, g_pre, g_post, out};
   for (const void* p : ptrs)
     if (p == nullptr) return LMOE_ERR_ARG;
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return LMOE_ERR_ALIGN;
+  const bool fp4 = cfg->weight_dtype == LMOE_NVFP4;
+  // NVFP4 weights arrive as host structs of device pointers: check what they point to
+  const lmoe_nvfp4_weight* q4[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  if (fp4) {
+    const void* wv[5] = {W_pool, W_gate, W_up, W_down, W_unpool};
+    for (int i = 0; i < 5; ++i) {
+      q4[i] = static_cast<const lmoe_nvfp4_weight*>(wv[i]);
+      if (!q4[i]->data || !q4[i]->scales || !q4[i]->tensor_scale) return LMOE_ERR_ARG;
+      if (!aligned16(q4[i]->data) || !aligned16(q4[i]->scales) || !aligned16(q4[i]->tensor_scale))
+        return LMOE_ERR_ALIGN;
+    }
+  }
+  for (const void* p : ptrs) {
+    const bool host_struct = fp4 && (p == W_pool || p == W_gate || p == W_up || p == W_down ||
+                                     p == W_unpool);
+    if (!host_struct && !aligned16(p)) return LMOE_ERR_ALIGN;
+  }
   if (x == out) return LMOE_ERR_ARG;
   Layout L;
   make_layout(cfg, &L);
@@ -280,8 +378,13 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   }
   const int xa_cols = L.pub.xa_cols;
 
-  // S1 pre-norm
-  LMOE_CUDA(launch_prenorm(x, x_f32, g_pre, T, D, eps, xa, xa_cols, s));
+  // S1 pre-norm (NVFP4: xn is also quantised per token for the pooler)
+  uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
+  if (fp4)
+    LMOE_CUDA(launch_prenorm_nvfp4(x, x_f32, g_pre, T, D, eps, xa, xa_cols, wsb + L.pub.xq,
+                                   wsb + L.pub.xq_scale, reinterpret_cast<float*>(wsb + L.pub.xq_rowscale), s));
+  else
+    LMOE_CUDA(launch_prenorm(x, x_f32, g_pre, T, D, eps, xa, xa_cols, s));
   LMOE_MARK(LMOE_STAGE_ROUTER);
   // S2 router logits = [xn_hi | xn_lo (| xn_hi)] . [W | W (| W_lo)]^T
   const int m_tiles_T = cdiv(T, kBM);
@@ -299,6 +402,47 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   LMOE_MARK(LMOE_STAGE_PERMUTE);
   // S4 permutation
   LMOE_CUDA(launch_permute(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, s));
+  if (fp4) {
+    const Fp4Operand xq{wsb + L.pub.xq, wsb + L.pub.xq_scale};
+    const Fp4Operand xeq{wsb + L.pub.xe, wsb + L.pub.xe_scale};
+    const Fp4Operand hq{wsb + L.pub.h, wsb + L.pub.h_scale};
+    const Fp4Operand cq{wsb + L.pub.c, wsb + L.pub.c_scale};
+    float* xq_s = reinterpret_cast<float*>(wsb + L.pub.xq_rowscale);
+    float* xe_s = reinterpret_cast<float*>(wsb + L.pub.xe_rowscale);
+    float* c_s = reinterpret_cast<float*>(wsb + L.pub.c_rowscale);
+    auto op = [](const lmoe_nvfp4_weight* w) { return Fp4Operand{w->data, w->scales}; };
+    LMOE_MARK(LMOE_STAGE_POOLER);
+    // S5 pooler p = s_x * s_W * (Q(xn) . W_pool^T), block-scaled FP4 MMA
+    st = run_gemm_fp4(kFp4EpiF32Ss, xq, T, D, op(q4[0]), Ld, nullptr, Ld, nullptr, nullptr, m_tiles_T,
+                      p, Ld, nullptr, ss_p, L.ld_ss_p, xq_s, q4[0]->tensor_scale, nullptr, err, budget, s);
+    if (st != LMOE_OK) return st;
+    LMOE_MARK(LMOE_STAGE_POOLNORM);
+    // S6 pool norm, quantised per token, copied to the k expert rows
+    LMOE_CUDA(launch_poolnorm_scatter_nvfp4(p, ss_p, L.ld_ss_p, g_pool, row_of, T, Ld, k, eps,
+                                            wsb + L.pub.xe, wsb + L.pub.xe_scale, xe_s, s));
+    LMOE_MARK(LMOE_STAGE_GATE_UP);
+    // S7 grouped gate/up + SwiGLU, h requantised to NVFP4 (scale 1)
+    const Fp4Operand up = op(q4[2]);
+    st = run_gemm_fp4(kFp4EpiSwiGLUQuant, xeq, R, Ld, op(q4[1]), 1LL * E * I, &up, I, tiles, n_tiles,
+                      L.max_tiles, wsb + L.pub.h, I, wsb + L.pub.h_scale, nullptr, 0, xe_s,
+                      q4[1]->tensor_scale, q4[2]->tensor_scale, err, budget, s);
+    if (st != LMOE_OK) return st;
+    LMOE_MARK(LMOE_STAGE_DOWN);
+    // S8 grouped down (fp32 y) with per-row partial sums of squares
+    st = run_gemm_fp4(kFp4EpiF32Ss, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
+                      L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
+                      nullptr, err, budget, s);
+    if (st != LMOE_OK) return st;
+    LMOE_MARK(LMOE_STAGE_COMBINE);
+    // S9 combine, c quantised per token
+    LMOE_CUDA(launch_combine_nvfp4(y, ss_y, L.ld_ss_y, row_of, tk_idx, tk_w, g_expert, T, Ld, k, eps,
+                                   wsb + L.pub.c, wsb + L.pub.c_scale, c_s, s));
+    LMOE_MARK(LMOE_STAGE_UNPOOLER);
+    // S10 unpooler u = s_c * s_W * (Q(c) . W_unpool^T)
+    st = run_gemm_fp4(kFp4EpiF32Ss, cq, T, Ld, op(q4[4]), D, nullptr, D, nullptr, nullptr, m_tiles_T, u,
+                      D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s);
+    if (st != LMOE_OK) return st;
+  } else {
   LMOE_MARK(LMOE_STAGE_POOLER);
   // S5 pooler p = xn_hi . W_pool^T, with row partial sums of squares
   const int pool_k = f32w ? 3 * D : D;
@@ -326,6 +470,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   st = run_gemm(kEpiF32Ss, c, T, Ld, Ld, wun, D, 1LL * wsplit * Ld, nullptr, D, wsplit * Ld / kBK,
                 nullptr, nullptr, m_tiles_T, u, D, ss_u, L.ld_ss_u, err, budget, s);
   if (st != LMOE_OK) return st;
+  }
   LMOE_MARK(LMOE_STAGE_POSTNORM);
   // S11 post-norm + residual
   LMOE_CUDA(launch_postnorm_residual(x, x_f32, u, ss_u, L.ld_ss_u, g_post, T, D, eps, out,
@@ -436,6 +581,18 @@ lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStrea
   if (detail) *detail = word;
   if (word & (kErrWaitProducer | kErrWaitMma | kErrWaitEpilogue | kErrDrain)) return LMOE_ERR_TIMEOUT;
   if (word & kErrBadIndex) return LMOE_ERR_ARG;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_quantize_nvfp4(const float* src, long long rows, int K, int row_scale,
+                                uint8_t* codes, uint8_t* scales, float* s_row,
+                                cudaStream_t stream) {
+  if (rows < 0 || rows > (1LL << 31) - 1 || K <= 0 || K % 16 || K > 32768) return LMOE_ERR_ARG;
+  if (rows == 0) return LMOE_OK;
+  if (src == nullptr || codes == nullptr || scales == nullptr) return LMOE_ERR_ARG;
+  if (!aligned16(src) || (reinterpret_cast<uintptr_t>(codes) & 7u)) return LMOE_ERR_ALIGN;
+  if (launch_quantize_nvfp4(src, rows, K, row_scale != 0, codes, scales, s_row, stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
   return LMOE_OK;
 }
 

@@ -1,0 +1,372 @@
+// gemm_fp4.cu — grouped NVFP4 x NVFP4 GEMM on the block-scaled 5th-generation tensor cores.
+//
+// out[r, n] = alpha_r,e * sum_k A[r, k] * B[e*N + n, k], with A and B packed E2M1 (two
+// values per byte, K contiguous) and one UE4M3 scale per 16 consecutive k on both operands
+// (LMSYS "SGLang and Miles Add Day-0 Support for Muse Spark Open", "NVFP4 as a third MMA
+// type": nvfp4 x nvfp4 with 16-element UE4M3 block scales; the per-token FP32 input scale
+// is applied to the accumulator).  alpha = row scale (per token / per routed row, or 1) *
+// tensor scale of the weight (per expert).
+//
+// One CTA computes a 128 x BN tile; a pipeline stage covers K = 256 (128 bytes of codes per
+// row and 16 scale bytes per row).  Roles (224 threads):
+//   warp 0 lane 0   TMA: A codes + A scales + B codes + B scales (+ B2 for gate/up)
+//   warp 1          TMEM allocation; lane 0 copies scale factors into TMEM (tcgen05.cp) and
+//                   issues tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//   warps 2..5      epilogue (warp w owns TMEM lanes 32*(w%4) ..)
+//   warp 6          scale-factor transposer: the tensor cores take the scales of one
+//                   K=64 step of 128 rows from a 512-byte block of 32 lines x 16 bytes, line
+//                   m0 holding the 4 scale bytes of rows m0, m0+32, m0+64, m0+96
+//                   (tcgen05.cp 32x128b, replicated to the four lane quadrants); the scales
+//                   arrive row-major (16 bytes per row per stage) and this warp regroups them
+//                   (the "4x32 transpose" the pages describe before the copy).
+// Epilogues: kFp4EpiF32Ss — alpha * acc as fp32 plus per-row partial sums of squares (the
+// norm that follows needs only these partials); kFp4EpiSwiGLUQuant — gate and up tiles of
+// the same columns, h = silu(alpha_g acc_g) * (alpha_u acc_u) requantised to NVFP4 with
+// scale 1 (block scales only, through the reciprocal table) for the down projection.
+#include "internal.h"
+#include "nvfp4.cuh"
+#include "ptx.cuh"
+
+namespace lmoe {
+
+namespace {
+
+LMOE_DEV void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+LMOE_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Shared-memory descriptor of a 512-byte scale block: 4 core matrices of 8 lines x 16 B,
+// contiguous (stride 128 B), no swizzle.
+LMOE_DEV uint64_t sf_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+LMOE_DEV void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Instruction descriptor of kind::mxf4nvf4 block-scaled MMA: A/B E2M1 ([7,10) = 1,
+// [10,13) = 1), K-major, N>>3 at [17,23), scale type UE4M3 ([23] = 0), M>>4 at [24,29),
+// scale-factor ids 0 ([4,6) and [29,31)).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+LMOE_DEV void mma_nvf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                       uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+      : "memory");
+}
+
+template <int BN, int EPI>
+struct Fp4Cfg {
+  static constexpr bool kDual = (EPI == kFp4EpiSwiGLUQuant);
+  static constexpr int kNB = kDual ? 2 : 1;
+  static constexpr int kStages = 3;
+  static constexpr int kKStep = 4;                 // MMAs (K = 64 each) per stage
+  static constexpr int kABytes = kBM * 128;        // codes
+  static constexpr int kBBytes = BN * 128;
+  static constexpr int kSfaRaw = kBM * 16;         // row-major scales of the stage
+  static constexpr int kSfbRaw = BN * 16;
+  static constexpr int kBAtoms = BN / 128;         // 128-row scale blocks per B operand
+  static constexpr int kSfaT = kKStep * 512;       // regrouped scales
+  static constexpr int kSfbT = kKStep * kBAtoms * 512;
+  // stage layout: [A codes][B codes x kNB][A sf raw][B sf raw x kNB][A sf][B sf x kNB]
+  static constexpr int kOffB = kABytes;
+  static constexpr int kOffSfaRaw = kOffB + kNB * kBBytes;
+  static constexpr int kOffSfbRaw = kOffSfaRaw + kSfaRaw;
+  static constexpr int kOffSfa = kOffSfbRaw + kNB * kSfbRaw;
+  static constexpr int kOffSfb = kOffSfa + kSfaT;
+  static constexpr int kStageBytes = kOffSfb + kNB * kSfbT;
+  static constexpr uint32_t kTxBytes = kABytes + kSfaRaw + kNB * (kBBytes + kSfbRaw);
+  // tensor memory: accumulators, then per-stage scale columns
+  static constexpr int kAccCols = kNB * BN;
+  static constexpr int kSfaCols = kKStep * 4;                // 4 columns per 128 rows per MMA
+  static constexpr int kSfbColsOne = kKStep * (BN / 32);
+  static constexpr int kSfCols = kSfaCols + kNB * kSfbColsOne;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024 /*recip*/ + 256;
+  static_assert(kAccCols + kStages * kSfCols <= 512, "tensor memory");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(kStageBytes % 1024 == 0, "1024-byte aligned stages");
+};
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(224, 1)
+    gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmSA,
+                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmSB,
+                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmSB2,
+                    const Fp4Args args) {
+  using C = Fp4Cfg<BN, EPI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float* recip = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(recip + 256);
+  uint64_t* sfready = full + C::kStages;
+  uint64_t* empty = sfready + C::kStages;
+  uint64_t* accum = empty + C::kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+
+  int expert = 0, row0, nrows;
+  if (args.tiles != nullptr) {
+    if (static_cast<int>(blockIdx.y) >= *args.n_tiles) return;
+    const Tile t = args.tiles[blockIdx.y];
+    expert = t.expert;
+    row0 = t.row0;
+    nrows = t.nrows;
+  } else {
+    row0 = blockIdx.y * kBM;
+    nrows = min(kBM, args.M - row0);
+  }
+  if (nrows <= 0) return;
+  const int n0 = blockIdx.x * BN;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&sfready[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp >= 2 && warp <= 5) {
+    for (int i = threadIdx.x - 64; i < 256; i += 128) recip[i] = c_e4m3_recip.v[i];
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const long long budget = args.budget;
+  const int nk = args.num_kb;  // stages of K = 256
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const int brow = expert * args.N + n0;
+      const uint64_t pol_b = policy_evict_first();
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % C::kStages;
+        const uint32_t ph = (kb / C::kStages) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, budget)) {
+          atomicOr(args.err, kErrWaitProducer);
+          break;
+        }
+        uint8_t* st = smem + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+        tma_load_2d(st, &tmA, &full[s], kb * 128, row0);
+        tma_load_2d(st + C::kOffSfaRaw, &tmSA, &full[s], kb * 16, row0);
+        tma_load_2d_hint(st + C::kOffB, &tmB, &full[s], kb * 128, brow, pol_b);
+        tma_load_2d_hint(st + C::kOffSfbRaw, &tmSB, &full[s], kb * 16, brow, pol_b);
+        if (C::kDual) {
+          tma_load_2d_hint(st + C::kOffB + C::kBBytes, &tmB2, &full[s], kb * 128, brow, pol_b);
+          tma_load_2d_hint(st + C::kOffSfbRaw + C::kSfbRaw, &tmSB2, &full[s], kb * 16, brow, pol_b);
+        }
+        issued = kb + 1;
+      }
+      for (int kb = max(0, issued - C::kStages); kb < issued; ++kb)
+        if (!mbar_wait(&full[kb % C::kStages], (kb / C::kStages) & 1, kDrainBudget))
+          atomicOr(args.err, kErrDrain);
+    }
+  } else if (warp == 6) {
+    // ---- scale-factor regrouping: row-major [rows][16 B] -> per MMA step, 128-row blocks of
+    // 32 lines x 16 B (line m0 = rows m0, m0+32, m0+64, m0+96; 4 bytes each)
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % C::kStages;
+      const uint32_t ph = (kb / C::kStages) & 1;
+      if (!mbar_wait(&full[s], ph, budget)) {
+        if (lane == 0) atomicOr(args.err, kErrWaitMma);
+        break;
+      }
+      uint8_t* st = smem + s * C::kStageBytes;
+      const uint32_t* ra = reinterpret_cast<const uint32_t*>(st + C::kOffSfaRaw);
+      uint32_t* ta = reinterpret_cast<uint32_t*>(st + C::kOffSfa);
+#pragma unroll
+      for (int j = 0; j < C::kKStep; ++j)
+#pragma unroll
+        for (int m1 = 0; m1 < 4; ++m1) ta[j * 128 + lane * 4 + m1] = ra[(lane + 32 * m1) * 4 + j];
+#pragma unroll
+      for (int b = 0; b < C::kNB; ++b) {
+        const uint32_t* rb = reinterpret_cast<const uint32_t*>(st + C::kOffSfbRaw + b * C::kSfbRaw);
+        uint32_t* tb = reinterpret_cast<uint32_t*>(st + C::kOffSfb + b * C::kSfbT);
+#pragma unroll
+        for (int j = 0; j < C::kKStep; ++j)
+#pragma unroll
+          for (int a = 0; a < C::kBAtoms; ++a)
+#pragma unroll
+            for (int m1 = 0; m1 < 4; ++m1)
+              tb[(j * C::kBAtoms + a) * 128 + lane * 4 + m1] = rb[(a * 128 + lane + 32 * m1) * 4 + j];
+      }
+      fence_proxy_async_smem();   // generic-proxy writes -> visible to tcgen05.cp
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfready[s]);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(kBM, BN);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % C::kStages;
+        const uint32_t ph = (kb / C::kStages) & 1;
+        if (!mbar_wait(&sfready[s], ph, budget)) {
+          atomicOr(args.err, kErrWaitMma);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+        const uint32_t sfa = tmem + C::kAccCols + s * C::kSfCols;
+        const uint32_t sfb = sfa + C::kSfaCols;
+#pragma unroll
+        for (int j = 0; j < C::kKStep; ++j) {
+          tmem_cp_32x128b_x4(sfa + j * 4, sf_desc(st + C::kOffSfa + j * 512));
+#pragma unroll
+          for (int b = 0; b < C::kNB; ++b)
+#pragma unroll
+            for (int a = 0; a < C::kBAtoms; ++a)
+              tmem_cp_32x128b_x4(sfb + b * C::kSfbColsOne + j * (BN / 32) + a * 4,
+                                 sf_desc(st + C::kOffSfb + b * C::kSfbT + (j * C::kBAtoms + a) * 512));
+        }
+#pragma unroll
+        for (int j = 0; j < C::kKStep; ++j) {
+          const uint64_t ad = sw128_kmajor_desc(st + j * 32);
+          const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+          mma_nvf4(tmem, ad, sw128_kmajor_desc(st + C::kOffB + j * 32), idesc, sfa + j * 4,
+                   sfb + j * (BN / 32), acc);
+          if (C::kDual)
+            mma_nvf4(tmem + BN, ad, sw128_kmajor_desc(st + C::kOffB + C::kBBytes + j * 32), idesc,
+                     sfa + j * 4, sfb + C::kSfbColsOne + j * (BN / 32), acc);
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(accum);
+    }
+  } else {
+    // ---- epilogue: warps 2..5
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const bool row_ok = r < nrows;
+    const long long grow = static_cast<long long>(row0) + r;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const bool ok = mbar_wait(accum, 0, budget);
+    if (!ok) {
+      atomicOr(args.err, kErrWaitEpilogue);
+      if (!mbar_wait(accum, 0, kDrainBudget)) atomicOr(args.err, kErrDrain);
+    }
+    tc_fence_after();
+    const float rs = (args.row_scale != nullptr && row_ok) ? args.row_scale[grow] : 1.f;
+    if (ok) {
+      if constexpr (EPI == kFp4EpiF32Ss) {
+        const float alpha = rs * args.tensor_scale[args.tiles ? expert : 0];
+        float* orow = static_cast<float*>(args.out) + grow * args.ldo;
+        float ss = 0.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32cols(tq + c0, v);
+          tmem_ld_wait();
+          const int col = n0 + c0;
+          if (row_ok && col + 32 <= args.N) {
+            float4* o = reinterpret_cast<float4*>(orow + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 f = make_float4(__uint_as_float(v[4 * i]) * alpha, __uint_as_float(v[4 * i + 1]) * alpha,
+                                           __uint_as_float(v[4 * i + 2]) * alpha, __uint_as_float(v[4 * i + 3]) * alpha);
+              ss = fmaf(f.x, f.x, ss);
+              ss = fmaf(f.y, f.y, ss);
+              ss = fmaf(f.z, f.z, ss);
+              ss = fmaf(f.w, f.w, ss);
+              o[i] = f;
+            }
+          }
+        }
+        if (row_ok) args.ss[grow * args.ld_ss + blockIdx.x] = ss;
+      } else {  // kFp4EpiSwiGLUQuant
+        const int e = args.tiles ? expert : 0;
+        const float ag = rs * args.tensor_scale[e], au = rs * args.tensor_scale2[e];
+        uint8_t* crow = static_cast<uint8_t*>(args.out) + grow * (args.ldo / 2);
+        uint8_t* srow = args.out_scales + grow * (args.ldo / 16);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld_32cols(tq + c0, g);
+          tmem_ld_32cols(tq + BN + c0, u);
+          tmem_ld_wait();
+          const int col = n0 + c0;
+          if (row_ok && col + 32 <= args.N) {
+            uint2 q[2];
+            uint32_t sc[2];
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+              float h[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float a = __uint_as_float(g[blk * 16 + i]) * ag;
+                h[i] = a / (1.f + __expf(-a)) * (__uint_as_float(u[blk * 16 + i]) * au);
+              }
+              sc[blk] = nvfp4_quant16(h, 6.f, 1.f, recip, q[blk]);
+            }
+            *reinterpret_cast<uint4*>(crow + col / 2) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
+            *reinterpret_cast<uint16_t*>(srow + col / 16) = static_cast<uint16_t>(sc[0] | (sc[1] << 8));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int BN, int EPI>
+cudaError_t launch_fp4_one(const CUtensorMap* maps, const Fp4Args& a, int m_tiles, cudaStream_t s) {
+  using C = Fp4Cfg<BN, EPI>;
+  auto kern = gemm_fp4_kernel<BN, EPI>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid((a.N + BN - 1) / BN, m_tiles);
+  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  count_launch();
+  kern<<<grid, 224, C::kSmemBytes, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_fp4(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Args& a, int m_tiles,
+                            cudaStream_t s) {
+  switch (epi) {
+    case kFp4EpiF32Ss: return launch_fp4_one<kBNWide, kFp4EpiF32Ss>(maps, a, m_tiles, s);
+    case kFp4EpiSwiGLUQuant: return launch_fp4_one<kBNSwiGLU, kFp4EpiSwiGLUQuant>(maps, a, m_tiles, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lmoe

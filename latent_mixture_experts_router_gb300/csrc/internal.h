@@ -29,6 +29,11 @@ enum EpiKind : int {
   kEpiSwiGLU = 2,   // two accumulators a, b -> bf16 silu(a) * b
 };
 
+enum Fp4EpiKind : int {
+  kFp4EpiF32Ss = 0,         // alpha * acc as fp32 + per-row partial sums of squares
+  kFp4EpiSwiGLUQuant = 1,   // silu(alpha_g a) * (alpha_u b), requantised to NVFP4 (scale 1)
+};
+
 // One M tile of a grouped GEMM: rows [row0, row0 + nrows) of A, all of expert `expert`.
 struct Tile {
   int expert, row0, nrows, pad;
@@ -49,6 +54,43 @@ struct GemmArgs {
   unsigned* err;           // device error word
   long long budget;        // wait budget, SM cycles
 };
+
+struct Fp4Args {
+  int M;                     // rows of A when tiles == nullptr
+  int N;                     // output columns (rows of one expert's B)
+  int num_kb;                // K / 256
+  const Tile* tiles;
+  const int* n_tiles;
+  void* out;                 // fp32 [rows, ldo] (kFp4EpiF32Ss) or codes [rows, ldo/2] (quant)
+  long long ldo;             // output row length in elements
+  uint8_t* out_scales;       // quant: E4M3 block scales [rows, ldo/16]
+  float* ss;                 // kFp4EpiF32Ss: [rows, ld_ss] partial sums of squares
+  int ld_ss;
+  const float* row_scale;    // per A row fp32 scale, or nullptr (1)
+  const float* tensor_scale; // per expert (grouped) or [0]: scale of B
+  const float* tensor_scale2;// quant: scale of B2 (up)
+  unsigned* err;
+  long long budget;
+};
+
+// NVFP4 GEMM; maps = {A codes, A scales, B codes, B scales, B2 codes, B2 scales}.
+cudaError_t launch_gemm_fp4(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Args& a, int m_tiles,
+                            cudaStream_t s);
+
+// NVFP4 row kernels (rowops.cu)
+cudaError_t launch_prenorm_nvfp4(const void* x, bool x_f32, const float* g_pre, int T, int D,
+                                 float eps, __nv_bfloat16* xa, int xa_cols, uint8_t* codes,
+                                 uint8_t* scales, float* s_row, cudaStream_t s);
+cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int ld_ss,
+                                          const float* g_pool, const int32_t* row_of, int T, int L,
+                                          int k, float eps, uint8_t* codes, uint8_t* scales,
+                                          float* s_rows, cudaStream_t s);
+cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, const int32_t* row_of,
+                                 const int32_t* idx, const float* w, const float* g_expert, int T,
+                                 int L, int k, float eps, uint8_t* codes, uint8_t* scales,
+                                 float* s_row, cudaStream_t s);
+cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool row_scale,
+                                  uint8_t* codes, uint8_t* scales, float* s_row, cudaStream_t s);
 
 // Counts every kernel launch of the library (lmoe_kernel_launches).
 void count_launch();

@@ -22,6 +22,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "nvfp4.cuh"
 #include "ptx.cuh"
 
 namespace lmoe {
@@ -401,6 +402,213 @@ __global__ void weight_split_kernel(const float* __restrict__ W, long long rows,
   }
 }
 
+// ------------------------------------------------------------------ NVFP4 rows
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    float t = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+    if (l == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+__device__ __forceinline__ void load_recip(float* recip) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) recip[i] = c_e4m3_recip.v[i];
+}
+
+// Quantises the K values of `buf` (shared memory) with row scale s into `nrows` destination
+// rows (codes row pitch K/2 bytes, scales row pitch K/16 bytes).
+__device__ __forceinline__ void quantize_row_to(const float* buf, int K, float s, const float* recip,
+                                                uint8_t* codes, uint8_t* scales, const int* rows,
+                                                int nrows) {
+  const float six_s = __fmul_rn(6.f, s), inv_s = __fdiv_rn(1.f, s);
+  for (int b = threadIdx.x; b < K / 16; b += blockDim.x) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = buf[b * 16 + i];
+    uint2 q;
+    const uint32_t sc = nvfp4_quant16(v, six_s, inv_s, recip, q);
+    for (int j = 0; j < nrows; ++j) {
+      const long long r = rows[j];
+      *reinterpret_cast<uint2*>(codes + r * (K / 2) + b * 8) = q;
+      scales[r * (K / 16) + b] = static_cast<uint8_t>(sc);
+    }
+  }
+}
+
+// Pre-norm that also emits xn in NVFP4 (row scale per token) for the pooler, besides the
+// bf16 hi/lo pair the router reads.  Dynamic smem: D + 256 floats.
+__global__ void __launch_bounds__(kRowThreads) prenorm_nvfp4_kernel(
+    const void* __restrict__ x, int x_f32, const float* __restrict__ g, int D, float eps,
+    __nv_bfloat16* __restrict__ xa, int xa_cols, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ s_row) {
+  extern __shared__ float dyn[];
+  float* buf = dyn;
+  float* recip = dyn + D;
+  __shared__ float red[33];
+  __shared__ int s_r;
+  load_recip(recip);
+  const long long t = blockIdx.x;
+  const long long xoff = t * D;
+  float ss = 0.f;
+  for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
+    float v[8];
+    load8(x, x_f32, xoff + i, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
+  }
+  const float rs = rsqrtf(block_sum(ss, red) / static_cast<float>(D) + eps);
+  __nv_bfloat16* row = xa + t * xa_cols;
+  float amax = 0.f;
+  for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
+    float v[8], gg[8], hi[8], lo[8];
+    load8(x, x_f32, xoff + i, v);
+    load8_f32(g + i, gg);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float xn = v[j] * rs * gg[j];
+      buf[i + j] = xn;
+      amax = fmaxf(amax, fabsf(xn));
+      hi[j] = bf16_round(xn);
+      lo[j] = xn - hi[j];
+    }
+    store8_bf16(row + i, hi);
+    store8_bf16(row + D + i, lo);
+  }
+  const float s = nvfp4_row_scale(block_max(amax, red));
+  if (threadIdx.x == 0) {
+    s_row[t] = s;
+    s_r = static_cast<int>(t);
+  }
+  __syncthreads();
+  quantize_row_to(buf, D, s, recip, codes, scales, &s_r, 1);
+}
+
+// Pool norm whose output is quantised once (row scale per token) and written to the token's
+// k expert rows.  Dynamic smem: L + 256 floats.
+__global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
+    const float* __restrict__ p, const float* __restrict__ ss_p, int ld_ss, const float* __restrict__ g,
+    const int32_t* __restrict__ row_of, int L, int k, float eps, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ s_rows) {
+  extern __shared__ float dyn[];
+  float* buf = dyn;
+  float* recip = dyn + L;
+  __shared__ float red[33];
+  __shared__ float s_rs;
+  __shared__ int s_rowsj[16];
+  load_recip(recip);
+  const long long t = blockIdx.x;
+  if (threadIdx.x == 0) {
+    float ss = 0.f;
+    for (int q = 0; q < ld_ss; ++q) ss += ss_p[t * ld_ss + q];
+    s_rs = rsqrtf(ss / static_cast<float>(L) + eps);
+  }
+  if (threadIdx.x < k) s_rowsj[threadIdx.x] = row_of[t * k + threadIdx.x];
+  __syncthreads();
+  const float rs = s_rs;
+  float amax = 0.f;
+  for (int i = threadIdx.x * 8; i < L; i += kRowThreads * 8) {
+    float v[8], gg[8];
+    load8_f32(p + t * L + i, v);
+    load8_f32(g + i, gg);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float h = v[j] * rs * gg[j];
+      buf[i + j] = h;
+      amax = fmaxf(amax, fabsf(h));
+    }
+  }
+  const float s = nvfp4_row_scale(block_max(amax, red));
+  if (threadIdx.x < k) s_rows[s_rowsj[threadIdx.x]] = s;
+  quantize_row_to(buf, L, s, recip, codes, scales, s_rowsj, k);
+}
+
+// Combine whose output c is quantised (row scale per token) for the unpooler.
+// Dynamic smem: L + 256 floats.
+__global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
+    const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
+    const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const float* __restrict__ w,
+    const float* __restrict__ g_expert, int L, int k, float eps, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ s_row) {
+  extern __shared__ float dyn[];
+  float* buf = dyn;
+  float* recip = dyn + L;
+  __shared__ float red[33];
+  __shared__ float s_coef[16];
+  __shared__ int s_rowj[16], s_e[16];
+  __shared__ int s_t;
+  load_recip(recip);
+  const long long t = blockIdx.x;
+  if (threadIdx.x < k) {
+    const int j = threadIdx.x;
+    const int row = row_of[t * k + j];
+    float ss = 0.f;
+    for (int q = 0; q < ld_ss; ++q) ss += ss_y[static_cast<long long>(row) * ld_ss + q];
+    s_coef[j] = w[t * k + j] * rsqrtf(ss / static_cast<float>(L) + eps);
+    s_rowj[j] = row;
+    s_e[j] = idx[t * k + j];
+  }
+  __syncthreads();
+  float amax = 0.f;
+  for (int i = threadIdx.x * 8; i < L; i += kRowThreads * 8) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < k; ++j) {
+      float v[8], gg[8];
+      load8_f32(y + static_cast<long long>(s_rowj[j]) * L + i, v);
+      load8_f32(g_expert + static_cast<long long>(s_e[j]) * L + i, gg);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_coef[j], v[q] * gg[q], acc[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      buf[i + q] = acc[q];
+      amax = fmaxf(amax, fabsf(acc[q]));
+    }
+  }
+  const float s = nvfp4_row_scale(block_max(amax, red));
+  if (threadIdx.x == 0) {
+    s_row[t] = s;
+    s_t = static_cast<int>(t);
+  }
+  __syncthreads();
+  quantize_row_to(buf, L, s, recip, codes, scales, &s_t, 1);
+}
+
+// Stand-alone quantiser: one CTA per row of src [rows, K] fp32.
+__global__ void __launch_bounds__(kRowThreads) quantize_nvfp4_kernel(
+    const float* __restrict__ src, int K, int row_scale, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ s_row) {
+  extern __shared__ float dyn[];
+  float* buf = dyn;
+  float* recip = dyn + K;
+  __shared__ float red[33];
+  __shared__ int s_t;
+  load_recip(recip);
+  const long long t = blockIdx.x;
+  float amax = 0.f;
+  for (int i = threadIdx.x; i < K; i += kRowThreads) {
+    const float v = src[t * K + i];
+    buf[i] = v;
+    amax = fmaxf(amax, fabsf(v));
+  }
+  amax = block_max(amax, red);
+  const float s = row_scale ? nvfp4_row_scale(amax) : 1.f;
+  if (threadIdx.x == 0) {
+    if (s_row) s_row[t] = s;
+    s_t = static_cast<int>(t);
+  }
+  __syncthreads();
+  quantize_row_to(buf, K, s, recip, codes, scales, &s_t, 1);
+}
+
 // ------------------------------------------------------------------ wait self-test
 // One thread waits on a barrier that is initialised for one arrival that never comes.
 __global__ void wait_selftest_kernel(long long budget, unsigned* err) {
@@ -415,6 +623,75 @@ __global__ void wait_selftest_kernel(long long budget, unsigned* err) {
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
+cudaError_t launch_prenorm_nvfp4(const void* x, bool x_f32, const float* g_pre, int T, int D,
+                                 float eps, __nv_bfloat16* xa, int xa_cols, uint8_t* codes,
+                                 uint8_t* scales, float* s_row, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const size_t smem = (static_cast<size_t>(D) + 256) * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(prenorm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  count_launch();
+  prenorm_nvfp4_kernel<<<T, kRowThreads, smem, s>>>(x, x_f32 ? 1 : 0, g_pre, D, eps, xa, xa_cols, codes,
+                                                    scales, s_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int ld_ss,
+                                          const float* g_pool, const int32_t* row_of, int T, int L,
+                                          int k, float eps, uint8_t* codes, uint8_t* scales,
+                                          float* s_rows, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const size_t smem = (static_cast<size_t>(L) + 256) * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(poolnorm_scatter_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  count_launch();
+  poolnorm_scatter_nvfp4_kernel<<<T, kRowThreads, smem, s>>>(p, ss_p, ld_ss, g_pool, row_of, L, k, eps,
+                                                             codes, scales, s_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, const int32_t* row_of,
+                                 const int32_t* idx, const float* w, const float* g_expert, int T,
+                                 int L, int k, float eps, uint8_t* codes, uint8_t* scales,
+                                 float* s_row, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const size_t smem = (static_cast<size_t>(L) + 256) * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(combine_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  count_launch();
+  combine_nvfp4_kernel<<<T, kRowThreads, smem, s>>>(y, ss_y, ld_ss, row_of, idx, w, g_expert, L, k, eps,
+                                                    codes, scales, s_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool row_scale,
+                                  uint8_t* codes, uint8_t* scales, float* s_row, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const size_t smem = (static_cast<size_t>(K) + 256) * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(quantize_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  count_launch();
+  quantize_nvfp4_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(src, K, row_scale ? 1 : 0,
+                                                                              codes, scales, s_row);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s) {
   count_launch();
   wait_selftest_kernel<<<1, 32, 0, s>>>(budget, err);

@@ -68,12 +68,15 @@ def views(blk, cfg) -> dict:
         "tok_of": get("tok_of", R, torch.int32),
         "n_tiles": get("n_tiles", 1, torch.int32),
         "p": get("p", T * L, torch.float32).view(T, L),
-        "xe": get("xe", R * L, bf).view(R, L),
-        "h": get("h", R * I, bf).view(R, I),
+        "xe": get("xe", R * L, bf).view(R, L) if cfg.weight_dtype != "nvfp4" else None,
+        "h": get("h", R * I, bf).view(R, I) if cfg.weight_dtype != "nvfp4" else None,
         "y": get("y", R * L, torch.float32).view(R, L),
-        "c": get("c", T * L, bf).view(T, L),
+        "c": get("c", T * L, bf).view(T, L) if cfg.weight_dtype != "nvfp4" else None,
         "u": get("u", T * D, torch.float32).view(T, D),
     }
+    if cfg.weight_dtype == "nvfp4":   # xe, h, c hold packed codes there (see the layout)
+        for name in ("xe", "h", "c"):
+            v.pop(name)
     return {name: t.to(torch.float64 if t.dtype in (bf, torch.float32) else torch.int64).cpu().numpy()
             for name, t in v.items()}
 
