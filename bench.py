@@ -35,7 +35,7 @@ import torch  # noqa: E402
 
 import workloads  # noqa: E402
 
-METRIC = "latent-MoE block tokens/s (BF16) at Muse shape"
+METRIC = "latent-MoE block tokens/s (BF16, NVFP4) at Muse shape; % of tensor/HBM roofline"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -132,29 +132,42 @@ def stage_costs(w: workloads.Workload, counts: np.ndarray):
     used = int(np.count_nonzero(counts))
     bf, f4 = 2, 4
     xb = 4 if w.act == "f32" else 2
+    # bytes per element of the pooler/expert/unpooler weights and of their activation operands:
+    # bf16, or NVFP4 = half a byte of code + one E4M3 byte per 16 elements
+    wb = 0.5625 if w.weights == "nvfp4" else 2
+    ab = 0.5625 if w.weights == "nvfp4" else 2
     c = {
-        "prenorm": (T * D * xb + T * 2 * D * bf, 0),
+        "prenorm": (T * D * xb + T * 2 * D * bf + (T * D * ab if w.weights == "nvfp4" else 0), 0),
         "router": (E * D * bf + T * 2 * D * bf + T * E * f4, 2 * T * E * 2 * D),
-        "pooler": (L * D * bf + T * D * bf + T * L * f4, 2 * T * L * D),
-        "gate_up": (used * 2 * I * L * bf + R * L * bf + R * I * bf, 2 * R * L * 2 * I),
-        "down": (used * L * I * bf + R * I * bf + R * L * f4, 2 * R * I * L),
-        "unpooler": (D * L * bf + T * L * bf + T * D * f4, 2 * T * D * L),
-        "combine": (R * L * f4 + T * L * bf, 0),
+        "pooler": (L * D * wb + T * D * ab + T * L * f4, 2 * T * L * D),
+        "gate_up": (used * 2 * I * L * wb + R * L * ab + R * I * ab, 2 * R * L * 2 * I),
+        "down": (used * L * I * wb + R * I * ab + R * L * f4, 2 * R * I * L),
+        "unpooler": (D * L * wb + T * L * ab + T * D * f4, 2 * T * D * L),
+        "combine": (R * L * f4 + T * L * ab, 0),
         "postnorm": (T * D * (xb + f4 + 4), 0),
     }
-    return c, used
+    return {kk: (int(b), f) for kk, (b, f) in c.items()}, used
 
 
-def roofline(stage: str, dur_ms: float, costs: dict, pk: dict, pk_kind: str, sustained: bool):
+FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 / BF16 tensor ratio of GB300
+
+
+def roofline(stage: str, dur_ms: float, costs: dict, pk: dict, pk_kind: str, sustained: bool,
+             fp4: bool = False):
     nbytes, flops = costs[stage]
     hbm = pk["hbm_gbs"]
     tf = pk["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    fp4 = fp4 and stage not in ("router",)
+    if fp4:
+        tf = round(tf * FP4_OVER_BF16, 1)
     t_hbm = nbytes / (hbm * 1e9)
     t_tc = flops / (tf * 1e12) if flops else 0.0
     if t_tc > t_hbm:
         ach = flops / (dur_ms * 1e-3) / 1e12
         return {"bound": "tensor", "kernel": stage, "achieved": round(ach, 2), "peak": tf, "unit": "TFLOP/s",
-                "frac": round(ach / tf, 4), "peak_source": f"{pk_kind} bf16_tflops{'_sustained' if sustained else ''}",
+                "frac": round(ach / tf, 4),
+                "peak_source": f"{pk_kind} bf16_tflops{'_sustained' if sustained else ''}"
+                               + (" x 6 (nominal fp4/bf16 ratio)" if fp4 else ""),
                 "algorithmic_flop": flops, "traffic": None}
     ach = nbytes / (dur_ms * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": stage, "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
@@ -369,7 +382,8 @@ def run_ours(args, ws, rank, local):
     line = {
         "metric": METRIC, "value": round(ws * T * args.steps / (ms_max * 1e-3), 1), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4" if w.weights == "nvfp4" else "bf16",
         "data": "synthetic (seeded counter-based generator; random-init weights of the Muse layer shapes)",
         "config": {"workload": w.name, "T_per_gpu": T, "d_model": w.D, "d_latent": w.L, "n_experts": w.E,
                    "d_ff": w.I, "top_k": w.k, "routing": w.routing, "weights": w.weights,
@@ -378,7 +392,8 @@ def run_ours(args, ws, rank, local):
                          f"{sum(b for b, _ in costs.values()) / 1e9:.1f} GB (129 MB L2)"},
         "tflops": round(total_flops / (ms_step * 1e-3) / 1e12, 2),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-        "roofline": {**roofline(dom, stage_ms[dom], costs, pk, pk_kind, sustained=False),
+        "roofline": {**roofline(dom, stage_ms[dom], costs, pk, pk_kind, sustained=False,
+                                fp4=w.weights == "nvfp4"),
                      "traffic": measured_traffic(dom, w, used)},
         "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
     }

@@ -65,3 +65,41 @@ def test_full_size_bf16(cuda, name, sample):
     print(name, rep)
     assert rep.ok, str(rep)
     del out, idx, blk, inp, v
+
+
+@pytest.mark.parametrize("name,T,sample", [("prefill_nvfp4", None, [0, 1234, 4095]),
+                                           ("decode_nvfp4_hot", 1, [0]),
+                                           ("decode_nvfp4_hot", 8, [0, 7]),
+                                           ("decode_nvfp4_hot", 32, [3, 31]),
+                                           ("decode_nvfp4_hot", 128, [0, 127]),
+                                           ("decode_nvfp4_hot", 512, [5, 300, 511])])
+def test_full_size_nvfp4(cuda, name, T, sample):
+    from oracle.compare import TOL_NVFP4
+    w = workloads.WORKLOADS[name]
+    if T is not None:
+        w = w.with_tokens(T)
+    inp = workloads.make_inputs(w, cuda)
+    out, idx, blk, cfg = run(inp)
+    gidx = idx.cpu().numpy()
+    P = oracle.params_from_inputs(inp)
+    x = inp.x.double().cpu().numpy()
+    forced = None if inp.forced_idx is None else inp.forced_idx.cpu().numpy()
+    if forced is not None:
+        assert np.array_equal(gidx, forced)
+    else:
+        _, tr = _full_router(inp, P)
+        exact, near, swaps, bad = classify_topk(gidx, tr, w.k)
+        print(f"{w.name}: top-k exact {int(exact.sum())}/{w.T}, near ties {len(near)}, swaps {len(swaps)}")
+        assert not bad, bad[:10]
+    v = views(blk, cfg)
+    counts, offsets, row_of, tok_of = expected_permutation(gidx, w.E)
+    assert np.array_equal(v["row_of"], row_of) and np.array_equal(v["tok_of"], tok_of)
+    xs = x[sample]
+    fs = None if forced is None else forced[sample]
+    tr_s = oracle.Trace()
+    ref = oracle.forward_batched(xs, P, w.k, forced_idx=fs, trace=tr_s)
+    rep = compare_block(out.cpu().numpy()[sample], gidx[sample], xs, P, w.k, TOL_NVFP4, tr=tr_s,
+                        ref=ref, forced_idx=fs)
+    print(w.name, rep)
+    assert rep.ok, str(rep)
+    del out, idx, blk, inp, v
