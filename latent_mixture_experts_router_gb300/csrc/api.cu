@@ -201,7 +201,7 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
                      long long b_cols, const void* B2, int N, int num_kb,
                      const Tile* tiles, const int* n_tiles, int m_tiles, void* out,
                      long long ldo, float* ss, int ld_ss, unsigned* err, long long budget,
-                     cudaStream_t s) {
+                     cudaStream_t s, long long rows_per_b) {
   const unsigned bn = epi == kEpiSwiGLU ? kBNSwiGLU : kBNWide;
   CUtensorMap ta, tb, tb2;
   if (!encode_bf16_2d(&ta, A, a_cols_used, a_rows, a_row_stride_elems * 2, kBK, kBM))
@@ -223,6 +223,7 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   a.ld_ss = ld_ss;
   a.err = err;
   a.budget = budget;
+  a.b_stream_once = rows_per_b <= kBM;
   LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s));
   return LMOE_OK;
 }
@@ -238,7 +239,7 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                          const int* n_tiles, int m_tiles, void* out, long long ldo,
                          uint8_t* out_scales, float* ss, int ld_ss, const float* row_scale,
                          const float* ts, const float* ts2, unsigned* err, long long budget,
-                         cudaStream_t s) {
+                         cudaStream_t s, long long rows_per_b) {
   const unsigned bn = epi == kFp4EpiSwiGLUQuant ? kBNSwiGLU : kBNWide;
   CUtensorMap maps[6];
   const unsigned long long kc = K / 2, ks = K / 16;
@@ -268,6 +269,7 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
   a.tensor_scale2 = ts2;
   a.err = err;
   a.budget = budget;
+  a.b_stream_once = rows_per_b <= kBM;
   LMOE_CUDA(launch_gemm_fp4(epi, maps, a, m_tiles, s));
   return LMOE_OK;
 }
@@ -390,7 +392,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   const int m_tiles_T = cdiv(T, kBM);
   st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
                 xa_cols / kBK, nullptr, nullptr, m_tiles_T, logits, L.ld_logits, nullptr, 0, err,
-                budget, s);
+                budget, s, T);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_TOPK);
   // S3 top-k + softmax
@@ -414,7 +416,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     LMOE_MARK(LMOE_STAGE_POOLER);
     // S5 pooler p = s_x * s_W * (Q(xn) . W_pool^T), block-scaled FP4 MMA
     st = run_gemm_fp4(kFp4EpiF32Ss, xq, T, D, op(q4[0]), Ld, nullptr, Ld, nullptr, nullptr, m_tiles_T,
-                      p, Ld, nullptr, ss_p, L.ld_ss_p, xq_s, q4[0]->tensor_scale, nullptr, err, budget, s);
+                      p, Ld, nullptr, ss_p, L.ld_ss_p, xq_s, q4[0]->tensor_scale, nullptr, err, budget, s, T);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_POOLNORM);
     // S6 pool norm, quantised per token, copied to the k expert rows
@@ -425,13 +427,13 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     const Fp4Operand up = op(q4[2]);
     st = run_gemm_fp4(kFp4EpiSwiGLUQuant, xeq, R, Ld, op(q4[1]), 1LL * E * I, &up, I, tiles, n_tiles,
                       L.max_tiles, wsb + L.pub.h, I, wsb + L.pub.h_scale, nullptr, 0, xe_s,
-                      q4[1]->tensor_scale, q4[2]->tensor_scale, err, budget, s);
+                      q4[1]->tensor_scale, q4[2]->tensor_scale, err, budget, s, R / E);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_DOWN);
     // S8 grouped down (fp32 y) with per-row partial sums of squares
     st = run_gemm_fp4(kFp4EpiF32Ss, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
                       L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
-                      nullptr, err, budget, s);
+                      nullptr, err, budget, s, R / E);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_COMBINE);
     // S9 combine, c quantised per token
@@ -440,14 +442,14 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     LMOE_MARK(LMOE_STAGE_UNPOOLER);
     // S10 unpooler u = s_c * s_W * (Q(c) . W_unpool^T)
     st = run_gemm_fp4(kFp4EpiF32Ss, cq, T, Ld, op(q4[4]), D, nullptr, D, nullptr, nullptr, m_tiles_T, u,
-                      D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s);
+                      D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s, T);
     if (st != LMOE_OK) return st;
   } else {
   LMOE_MARK(LMOE_STAGE_POOLER);
   // S5 pooler p = xn_hi . W_pool^T, with row partial sums of squares
   const int pool_k = f32w ? 3 * D : D;
   st = run_gemm(kEpiF32Ss, xa, T, pool_k, xa_cols, wp, Ld, pool_k, nullptr, Ld, pool_k / kBK,
-                nullptr, nullptr, m_tiles_T, p, Ld, ss_p, L.ld_ss_p, err, budget, s);
+                nullptr, nullptr, m_tiles_T, p, Ld, ss_p, L.ld_ss_p, err, budget, s, T);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_POOLNORM);
   // S6 pool norm, scattered to the k expert-contiguous rows of each token
@@ -455,12 +457,12 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   LMOE_MARK(LMOE_STAGE_GATE_UP);
   // S7 grouped gate/up + SwiGLU
   st = run_gemm(kEpiSwiGLU, xe, R, Ld, Ld, wg, 1LL * E * I, 1LL * wsplit * Ld, wu, I,
-                wsplit * Ld / kBK, tiles, n_tiles, L.max_tiles, h, I, nullptr, 0, err, budget, s);
+                wsplit * Ld / kBK, tiles, n_tiles, L.max_tiles, h, I, nullptr, 0, err, budget, s, R / E);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_DOWN);
   // S8 grouped down (fp32 y), with per-row partial sums of squares
   st = run_gemm(kEpiF32Ss, h, R, I, I, wd, 1LL * E * Ld, 1LL * wsplit * I, nullptr, Ld,
-                wsplit * I / kBK, tiles, n_tiles, L.max_tiles, y, Ld, ss_y, L.ld_ss_y, err, budget, s);
+                wsplit * I / kBK, tiles, n_tiles, L.max_tiles, y, Ld, ss_y, L.ld_ss_y, err, budget, s, R / E);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_COMBINE);
   // S9 combine: per-expert RMSNorm, routing weight, fp32 sum in slot order
@@ -468,7 +470,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   LMOE_MARK(LMOE_STAGE_UNPOOLER);
   // S10 unpooler u = c . W_unpool^T with row partial sums of squares
   st = run_gemm(kEpiF32Ss, c, T, Ld, Ld, wun, D, 1LL * wsplit * Ld, nullptr, D, wsplit * Ld / kBK,
-                nullptr, nullptr, m_tiles_T, u, D, ss_u, L.ld_ss_u, err, budget, s);
+                nullptr, nullptr, m_tiles_T, u, D, ss_u, L.ld_ss_u, err, budget, s, T);
   if (st != LMOE_OK) return st;
   }
   LMOE_MARK(LMOE_STAGE_POSTNORM);

@@ -1,26 +1,31 @@
-// gemm.cu — grouped BF16 GEMM on the 5th-generation tensor cores (tcgen05).
+// gemm.cu — grouped BF16 GEMM on the 5th-generation tensor cores (tcgen05), persistent.
 //
 // out[r, n] = sum_kb A[r, kA(kb)] * B[e*N + n, kB(kb)]  for the rows r of each M tile,
 // where e is the tile's expert (0 for a plain GEMM) and the k coordinates of A and B
 // wrap at their own periods, so that one operand can be paired with a hi/lo split of
-// the other (K-concatenation without copying).  A and B are K-major bf16 and are
-// staged in shared memory by TMA (128-byte swizzle); the fp32 accumulator lives
-// in tensor memory.  One CTA computes one 128 x BN output tile with three roles:
-//   warp 0, lane 0   TMA producer over a STAGES-deep ring of smem slots
-//   warp 1, lane 0   tcgen05.mma issuer (warp 1 also owns the TMEM allocation)
+// the other (K-concatenation without copying).  A and B are K-major bf16 staged in shared
+// memory by TMA (128-byte swizzle); fp32 accumulators live in tensor memory.
+//
+// One CTA per SM walks the 128 x BN output tiles in grouped order (groups of 16 M tiles,
+// M fastest inside a group, ids strided by the grid size), with three roles:
+//   warp 0, lane 0   TMA producer over a 4-deep ring of smem stages (the ring runs on
+//                    across tiles)
+//   warp 1, lane 0   tcgen05.mma issuer; warp 1 also owns the TMEM allocation (512 columns:
+//                    two accumulator buffers, so the next tile's MMAs run while the
+//                    epilogue drains the previous one)
 //   warps 2..5       epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (one row each)
 // Epilogues (one per use in the latent-MoE block):
 //   kEpiF32     fp32 logits (router)
-//   kEpiF32Ss   fp32 output plus, per row, the partial sum of squares of the
-//               values of this tile's columns.  The row's RMS is finished later from
-//               these partials, so no kernel re-reads the row to normalise it (the
-//               "fused per-expert post-norm" of the LMSYS Muse Spark Open post: each
-//               second-GEMM tile accumulates a partial sum of squares of the values it
-//               holds in registers; here partials go to [rows, N/BN] without atomics, so
-//               the result is deterministic).  The outputs stay fp32 because they are
-//               not tensor-core operands: rounding them would only add error.
-//   kEpiSwiGLU  gate and up tiles of the same columns in one CTA (two B loads per
-//               stage, two accumulators), output bf16 silu(a) * b.
+//   kEpiF32Ss   fp32 output plus, per row, the partial sum of squares of the values of
+//               this tile's columns.  The row's RMS is finished later from these partials,
+//               so no kernel re-reads the row to normalise it (the "fused per-expert
+//               post-norm" of the LMSYS Muse Spark Open post: each second-GEMM tile
+//               accumulates a partial sum of squares of the values it holds in registers;
+//               here partials go to [rows, N/BN] without atomics, so the result is
+//               deterministic).  The outputs stay fp32 because they are not tensor-core
+//               operands: rounding them would only add error.
+//   kEpiSwiGLU  gate and up tiles of the same columns in one CTA (two B loads per stage,
+//               two accumulators), output bf16 silu(a) * b.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -33,15 +38,39 @@ struct GemmCfg {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes * (kDual ? 2 : 1);
-  static constexpr int kAccCols = kDual ? 2 * BN : BN;
-  static constexpr uint32_t kTmemCols = kAccCols <= 32    ? 32
-                                        : kAccCols <= 64  ? 64
-                                        : kAccCols <= 128 ? 128
-                                        : kAccCols <= 256 ? 256
-                                                          : 512;
+  static constexpr int kAccCols = kDual ? 2 * BN : BN;   // one accumulator buffer
+  static constexpr uint32_t kTmemCols = 512;              // two buffers
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static_assert(2 * kAccCols <= 512, "two accumulator buffers in tensor memory");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
+};
+
+// The tile sequence every role of a CTA walks: ids blockIdx.x, + gridDim.x, ...; ids that
+// fall in the padding of the last raster group are skipped by all roles alike.
+struct TileWalk {
+  int total_m, nt, n_ids;
+  LMOE_DEV TileWalk(const GemmArgs& a, int bn) {
+    total_m = a.tiles != nullptr ? *a.n_tiles : (a.M + kBM - 1) / kBM;
+    nt = (a.N + bn - 1) / bn;
+    n_ids = ((total_m + kRasterGroup - 1) / kRasterGroup) * kRasterGroup * nt;
+  }
+  // (expert, first row, rows, N tile) of tile id; false if the id is padding
+  LMOE_DEV bool at(const GemmArgs& a, int id, int& expert, int& row0, int& nrows, int& ntile) const {
+    int mt;
+    if (!grouped_tile(id, total_m, nt, kRasterGroup, mt, ntile)) return false;
+    if (a.tiles != nullptr) {
+      const Tile t = a.tiles[mt];
+      expert = t.expert;
+      row0 = t.row0;
+      nrows = t.nrows;
+    } else {
+      expert = 0;
+      row0 = mt * kBM;
+      nrows = min(kBM, a.M - row0);
+    }
+    return nrows > 0;
+  }
 };
 
 template <int BN, int EPI>
@@ -55,34 +84,25 @@ __global__ void __launch_bounds__(192, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
   uint64_t* empty = full + C::kStages;
-  uint64_t* accum = empty + C::kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
-  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  uint64_t* acc_full = empty + C::kStages;    // [2] MMA -> epilogue
+  uint64_t* acc_empty = acc_full + 2;         // [2] epilogue (4 warps) -> MMA
+  uint64_t* mma_done = acc_empty + 2;         // every MMA of this CTA has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
-  // ---- which tile
-  int expert = 0, row0, nrows;
-  if (args.tiles != nullptr) {
-    if (static_cast<int>(blockIdx.y) >= *args.n_tiles) return;
-    const Tile t = args.tiles[blockIdx.y];
-    expert = t.expert;
-    row0 = t.row0;
-    nrows = t.nrows;
-  } else {
-    row0 = blockIdx.y * kBM;
-    nrows = min(kBM, args.M - row0);
-  }
-  if (nrows <= 0) return;
-  const int n0 = blockIdx.x * BN;
+  const TileWalk walk(args, BN);
+  if (static_cast<int>(blockIdx.x) >= walk.n_ids) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // ---- setup
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum, 1);
-    *abort_flag = 0;
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(mma_done, 1);
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -101,73 +121,99 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA producer
-      const int brow = expert * args.N + n0;
-      const uint64_t pol_b = policy_evict_first();  // weights: streamed once per tile
-      int issued = 0;
-      for (int kb = 0; kb < args.num_kb; ++kb) {
-        const int s = kb % C::kStages;
-        const uint32_t ph = (kb / C::kStages) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, budget)) {
-          atomicOr(args.err, kErrWaitProducer);
-          atomicExch(abort_flag, 1);
-          break;
+      const uint64_t pol_b = args.b_stream_once ? policy_evict_first() : policy_evict_normal();
+      int it = 0;
+      bool ok = true;
+      for (int id = blockIdx.x; ok && id < walk.n_ids; id += gridDim.x) {
+        int expert, row0, nrows, ntile;
+        if (!walk.at(args, id, expert, row0, nrows, ntile)) continue;
+        const int brow = expert * args.N + ntile * BN;
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          const int s = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, budget)) {
+            atomicOr(args.err, kErrWaitProducer);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + s * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+          tma_load_2d(sa, &tmA, &full[s], (kb % args.kb_period_a) * kBK, row0);
+          const int kbb = (kb % args.kb_period_b) * kBK;
+          tma_load_2d_hint(sa + C::kABytes, &tmB, &full[s], kbb, brow, pol_b);
+          if (C::kDual) tma_load_2d_hint(sa + C::kABytes + C::kBBytes, &tmB2, &full[s], kbb, brow, pol_b);
+          ++it;
         }
-        uint8_t* sa = smem + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-        tma_load_2d(sa, &tmA, &full[s], (kb % args.kb_period_a) * kBK, row0);
-        const int kbb = (kb % args.kb_period_b) * kBK;
-        tma_load_2d_hint(sa + C::kABytes, &tmB, &full[s], kbb, brow, pol_b);
-        if (C::kDual) tma_load_2d_hint(sa + C::kABytes + C::kBBytes, &tmB2, &full[s], kbb, brow, pol_b);
-        issued = kb + 1;
       }
       // before leaving, let every copy this thread issued land (drain budget, independent
       // of the caller's: the CTA must not exit with a copy still writing its smem)
-      for (int kb = max(0, issued - C::kStages); kb < issued; ++kb)
-        if (!mbar_wait(&full[kb % C::kStages], (kb / C::kStages) & 1, kDrainBudget))
+      for (int j = max(0, it - C::kStages); j < it; ++j)
+        if (!mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, kDrainBudget))
           atomicOr(args.err, kErrDrain);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---- MMA issuer
       constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
-      for (int kb = 0; kb < args.num_kb; ++kb) {
-        const int s = kb % C::kStages;
-        const uint32_t ph = (kb / C::kStages) & 1;
-        if (!mbar_wait(&full[s], ph, budget)) {
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int id = blockIdx.x; ok && id < walk.n_ids; id += gridDim.x) {
+        int expert, row0, nrows, ntile;
+        if (!walk.at(args, id, expert, row0, nrows, ntile)) continue;
+        const int buf = tc & 1;
+        const uint32_t use = (tc >> 1) & 1;
+        if (!mbar_wait(&acc_empty[buf], use ^ 1, budget)) {   // epilogue released this buffer
           atomicOr(args.err, kErrWaitMma);
-          atomicExch(abort_flag, 1);
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(smem + s * C::kStageBytes);
-        const uint32_t b0 = a0 + C::kABytes;
+        const uint32_t acc = tmem + buf * C::kAccCols;
+        for (int kb = 0; kb < args.num_kb; ++kb) {
+          const int s = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (!mbar_wait(&full[s], ph, budget)) {
+            atomicOr(args.err, kErrWaitMma);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t b0 = a0 + C::kABytes;
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t ad = sw128_kmajor_desc(a0 + kk * 32);
-          const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-          mma_bf16(tmem, ad, sw128_kmajor_desc(b0 + kk * 32), idesc, acc);
-          if (C::kDual)
-            mma_bf16(tmem + BN, ad, sw128_kmajor_desc(b0 + C::kBBytes + kk * 32), idesc, acc);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = sw128_kmajor_desc(a0 + kk * 32);
+            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            mma_bf16(acc, ad, sw128_kmajor_desc(b0 + kk * 32), idesc, accum);
+            if (C::kDual)
+              mma_bf16(acc + BN, ad, sw128_kmajor_desc(b0 + C::kBBytes + kk * 32), idesc, accum);
+          }
+          mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+          ++it;
         }
-        mma_commit(&empty[s]);  // the slot is free once these MMAs have read it
+        mma_commit(&acc_full[buf]);  // accumulator of this tile complete (or abandoned)
+        ++tc;
       }
-      mma_commit(accum);        // accumulator complete
+      mma_commit(mma_done);
     }
   } else {
     // ---- epilogue: warps 2..5 ; TMEM lane quadrant = warp % 4
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const bool row_ok = r < nrows;
-    const long long grow = static_cast<long long>(row0) + r;
-    const uint32_t tq = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const bool ok = mbar_wait(accum, 0, budget);
-    if (!ok) {
-      atomicOr(args.err, kErrWaitEpilogue);
-      // the MMAs already issued must finish before TMEM is released
-      if (!mbar_wait(accum, 0, kDrainBudget)) atomicOr(args.err, kErrDrain);
-    }
-    tc_fence_after();
-    if (ok) {
+    int tc = 0;
+    for (int id = blockIdx.x; id < walk.n_ids; id += gridDim.x) {
+      int expert, row0, nrows, ntile;
+      if (!walk.at(args, id, expert, row0, nrows, ntile)) continue;
+      const int buf = tc & 1;
+      const uint32_t use = (tc >> 1) & 1;
+      if (!mbar_wait(&acc_full[buf], use, budget)) {
+        atomicOr(args.err, kErrWaitEpilogue);
+        break;
+      }
+      tc_fence_after();
+      const bool row_ok = r < nrows;
+      const long long grow = static_cast<long long>(row0) + r;
+      const int n0 = ntile * BN;
+      const uint32_t tq = tmem + buf * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       if constexpr (EPI == kEpiF32) {
         float* orow = static_cast<float*>(args.out) + grow * args.ldo;
 #pragma unroll 1
@@ -211,7 +257,7 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
         }
-        if (row_ok) args.ss[grow * args.ld_ss + blockIdx.x] = ss;
+        if (row_ok) args.ss[grow * args.ld_ss + ntile] = ss;
       } else {  // kEpiSwiGLU
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo;
 #pragma unroll 1
@@ -236,16 +282,34 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      // every TMEM read of this buffer is complete: hand it back to the MMA issuer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      ++tc;
     }
   }
 
-  // ---- teardown: every TMEM read is complete before the columns are released
+  // ---- teardown: all MMAs of this CTA have completed before the columns are released
+  if (warp == 1 && lane == 0)
+    if (!mbar_wait(mma_done, 0, kDrainBudget)) atomicOr(args.err, kErrDrain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
 }
 
 template <int BN, int EPI>
@@ -261,8 +325,11 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid((a.N + BN - 1) / BN, m_tiles);
-  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  // upper bound of the tile ids (the live M-tile count of a grouped GEMM is on the device)
+  const long long nt = (a.N + BN - 1) / BN;
+  const long long ids = (m_tiles + kRasterGroup - 1) / kRasterGroup * kRasterGroup * nt;
+  if (ids == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
   count_launch();
   kern<<<grid, 192, C::kSmemBytes, s>>>(tmA, tmB, tmB2, a);
   return cudaGetLastError();

@@ -34,9 +34,6 @@ namespace {
 LMOE_DEV void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-LMOE_DEV void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 // Shared-memory descriptor of a 512-byte scale block: 4 core matrices of 8 lines x 16 B,
 // contiguous (stride 128 B), no swizzle.
@@ -121,19 +118,21 @@ __global__ void __launch_bounds__(224, 1)
   uint64_t* accum = empty + C::kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
 
-  int expert = 0, row0, nrows;
+  int expert = 0, row0, nrows, mt, ntile;
+  const int nt = (args.N + BN - 1) / BN;
+  const int total_m = args.tiles != nullptr ? *args.n_tiles : (args.M + kBM - 1) / kBM;
+  if (!grouped_tile(static_cast<int>(blockIdx.x), total_m, nt, kRasterGroup, mt, ntile)) return;
   if (args.tiles != nullptr) {
-    if (static_cast<int>(blockIdx.y) >= *args.n_tiles) return;
-    const Tile t = args.tiles[blockIdx.y];
+    const Tile t = args.tiles[mt];
     expert = t.expert;
     row0 = t.row0;
     nrows = t.nrows;
   } else {
-    row0 = blockIdx.y * kBM;
+    row0 = mt * kBM;
     nrows = min(kBM, args.M - row0);
   }
   if (nrows <= 0) return;
-  const int n0 = blockIdx.x * BN;
+  const int n0 = ntile * BN;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -164,7 +163,7 @@ __global__ void __launch_bounds__(224, 1)
   if (warp == 0) {
     if (lane == 0) {
       const int brow = expert * args.N + n0;
-      const uint64_t pol_b = policy_evict_first();
+      const uint64_t pol_b = args.b_stream_once ? policy_evict_first() : policy_evict_normal();
       int issued = 0;
       for (int kb = 0; kb < nk; ++kb) {
         const int s = kb % C::kStages;
@@ -299,7 +298,7 @@ __global__ void __launch_bounds__(224, 1)
             }
           }
         }
-        if (row_ok) args.ss[grow * args.ld_ss + blockIdx.x] = ss;
+        if (row_ok) args.ss[grow * args.ld_ss + ntile] = ss;
       } else {  // kFp4EpiSwiGLUQuant
         const int e = args.tiles ? expert : 0;
         const float ag = rs * args.tensor_scale[e], au = rs * args.tensor_scale2[e];
@@ -351,8 +350,9 @@ cudaError_t launch_fp4_one(const CUtensorMap* maps, const Fp4Args& a, int m_tile
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid((a.N + BN - 1) / BN, m_tiles);
-  if (grid.x == 0 || grid.y == 0) return cudaSuccess;
+  const long long ctas = static_cast<long long>((a.N + BN - 1) / BN) * m_tiles;
+  if (ctas == 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(ctas));
   count_launch();
   kern<<<grid, 224, C::kSmemBytes, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
   return cudaGetLastError();

@@ -53,6 +53,7 @@ struct GemmArgs {
   int ld_ss;
   unsigned* err;           // device error word
   long long budget;        // wait budget, SM cycles
+  int b_stream_once;       // B tiles are read by ~one M tile each: stream them evict-first
 };
 
 struct Fp4Args {
@@ -71,6 +72,7 @@ struct Fp4Args {
   const float* tensor_scale2;// quant: scale of B2 (up)
   unsigned* err;
   long long budget;
+  int b_stream_once;         // B tiles are read by ~one M tile each: stream them evict-first
 };
 
 // NVFP4 GEMM; maps = {A codes, A scales, B codes, B scales, B2 codes, B2 scales}.
@@ -91,6 +93,9 @@ cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, c
                                  float* s_row, cudaStream_t s);
 cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool row_scale,
                                   uint8_t* codes, uint8_t* scales, float* s_row, cudaStream_t s);
+
+// Streaming multiprocessors of the current device (persistent grids).
+int sm_count();
 
 // Counts every kernel launch of the library (lmoe_kernel_launches).
 void count_launch();

@@ -30,6 +30,9 @@ LMOE_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
+LMOE_DEV void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 LMOE_DEV bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -77,6 +80,11 @@ LMOE_DEV void tma_load_2d_hint(void* dst, const CUtensorMap* m, uint64_t* bar, i
 LMOE_DEV uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+LMOE_DEV uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 LMOE_DEV uint64_t policy_evict_last() {
@@ -160,6 +168,25 @@ LMOE_DEV void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 LMOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------------ tile order
+// Grouped rasterisation of a 1-D grid over (M tile, N tile): groups of `group` consecutive M
+// tiles; inside a group the M index runs fastest, so the CTAs resident at one time share
+// each B (weight) tile while the group's A tiles stay in L2.  Returns false for ids past the
+// live tile count (it is read on the device for grouped GEMMs).
+LMOE_DEV bool grouped_tile(int id, int total_m, int nt, int group, int& m, int& n) {
+  const int gsz = group * nt;
+  const int g = id / gsz;
+  const int first = g * group;
+  const int gm = min(group, total_m - first);
+  if (gm <= 0) return false;
+  const int local = id - g * gsz;
+  if (local >= gm * nt) return false;
+  m = first + local % gm;
+  n = local / gm;
+  return true;
+}
+constexpr int kRasterGroup = 16;
 
 // ------------------------------------------------------------------ misc
 LMOE_DEV float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
