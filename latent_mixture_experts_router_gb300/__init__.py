@@ -22,7 +22,7 @@ from ._lib import (Config, LmoeError, lmoe_workspace_size, lmoe_workspace_size_h
                    lmoe_get_workspace_layout, latent_moe_forward, latent_moe_forward_ex,
                    latent_moe_forward_host_io, lmoe_check_status, lmoe_wait_selftest, load,
                    LIB_PATH, STAGES, NUM_STAGE_EVENTS, lmoe_kernel_launches,
-                   lmoe_quantize_nvfp4)
+                   lmoe_quantize_nvfp4, lmoe_nvfp4_block_scales)
 
 load()
 
@@ -32,10 +32,17 @@ class LatentMoEBlock:
 
     Weights: W_router [E, D]; W_pool [L, D]; W_gate, W_up [E, I, L]; W_down [E, L, I];
     W_unpool [D, L]; gammas g_pre [D], g_pool [L], g_expert [E, L], g_post [D] (fp32).
+    NVFP4 weights are (codes, row-major E4M3 scales, tensor scale) triples; their scales are
+    converted once into the block layout the kernels read.
     """
 
     def __init__(self, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool, g_pre,
                  g_post, top_k: int, eps: float = 1e-6, weight_dtype: str = "bf16"):
+        if weight_dtype == "nvfp4":   # (codes, row-major scales, s) -> scales in block layout
+            def blocked(w):
+                codes, scales, s = w
+                return codes, lmoe_nvfp4_block_scales(scales, codes.shape[-1] * 2), s
+            W_pool, W_gate, W_up, W_down, W_unpool = map(blocked, (W_pool, W_gate, W_up, W_down, W_unpool))
         self.W = dict(W_router=W_router, W_pool=W_pool, g_pool=g_pool, W_gate=W_gate, W_up=W_up,
                       W_down=W_down, g_expert=g_expert, W_unpool=W_unpool, g_pre=g_pre, g_post=g_post)
         self.top_k, self.eps, self.weight_dtype = top_k, eps, weight_dtype

@@ -268,3 +268,17 @@ def lmoe_quantize_nvfp4(src, codes, scales, s_row=None, row_scale=True, stream=N
     rows, K = src.shape
     _check(fn(_ptr(src), rows, K, 1 if row_scale else 0, _ptr(codes), _ptr(scales), _ptr(s_row),
               _stream(stream)), "lmoe_quantize_nvfp4")
+
+
+def lmoe_nvfp4_block_scales(src, K: int, dst=None, stream=None):
+    """Row-major E4M3 scales ``src`` [..., rows, K/16] (uint8, device) -> the block layout the
+    NVFP4 GEMMs read (a new tensor of the same size unless ``dst`` is given)."""
+    L = _lib()
+    fn = L.lmoe_nvfp4_block_scales
+    fn.argtypes = [_P, ctypes.c_longlong, ctypes.c_int, _P, _P]
+    fn.restype = ctypes.c_int
+    rows = src.numel() // (K // 16)
+    if dst is None:
+        dst = torch.empty_like(src)
+    _check(fn(_ptr(src), rows, int(K), _ptr(dst), _stream(stream)), "lmoe_nvfp4_block_scales")
+    return dst

@@ -37,6 +37,7 @@ int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 struct Layout {
   lmoe_workspace_layout pub;
   long long near_tie;
+  long long tile_base;  // [E] first M tile of each expert
   // fp32-weight mode: bf16 copies of the weights
   long long w_router, w_pool, w_gate, w_up, w_down, w_unpool;
   long long x_stage, out_stage, host_io_total;
@@ -79,9 +80,10 @@ void make_layout(const lmoe_config* c, Layout* L) {
   lmoe_workspace_layout& P = L->pub;
   P.xa_cols = static_cast<int>((f32w ? 3 : 2) * D);
   L->ld_logits = static_cast<int>(align_up(E, 32));
-  L->ld_ss_p = cdiv(Ld, kBNWide);
-  L->ld_ss_y = cdiv(Ld, kBNWide);
-  L->ld_ss_u = cdiv(D, kBNWide);
+  const int bn_ss = c->weight_dtype == LMOE_NVFP4 ? kBNFp4 : kBNWide;  // N of the GEMM tiles
+  L->ld_ss_p = cdiv(Ld, bn_ss);
+  L->ld_ss_y = cdiv(Ld, bn_ss);
+  L->ld_ss_u = cdiv(D, bn_ss);
   L->max_tiles = cdiv(R, kBM) + static_cast<int>(E < R ? E : R);
   P.err = take(kAlign);  // error word; the near-tie counter shares this line
   L->near_tie = P.err + 4;
@@ -95,18 +97,23 @@ void make_layout(const lmoe_config* c, Layout* L) {
   P.tok_of = take(R * 4);
   P.tiles = take(static_cast<size_t>(L->max_tiles) * sizeof(Tile));
   P.n_tiles = take(4);
+  L->tile_base = take(E * 4);
   P.p = take(T * Ld * 4);
   P.ss_p = take(T * L->ld_ss_p * 4);
   const bool fp4 = c->weight_dtype == LMOE_NVFP4;
+  // NVFP4 block scales are kept in the tensor cores' block layout: whole 128-row blocks, one
+  // per 128 rows of a dense operand, one per M tile of a grouped one
+  const long long tb = cdiv(T, kBM) * static_cast<long long>(kBM);
+  const long long gb = static_cast<long long>(L->max_tiles) * kBM;
   if (fp4) {  // quantised GEMM inputs: codes (2 per byte), E4M3 block scales, fp32 row scales
     P.xq = take(T * D / 2);
-    P.xq_scale = take(T * D / 16);
+    P.xq_scale = take(tb * D / 16);
     P.xq_rowscale = take(T * 4);
     P.xe = take(R * Ld / 2);
-    P.xe_scale = take(R * Ld / 16);
+    P.xe_scale = take(gb * Ld / 16);
     P.xe_rowscale = take(R * 4);
     P.h = take(R * I / 2);
-    P.h_scale = take(R * I / 16);
+    P.h_scale = take(gb * I / 16);
   } else {
     P.xe = take(R * Ld * 2);
     P.h = take(R * I * 2);
@@ -115,7 +122,7 @@ void make_layout(const lmoe_config* c, Layout* L) {
   P.ss_y = take(R * L->ld_ss_y * 4);
   if (fp4) {
     P.c = take(T * Ld / 2);
-    P.c_scale = take(T * Ld / 16);
+    P.c_scale = take(tb * Ld / 16);
     P.c_rowscale = take(T * 4);
   } else {
     P.c = take(T * Ld * 2);
@@ -240,19 +247,13 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                          uint8_t* out_scales, float* ss, int ld_ss, const float* row_scale,
                          const float* ts, const float* ts2, unsigned* err, long long budget,
                          cudaStream_t s, long long rows_per_b) {
-  const unsigned bn = epi == kFp4EpiSwiGLUQuant ? kBNSwiGLU : kBNWide;
-  CUtensorMap maps[6];
-  const unsigned long long kc = K / 2, ks = K / 16;
+  CUtensorMap maps[3];
+  const unsigned long long kc = K / 2;
   if (!encode_u8_2d(&maps[0], A.codes, kc, a_rows, kc, 128, kBM, true) ||
-      !encode_u8_2d(&maps[1], A.scales, ks, a_rows, ks, 16, kBM, false) ||
-      !encode_u8_2d(&maps[2], B.codes, kc, b_rows, kc, 128, bn, true) ||
-      !encode_u8_2d(&maps[3], B.scales, ks, b_rows, ks, 16, bn, false))
+      !encode_u8_2d(&maps[1], B.codes, kc, b_rows, kc, 128, kBNFp4, true))
     return LMOE_ERR_CUDA;
-  maps[4] = maps[2];
-  maps[5] = maps[3];
-  if (B2 && (!encode_u8_2d(&maps[4], B2->codes, kc, b_rows, kc, 128, bn, true) ||
-             !encode_u8_2d(&maps[5], B2->scales, ks, b_rows, ks, 16, bn, false)))
-    return LMOE_ERR_CUDA;
+  maps[2] = maps[1];
+  if (B2 && !encode_u8_2d(&maps[2], B2->codes, kc, b_rows, kc, 128, kBNFp4, true)) return LMOE_ERR_CUDA;
   Fp4Args a{};
   a.M = static_cast<int>(a_rows);
   a.N = N;
@@ -267,6 +268,9 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
   a.row_scale = row_scale;
   a.tensor_scale = ts;
   a.tensor_scale2 = ts2;
+  a.a_scales = A.scales;
+  a.b_scales = B.scales;
+  a.b2_scales = B2 ? B2->scales : nullptr;
   a.err = err;
   a.budget = budget;
   a.b_stream_once = rows_per_b <= kBM;
@@ -403,7 +407,9 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     LMOE_CUDA(cudaMemcpyAsync(ex->near_tie_count_out, near_tie, 4, cudaMemcpyDeviceToDevice, s));
   LMOE_MARK(LMOE_STAGE_PERMUTE);
   // S4 permutation
-  LMOE_CUDA(launch_permute(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, s));
+  int32_t* tile_base = static_cast<int32_t*>(at(L.tile_base));
+  LMOE_CUDA(launch_permute(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, s,
+                           tile_base));
   if (fp4) {
     const Fp4Operand xq{wsb + L.pub.xq, wsb + L.pub.xq_scale};
     const Fp4Operand xeq{wsb + L.pub.xe, wsb + L.pub.xe_scale};
@@ -420,8 +426,9 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_POOLNORM);
     // S6 pool norm, quantised per token, copied to the k expert rows
-    LMOE_CUDA(launch_poolnorm_scatter_nvfp4(p, ss_p, L.ld_ss_p, g_pool, row_of, T, Ld, k, eps,
-                                            wsb + L.pub.xe, wsb + L.pub.xe_scale, xe_s, s));
+    LMOE_CUDA(launch_poolnorm_scatter_nvfp4(p, ss_p, L.ld_ss_p, g_pool, row_of, tk_idx, offsets,
+                                            tile_base, T, Ld, k, eps, wsb + L.pub.xe,
+                                            wsb + L.pub.xe_scale, xe_s, s));
     LMOE_MARK(LMOE_STAGE_GATE_UP);
     // S7 grouped gate/up + SwiGLU, h requantised to NVFP4 (scale 1)
     const Fp4Operand up = op(q4[2]);
@@ -595,6 +602,17 @@ lmoe_status lmoe_quantize_nvfp4(const float* src, long long rows, int K, int row
   if (!aligned16(src) || (reinterpret_cast<uintptr_t>(codes) & 7u)) return LMOE_ERR_ALIGN;
   if (launch_quantize_nvfp4(src, rows, K, row_scale != 0, codes, scales, s_row, stream) != cudaSuccess)
     return LMOE_ERR_CUDA;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_nvfp4_block_scales(const uint8_t* src, long long rows, int K, uint8_t* dst,
+                                    cudaStream_t stream) {
+  if (rows < 0 || rows % kBM || K <= 0 || K % 64) return LMOE_ERR_ARG;
+  if (rows == 0) return LMOE_OK;
+  if (src == nullptr || dst == nullptr || src == dst) return LMOE_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(dst) & 3u) || (reinterpret_cast<uintptr_t>(src) & 3u))
+    return LMOE_ERR_ALIGN;
+  if (launch_nvfp4_block_scales(src, rows, K, dst, stream) != cudaSuccess) return LMOE_ERR_CUDA;
   return LMOE_OK;
 }
 

@@ -28,6 +28,7 @@
 //               two accumulators), output bf16 silu(a) * b.
 #include "internal.h"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace lmoe {
 
@@ -46,33 +47,6 @@ struct GemmCfg {
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
 };
 
-// The tile sequence every role of a CTA walks: ids blockIdx.x, + gridDim.x, ...; ids that
-// fall in the padding of the last raster group are skipped by all roles alike.
-struct TileWalk {
-  int total_m, nt, n_ids;
-  LMOE_DEV TileWalk(const GemmArgs& a, int bn) {
-    total_m = a.tiles != nullptr ? *a.n_tiles : (a.M + kBM - 1) / kBM;
-    nt = (a.N + bn - 1) / bn;
-    n_ids = ((total_m + kRasterGroup - 1) / kRasterGroup) * kRasterGroup * nt;
-  }
-  // (expert, first row, rows, N tile) of tile id; false if the id is padding
-  LMOE_DEV bool at(const GemmArgs& a, int id, int& expert, int& row0, int& nrows, int& ntile) const {
-    int mt;
-    if (!grouped_tile(id, total_m, nt, kRasterGroup, mt, ntile)) return false;
-    if (a.tiles != nullptr) {
-      const Tile t = a.tiles[mt];
-      expert = t.expert;
-      row0 = t.row0;
-      nrows = t.nrows;
-    } else {
-      expert = 0;
-      row0 = mt * kBM;
-      nrows = min(kBM, a.M - row0);
-    }
-    return nrows > 0;
-  }
-};
-
 template <int BN, int EPI>
 __global__ void __launch_bounds__(192, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -89,7 +63,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* mma_done = acc_empty + 2;         // every MMA of this CTA has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
-  const TileWalk walk(args, BN);
+  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN);
   if (static_cast<int>(blockIdx.x) >= walk.n_ids) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -126,7 +100,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int id = blockIdx.x; ok && id < walk.n_ids; id += gridDim.x) {
         int expert, row0, nrows, ntile;
-        if (!walk.at(args, id, expert, row0, nrows, ntile)) continue;
+        if (!walk.at(id, expert, row0, nrows, ntile)) continue;
         const int brow = expert * args.N + ntile * BN;
         for (int kb = 0; kb < args.num_kb; ++kb) {
           const int s = it % C::kStages;
@@ -159,7 +133,7 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (int id = blockIdx.x; ok && id < walk.n_ids; id += gridDim.x) {
         int expert, row0, nrows, ntile;
-        if (!walk.at(args, id, expert, row0, nrows, ntile)) continue;
+        if (!walk.at(id, expert, row0, nrows, ntile)) continue;
         const int buf = tc & 1;
         const uint32_t use = (tc >> 1) & 1;
         if (!mbar_wait(&acc_empty[buf], use ^ 1, budget)) {   // epilogue released this buffer
@@ -202,7 +176,7 @@ __global__ void __launch_bounds__(192, 1)
     int tc = 0;
     for (int id = blockIdx.x; id < walk.n_ids; id += gridDim.x) {
       int expert, row0, nrows, ntile;
-      if (!walk.at(args, id, expert, row0, nrows, ntile)) continue;
+      if (!walk.at(id, expert, row0, nrows, ntile)) continue;
       const int buf = tc & 1;
       const uint32_t use = (tc >> 1) & 1;
       if (!mbar_wait(&acc_full[buf], use, budget)) {
@@ -326,8 +300,7 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
     attr_set = true;
   }
   // upper bound of the tile ids (the live M-tile count of a grouped GEMM is on the device)
-  const long long nt = (a.N + BN - 1) / BN;
-  const long long ids = (m_tiles + kRasterGroup - 1) / kRasterGroup * kRasterGroup * nt;
+  const long long ids = tile_id_bound(m_tiles, a.N, BN);
   if (ids == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
   count_launch();

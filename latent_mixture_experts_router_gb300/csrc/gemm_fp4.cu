@@ -1,4 +1,5 @@
-// gemm_fp4.cu — grouped NVFP4 x NVFP4 GEMM on the block-scaled 5th-generation tensor cores.
+// gemm_fp4.cu — grouped NVFP4 x NVFP4 GEMM on the block-scaled 5th-generation tensor cores,
+// persistent.
 //
 // out[r, n] = alpha_r,e * sum_k A[r, k] * B[e*N + n, k], with A and B packed E2M1 (two
 // values per byte, K contiguous) and one UE4M3 scale per 16 consecutive k on both operands
@@ -7,25 +8,27 @@
 // is applied to the accumulator).  alpha = row scale (per token / per routed row, or 1) *
 // tensor scale of the weight (per expert).
 //
-// One CTA computes a 128 x BN tile; a pipeline stage covers K = 256 (128 bytes of codes per
-// row and 16 scale bytes per row).  Roles (224 threads):
-//   warp 0 lane 0   TMA: A codes + A scales + B codes + B scales (+ B2 for gate/up)
+// One CTA per SM walks the 128 x BN output tiles in grouped order (as the BF16 GEMM); a
+// pipeline stage covers K = 256 (128 bytes of codes per row, and the 2 KB of scales of the
+// stage's 128-row block).  The scales are kept in memory in the layout the tensor cores
+// read through tcgen05.cp 32x128b (blocks of 32 lines x 16 bytes, line m0 holding the 4
+// scale bytes of rows m0, m0+32, m0+64, m0+96 — the "4x32 transpose" the pages apply before
+// the copy, done once when the scales are written), so a stage's scales are one bulk copy.
+// Roles (192 threads):
+//   warp 0 lane 0   TMA: A codes + B codes (+ B2 for gate/up) + bulk copies of their scales
 //   warp 1          TMEM allocation; lane 0 copies scale factors into TMEM (tcgen05.cp) and
 //                   issues tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //   warps 2..5      epilogue (warp w owns TMEM lanes 32*(w%4) ..)
-//   warp 6          scale-factor transposer: the tensor cores take the scales of one
-//                   K=64 step of 128 rows from a 512-byte block of 32 lines x 16 bytes, line
-//                   m0 holding the 4 scale bytes of rows m0, m0+32, m0+64, m0+96
-//                   (tcgen05.cp 32x128b, replicated to the four lane quadrants); the scales
-//                   arrive row-major (16 bytes per row per stage) and this warp regroups them
-//                   (the "4x32 transpose" the pages describe before the copy).
-// Epilogues: kFp4EpiF32Ss — alpha * acc as fp32 plus per-row partial sums of squares (the
-// norm that follows needs only these partials); kFp4EpiSwiGLUQuant — gate and up tiles of
-// the same columns, h = silu(alpha_g acc_g) * (alpha_u acc_u) requantised to NVFP4 with
-// scale 1 (block scales only, through the reciprocal table) for the down projection.
+// Epilogues: kFp4EpiF32Ss — alpha * acc as fp32 plus per-row partial sums of squares; two
+// accumulator buffers, so the next tile's MMAs overlap this tile's epilogue.
+// kFp4EpiSwiGLUQuant — gate and up tiles of the same columns, h = silu(alpha_g acc_g) *
+// (alpha_u acc_u) requantised to NVFP4 with scale 1 (block scales only, through the
+// reciprocal table) for the down projection; one accumulator buffer (two would not leave
+// tensor memory for the scale factors), while TMA and the regrouping run ahead.
 #include "internal.h"
 #include "nvfp4.cuh"
 #include "ptx.cuh"
+#include "tiles.cuh"
 
 namespace lmoe {
 
@@ -72,76 +75,64 @@ template <int BN, int EPI>
 struct Fp4Cfg {
   static constexpr bool kDual = (EPI == kFp4EpiSwiGLUQuant);
   static constexpr int kNB = kDual ? 2 : 1;
-  static constexpr int kStages = 3;
+  static constexpr int kStages = kDual ? 4 : 6;
   static constexpr int kKStep = 4;                 // MMAs (K = 64 each) per stage
   static constexpr int kABytes = kBM * 128;        // codes
   static constexpr int kBBytes = BN * 128;
-  static constexpr int kSfaRaw = kBM * 16;         // row-major scales of the stage
-  static constexpr int kSfbRaw = BN * 16;
+  static constexpr int kSfaBytes = kBM * 16;       // block-layout scales of the stage
+  static constexpr int kSfbBytes = BN * 16;
   static constexpr int kBAtoms = BN / 128;         // 128-row scale blocks per B operand
-  static constexpr int kSfaT = kKStep * 512;       // regrouped scales
-  static constexpr int kSfbT = kKStep * kBAtoms * 512;
-  // stage layout: [A codes][B codes x kNB][A sf raw][B sf raw x kNB][A sf][B sf x kNB]
+  // stage layout: [A codes][B codes x kNB][A scales][B scales x kNB]
   static constexpr int kOffB = kABytes;
-  static constexpr int kOffSfaRaw = kOffB + kNB * kBBytes;
-  static constexpr int kOffSfbRaw = kOffSfaRaw + kSfaRaw;
-  static constexpr int kOffSfa = kOffSfbRaw + kNB * kSfbRaw;
-  static constexpr int kOffSfb = kOffSfa + kSfaT;
-  static constexpr int kStageBytes = kOffSfb + kNB * kSfbT;
-  static constexpr uint32_t kTxBytes = kABytes + kSfaRaw + kNB * (kBBytes + kSfbRaw);
-  // tensor memory: accumulators, then per-stage scale columns
+  static constexpr int kOffSfa = kOffB + kNB * kBBytes;
+  static constexpr int kOffSfb = kOffSfa + kSfaBytes;
+  static constexpr int kStageBytes = kOffSfb + kNB * kSfbBytes;
+  static constexpr uint32_t kTxBytes = kStageBytes;
+  // tensor memory: accumulator buffer(s), then per-stage scale columns
   static constexpr int kAccCols = kNB * BN;
+  static constexpr int kAccBufs = kDual ? 1 : 2;
   static constexpr int kSfaCols = kKStep * 4;                // 4 columns per 128 rows per MMA
   static constexpr int kSfbColsOne = kKStep * (BN / 32);
   static constexpr int kSfCols = kSfaCols + kNB * kSfbColsOne;
+  static constexpr int kSfCol0 = kAccBufs * kAccCols;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024 /*recip*/ + 256;
-  static_assert(kAccCols + kStages * kSfCols <= 512, "tensor memory");
+  static_assert(kSfCol0 + kStages * kSfCols <= 512, "tensor memory");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kStageBytes % 1024 == 0, "1024-byte aligned stages");
+  static_assert(BN == 128, "one 128-row scale block of B per stage");
 };
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(224, 1)
-    gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmSA,
-                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmSB,
-                    const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmSB2,
-                    const Fp4Args args) {
+__global__ void __launch_bounds__(192, 1)
+    gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB2, const Fp4Args args) {
   using C = Fp4Cfg<BN, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   float* recip = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(recip + 256);
-  uint64_t* sfready = full + C::kStages;
-  uint64_t* empty = sfready + C::kStages;
-  uint64_t* accum = empty + C::kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* acc_full = empty + C::kStages;     // [kAccBufs]
+  uint64_t* acc_empty = acc_full + 2;          // [kAccBufs], 4 epilogue warps arrive
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
-  int expert = 0, row0, nrows, mt, ntile;
-  const int nt = (args.N + BN - 1) / BN;
-  const int total_m = args.tiles != nullptr ? *args.n_tiles : (args.M + kBM - 1) / kBM;
-  if (!grouped_tile(static_cast<int>(blockIdx.x), total_m, nt, kRasterGroup, mt, ntile)) return;
-  if (args.tiles != nullptr) {
-    const Tile t = args.tiles[mt];
-    expert = t.expert;
-    row0 = t.row0;
-    nrows = t.nrows;
-  } else {
-    row0 = mt * kBM;
-    nrows = min(kBM, args.M - row0);
-  }
-  if (nrows <= 0) return;
-  const int n0 = ntile * BN;
+  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN);
+  if (static_cast<int>(blockIdx.x) >= walk.n_ids) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&sfready[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum, 1);
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 4);
+    }
+    mbar_init(mma_done, 1);
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -162,118 +153,120 @@ __global__ void __launch_bounds__(224, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      const int brow = expert * args.N + n0;
+      // ---- TMA producer
       const uint64_t pol_b = args.b_stream_once ? policy_evict_first() : policy_evict_normal();
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % C::kStages;
-        const uint32_t ph = (kb / C::kStages) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, budget)) {
-          atomicOr(args.err, kErrWaitProducer);
-          break;
+      int it = 0;
+      bool ok = true;
+      for (int id = blockIdx.x; ok && id < walk.n_ids; id += gridDim.x) {
+        int mt, expert, row0, nrows, ntile;
+        if (!walk.at(id, mt, expert, row0, nrows, ntile)) continue;
+        const int brow = expert * args.N + ntile * BN;
+        const int kblk = args.num_kb * 4;   // 512-byte scale blocks per 128-row block
+        const uint8_t* sfa_src = args.a_scales + static_cast<size_t>(mt) * kblk * 512;
+        const uint8_t* sfb_src = args.b_scales + static_cast<size_t>(brow / kBM) * kblk * 512;
+        const uint8_t* sfb2_src = C::kDual ? args.b2_scales + static_cast<size_t>(brow / kBM) * kblk * 512 : nullptr;
+        for (int kb = 0; kb < nk; ++kb) {
+          const int s = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, budget)) {
+            atomicOr(args.err, kErrWaitProducer);
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + s * C::kStageBytes;
+          mbar_arrive_expect_tx(&full[s], C::kTxBytes);
+          tma_load_2d(st, &tmA, &full[s], kb * 128, row0);
+          bulk_load(st + C::kOffSfa, sfa_src + kb * 2048, C::kSfaBytes, &full[s]);
+          tma_load_2d_hint(st + C::kOffB, &tmB, &full[s], kb * 128, brow, pol_b);
+          bulk_load(st + C::kOffSfb, sfb_src + kb * 2048, C::kSfbBytes, &full[s]);
+          if (C::kDual) {
+            tma_load_2d_hint(st + C::kOffB + C::kBBytes, &tmB2, &full[s], kb * 128, brow, pol_b);
+            bulk_load(st + C::kOffSfb + C::kSfbBytes, sfb2_src + kb * 2048, C::kSfbBytes, &full[s]);
+          }
+          ++it;
         }
-        uint8_t* st = smem + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], C::kTxBytes);
-        tma_load_2d(st, &tmA, &full[s], kb * 128, row0);
-        tma_load_2d(st + C::kOffSfaRaw, &tmSA, &full[s], kb * 16, row0);
-        tma_load_2d_hint(st + C::kOffB, &tmB, &full[s], kb * 128, brow, pol_b);
-        tma_load_2d_hint(st + C::kOffSfbRaw, &tmSB, &full[s], kb * 16, brow, pol_b);
-        if (C::kDual) {
-          tma_load_2d_hint(st + C::kOffB + C::kBBytes, &tmB2, &full[s], kb * 128, brow, pol_b);
-          tma_load_2d_hint(st + C::kOffSfbRaw + C::kSfbRaw, &tmSB2, &full[s], kb * 16, brow, pol_b);
-        }
-        issued = kb + 1;
       }
-      for (int kb = max(0, issued - C::kStages); kb < issued; ++kb)
-        if (!mbar_wait(&full[kb % C::kStages], (kb / C::kStages) & 1, kDrainBudget))
+      for (int j = max(0, it - C::kStages); j < it; ++j)
+        if (!mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, kDrainBudget))
           atomicOr(args.err, kErrDrain);
-    }
-  } else if (warp == 6) {
-    // ---- scale-factor regrouping: row-major [rows][16 B] -> per MMA step, 128-row blocks of
-    // 32 lines x 16 B (line m0 = rows m0, m0+32, m0+64, m0+96; 4 bytes each)
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % C::kStages;
-      const uint32_t ph = (kb / C::kStages) & 1;
-      if (!mbar_wait(&full[s], ph, budget)) {
-        if (lane == 0) atomicOr(args.err, kErrWaitMma);
-        break;
-      }
-      uint8_t* st = smem + s * C::kStageBytes;
-      const uint32_t* ra = reinterpret_cast<const uint32_t*>(st + C::kOffSfaRaw);
-      uint32_t* ta = reinterpret_cast<uint32_t*>(st + C::kOffSfa);
-#pragma unroll
-      for (int j = 0; j < C::kKStep; ++j)
-#pragma unroll
-        for (int m1 = 0; m1 < 4; ++m1) ta[j * 128 + lane * 4 + m1] = ra[(lane + 32 * m1) * 4 + j];
-#pragma unroll
-      for (int b = 0; b < C::kNB; ++b) {
-        const uint32_t* rb = reinterpret_cast<const uint32_t*>(st + C::kOffSfbRaw + b * C::kSfbRaw);
-        uint32_t* tb = reinterpret_cast<uint32_t*>(st + C::kOffSfb + b * C::kSfbT);
-#pragma unroll
-        for (int j = 0; j < C::kKStep; ++j)
-#pragma unroll
-          for (int a = 0; a < C::kBAtoms; ++a)
-#pragma unroll
-            for (int m1 = 0; m1 < 4; ++m1)
-              tb[(j * C::kBAtoms + a) * 128 + lane * 4 + m1] = rb[(a * 128 + lane + 32 * m1) * 4 + j];
-      }
-      fence_proxy_async_smem();   // generic-proxy writes -> visible to tcgen05.cp
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sfready[s]);
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // ---- MMA issuer
       constexpr uint32_t idesc = idesc_nvf4(kBM, BN);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % C::kStages;
-        const uint32_t ph = (kb / C::kStages) & 1;
-        if (!mbar_wait(&sfready[s], ph, budget)) {
+      int it = 0, tc = 0;
+      bool ok = true;
+      for (int id = blockIdx.x; ok && id < walk.n_ids; id += gridDim.x) {
+        int expert, row0, nrows, ntile;
+        if (!walk.at(id, expert, row0, nrows, ntile)) continue;
+        const int buf = tc % C::kAccBufs;
+        const uint32_t use = (tc / C::kAccBufs) & 1;
+        if (!mbar_wait(&acc_empty[buf], use ^ 1, budget)) {
           atomicOr(args.err, kErrWaitMma);
           break;
         }
         tc_fence_after();
-        const uint32_t st = smem_u32(smem + s * C::kStageBytes);
-        const uint32_t sfa = tmem + C::kAccCols + s * C::kSfCols;
-        const uint32_t sfb = sfa + C::kSfaCols;
+        const uint32_t acc = tmem + buf * C::kAccCols;
+        for (int kb = 0; kb < nk; ++kb) {
+          const int s = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (!mbar_wait(&full[s], ph, budget)) {
+            atomicOr(args.err, kErrWaitMma);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t sfa = tmem + C::kSfCol0 + s * C::kSfCols;
+          const uint32_t sfb = sfa + C::kSfaCols;
 #pragma unroll
-        for (int j = 0; j < C::kKStep; ++j) {
-          tmem_cp_32x128b_x4(sfa + j * 4, sf_desc(st + C::kOffSfa + j * 512));
+          for (int j = 0; j < C::kKStep; ++j) {
+            tmem_cp_32x128b_x4(sfa + j * 4, sf_desc(st + C::kOffSfa + j * 512));
 #pragma unroll
-          for (int b = 0; b < C::kNB; ++b)
+            for (int b = 0; b < C::kNB; ++b)
 #pragma unroll
-            for (int a = 0; a < C::kBAtoms; ++a)
-              tmem_cp_32x128b_x4(sfb + b * C::kSfbColsOne + j * (BN / 32) + a * 4,
-                                 sf_desc(st + C::kOffSfb + b * C::kSfbT + (j * C::kBAtoms + a) * 512));
+              for (int a = 0; a < C::kBAtoms; ++a)
+                tmem_cp_32x128b_x4(sfb + b * C::kSfbColsOne + j * (BN / 32) + a * 4,
+                                   sf_desc(st + C::kOffSfb + b * C::kSfbBytes + j * C::kBAtoms * 512 + a * 512));
+          }
+#pragma unroll
+          for (int j = 0; j < C::kKStep; ++j) {
+            const uint64_t ad = sw128_kmajor_desc(st + j * 32);
+            const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
+            mma_nvf4(acc, ad, sw128_kmajor_desc(st + C::kOffB + j * 32), idesc, sfa + j * 4,
+                     sfb + j * (BN / 32), accum);
+            if (C::kDual)
+              mma_nvf4(acc + BN, ad, sw128_kmajor_desc(st + C::kOffB + C::kBBytes + j * 32), idesc,
+                       sfa + j * 4, sfb + C::kSfbColsOne + j * (BN / 32), accum);
+          }
+          mma_commit(&empty[s]);
+          ++it;
         }
-#pragma unroll
-        for (int j = 0; j < C::kKStep; ++j) {
-          const uint64_t ad = sw128_kmajor_desc(st + j * 32);
-          const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
-          mma_nvf4(tmem, ad, sw128_kmajor_desc(st + C::kOffB + j * 32), idesc, sfa + j * 4,
-                   sfb + j * (BN / 32), acc);
-          if (C::kDual)
-            mma_nvf4(tmem + BN, ad, sw128_kmajor_desc(st + C::kOffB + C::kBBytes + j * 32), idesc,
-                     sfa + j * 4, sfb + C::kSfbColsOne + j * (BN / 32), acc);
-        }
-        mma_commit(&empty[s]);
+        mma_commit(&acc_full[buf]);
+        ++tc;
       }
-      mma_commit(accum);
+      mma_commit(mma_done);
     }
   } else {
     // ---- epilogue: warps 2..5
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const bool row_ok = r < nrows;
-    const long long grow = static_cast<long long>(row0) + r;
-    const uint32_t tq = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const bool ok = mbar_wait(accum, 0, budget);
-    if (!ok) {
-      atomicOr(args.err, kErrWaitEpilogue);
-      if (!mbar_wait(accum, 0, kDrainBudget)) atomicOr(args.err, kErrDrain);
-    }
-    tc_fence_after();
-    const float rs = (args.row_scale != nullptr && row_ok) ? args.row_scale[grow] : 1.f;
-    if (ok) {
+    int tc = 0;
+    for (int id = blockIdx.x; id < walk.n_ids; id += gridDim.x) {
+      int mt, expert, row0, nrows, ntile;
+      if (!walk.at(id, mt, expert, row0, nrows, ntile)) continue;
+      const int buf = tc % C::kAccBufs;
+      const uint32_t use = (tc / C::kAccBufs) & 1;
+      if (!mbar_wait(&acc_full[buf], use, budget)) {
+        atomicOr(args.err, kErrWaitEpilogue);
+        break;
+      }
+      tc_fence_after();
+      const bool row_ok = r < nrows;
+      const long long grow = static_cast<long long>(row0) + r;
+      const int n0 = ntile * BN;
+      const uint32_t tq = tmem + buf * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+      const float rs = (args.row_scale != nullptr && row_ok) ? args.row_scale[grow] : 1.f;
       if constexpr (EPI == kFp4EpiF32Ss) {
         const float alpha = rs * args.tensor_scale[args.tiles ? expert : 0];
         float* orow = static_cast<float*>(args.out) + grow * args.ldo;
@@ -303,7 +296,7 @@ __global__ void __launch_bounds__(224, 1)
         const int e = args.tiles ? expert : 0;
         const float ag = rs * args.tensor_scale[e], au = rs * args.tensor_scale2[e];
         uint8_t* crow = static_cast<uint8_t*>(args.out) + grow * (args.ldo / 2);
-        uint8_t* srow = args.out_scales + grow * (args.ldo / 16);
+        const int K_h = static_cast<int>(args.ldo);   // h is the next GEMM's A: scales by M tile
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t g[32], u[32];
@@ -325,13 +318,21 @@ __global__ void __launch_bounds__(224, 1)
               sc[blk] = nvfp4_quant16(h, 6.f, 1.f, recip, q[blk]);
             }
             *reinterpret_cast<uint4*>(crow + col / 2) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
-            *reinterpret_cast<uint16_t*>(srow + col / 16) = static_cast<uint16_t>(sc[0] | (sc[1] << 8));
+            *reinterpret_cast<uint16_t*>(args.out_scales + blocked_sf_offset(mt, r, col / 16, K_h)) =
+                static_cast<uint16_t>(sc[0] | (sc[1] << 8));
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      ++tc;
     }
   }
 
+  // ---- teardown: all MMAs of this CTA have completed before the columns are released
+  if (warp == 1 && lane == 0)
+    if (!mbar_wait(mma_done, 0, kDrainBudget)) atomicOr(args.err, kErrDrain);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -350,11 +351,11 @@ cudaError_t launch_fp4_one(const CUtensorMap* maps, const Fp4Args& a, int m_tile
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long long ctas = static_cast<long long>((a.N + BN - 1) / BN) * m_tiles;
-  if (ctas == 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>(ctas));
+  const long long ids = tile_id_bound(m_tiles, a.N, BN);
+  if (ids == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
   count_launch();
-  kern<<<grid, 224, C::kSmemBytes, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+  kern<<<grid, 192, C::kSmemBytes, s>>>(maps[0], maps[1], maps[2], a);
   return cudaGetLastError();
 }
 
@@ -363,8 +364,8 @@ cudaError_t launch_fp4_one(const CUtensorMap* maps, const Fp4Args& a, int m_tile
 cudaError_t launch_gemm_fp4(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Args& a, int m_tiles,
                             cudaStream_t s) {
   switch (epi) {
-    case kFp4EpiF32Ss: return launch_fp4_one<kBNWide, kFp4EpiF32Ss>(maps, a, m_tiles, s);
-    case kFp4EpiSwiGLUQuant: return launch_fp4_one<kBNSwiGLU, kFp4EpiSwiGLUQuant>(maps, a, m_tiles, s);
+    case kFp4EpiF32Ss: return launch_fp4_one<kBNFp4, kFp4EpiF32Ss>(maps, a, m_tiles, s);
+    case kFp4EpiSwiGLUQuant: return launch_fp4_one<kBNFp4, kFp4EpiSwiGLUQuant>(maps, a, m_tiles, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -11,6 +11,7 @@ constexpr int kBM = 128;            // rows of one GEMM tile (tcgen05 M)
 constexpr int kBK = 64;             // K elements of one pipeline stage (128 B of bf16)
 constexpr int kBNWide = 256;        // N of the single-B GEMM tiles
 constexpr int kBNSwiGLU = 128;      // N of each of the gate and up tiles
+constexpr int kBNFp4 = 128;         // N of the NVFP4 tiles (each of gate and up for SwiGLU)
 constexpr long long kDefaultWaitBudget = 4000000000LL;  // ~2 s of SM clock
 constexpr long long kDrainBudget = 4000000000LL;        // waits for a CTA's own async work
 
@@ -70,12 +71,15 @@ struct Fp4Args {
   const float* row_scale;    // per A row fp32 scale, or nullptr (1)
   const float* tensor_scale; // per expert (grouped) or [0]: scale of B
   const float* tensor_scale2;// quant: scale of B2 (up)
+  const uint8_t* a_scales;   // block-layout scales of A: row block = M tile (grouped) or row/128
+  const uint8_t* b_scales;   // block-layout scales of B and B2 (row block = row / 128)
+  const uint8_t* b2_scales;
   unsigned* err;
   long long budget;
   int b_stream_once;         // B tiles are read by ~one M tile each: stream them evict-first
 };
 
-// NVFP4 GEMM; maps = {A codes, A scales, B codes, B scales, B2 codes, B2 scales}.
+// NVFP4 GEMM; maps = {A codes, B codes, B2 codes}; scales come from the Fp4Args pointers.
 cudaError_t launch_gemm_fp4(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Args& a, int m_tiles,
                             cudaStream_t s);
 
@@ -84,9 +88,14 @@ cudaError_t launch_prenorm_nvfp4(const void* x, bool x_f32, const float* g_pre, 
                                  float eps, __nv_bfloat16* xa, int xa_cols, uint8_t* codes,
                                  uint8_t* scales, float* s_row, cudaStream_t s);
 cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int ld_ss,
-                                          const float* g_pool, const int32_t* row_of, int T, int L,
-                                          int k, float eps, uint8_t* codes, uint8_t* scales,
-                                          float* s_rows, cudaStream_t s);
+                                          const float* g_pool, const int32_t* row_of,
+                                          const int32_t* idx, const int32_t* offsets,
+                                          const int32_t* tile_base, int T, int L, int k, float eps,
+                                          uint8_t* codes, uint8_t* scales, float* s_rows,
+                                          cudaStream_t s);
+// row-major E4M3 scales [rows, K/16] -> block layout (rows a multiple of 128, K of 64)
+cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K, uint8_t* dst,
+                                      cudaStream_t s);
 cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, const int32_t* row_of,
                                  const int32_t* idx, const float* w, const float* g_expert, int T,
                                  int L, int k, float eps, uint8_t* codes, uint8_t* scales,
@@ -111,9 +120,10 @@ cudaError_t launch_prenorm(const void* x, bool x_f32, const float* g_pre, int T,
 cudaError_t launch_topk(const float* logits, int ld, const float* bias, const int32_t* forced,
                         int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
                         int32_t* idx_copy, float* w_copy, unsigned* err, cudaStream_t s);
+// tile_base (optional, [E]): first M tile of each expert in the tile table
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
-                           int32_t* n_tiles, cudaStream_t s);
+                           int32_t* n_tiles, cudaStream_t s, int32_t* tile_base = nullptr);
 cudaError_t launch_poolnorm_scatter(const float* p, const float* ss_p, int ld_ss,
                                     const float* g_pool, const int32_t* row_of, int T, int L,
                                     int k, float eps, __nv_bfloat16* xe, cudaStream_t s);

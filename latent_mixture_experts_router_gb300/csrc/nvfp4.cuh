@@ -65,6 +65,16 @@ LMOE_DEV uint32_t cvt_e4m3(float v) {
   return r & 0xFFu;
 }
 
+// ---- block layout of the E4M3 scales (the layout the block-scaled MMA reads through
+// tcgen05.cp 32x128b): the scales of a [rows, K] matrix are stored as 512-byte blocks of
+// 128 rows x 64 K, ordered [row block][K/64]; inside a block, row m = m0 + 32*m1 and 16-wide
+// sub-block kk land at byte 16*m0 + 4*m1 + kk.  A stage of K = 256 of one row block is then
+// 2 KB contiguous.
+LMOE_DEV size_t blocked_sf_offset(long long blk, int m, int kb16, int K) {
+  return (static_cast<size_t>(blk) * (K / 64) + (kb16 >> 2)) * 512 + (m & 31) * 16 + (m >> 5) * 4 +
+         (kb16 & 3);
+}
+
 // Row scale of the rule: s = amax / 2688 (1 for an all-zero row).
 LMOE_DEV float nvfp4_row_scale(float amax) { return amax > 0.f ? __fdiv_rn(amax, 2688.f) : 1.f; }
 

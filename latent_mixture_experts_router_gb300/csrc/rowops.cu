@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kPermThreads) expert_count_kernel(const int32_
 __global__ void __launch_bounds__(kPermThreads) expert_scatter_kernel(
     const int32_t* __restrict__ idx, int n, int k, int E, const int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of,
-    Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles) {
+    Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles, int32_t* __restrict__ tile_base) {
   __shared__ int wsum[kPermThreads / 32];
   __shared__ int red[33];
   const int e = blockIdx.x;
@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(kPermThreads) expert_scatter_kernel(
   const int cnt = counts[e];
   if (threadIdx.x == 0) {
     offsets[e] = off;
+    if (tile_base != nullptr) tile_base[e] = tile0;   // first M tile of expert e
     if (e == E - 1) {
       offsets[E] = off + cnt;
       *n_tiles = tile0 + (cnt + kBM - 1) / kBM;
@@ -424,11 +425,20 @@ __device__ __forceinline__ void load_recip(float* recip) {
   for (int i = threadIdx.x; i < 256; i += blockDim.x) recip[i] = c_e4m3_recip.v[i];
 }
 
-// Quantises the K values of `buf` (shared memory) with row scale s into `nrows` destination
-// rows (codes row pitch K/2 bytes, scales row pitch K/16 bytes).
+// Destination row of a quantised row: codes at row `code_row` (pitch K/2 bytes); scales
+// row-major at `code_row` (pitch K/16) when blk < 0, else in the block layout at row block
+// `blk`, position `m`.
+struct QDest {
+  long long code_row;
+  long long blk;
+  int m;
+};
+
+// Quantises the K values of `buf` (shared memory) with row scale s into `ndst` destination
+// rows.
 __device__ __forceinline__ void quantize_row_to(const float* buf, int K, float s, const float* recip,
-                                                uint8_t* codes, uint8_t* scales, const int* rows,
-                                                int nrows) {
+                                                uint8_t* codes, uint8_t* scales, const QDest* dst,
+                                                int ndst) {
   const float six_s = __fmul_rn(6.f, s), inv_s = __fdiv_rn(1.f, s);
   for (int b = threadIdx.x; b < K / 16; b += blockDim.x) {
     float v[16];
@@ -436,10 +446,12 @@ __device__ __forceinline__ void quantize_row_to(const float* buf, int K, float s
     for (int i = 0; i < 16; ++i) v[i] = buf[b * 16 + i];
     uint2 q;
     const uint32_t sc = nvfp4_quant16(v, six_s, inv_s, recip, q);
-    for (int j = 0; j < nrows; ++j) {
-      const long long r = rows[j];
-      *reinterpret_cast<uint2*>(codes + r * (K / 2) + b * 8) = q;
-      scales[r * (K / 16) + b] = static_cast<uint8_t>(sc);
+    for (int j = 0; j < ndst; ++j) {
+      const QDest d = dst[j];
+      *reinterpret_cast<uint2*>(codes + d.code_row * (K / 2) + b * 8) = q;
+      const size_t so = d.blk < 0 ? static_cast<size_t>(d.code_row) * (K / 16) + b
+                                  : blocked_sf_offset(d.blk, d.m, b, K);
+      scales[so] = static_cast<uint8_t>(sc);
     }
   }
 }
@@ -454,7 +466,7 @@ __global__ void __launch_bounds__(kRowThreads) prenorm_nvfp4_kernel(
   float* buf = dyn;
   float* recip = dyn + D;
   __shared__ float red[33];
-  __shared__ int s_r;
+  __shared__ QDest s_d;
   load_recip(recip);
   const long long t = blockIdx.x;
   const long long xoff = t * D;
@@ -486,24 +498,25 @@ __global__ void __launch_bounds__(kRowThreads) prenorm_nvfp4_kernel(
   const float s = nvfp4_row_scale(block_max(amax, red));
   if (threadIdx.x == 0) {
     s_row[t] = s;
-    s_r = static_cast<int>(t);
+    s_d = QDest{t, t / kBM, static_cast<int>(t % kBM)};
   }
   __syncthreads();
-  quantize_row_to(buf, D, s, recip, codes, scales, &s_r, 1);
+  quantize_row_to(buf, D, s, recip, codes, scales, &s_d, 1);
 }
 
 // Pool norm whose output is quantised once (row scale per token) and written to the token's
 // k expert rows.  Dynamic smem: L + 256 floats.
 __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
     const float* __restrict__ p, const float* __restrict__ ss_p, int ld_ss, const float* __restrict__ g,
-    const int32_t* __restrict__ row_of, int L, int k, float eps, uint8_t* __restrict__ codes,
+    const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ tile_base, int L, int k, float eps, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, float* __restrict__ s_rows) {
   extern __shared__ float dyn[];
   float* buf = dyn;
   float* recip = dyn + L;
   __shared__ float red[33];
   __shared__ float s_rs;
-  __shared__ int s_rowsj[16];
+  __shared__ QDest s_dst[16];
   load_recip(recip);
   const long long t = blockIdx.x;
   if (threadIdx.x == 0) {
@@ -511,7 +524,12 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
     for (int q = 0; q < ld_ss; ++q) ss += ss_p[t * ld_ss + q];
     s_rs = rsqrtf(ss / static_cast<float>(L) + eps);
   }
-  if (threadIdx.x < k) s_rowsj[threadIdx.x] = row_of[t * k + threadIdx.x];
+  if (threadIdx.x < k) {   // the expert row, and its M tile (the scale block) and place in it
+    const int row = row_of[t * k + threadIdx.x];
+    const int e = idx[t * k + threadIdx.x];
+    const int pos = row - offsets[e];
+    s_dst[threadIdx.x] = QDest{row, tile_base[e] + pos / kBM, pos % kBM};
+  }
   __syncthreads();
   const float rs = s_rs;
   float amax = 0.f;
@@ -527,8 +545,8 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
     }
   }
   const float s = nvfp4_row_scale(block_max(amax, red));
-  if (threadIdx.x < k) s_rows[s_rowsj[threadIdx.x]] = s;
-  quantize_row_to(buf, L, s, recip, codes, scales, s_rowsj, k);
+  if (threadIdx.x < k) s_rows[s_dst[threadIdx.x].code_row] = s;
+  quantize_row_to(buf, L, s, recip, codes, scales, s_dst, k);
 }
 
 // Combine whose output c is quantised (row scale per token) for the unpooler.
@@ -544,7 +562,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
   __shared__ float red[33];
   __shared__ float s_coef[16];
   __shared__ int s_rowj[16], s_e[16];
-  __shared__ int s_t;
+  __shared__ QDest s_d;
   load_recip(recip);
   const long long t = blockIdx.x;
   if (threadIdx.x < k) {
@@ -576,10 +594,10 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
   const float s = nvfp4_row_scale(block_max(amax, red));
   if (threadIdx.x == 0) {
     s_row[t] = s;
-    s_t = static_cast<int>(t);
+    s_d = QDest{t, t / kBM, static_cast<int>(t % kBM)};
   }
   __syncthreads();
-  quantize_row_to(buf, L, s, recip, codes, scales, &s_t, 1);
+  quantize_row_to(buf, L, s, recip, codes, scales, &s_d, 1);
 }
 
 // Stand-alone quantiser: one CTA per row of src [rows, K] fp32.
@@ -590,7 +608,7 @@ __global__ void __launch_bounds__(kRowThreads) quantize_nvfp4_kernel(
   float* buf = dyn;
   float* recip = dyn + K;
   __shared__ float red[33];
-  __shared__ int s_t;
+  __shared__ QDest s_d;
   load_recip(recip);
   const long long t = blockIdx.x;
   float amax = 0.f;
@@ -603,10 +621,26 @@ __global__ void __launch_bounds__(kRowThreads) quantize_nvfp4_kernel(
   const float s = row_scale ? nvfp4_row_scale(amax) : 1.f;
   if (threadIdx.x == 0) {
     if (s_row) s_row[t] = s;
-    s_t = static_cast<int>(t);
+    s_d = QDest{t, -1, 0};   // row-major scales
   }
   __syncthreads();
-  quantize_row_to(buf, K, s, recip, codes, scales, &s_t, 1);
+  quantize_row_to(buf, K, s, recip, codes, scales, &s_d, 1);
+}
+
+// Row-major E4M3 scales [rows, K/16] -> block layout (rows a multiple of 128): one thread
+// moves the 4 scale bytes of one (row, 64-wide K step) as one word.
+__global__ void nvfp4_block_scales_kernel(const uint8_t* __restrict__ src, long long rows, int K,
+                                          uint8_t* __restrict__ dst) {
+  const long long words = rows * (K / 64);
+  for (long long w = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; w < words;
+       w += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = w / (K / 64);
+    const int k64 = static_cast<int>(w % (K / 64));
+    const uint8_t* p = src + r * (K / 16) + k64 * 4;
+    const uint32_t v = static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) |
+                       (static_cast<uint32_t>(p[2]) << 16) | (static_cast<uint32_t>(p[3]) << 24);
+    *reinterpret_cast<uint32_t*>(dst + blocked_sf_offset(r / kBM, static_cast<int>(r % kBM), k64 * 4, K)) = v;
+  }
 }
 
 // ------------------------------------------------------------------ wait self-test
@@ -641,9 +675,11 @@ cudaError_t launch_prenorm_nvfp4(const void* x, bool x_f32, const float* g_pre, 
 }
 
 cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int ld_ss,
-                                          const float* g_pool, const int32_t* row_of, int T, int L,
-                                          int k, float eps, uint8_t* codes, uint8_t* scales,
-                                          float* s_rows, cudaStream_t s) {
+                                          const float* g_pool, const int32_t* row_of,
+                                          const int32_t* idx, const int32_t* offsets,
+                                          const int32_t* tile_base, int T, int L, int k, float eps,
+                                          uint8_t* codes, uint8_t* scales, float* s_rows,
+                                          cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const size_t smem = (static_cast<size_t>(L) + 256) * sizeof(float);
   static bool attr = false;
@@ -653,8 +689,8 @@ cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int
     attr = true;
   }
   count_launch();
-  poolnorm_scatter_nvfp4_kernel<<<T, kRowThreads, smem, s>>>(p, ss_p, ld_ss, g_pool, row_of, L, k, eps,
-                                                             codes, scales, s_rows);
+  poolnorm_scatter_nvfp4_kernel<<<T, kRowThreads, smem, s>>>(p, ss_p, ld_ss, g_pool, row_of, idx, offsets,
+                                                             tile_base, L, k, eps, codes, scales, s_rows);
   return cudaGetLastError();
 }
 
@@ -692,6 +728,16 @@ cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool 
   return cudaGetLastError();
 }
 
+cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K, uint8_t* dst,
+                                      cudaStream_t s) {
+  const long long words = rows * (K / 64);
+  if (words == 0) return cudaSuccess;
+  const int blocks = static_cast<int>(std::min<long long>((words + 255) / 256, 152 * 32));
+  count_launch();
+  nvfp4_block_scales_kernel<<<blocks, 256, 0, s>>>(src, rows, K, dst);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s) {
   count_launch();
   wait_selftest_kernel<<<1, 32, 0, s>>>(budget, err);
@@ -720,7 +766,7 @@ cudaError_t launch_topk(const float* logits, int ld, const float* bias, const in
 
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
-                           int32_t* n_tiles, cudaStream_t s) {
+                           int32_t* n_tiles, cudaStream_t s, int32_t* tile_base) {
   const int n = T * k;
   count_launch();
   expert_count_kernel<<<E, kPermThreads, 0, s>>>(idx, n, counts);
@@ -728,7 +774,7 @@ cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* cou
   if (e != cudaSuccess) return e;
   count_launch();
   expert_scatter_kernel<<<E, kPermThreads, 0, s>>>(idx, n, k, E, counts, offsets, row_of, tok_of,
-                                                   tiles, n_tiles);
+                                                   tiles, n_tiles, tile_base);
   return cudaGetLastError();
 }
 
