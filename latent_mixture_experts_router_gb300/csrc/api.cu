@@ -13,6 +13,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <atomic>
 #include <mutex>
@@ -38,11 +39,44 @@ struct Layout {
   lmoe_workspace_layout pub;
   long long near_tie;
   long long tile_base;  // [E] first M tile of each expert
+  long long partial;    // split-K partial products of the dense GEMMs
   // fp32-weight mode: bf16 copies of the weights
   long long w_router, w_pool, w_gate, w_up, w_down, w_unpool;
   long long x_stage, out_stage, host_io_total;
   int ld_logits, ld_ss_p, ld_ss_y, ld_ss_u, max_tiles;
 };
+
+// Split-K for dense GEMMs with few output tiles (small T): enough K ranges to give the 152
+// SMs of a GB300 work, at least `min_kb` K blocks each, at most 32.  A fixed SM count keeps
+// the workspace layout independent of the device a call runs on.
+constexpr int kSplitSms = 152;
+int dense_splits(int T, int N, int bn, int num_kb, int min_kb) {
+  const long long tiles = static_cast<long long>((T + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+  if (tiles == 0 || tiles * 2 >= kSplitSms) return 1;
+  long long sp = kSplitSms / tiles;
+  if (sp > num_kb / min_kb) sp = num_kb / min_kb;
+  if (sp > 32) sp = 32;
+  return sp < 1 ? 1 : static_cast<int>(sp);
+}
+
+struct DenseSplits {
+  int router, pooler, unpool;
+};
+DenseSplits dense_split_plan(const lmoe_config* c) {
+  const bool f32w = c->weight_dtype == LMOE_F32, fp4 = c->weight_dtype == LMOE_NVFP4;
+  const int D = c->d_model, L = c->d_latent;
+  const int xa_cols = (f32w ? 3 : 2) * D, wsplit = f32w ? 2 : 1;
+  DenseSplits d;
+  d.router = dense_splits(c->T, c->n_experts, kBNWide, xa_cols / kBK, 4);
+  if (fp4) {
+    d.pooler = dense_splits(c->T, L, kBNFp4, D / 256, 2);
+    d.unpool = dense_splits(c->T, D, kBNFp4, L / 256, 2);
+  } else {
+    d.pooler = dense_splits(c->T, L, kBNWide, (f32w ? 3 * D : D) / kBK, 4);
+    d.unpool = dense_splits(c->T, D, kBNWide, wsplit * L / kBK, 4);
+  }
+  return d;
+}
 
 lmoe_status check_config(const lmoe_config* c) {
   if (c == nullptr) return LMOE_ERR_ARG;
@@ -137,6 +171,14 @@ void make_layout(const lmoe_config* c, Layout* L) {
     L->w_down = take(E * Ld * 2 * I * 2);
     L->w_unpool = take(D * 2 * Ld * 2);
   }
+  {  // split-K partials: the largest of the dense GEMMs' [splits][T][N]
+    const DenseSplits d = dense_split_plan(c);
+    long long need = 0;
+    if (d.router > 1) need = std::max(need, d.router * T * E);
+    if (d.pooler > 1) need = std::max(need, d.pooler * T * Ld);
+    if (d.unpool > 1) need = std::max(need, d.unpool * T * D);
+    L->partial = need > 0 ? take(need * 4) : -1;
+  }
   P.total = static_cast<long long>(off);
   L->x_stage = take(T * D * (c->act_dtype == LMOE_F32 ? 4 : 2));
   L->out_stage = take(T * D * (c->out_dtype == LMOE_F32 ? 4 : 2));
@@ -208,7 +250,8 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
                      long long b_cols, const void* B2, int N, int num_kb,
                      const Tile* tiles, const int* n_tiles, int m_tiles, void* out,
                      long long ldo, float* ss, int ld_ss, unsigned* err, long long budget,
-                     cudaStream_t s, long long rows_per_b) {
+                     cudaStream_t s, long long rows_per_b, int splits = 1,
+                     float* partial = nullptr) {
   const unsigned bn = epi == kEpiSwiGLU ? kBNSwiGLU : kBNWide;
   CUtensorMap ta, tb, tb2;
   if (!encode_bf16_2d(&ta, A, a_cols_used, a_rows, a_row_stride_elems * 2, kBK, kBM))
@@ -231,7 +274,12 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   a.err = err;
   a.budget = budget;
   a.b_stream_once = rows_per_b <= kBM;
+  a.k_splits = splits > 1 ? splits : 1;
+  a.partial = partial;
   LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s));
+  if (splits > 1)
+    LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
+                                   ldo, ss, ld_ss, kBNWide, s));
   return LMOE_OK;
 }
 
@@ -246,7 +294,8 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                          const int* n_tiles, int m_tiles, void* out, long long ldo,
                          uint8_t* out_scales, float* ss, int ld_ss, const float* row_scale,
                          const float* ts, const float* ts2, unsigned* err, long long budget,
-                         cudaStream_t s, long long rows_per_b) {
+                         cudaStream_t s, long long rows_per_b, int splits = 1,
+                         float* partial = nullptr) {
   CUtensorMap maps[3];
   const unsigned long long kc = K / 2;
   if (!encode_u8_2d(&maps[0], A.codes, kc, a_rows, kc, 128, kBM, true) ||
@@ -274,7 +323,12 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
   a.err = err;
   a.budget = budget;
   a.b_stream_once = rows_per_b <= kBM;
+  a.k_splits = splits > 1 ? splits : 1;
+  a.partial = partial;
   LMOE_CUDA(launch_gemm_fp4(epi, maps, a, m_tiles, s));
+  if (splits > 1)
+    LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
+                                   ldo, ss, ld_ss, kBNFp4, s));
   return LMOE_OK;
 }
 
@@ -383,6 +437,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     wun = at(L.w_unpool);
   }
   const int xa_cols = L.pub.xa_cols;
+  const DenseSplits dsp = dense_split_plan(cfg);
+  float* partial = L.partial >= 0 ? static_cast<float*>(at(L.partial)) : nullptr;
 
   // S1 pre-norm (NVFP4: xn is also quantised per token for the pooler)
   uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
@@ -396,7 +452,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   const int m_tiles_T = cdiv(T, kBM);
   st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
                 xa_cols / kBK, nullptr, nullptr, m_tiles_T, logits, L.ld_logits, nullptr, 0, err,
-                budget, s, T);
+                budget, s, T, dsp.router, partial);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_TOPK);
   // S3 top-k + softmax
@@ -422,7 +478,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     LMOE_MARK(LMOE_STAGE_POOLER);
     // S5 pooler p = s_x * s_W * (Q(xn) . W_pool^T), block-scaled FP4 MMA
     st = run_gemm_fp4(kFp4EpiF32Ss, xq, T, D, op(q4[0]), Ld, nullptr, Ld, nullptr, nullptr, m_tiles_T,
-                      p, Ld, nullptr, ss_p, L.ld_ss_p, xq_s, q4[0]->tensor_scale, nullptr, err, budget, s, T);
+                      p, Ld, nullptr, ss_p, L.ld_ss_p, xq_s, q4[0]->tensor_scale, nullptr, err, budget, s, T, dsp.pooler, partial);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_POOLNORM);
     // S6 pool norm, quantised per token, copied to the k expert rows
@@ -449,14 +505,14 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     LMOE_MARK(LMOE_STAGE_UNPOOLER);
     // S10 unpooler u = s_c * s_W * (Q(c) . W_unpool^T)
     st = run_gemm_fp4(kFp4EpiF32Ss, cq, T, Ld, op(q4[4]), D, nullptr, D, nullptr, nullptr, m_tiles_T, u,
-                      D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s, T);
+                      D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s, T, dsp.unpool, partial);
     if (st != LMOE_OK) return st;
   } else {
   LMOE_MARK(LMOE_STAGE_POOLER);
   // S5 pooler p = xn_hi . W_pool^T, with row partial sums of squares
   const int pool_k = f32w ? 3 * D : D;
   st = run_gemm(kEpiF32Ss, xa, T, pool_k, xa_cols, wp, Ld, pool_k, nullptr, Ld, pool_k / kBK,
-                nullptr, nullptr, m_tiles_T, p, Ld, ss_p, L.ld_ss_p, err, budget, s, T);
+                nullptr, nullptr, m_tiles_T, p, Ld, ss_p, L.ld_ss_p, err, budget, s, T, dsp.pooler, partial);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_POOLNORM);
   // S6 pool norm, scattered to the k expert-contiguous rows of each token
@@ -477,7 +533,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   LMOE_MARK(LMOE_STAGE_UNPOOLER);
   // S10 unpooler u = c . W_unpool^T with row partial sums of squares
   st = run_gemm(kEpiF32Ss, c, T, Ld, Ld, wun, D, 1LL * wsplit * Ld, nullptr, D, wsplit * Ld / kBK,
-                nullptr, nullptr, m_tiles_T, u, D, ss_u, L.ld_ss_u, err, budget, s, T);
+                nullptr, nullptr, m_tiles_T, u, D, ss_u, L.ld_ss_u, err, budget, s, T, dsp.unpool, partial);
   if (st != LMOE_OK) return st;
   }
   LMOE_MARK(LMOE_STAGE_POSTNORM);

@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* mma_done = acc_empty + 2;         // every MMA of this CTA has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
-  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN);
+  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb);
   if (static_cast<int>(blockIdx.x) >= walk.n_ids) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -102,7 +102,9 @@ __global__ void __launch_bounds__(192, 1)
         int expert, row0, nrows, ntile;
         if (!walk.at(id, expert, row0, nrows, ntile)) continue;
         const int brow = expert * args.N + ntile * BN;
-        for (int kb = 0; kb < args.num_kb; ++kb) {
+        int kb0, kb1;
+        walk.k_range(id, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           const int s = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, budget)) {
@@ -142,7 +144,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_fence_after();
         const uint32_t acc = tmem + buf * C::kAccCols;
-        for (int kb = 0; kb < args.num_kb; ++kb) {
+        int kb0, kb1;
+        walk.k_range(id, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           const int s = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
           if (!mbar_wait(&full[s], ph, budget)) {
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t ad = sw128_kmajor_desc(a0 + kk * 32);
-            const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
             mma_bf16(acc, ad, sw128_kmajor_desc(b0 + kk * 32), idesc, accum);
             if (C::kDual)
               mma_bf16(acc + BN, ad, sw128_kmajor_desc(b0 + C::kBBytes + kk * 32), idesc, accum);
@@ -188,7 +192,28 @@ __global__ void __launch_bounds__(192, 1)
       const long long grow = static_cast<long long>(row0) + r;
       const int n0 = ntile * BN;
       const uint32_t tq = tmem + buf * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
-      if constexpr (EPI == kEpiF32) {
+      if (EPI != kEpiSwiGLU && args.k_splits > 1) {
+        // split-K: raw fp32 partial product of this K range; the reduction finishes the tile
+        float* prow = args.partial + (static_cast<long long>(id % args.k_splits) * args.M + grow) * args.N;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_32cols(tq + c0, v);
+          tmem_ld_wait();
+          const int col = n0 + c0;
+          if (row_ok && col + 32 <= args.N) {
+            float4* o = reinterpret_cast<float4*>(prow + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              o[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          } else if (row_ok && col < args.N) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col + i < args.N) prow[col + i] = __uint_as_float(v[i]);
+          }
+        }
+      } else if constexpr (EPI == kEpiF32) {
         float* orow = static_cast<float*>(args.out) + grow * args.ldo;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -300,7 +325,7 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
     attr_set = true;
   }
   // upper bound of the tile ids (the live M-tile count of a grouped GEMM is on the device)
-  const long long ids = tile_id_bound(m_tiles, a.N, BN);
+  const long long ids = tile_id_bound(m_tiles, a.N, BN, a.k_splits > 1 ? a.k_splits : 1);
   if (ids == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
   count_launch();

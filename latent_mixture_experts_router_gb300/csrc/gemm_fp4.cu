@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
-  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN);
+  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb);
   if (static_cast<int>(blockIdx.x) >= walk.n_ids) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -165,7 +165,9 @@ __global__ void __launch_bounds__(192, 1)
         const uint8_t* sfa_src = args.a_scales + static_cast<size_t>(mt) * kblk * 512;
         const uint8_t* sfb_src = args.b_scales + static_cast<size_t>(brow / kBM) * kblk * 512;
         const uint8_t* sfb2_src = C::kDual ? args.b2_scales + static_cast<size_t>(brow / kBM) * kblk * 512 : nullptr;
-        for (int kb = 0; kb < nk; ++kb) {
+        int kb0, kb1;
+        walk.k_range(id, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           const int s = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, budget)) {
@@ -207,7 +209,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_fence_after();
         const uint32_t acc = tmem + buf * C::kAccCols;
-        for (int kb = 0; kb < nk; ++kb) {
+        int kb0, kb1;
+        walk.k_range(id, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           const int s = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
           if (!mbar_wait(&full[s], ph, budget)) {
@@ -232,7 +236,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < C::kKStep; ++j) {
             const uint64_t ad = sw128_kmajor_desc(st + j * 32);
-            const uint32_t accum = (kb > 0 || j > 0) ? 1u : 0u;
+            const uint32_t accum = (kb > kb0 || j > 0) ? 1u : 0u;
             mma_nvf4(acc, ad, sw128_kmajor_desc(st + C::kOffB + j * 32), idesc, sfa + j * 4,
                      sfb + j * (BN / 32), accum);
             if (C::kDual)
@@ -269,7 +273,9 @@ __global__ void __launch_bounds__(192, 1)
       const float rs = (args.row_scale != nullptr && row_ok) ? args.row_scale[grow] : 1.f;
       if constexpr (EPI == kFp4EpiF32Ss) {
         const float alpha = rs * args.tensor_scale[args.tiles ? expert : 0];
-        float* orow = static_cast<float*>(args.out) + grow * args.ldo;
+        const bool split = args.k_splits > 1;   // split-K: alpha * partial product, no ss
+        float* orow = split ? args.partial + (static_cast<long long>(id % args.k_splits) * args.M + grow) * args.N
+                            : static_cast<float*>(args.out) + grow * args.ldo;
         float ss = 0.f;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(192, 1)
             }
           }
         }
-        if (row_ok) args.ss[grow * args.ld_ss + ntile] = ss;
+        if (row_ok && !split) args.ss[grow * args.ld_ss + ntile] = ss;
       } else {  // kFp4EpiSwiGLUQuant
         const int e = args.tiles ? expert : 0;
         const float ag = rs * args.tensor_scale[e], au = rs * args.tensor_scale2[e];
@@ -351,7 +357,7 @@ cudaError_t launch_fp4_one(const CUtensorMap* maps, const Fp4Args& a, int m_tile
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long long ids = tile_id_bound(m_tiles, a.N, BN);
+  const long long ids = tile_id_bound(m_tiles, a.N, BN, a.k_splits > 1 ? a.k_splits : 1);
   if (ids == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
   count_launch();

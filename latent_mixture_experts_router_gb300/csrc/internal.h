@@ -55,6 +55,8 @@ struct GemmArgs {
   unsigned* err;           // device error word
   long long budget;        // wait budget, SM cycles
   int b_stream_once;       // B tiles are read by ~one M tile each: stream them evict-first
+  int k_splits;            // > 1: split-K; the epilogue writes raw fp32 partial products
+  float* partial;          // [k_splits][rows][N] (split-K), reduced by launch_splitk_reduce
 };
 
 struct Fp4Args {
@@ -77,6 +79,8 @@ struct Fp4Args {
   unsigned* err;
   long long budget;
   int b_stream_once;         // B tiles are read by ~one M tile each: stream them evict-first
+  int k_splits;              // > 1: split-K; the epilogue writes alpha * partial products
+  float* partial;            // [k_splits][rows][N] (split-K), reduced by launch_splitk_reduce
 };
 
 // NVFP4 GEMM; maps = {A codes, B codes, B2 codes}; scales come from the Fp4Args pointers.
@@ -105,6 +109,11 @@ cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool 
 
 // Streaming multiprocessors of the current device (persistent grids).
 int sm_count();
+
+// Sums split-K partials [splits][rows][N] in split order into out [rows, ldo] (fp32) and, when
+// ss != nullptr, writes per-row partial sums of squares per group of `group` columns.
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, float* out,
+                                 long long ldo, float* ss, int ld_ss, int group, cudaStream_t s);
 
 // Counts every kernel launch of the library (lmoe_kernel_launches).
 void count_launch();

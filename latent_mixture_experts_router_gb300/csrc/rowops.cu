@@ -643,6 +643,26 @@ __global__ void nvfp4_block_scales_kernel(const uint8_t* __restrict__ src, long 
   }
 }
 
+// ------------------------------------------------------------------ split-K reduction
+// One CTA of `group` threads per (row, column group): sums the partials in split order (the
+// result does not depend on scheduling) and writes the group's sum of squares.
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, int rows, int N,
+                                     float* __restrict__ out, long long ldo, float* __restrict__ ss,
+                                     int ld_ss) {
+  __shared__ float red[33];
+  const int r = blockIdx.x, grp = blockIdx.y;
+  const int col = grp * blockDim.x + threadIdx.x;
+  float v = 0.f;
+  if (col < N) {
+    for (int q = 0; q < splits; ++q) v += partial[(static_cast<long long>(q) * rows + r) * N + col];
+    out[static_cast<long long>(r) * ldo + col] = v;
+  }
+  if (ss != nullptr) {
+    const float t = block_sum(col < N ? v * v : 0.f, red);
+    if (threadIdx.x == 0) ss[static_cast<long long>(r) * ld_ss + grp] = t;
+  }
+}
+
 // ------------------------------------------------------------------ wait self-test
 // One thread waits on a barrier that is initialised for one arrival that never comes.
 __global__ void wait_selftest_kernel(long long budget, unsigned* err) {
@@ -735,6 +755,15 @@ cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K,
   const int blocks = static_cast<int>(std::min<long long>((words + 255) / 256, 152 * 32));
   count_launch();
   nvfp4_block_scales_kernel<<<blocks, 256, 0, s>>>(src, rows, K, dst);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, float* out,
+                                 long long ldo, float* ss, int ld_ss, int group, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  dim3 grid(rows, (N + group - 1) / group);
+  count_launch();
+  splitk_reduce_kernel<<<grid, group, 0, s>>>(partial, splits, rows, N, out, ldo, ss, ld_ss);
   return cudaGetLastError();
 }
 

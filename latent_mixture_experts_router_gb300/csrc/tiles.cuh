@@ -10,12 +10,22 @@ namespace lmoe {
 // alike.  Grouped GEMMs take their M tiles from the device tile table.
 struct TileWalk {
   const Tile* tiles;
-  int M, N, total_m, nt, n_ids, bn;
-  LMOE_DEV TileWalk(const Tile* tiles_, const int* n_tiles, int M_, int N_, int bn_)
-      : tiles(tiles_), M(M_), N(N_), bn(bn_) {
+  int M, N, total_m, nt, n_ids, bn, splits, num_kb, kb_per_split;
+  // splits > 1: every output tile is computed as `splits` partial products over disjoint K
+  // ranges (split-K), consecutive ids taking the K ranges of one tile
+  LMOE_DEV TileWalk(const Tile* tiles_, const int* n_tiles, int M_, int N_, int bn_, int splits_ = 1,
+                    int num_kb_ = 1)
+      : tiles(tiles_), M(M_), N(N_), bn(bn_), splits(splits_ < 1 ? 1 : splits_), num_kb(num_kb_) {
     total_m = tiles != nullptr ? *n_tiles : (M + kBM - 1) / kBM;
     nt = (N + bn - 1) / bn;
-    n_ids = ((total_m + kRasterGroup - 1) / kRasterGroup) * kRasterGroup * nt;
+    n_ids = ((total_m + kRasterGroup - 1) / kRasterGroup) * kRasterGroup * nt * splits;
+    kb_per_split = (num_kb + splits - 1) / splits;
+  }
+  // K blocks [kb0, kb1) of tile id (all of K without split-K)
+  LMOE_DEV void k_range(int id, int& kb0, int& kb1) const {
+    const int ks = id % splits;
+    kb0 = ks * kb_per_split;
+    kb1 = min(num_kb, kb0 + kb_per_split);
   }
   // (expert, first row, rows, N tile) of tile id; false if the id is padding
   LMOE_DEV bool at(int id, int& expert, int& row0, int& nrows, int& ntile) const {
@@ -24,7 +34,10 @@ struct TileWalk {
   }
   // same, also returning the M tile index (the row block of block-layout scales)
   LMOE_DEV bool at(int id, int& mt, int& expert, int& row0, int& nrows, int& ntile) const {
-    if (!grouped_tile(id, total_m, nt, kRasterGroup, mt, ntile)) return false;
+    if (!grouped_tile(id / splits, total_m, nt, kRasterGroup, mt, ntile)) return false;
+    int kb0, kb1;
+    k_range(id, kb0, kb1);
+    if (kb0 >= kb1) return false;
     if (tiles != nullptr) {
       const Tile t = tiles[mt];
       expert = t.expert;
@@ -40,9 +53,9 @@ struct TileWalk {
 };
 
 // Upper bound of the tile ids of a launch (host side): m_tiles M tiles of at most kBM rows.
-inline long long tile_id_bound(int m_tiles, int N, int bn) {
+inline long long tile_id_bound(int m_tiles, int N, int bn, int splits = 1) {
   const long long nt = (N + bn - 1) / bn;
-  return (m_tiles + kRasterGroup - 1) / kRasterGroup * kRasterGroup * nt;
+  return (m_tiles + kRasterGroup - 1) / kRasterGroup * kRasterGroup * nt * splits;
 }
 
 }  // namespace lmoe
