@@ -78,10 +78,11 @@ typedef struct {
 /* One NVFP4-packed weight (host struct holding device pointers), "out x in" [rows, K]:
  *  data          [rows, K/2] bytes, two E2M1 codes per byte, the low nibble holds the even k
  *  scales        E4M3 block-scale codes (one per 16 consecutive k) in the tensor cores' block
- *                layout: 512-byte blocks of 128 rows x 64 k, ordered [rows/128][K/64]; inside a
- *                block the scale of row m = m0 + 32*m1 and 16-wide group kk sits at byte
- *                16*m0 + 4*m1 + kk.  lmoe_nvfp4_block_scales() converts the row-major
- *                [rows, K/16] array once (for expert stacks, rows = E*rows_per_expert).
+ *                layout: 512-byte blocks of 128 rows x 64 k, ordered [rows/128][K/64]; inside
+ *                a block the scale of row m = m0 + 32*m1 and 16-wide group kk sits at byte
+ *                16*m0 + 4*m1 + kk.
+ *                lmoe_nvfp4_block_scales() converts the row-major [rows, K/16] array once
+ *                (for expert stacks, rows = E*rows_per_expert).
  *  tensor_scale  fp32 second-level scale: 1 value, or one per expert for expert stacks
  *  value = e2m1(code) * e4m3(scale) * tensor_scale.                                    */
 typedef struct {
@@ -206,10 +207,12 @@ lmoe_status lmoe_quantize_nvfp4(const float* src, long long rows, int K, int row
                                 cudaStream_t stream);
 
 /* Converts row-major E4M3 block scales [rows, K/16] (device) into the block layout that
- * lmoe_nvfp4_weight.scales uses (device, rows*K/16 bytes, may not alias src).  rows must be
- * a multiple of 128 and K of 64.  Asynchronous on `stream`; a one-time weight preparation. */
-lmoe_status lmoe_nvfp4_block_scales(const uint8_t* src, long long rows, int K, uint8_t* dst,
-                                    cudaStream_t stream);
+ * lmoe_nvfp4_weight.scales uses, with blocks of block_rows = 128 or 64 rows (device,
+ * (rows/block_rows) * (K/64) * 512 bytes: rows*K/16 for 128, twice that for 64; may not alias
+ * src).  rows must be a multiple of block_rows and K of 64.  Asynchronous on `stream`; a
+ * one-time weight preparation.                                                            */
+lmoe_status lmoe_nvfp4_block_scales(const uint8_t* src, long long rows, int K, int block_rows,
+                                    uint8_t* dst, cudaStream_t stream);
 
 /* Diagnostic of the device wait-timeout path: launches one CTA that waits on an
  * mbarrier nothing ever arrives on, with a budget of `budget_cycles` SM cycles

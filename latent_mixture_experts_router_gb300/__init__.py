@@ -39,9 +39,9 @@ class LatentMoEBlock:
     def __init__(self, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool, g_pre,
                  g_post, top_k: int, eps: float = 1e-6, weight_dtype: str = "bf16"):
         if weight_dtype == "nvfp4":   # (codes, row-major scales, s) -> scales in block layout
-            def blocked(w):
+            def blocked(w, block_rows=128):
                 codes, scales, s = w
-                return codes, lmoe_nvfp4_block_scales(scales, codes.shape[-1] * 2), s
+                return codes, lmoe_nvfp4_block_scales(scales, codes.shape[-1] * 2, block_rows), s
             W_pool, W_gate, W_up, W_down, W_unpool = map(blocked, (W_pool, W_gate, W_up, W_down, W_unpool))
         self.W = dict(W_router=W_router, W_pool=W_pool, g_pool=g_pool, W_gate=W_gate, W_up=W_up,
                       W_down=W_down, g_expert=g_expert, W_unpool=W_unpool, g_pre=g_pre, g_post=g_post)

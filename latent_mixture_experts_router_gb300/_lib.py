@@ -270,15 +270,17 @@ def lmoe_quantize_nvfp4(src, codes, scales, s_row=None, row_scale=True, stream=N
               _stream(stream)), "lmoe_quantize_nvfp4")
 
 
-def lmoe_nvfp4_block_scales(src, K: int, dst=None, stream=None):
+def lmoe_nvfp4_block_scales(src, K: int, block_rows: int = 128, dst=None, stream=None):
     """Row-major E4M3 scales ``src`` [..., rows, K/16] (uint8, device) -> the block layout the
-    NVFP4 GEMMs read (a new tensor of the same size unless ``dst`` is given)."""
+    NVFP4 GEMMs read, in blocks of ``block_rows`` (128, or 64 for W_gate/W_up) rows; returns a
+    flat uint8 tensor unless ``dst`` is given."""
     L = _lib()
     fn = L.lmoe_nvfp4_block_scales
-    fn.argtypes = [_P, ctypes.c_longlong, ctypes.c_int, _P, _P]
+    fn.argtypes = [_P, ctypes.c_longlong, ctypes.c_int, ctypes.c_int, _P, _P]
     fn.restype = ctypes.c_int
     rows = src.numel() // (K // 16)
     if dst is None:
-        dst = torch.empty_like(src)
-    _check(fn(_ptr(src), rows, int(K), _ptr(dst), _stream(stream)), "lmoe_nvfp4_block_scales")
+        dst = torch.zeros(rows // block_rows * (K // 64) * 512, dtype=torch.uint8, device=src.device)
+    _check(fn(_ptr(src), rows, int(K), int(block_rows), _ptr(dst), _stream(stream)),
+           "lmoe_nvfp4_block_scales")
     return dst

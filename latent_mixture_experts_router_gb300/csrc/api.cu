@@ -296,13 +296,14 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                          const float* ts, const float* ts2, unsigned* err, long long budget,
                          cudaStream_t s, long long rows_per_b, int splits = 1,
                          float* partial = nullptr) {
-  CUtensorMap maps[3];
+  CUtensorMap maps[6];
   const unsigned long long kc = K / 2;
-  if (!encode_u8_2d(&maps[0], A.codes, kc, a_rows, kc, 128, kBM, true) ||
-      !encode_u8_2d(&maps[1], B.codes, kc, b_rows, kc, 128, kBNFp4, true))
-    return LMOE_ERR_CUDA;
-  maps[2] = maps[1];
-  if (B2 && !encode_u8_2d(&maps[2], B2->codes, kc, b_rows, kc, 128, kBNFp4, true)) return LMOE_ERR_CUDA;
+  const unsigned bn = kBNFp4;
+  for (int i = 0; i < 4; ++i)  // A boxes of 32, 64, 96, 128 rows (the tile's live rows)
+    if (!encode_u8_2d(&maps[i], A.codes, kc, a_rows, kc, 128, 32 * (i + 1), true)) return LMOE_ERR_CUDA;
+  if (!encode_u8_2d(&maps[4], B.codes, kc, b_rows, kc, 128, bn, true)) return LMOE_ERR_CUDA;
+  maps[5] = maps[4];
+  if (B2 && !encode_u8_2d(&maps[5], B2->codes, kc, b_rows, kc, 128, bn, true)) return LMOE_ERR_CUDA;
   Fp4Args a{};
   a.M = static_cast<int>(a_rows);
   a.N = N;
@@ -661,14 +662,16 @@ lmoe_status lmoe_quantize_nvfp4(const float* src, long long rows, int K, int row
   return LMOE_OK;
 }
 
-lmoe_status lmoe_nvfp4_block_scales(const uint8_t* src, long long rows, int K, uint8_t* dst,
-                                    cudaStream_t stream) {
-  if (rows < 0 || rows % kBM || K <= 0 || K % 64) return LMOE_ERR_ARG;
+lmoe_status lmoe_nvfp4_block_scales(const uint8_t* src, long long rows, int K, int block_rows,
+                                    uint8_t* dst, cudaStream_t stream) {
+  if (block_rows != 64 && block_rows != 128) return LMOE_ERR_ARG;
+  if (rows < 0 || rows % block_rows || K <= 0 || K % 64) return LMOE_ERR_ARG;
   if (rows == 0) return LMOE_OK;
   if (src == nullptr || dst == nullptr || src == dst) return LMOE_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(dst) & 3u) || (reinterpret_cast<uintptr_t>(src) & 3u))
     return LMOE_ERR_ALIGN;
-  if (launch_nvfp4_block_scales(src, rows, K, dst, stream) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (launch_nvfp4_block_scales(src, rows, K, block_rows, dst, stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
   return LMOE_OK;
 }
 

@@ -271,8 +271,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float a0 = __uint_as_float(g[2 * i]), a1 = __uint_as_float(g[2 * i + 1]);
-              const float h0 = a0 / (1.f + __expf(-a0)) * __uint_as_float(u[2 * i]);
-              const float h1 = a1 / (1.f + __expf(-a1)) * __uint_as_float(u[2 * i + 1]);
+              const float h0 = __fdividef(a0, 1.f + __expf(-a0)) * __uint_as_float(u[2 * i]);
+              const float h1 = __fdividef(a1, 1.f + __expf(-a1)) * __uint_as_float(u[2 * i + 1]);
               pk[i] = pack_bf16x2(h0, h1);
             }
             uint4* o = reinterpret_cast<uint4*>(orow + col);

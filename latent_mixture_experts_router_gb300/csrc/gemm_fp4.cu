@@ -19,12 +19,14 @@
 //   warp 1          TMEM allocation; lane 0 copies scale factors into TMEM (tcgen05.cp) and
 //                   issues tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //   warps 2..5      epilogue (warp w owns TMEM lanes 32*(w%4) ..)
+// The A box covers only the tile's live rows rounded up to 32 (a decode tile holds a few
+// rows of one expert), and the producer loads the next tile's table entry one tile ahead.
 // Epilogues: kFp4EpiF32Ss — alpha * acc as fp32 plus per-row partial sums of squares; two
 // accumulator buffers, so the next tile's MMAs overlap this tile's epilogue.
 // kFp4EpiSwiGLUQuant — gate and up tiles of the same columns, h = silu(alpha_g acc_g) *
 // (alpha_u acc_u) requantised to NVFP4 with scale 1 (block scales only, through the
-// reciprocal table) for the down projection; one accumulator buffer (two would not leave
-// tensor memory for the scale factors), while TMA and the regrouping run ahead.
+// reciprocal table) for the down projection; one accumulator buffer (two would leave no
+// tensor memory for the scale factors), while TMA runs ahead.
 #include "internal.h"
 #include "nvfp4.cuh"
 #include "ptx.cuh"
@@ -77,22 +79,24 @@ struct Fp4Cfg {
   static constexpr int kNB = kDual ? 2 : 1;
   static constexpr int kStages = kDual ? 4 : 6;
   static constexpr int kKStep = 4;                 // MMAs (K = 64 each) per stage
-  static constexpr int kABytes = kBM * 128;        // codes
+  static constexpr int kABytes = kBM * 128;        // codes (at most; the box follows the live rows)
   static constexpr int kBBytes = BN * 128;
-  static constexpr int kSfaBytes = kBM * 16;       // block-layout scales of the stage
-  static constexpr int kSfbBytes = BN * 16;
-  static constexpr int kBAtoms = BN / 128;         // 128-row scale blocks per B operand
+  static constexpr int kSfaBytes = 4 * 512;        // block-layout scales of the stage: one
+  static constexpr int kSfbBytes = 4 * 512;        // 512-byte block per K step (B: BN-row blocks)
   // stage layout: [A codes][B codes x kNB][A scales][B scales x kNB]
   static constexpr int kOffB = kABytes;
   static constexpr int kOffSfa = kOffB + kNB * kBBytes;
   static constexpr int kOffSfb = kOffSfa + kSfaBytes;
   static constexpr int kStageBytes = kOffSfb + kNB * kSfbBytes;
-  static constexpr uint32_t kTxBytes = kStageBytes;
-  // tensor memory: accumulator buffer(s), then per-stage scale columns
+  // bytes landing per stage when the A box has `arows` rows
+  static constexpr __host__ __device__ uint32_t tx_bytes(int arows) {
+    return static_cast<uint32_t>(arows * 128 + kSfaBytes + kNB * (kBBytes + kSfbBytes));
+  }
+  // tensor memory: accumulator buffer(s), then per-stage scale columns (4 per K step)
   static constexpr int kAccCols = kNB * BN;
-  static constexpr int kAccBufs = kDual ? 1 : 2;
-  static constexpr int kSfaCols = kKStep * 4;                // 4 columns per 128 rows per MMA
-  static constexpr int kSfbColsOne = kKStep * (BN / 32);
+  static constexpr int kAccBufs = kDual ? 1 : 2;   // two gate+up buffers would leave no room for scales
+  static constexpr int kSfaCols = kKStep * 4;
+  static constexpr int kSfbColsOne = kKStep * 4;
   static constexpr int kSfCols = kSfaCols + kNB * kSfbColsOne;
   static constexpr int kSfCol0 = kAccBufs * kAccCols;
   static constexpr uint32_t kTmemCols = 512;
@@ -105,8 +109,10 @@ struct Fp4Cfg {
 
 template <int BN, int EPI>
 __global__ void __launch_bounds__(192, 1)
-    gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmB2, const Fp4Args args) {
+    gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA32, const __grid_constant__ CUtensorMap tmA64,
+                    const __grid_constant__ CUtensorMap tmA96, const __grid_constant__ CUtensorMap tmA128,
+                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
+                    const Fp4Args args) {
   using C = Fp4Cfg<BN, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -134,7 +140,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
-    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmA128);
     prefetch_tmap(&tmB);
   }
   if (warp >= 2 && warp <= 5) {
@@ -155,18 +161,26 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       // ---- TMA producer
       const uint64_t pol_b = args.b_stream_once ? policy_evict_first() : policy_evict_normal();
+      const CUtensorMap* amap[4] = {&tmA32, &tmA64, &tmA96, &tmA128};  // A box of 32/64/96/128 rows
+      const int kblk = args.num_kb * 4;   // 512-byte scale blocks per row block
       int it = 0;
       bool ok = true;
-      for (int id = blockIdx.x; ok && id < walk.n_ids; id += gridDim.x) {
-        int mt, expert, row0, nrows, ntile;
-        if (!walk.at(id, mt, expert, row0, nrows, ntile)) continue;
-        const int brow = expert * args.N + ntile * BN;
-        const int kblk = args.num_kb * 4;   // 512-byte scale blocks per 128-row block
-        const uint8_t* sfa_src = args.a_scales + static_cast<size_t>(mt) * kblk * 512;
-        const uint8_t* sfb_src = args.b_scales + static_cast<size_t>(brow / kBM) * kblk * 512;
-        const uint8_t* sfb2_src = C::kDual ? args.b2_scales + static_cast<size_t>(brow / kBM) * kblk * 512 : nullptr;
+      TileRef cur = find_tile(walk, blockIdx.x);
+      Tile ct = cur.valid ? tile_of(walk, cur.mt) : Tile{0, 0, 0, 0};
+      while (ok && cur.valid) {
+        // the next tile's table entry is loaded now and used after this tile has streamed
+        const TileRef nxt = find_tile(walk, cur.id + gridDim.x);
+        const Tile nt = nxt.valid ? tile_of(walk, nxt.mt) : Tile{0, 0, 0, 0};
+        const int row0 = ct.row0;
+        const int brow = ct.expert * args.N + cur.ntile * BN;
+        const int abox = min(4, (ct.nrows + 31) / 32);   // A rows past the live ones are not read
+        const CUtensorMap* tA = amap[abox - 1];
+        const uint32_t tx = C::tx_bytes(abox * 32);
+        const uint8_t* sfa_src = args.a_scales + static_cast<size_t>(cur.mt) * kblk * 512;
+        const uint8_t* sfb_src = args.b_scales + static_cast<size_t>(brow / BN) * kblk * 512;
+        const uint8_t* sfb2_src = C::kDual ? args.b2_scales + static_cast<size_t>(brow / BN) * kblk * 512 : nullptr;
         int kb0, kb1;
-        walk.k_range(id, kb0, kb1);
+        walk.k_range(cur.id, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
           const int s = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
@@ -176,8 +190,8 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           uint8_t* st = smem + s * C::kStageBytes;
-          mbar_arrive_expect_tx(&full[s], C::kTxBytes);
-          tma_load_2d(st, &tmA, &full[s], kb * 128, row0);
+          mbar_arrive_expect_tx(&full[s], tx);
+          tma_load_2d(st, tA, &full[s], kb * 128, row0);
           bulk_load(st + C::kOffSfa, sfa_src + kb * 2048, C::kSfaBytes, &full[s]);
           tma_load_2d_hint(st + C::kOffB, &tmB, &full[s], kb * 128, brow, pol_b);
           bulk_load(st + C::kOffSfb, sfb_src + kb * 2048, C::kSfbBytes, &full[s]);
@@ -187,6 +201,8 @@ __global__ void __launch_bounds__(192, 1)
           }
           ++it;
         }
+        cur = nxt;
+        ct = nt;
       }
       for (int j = max(0, it - C::kStages); j < it; ++j)
         if (!mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, kDrainBudget))
@@ -228,20 +244,18 @@ __global__ void __launch_bounds__(192, 1)
             tmem_cp_32x128b_x4(sfa + j * 4, sf_desc(st + C::kOffSfa + j * 512));
 #pragma unroll
             for (int b = 0; b < C::kNB; ++b)
-#pragma unroll
-              for (int a = 0; a < C::kBAtoms; ++a)
-                tmem_cp_32x128b_x4(sfb + b * C::kSfbColsOne + j * (BN / 32) + a * 4,
-                                   sf_desc(st + C::kOffSfb + b * C::kSfbBytes + j * C::kBAtoms * 512 + a * 512));
+              tmem_cp_32x128b_x4(sfb + b * C::kSfbColsOne + j * 4,
+                                 sf_desc(st + C::kOffSfb + b * C::kSfbBytes + j * 512));
           }
 #pragma unroll
           for (int j = 0; j < C::kKStep; ++j) {
             const uint64_t ad = sw128_kmajor_desc(st + j * 32);
             const uint32_t accum = (kb > kb0 || j > 0) ? 1u : 0u;
             mma_nvf4(acc, ad, sw128_kmajor_desc(st + C::kOffB + j * 32), idesc, sfa + j * 4,
-                     sfb + j * (BN / 32), accum);
+                     sfb + j * 4, accum);
             if (C::kDual)
               mma_nvf4(acc + BN, ad, sw128_kmajor_desc(st + C::kOffB + C::kBBytes + j * 32), idesc,
-                       sfa + j * 4, sfb + C::kSfbColsOne + j * (BN / 32), accum);
+                       sfa + j * 4, sfb + C::kSfbColsOne + j * 4, accum);
           }
           mma_commit(&empty[s]);
           ++it;
@@ -319,7 +333,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 const float a = __uint_as_float(g[blk * 16 + i]) * ag;
-                h[i] = a / (1.f + __expf(-a)) * (__uint_as_float(u[blk * 16 + i]) * au);
+                h[i] = __fdividef(a, 1.f + __expf(-a)) * (__uint_as_float(u[blk * 16 + i]) * au);  // silu(a) * b
               }
               sc[blk] = nvfp4_quant16(h, 6.f, 1.f, recip, q[blk]);
             }
@@ -361,7 +375,7 @@ cudaError_t launch_fp4_one(const CUtensorMap* maps, const Fp4Args& a, int m_tile
   if (ids == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
   count_launch();
-  kern<<<grid, 192, C::kSmemBytes, s>>>(maps[0], maps[1], maps[2], a);
+  kern<<<grid, 192, C::kSmemBytes, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
   return cudaGetLastError();
 }
 

@@ -83,7 +83,8 @@ struct Fp4Args {
   float* partial;            // [k_splits][rows][N] (split-K), reduced by launch_splitk_reduce
 };
 
-// NVFP4 GEMM; maps = {A codes, B codes, B2 codes}; scales come from the Fp4Args pointers.
+// NVFP4 GEMM; maps = {A codes with boxes of 32, 64, 96, 128 rows, B codes, B2 codes}; scales
+// come from the Fp4Args pointers (block layout; B in blocks of the tile's N rows).
 cudaError_t launch_gemm_fp4(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Args& a, int m_tiles,
                             cudaStream_t s);
 
@@ -97,9 +98,9 @@ cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int
                                           const int32_t* tile_base, int T, int L, int k, float eps,
                                           uint8_t* codes, uint8_t* scales, float* s_rows,
                                           cudaStream_t s);
-// row-major E4M3 scales [rows, K/16] -> block layout (rows a multiple of 128, K of 64)
-cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K, uint8_t* dst,
-                                      cudaStream_t s);
+// row-major E4M3 scales [rows, K/16] -> block layout with blocks of block_rows (64 or 128) rows
+cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K, int block_rows,
+                                      uint8_t* dst, cudaStream_t s);
 cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, const int32_t* row_of,
                                  const int32_t* idx, const float* w, const float* g_expert, int T,
                                  int L, int k, float eps, uint8_t* codes, uint8_t* scales,

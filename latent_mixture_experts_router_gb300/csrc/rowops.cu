@@ -627,10 +627,11 @@ __global__ void __launch_bounds__(kRowThreads) quantize_nvfp4_kernel(
   quantize_row_to(buf, K, s, recip, codes, scales, &s_d, 1);
 }
 
-// Row-major E4M3 scales [rows, K/16] -> block layout (rows a multiple of 128): one thread
-// moves the 4 scale bytes of one (row, 64-wide K step) as one word.
+// Row-major E4M3 scales [rows, K/16] -> block layout with blocks of block_rows rows (128, or
+// 64: then a line's last two words stay unused): one thread moves the 4 scale bytes of one
+// (row, 64-wide K step) as one word.
 __global__ void nvfp4_block_scales_kernel(const uint8_t* __restrict__ src, long long rows, int K,
-                                          uint8_t* __restrict__ dst) {
+                                          int block_rows, uint8_t* __restrict__ dst) {
   const long long words = rows * (K / 64);
   for (long long w = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; w < words;
        w += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -639,7 +640,7 @@ __global__ void nvfp4_block_scales_kernel(const uint8_t* __restrict__ src, long 
     const uint8_t* p = src + r * (K / 16) + k64 * 4;
     const uint32_t v = static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[1]) << 8) |
                        (static_cast<uint32_t>(p[2]) << 16) | (static_cast<uint32_t>(p[3]) << 24);
-    *reinterpret_cast<uint32_t*>(dst + blocked_sf_offset(r / kBM, static_cast<int>(r % kBM), k64 * 4, K)) = v;
+    *reinterpret_cast<uint32_t*>(dst + blocked_sf_offset(r / block_rows, static_cast<int>(r % block_rows), k64 * 4, K)) = v;
   }
 }
 
@@ -748,13 +749,13 @@ cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool 
   return cudaGetLastError();
 }
 
-cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K, uint8_t* dst,
-                                      cudaStream_t s) {
+cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K, int block_rows,
+                                      uint8_t* dst, cudaStream_t s) {
   const long long words = rows * (K / 64);
   if (words == 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<long long>((words + 255) / 256, 152 * 32));
   count_launch();
-  nvfp4_block_scales_kernel<<<blocks, 256, 0, s>>>(src, rows, K, dst);
+  nvfp4_block_scales_kernel<<<blocks, 256, 0, s>>>(src, rows, K, block_rows, dst);
   return cudaGetLastError();
 }
 

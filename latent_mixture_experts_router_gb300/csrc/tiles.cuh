@@ -52,6 +52,27 @@ struct TileWalk {
   }
 };
 
+// A tile id resolved to its raster position (arithmetic only; the tile-table entry is
+// loaded separately, so that a producer can issue that load one tile ahead).
+struct TileRef {
+  int id, mt, ntile;
+  bool valid;
+};
+LMOE_DEV TileRef find_tile(const TileWalk& w, int from) {
+  for (int id = from; id < w.n_ids; id += gridDim.x) {
+    int mt, nt_;
+    if (!grouped_tile(id / w.splits, w.total_m, w.nt, kRasterGroup, mt, nt_)) continue;
+    int kb0, kb1;
+    w.k_range(id, kb0, kb1);
+    if (kb0 < kb1) return TileRef{id, mt, nt_, true};
+  }
+  return TileRef{w.n_ids, 0, 0, false};
+}
+LMOE_DEV Tile tile_of(const TileWalk& w, int mt) {
+  if (w.tiles != nullptr) return w.tiles[mt];
+  return Tile{0, mt * kBM, min(kBM, w.M - mt * kBM), 0};
+}
+
 // Upper bound of the tile ids of a launch (host side): m_tiles M tiles of at most kBM rows.
 inline long long tile_id_bound(int m_tiles, int N, int bn, int splits = 1) {
   const long long nt = (N + bn - 1) / bn;
