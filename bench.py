@@ -281,6 +281,13 @@ def pick_workload(args) -> workloads.Workload:
     return w
 
 
+def replica_x(w: workloads.Workload, rank: int, device="cpu"):
+    """Tokens of replica `rank`: rows [rank*T, (rank+1)*T) of one long seeded batch (the block is
+    token-independent, so replicas exchange nothing)."""
+    return workloads.configs.normal_tensor(w, workloads.configs.S_X, (w.T, w.D), 1.0, w.act, device,
+                                           start=rank * w.T * w.D)
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args, ws, rank, local):
     import latent_mixture_experts_router_gb300 as lm
@@ -289,9 +296,8 @@ def run_ours(args, ws, rank, local):
     w = pick_workload(args)
     T = w.T
     inp = workloads.make_inputs(w, dev)
-    if ws > 1:   # each replica gets its own tokens: rows [rank*T, (rank+1)*T) of one long batch
-        inp.x = workloads.configs.normal_tensor(w, workloads.configs.S_X, (T, w.D), 1.0, w.act, dev,
-                                                start=rank * T * w.D)
+    if ws > 1:
+        inp.x = replica_x(w, rank, dev)
     blk = lm.LatentMoEBlock(inp.W_router, inp.W_pool, inp.g_pool, inp.W_gate, inp.W_up, inp.W_down,
                             inp.g_expert, inp.W_unpool, inp.g_pre, inp.g_post, w.k, w.eps, weight_dtype=w.weights)
     cfg = blk.config(T, w.act, "f32")
