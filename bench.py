@@ -181,13 +181,13 @@ def measured_traffic(stage: str, w: workloads.Workload, units: int):
     covers this kernel in this regime or the kernel source changed since it was taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or w.T > 512:   # captures cover the decode regime
         return None
-    rec = json.load(open(path)).get(stage)
-    src = os.path.join(ROOT, "latent_mixture_experts_router_gb300", "csrc", "gemm.cu")
-    if rec is None or hashlib.md5(open(src, "rb").read()).hexdigest() != rec["kernel_source_md5"]:
+    rec = json.load(open(path)).get(f"{stage}/{w.weights}/decode")
+    if rec is None:
         return None
-    if w.weights != "bf16" or w.T > 512:   # captured in the decode regime (few rows per expert)
+    src = os.path.join(ROOT, rec["kernel_source"])
+    if hashlib.md5(open(src, "rb").read()).hexdigest() != rec["kernel_source_md5"]:
         return None
     return int(rec["traffic_per_unit"] * units)
 
