@@ -118,7 +118,10 @@ enum {
  *  near_tie_count_out  [1] int32 device: tokens whose k-th and (k+1)-th logits differ by < 1e-3
  *  wait_budget_cycles  SM clock cycles a device wait may spin before it gives up (0: default)
  *  stage_events      host array of LMOE_NUM_STAGE_EVENTS caller-created cudaEvent_t, or NULL:
- *                    recorded on the stream at the stage boundaries above (timing only) */
+ *                    recorded on the stream at the stage boundaries above (timing only);
+ *                    a NULL entry is skipped.  Kernels of one call are launched with
+ *                    programmatic dependent launch, so a kernel's set-up overlaps the end of
+ *                    the previous one; an event between two kernels serialises them fully. */
 typedef struct {
   const float* router_bias;
   const int32_t* forced_idx;

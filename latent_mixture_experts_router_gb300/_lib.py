@@ -199,8 +199,9 @@ def latent_moe_forward_ex(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down
                           g_pre, g_post, top_k, out, workspace, stream=None, router_bias=None,
                           forced_idx=None, topk_idx_out=None, topk_w_out=None, near_tie_count_out=None,
                           wait_budget_cycles=0, stage_events=None):
-    """``stage_events``: a list of NUM_STAGE_EVENTS torch.cuda.Event(enable_timing=True), recorded
-    by the library at the stage boundaries (for per-stage timing)."""
+    """``stage_events``: a list of NUM_STAGE_EVENTS torch.cuda.Event(enable_timing=True) or None,
+    recorded by the library at the stage boundaries (for per-stage timing; None entries are
+    skipped)."""
     keep = []
     args = _fwd_args(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool, g_pre,
                      g_post, top_k, out, workspace, stream, keep)
@@ -208,9 +209,10 @@ def latent_moe_forward_ex(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down
     if stage_events is not None:
         assert len(stage_events) == NUM_STAGE_EVENTS
         for e in stage_events:   # torch creates the CUDA event lazily
-            if e.cuda_event == 0:
+            if e is not None and e.cuda_event == 0:
                 e.record()
-        evs = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event for e in stage_events])
+        evs = (ctypes.c_void_p * NUM_STAGE_EVENTS)(*[e.cuda_event if e is not None else None
+                                                     for e in stage_events])
         keep.append(evs)
     ex = lmoe_ex(_ptr(router_bias), _ptr(forced_idx), _ptr(topk_idx_out), _ptr(topk_w_out),
                  _ptr(near_tie_count_out), int(wait_budget_cycles),

@@ -409,13 +409,17 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   float* ss_u = static_cast<float*>(at(L.pub.ss_u));
 
   cudaEvent_t* ev = ex ? ex->stage_events : nullptr;
-  auto mark = [&](int i) -> bool { return ev == nullptr || cudaEventRecord(ev[i], s) == cudaSuccess; };
+  auto mark = [&](int i) -> bool {
+    return ev == nullptr || ev[i] == nullptr || cudaEventRecord(ev[i], s) == cudaSuccess;
+  };
 #define LMOE_MARK(i) \
   if (!mark(i)) return LMOE_ERR_CUDA;
 
   LMOE_MARK(LMOE_STAGE_PRENORM);
-  // error word and near-tie counter start at zero on every call
-  LMOE_CUDA(cudaMemsetAsync(err, 0, 8, s));
+  // the error word and near-tie counter start at zero on every call: the pre-norm kernel
+  // clears them, unless weight conversions run first (they are cleared before those)
+  if (f32w) LMOE_CUDA(cudaMemsetAsync(err, 0, 8, s));
+  unsigned* status2 = f32w ? nullptr : err;
 
   // weights as bf16 K-major operands; fp32 weights become hi/lo bf16 pairs laid side by
   // side along K, so every product keeps ~16 significant bits of the weight
@@ -445,9 +449,10 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
   if (fp4)
     LMOE_CUDA(launch_prenorm_nvfp4(x, x_f32, g_pre, T, D, eps, xa, xa_cols, wsb + L.pub.xq,
-                                   wsb + L.pub.xq_scale, reinterpret_cast<float*>(wsb + L.pub.xq_rowscale), s));
+                                   wsb + L.pub.xq_scale, reinterpret_cast<float*>(wsb + L.pub.xq_rowscale),
+                                   status2, s));
   else
-    LMOE_CUDA(launch_prenorm(x, x_f32, g_pre, T, D, eps, xa, xa_cols, s));
+    LMOE_CUDA(launch_prenorm(x, x_f32, g_pre, T, D, eps, xa, xa_cols, status2, s));
   LMOE_MARK(LMOE_STAGE_ROUTER);
   // S2 router logits = [xn_hi | xn_lo (| xn_hi)] . [W | W (| W_lo)]^T
   const int m_tiles_T = cdiv(T, kBM);

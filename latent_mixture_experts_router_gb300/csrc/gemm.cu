@@ -63,6 +63,11 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* mma_done = acc_empty + 2;         // every MMA of this CTA has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
+  // A grouped GEMM takes its tile table from the previous kernel: wait for it before the walk.
+  // A dense GEMM's tiles are known up front, so it sets up and warms L2 with its first
+  // weight tile while the previous kernel finishes.
+  const bool grouped = args.tiles != nullptr;
+  if (grouped) griddep_wait();
   const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb);
   if (static_cast<int>(blockIdx.x) >= walk.n_ids) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -81,6 +86,19 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (C::kDual) prefetch_tmap(&tmB2);
+    if (!grouped) {
+      // one CTA per raster group and N tile warms it (the group's M tiles share the tile)
+      int mt, expert, row0, nrows, ntile, kb0, kb1;
+      if (walk.at(blockIdx.x, mt, expert, row0, nrows, ntile) && mt % kRasterGroup == 0) {
+        walk.k_range(blockIdx.x, kb0, kb1);
+        const int brow = ntile * BN;
+        for (int kb = kb0; kb < min(kb1, kb0 + kPrefetchKb); ++kb) {
+          const int kbb = (kb % args.kb_period_b) * kBK;
+          prefetch_l2_tile_2d(&tmB, kbb, brow);
+          if (C::kDual) prefetch_l2_tile_2d(&tmB2, kbb, brow);
+        }
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -90,6 +108,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_enter();
   const long long budget = args.budget;
 
   if (warp == 0) {
@@ -328,9 +347,7 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
   const long long ids = tile_id_bound(m_tiles, a.N, BN, a.k_splits > 1 ? a.k_splits : 1);
   if (ids == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
-  count_launch();
-  kern<<<grid, 192, C::kSmemBytes, s>>>(tmA, tmB, tmB2, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(192), C::kSmemBytes, s, tmA, tmB, tmB2, a);
 }
 
 cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& tmB,

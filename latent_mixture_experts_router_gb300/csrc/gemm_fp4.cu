@@ -125,6 +125,10 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
+  // grouped: the tile table comes from the previous kernel; dense: warm L2 with the first
+  // weight tile (codes and scale blocks) while the previous kernel finishes
+  const bool grouped = args.tiles != nullptr;
+  if (grouped) griddep_wait();
   const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb);
   if (static_cast<int>(blockIdx.x) >= walk.n_ids) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -142,6 +146,19 @@ __global__ void __launch_bounds__(192, 1)
     fence_mbar_init();
     prefetch_tmap(&tmA128);
     prefetch_tmap(&tmB);
+    if (!grouped) {
+      int mt, expert, row0, nrows, ntile, kb0, kb1;
+      if (walk.at(blockIdx.x, mt, expert, row0, nrows, ntile) && mt % kRasterGroup == 0) {
+        walk.k_range(blockIdx.x, kb0, kb1);
+        kb1 = min(kb1, kb0 + kPrefetchKb);
+        const int brow = ntile * BN;
+        const uint8_t* sfb = args.b_scales + static_cast<size_t>(brow / BN) * args.num_kb * 4 * 512;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          prefetch_l2_tile_2d(&tmB, kb * 128, brow);
+          prefetch_l2_bulk(sfb + kb * 2048, 2048u);
+        }
+      }
+    }
   }
   if (warp >= 2 && warp <= 5) {
     for (int i = threadIdx.x - 64; i < 256; i += 128) recip[i] = c_e4m3_recip.v[i];
@@ -154,6 +171,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_enter();
   const long long budget = args.budget;
   const int nk = args.num_kb;  // stages of K = 256
 
@@ -374,9 +392,8 @@ cudaError_t launch_fp4_one(const CUtensorMap* maps, const Fp4Args& a, int m_tile
   const long long ids = tile_id_bound(m_tiles, a.N, BN, a.k_splits > 1 ? a.k_splits : 1);
   if (ids == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
-  count_launch();
-  kern<<<grid, 192, C::kSmemBytes, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(192), C::kSmemBytes, s, maps[0], maps[1], maps[2], maps[3],
+                    maps[4], maps[5], a);
 }
 
 }  // namespace

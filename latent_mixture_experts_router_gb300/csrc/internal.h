@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace lmoe {
 
 constexpr int kBM = 128;            // rows of one GEMM tile (tcgen05 M)
@@ -12,6 +14,9 @@ constexpr int kBK = 64;             // K elements of one pipeline stage (128 B o
 constexpr int kBNWide = 256;        // N of the single-B GEMM tiles
 constexpr int kBNSwiGLU = 128;      // N of each of the gate and up tiles
 constexpr int kBNFp4 = 128;         // N of the NVFP4 tiles (each of gate and up for SwiGLU)
+// K blocks of its first weight tile a dense GEMM CTA prefetches into L2 before it waits on
+// the previous kernel
+constexpr int kPrefetchKb = 64;
 constexpr long long kDefaultWaitBudget = 4000000000LL;  // ~2 s of SM clock
 constexpr long long kDrainBudget = 4000000000LL;        // waits for a CTA's own async work
 
@@ -91,7 +96,7 @@ cudaError_t launch_gemm_fp4(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Ar
 // NVFP4 row kernels (rowops.cu)
 cudaError_t launch_prenorm_nvfp4(const void* x, bool x_f32, const float* g_pre, int T, int D,
                                  float eps, __nv_bfloat16* xa, int xa_cols, uint8_t* codes,
-                                 uint8_t* scales, float* s_row, cudaStream_t s);
+                                 uint8_t* scales, float* s_row, unsigned* status2, cudaStream_t s);
 cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int ld_ss,
                                           const float* g_pool, const int32_t* row_of,
                                           const int32_t* idx, const int32_t* offsets,
@@ -119,14 +124,34 @@ cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int
 // Counts every kernel launch of the library (lmoe_kernel_launches).
 void count_launch();
 
+// Launches `kern` with programmatic stream serialisation and counts it.  The kernel must call
+// griddep_wait() (ptx.cuh) before it reads anything an earlier kernel of the stream wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Launches one tcgen05 GEMM: out = A * B^T over grid (ceil(N/BN), m_tiles).
 cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         const CUtensorMap& tmB2, const GemmArgs& a, int m_tiles,
                         cudaStream_t s);
 
-// Row kernels (rowops.cu)
+// Row kernels (rowops.cu).  The pre-norm kernels, the first of a call, also zero the two
+// status words at status2 (error word, near-tie count) when status2 != nullptr.
 cudaError_t launch_prenorm(const void* x, bool x_f32, const float* g_pre, int T, int D, float eps,
-                           __nv_bfloat16* xa, int xa_cols, cudaStream_t s);
+                           __nv_bfloat16* xa, int xa_cols, unsigned* status2, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int ld, const float* bias, const int32_t* forced,
                         int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
                         int32_t* idx_copy, float* w_copy, unsigned* err, cudaStream_t s);

@@ -177,6 +177,31 @@ LMOE_DEV void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
 }
 LMOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream serialisation: its CTAs
+// may become resident while the previous kernel of the stream is still finishing, and they
+// block in griddep_wait() until that kernel has completed and its writes are visible.  Each
+// kernel calls griddep_wait() before touching anything an earlier kernel wrote, then lets
+// its own dependents launch (they wait likewise, so the trigger point only affects overlap).
+LMOE_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+LMOE_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+LMOE_DEV void griddep_enter() {
+  griddep_wait();
+  griddep_launch_dependents();
+}
+
+// L2 prefetch of one tensor-map box (no shared memory, no barrier) and of a contiguous range
+// (16-byte aligned address and size).  Used for operands no earlier kernel writes (weights),
+// ahead of griddep_wait().
+LMOE_DEV void prefetch_l2_tile_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
+}
+LMOE_DEV void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+               :: "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------------ tile order
 // Grouped rasterisation of a 1-D grid over (M tile, N tile): groups of `group` consecutive M
 // tiles; inside a group the M index runs fastest, so the CTAs resident at one time share

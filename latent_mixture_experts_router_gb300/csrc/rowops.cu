@@ -105,7 +105,9 @@ __global__ void __launch_bounds__(kRowThreads) prenorm_kernel(const void* __rest
                                                               const float* __restrict__ g,
                                                               int D, float eps,
                                                               __nv_bfloat16* __restrict__ xa,
-                                                              int xa_cols) {
+                                                              int xa_cols, unsigned* status2) {
+  griddep_enter();
+  if (status2 != nullptr && blockIdx.x == 0 && threadIdx.x == 0) status2[0] = status2[1] = 0u;
   __shared__ float red[33];
   const long long t = blockIdx.x;
   const long long xoff = t * D;
@@ -144,6 +146,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
     const int32_t* __restrict__ forced, int T, int E, int k, int32_t* __restrict__ idx_out,
     float* __restrict__ w_out, int32_t* __restrict__ near_tie, int32_t* __restrict__ idx_copy,
     float* __restrict__ w_copy, unsigned* __restrict__ err) {
+  griddep_enter();
   extern __shared__ float vals_all[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long t = static_cast<long long>(blockIdx.x) * kTopkWarps + warp;
@@ -220,6 +223,7 @@ constexpr int kPermPerThread = 16;
 
 __global__ void __launch_bounds__(kPermThreads) expert_count_kernel(const int32_t* __restrict__ idx,
                                                                     int n, int32_t* counts) {
+  griddep_enter();
   __shared__ int red[33];
   const int e = blockIdx.x;
   int c = 0;
@@ -232,6 +236,7 @@ __global__ void __launch_bounds__(kPermThreads) expert_scatter_kernel(
     const int32_t* __restrict__ idx, int n, int k, int E, const int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of,
     Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles, int32_t* __restrict__ tile_base) {
+  griddep_enter();
   __shared__ int wsum[kPermThreads / 32];
   __shared__ int red[33];
   const int e = blockIdx.x;
@@ -298,6 +303,7 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
     const float* __restrict__ p, const float* __restrict__ ss_p, int ld_ss,
     const float* __restrict__ g, const int32_t* __restrict__ row_of, int L, int k, float eps,
     __nv_bfloat16* __restrict__ xe) {
+  griddep_enter();
   __shared__ float s_rs;
   __shared__ int s_rows[16];
   const long long t = blockIdx.x;
@@ -325,6 +331,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx,
     const float* __restrict__ w, const float* __restrict__ g_expert, int L, int k, float eps,
     __nv_bfloat16* __restrict__ c) {
+  griddep_enter();
   __shared__ float s_coef[16];
   __shared__ int s_row[16], s_e[16];
   const long long t = blockIdx.x;
@@ -356,6 +363,7 @@ __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
     const void* __restrict__ x, int x_f32, const float* __restrict__ u,
     const float* __restrict__ ss_u, int ld_ss, const float* __restrict__ g, int D, float eps,
     void* __restrict__ out, int out_f32) {
+  griddep_enter();
   __shared__ float s_rs;
   const long long t = blockIdx.x;
   if (threadIdx.x == 0) {
@@ -386,6 +394,7 @@ __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
 // W [rows, K] fp32 -> [rows, parts*K] bf16; part q = W_lo if bit q of lo_mask else W_hi
 __global__ void weight_split_kernel(const float* __restrict__ W, long long rows, int K, int parts,
                                     unsigned lo_mask, __nv_bfloat16* __restrict__ dst) {
+  griddep_enter();
   const long long chunks = rows * (K / 8);
   for (long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
        c += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -461,7 +470,9 @@ __device__ __forceinline__ void quantize_row_to(const float* buf, int K, float s
 __global__ void __launch_bounds__(kRowThreads) prenorm_nvfp4_kernel(
     const void* __restrict__ x, int x_f32, const float* __restrict__ g, int D, float eps,
     __nv_bfloat16* __restrict__ xa, int xa_cols, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, float* __restrict__ s_row) {
+    uint8_t* __restrict__ scales, float* __restrict__ s_row, unsigned* status2) {
+  griddep_enter();
+  if (status2 != nullptr && blockIdx.x == 0 && threadIdx.x == 0) status2[0] = status2[1] = 0u;
   extern __shared__ float dyn[];
   float* buf = dyn;
   float* recip = dyn + D;
@@ -511,6 +522,7 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ tile_base, int L, int k, float eps, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, float* __restrict__ s_rows) {
+  griddep_enter();
   extern __shared__ float dyn[];
   float* buf = dyn;
   float* recip = dyn + L;
@@ -556,6 +568,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const float* __restrict__ w,
     const float* __restrict__ g_expert, int L, int k, float eps, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, float* __restrict__ s_row) {
+  griddep_enter();
   extern __shared__ float dyn[];
   float* buf = dyn;
   float* recip = dyn + L;
@@ -604,6 +617,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
 __global__ void __launch_bounds__(kRowThreads) quantize_nvfp4_kernel(
     const float* __restrict__ src, int K, int row_scale, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, float* __restrict__ s_row) {
+  griddep_enter();
   extern __shared__ float dyn[];
   float* buf = dyn;
   float* recip = dyn + K;
@@ -632,6 +646,7 @@ __global__ void __launch_bounds__(kRowThreads) quantize_nvfp4_kernel(
 // (row, 64-wide K step) as one word.
 __global__ void nvfp4_block_scales_kernel(const uint8_t* __restrict__ src, long long rows, int K,
                                           int block_rows, uint8_t* __restrict__ dst) {
+  griddep_enter();
   const long long words = rows * (K / 64);
   for (long long w = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; w < words;
        w += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -650,6 +665,7 @@ __global__ void nvfp4_block_scales_kernel(const uint8_t* __restrict__ src, long 
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, int rows, int N,
                                      float* __restrict__ out, long long ldo, float* __restrict__ ss,
                                      int ld_ss) {
+  griddep_enter();
   __shared__ float red[33];
   const int r = blockIdx.x, grp = blockIdx.y;
   const int col = grp * blockDim.x + threadIdx.x;
@@ -667,6 +683,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int spli
 // ------------------------------------------------------------------ wait self-test
 // One thread waits on a barrier that is initialised for one arrival that never comes.
 __global__ void wait_selftest_kernel(long long budget, unsigned* err) {
+  griddep_enter();
   __shared__ uint64_t bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
@@ -680,7 +697,7 @@ __global__ void wait_selftest_kernel(long long budget, unsigned* err) {
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_prenorm_nvfp4(const void* x, bool x_f32, const float* g_pre, int T, int D,
                                  float eps, __nv_bfloat16* xa, int xa_cols, uint8_t* codes,
-                                 uint8_t* scales, float* s_row, cudaStream_t s) {
+                                 uint8_t* scales, float* s_row, unsigned* status2, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const size_t smem = (static_cast<size_t>(D) + 256) * sizeof(float);
   static bool attr = false;
@@ -689,10 +706,8 @@ cudaError_t launch_prenorm_nvfp4(const void* x, bool x_f32, const float* g_pre, 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  count_launch();
-  prenorm_nvfp4_kernel<<<T, kRowThreads, smem, s>>>(x, x_f32 ? 1 : 0, g_pre, D, eps, xa, xa_cols, codes,
-                                                    scales, s_row);
-  return cudaGetLastError();
+  return launch_pdl(prenorm_nvfp4_kernel, dim3(T), dim3(kRowThreads), smem, s, x, x_f32 ? 1 : 0,
+                    g_pre, D, eps, xa, xa_cols, codes, scales, s_row, status2);
 }
 
 cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int ld_ss,
@@ -709,10 +724,9 @@ cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  count_launch();
-  poolnorm_scatter_nvfp4_kernel<<<T, kRowThreads, smem, s>>>(p, ss_p, ld_ss, g_pool, row_of, idx, offsets,
-                                                             tile_base, L, k, eps, codes, scales, s_rows);
-  return cudaGetLastError();
+  return launch_pdl(poolnorm_scatter_nvfp4_kernel, dim3(T), dim3(kRowThreads), smem, s, p, ss_p,
+                    ld_ss, g_pool, row_of, idx, offsets, tile_base, L, k, eps, codes, scales,
+                    s_rows);
 }
 
 cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, const int32_t* row_of,
@@ -727,10 +741,8 @@ cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, c
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  count_launch();
-  combine_nvfp4_kernel<<<T, kRowThreads, smem, s>>>(y, ss_y, ld_ss, row_of, idx, w, g_expert, L, k, eps,
-                                                    codes, scales, s_row);
-  return cudaGetLastError();
+  return launch_pdl(combine_nvfp4_kernel, dim3(T), dim3(kRowThreads), smem, s, y, ss_y, ld_ss,
+                    row_of, idx, w, g_expert, L, k, eps, codes, scales, s_row);
 }
 
 cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool row_scale,
@@ -743,10 +755,8 @@ cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  count_launch();
-  quantize_nvfp4_kernel<<<static_cast<unsigned>(rows), kRowThreads, smem, s>>>(src, K, row_scale ? 1 : 0,
-                                                                              codes, scales, s_row);
-  return cudaGetLastError();
+  return launch_pdl(quantize_nvfp4_kernel, dim3(static_cast<unsigned>(rows)), dim3(kRowThreads),
+                    smem, s, src, K, row_scale ? 1 : 0, codes, scales, s_row);
 }
 
 cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K, int block_rows,
@@ -754,32 +764,27 @@ cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K,
   const long long words = rows * (K / 64);
   if (words == 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<long long>((words + 255) / 256, 152 * 32));
-  count_launch();
-  nvfp4_block_scales_kernel<<<blocks, 256, 0, s>>>(src, rows, K, block_rows, dst);
-  return cudaGetLastError();
+  return launch_pdl(nvfp4_block_scales_kernel, dim3(blocks), dim3(256), 0, s, src, rows, K,
+                    block_rows, dst);
 }
 
 cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, float* out,
                                  long long ldo, float* ss, int ld_ss, int group, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   dim3 grid(rows, (N + group - 1) / group);
-  count_launch();
-  splitk_reduce_kernel<<<grid, group, 0, s>>>(partial, splits, rows, N, out, ldo, ss, ld_ss);
-  return cudaGetLastError();
+  return launch_pdl(splitk_reduce_kernel, dim3(grid), dim3(group), 0, s, partial, splits, rows, N,
+                    out, ldo, ss, ld_ss);
 }
 
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s) {
-  count_launch();
-  wait_selftest_kernel<<<1, 32, 0, s>>>(budget, err);
-  return cudaGetLastError();
+  return launch_pdl(wait_selftest_kernel, dim3(1), dim3(32), 0, s, budget, err);
 }
 
 cudaError_t launch_prenorm(const void* x, bool x_f32, const float* g_pre, int T, int D, float eps,
-                           __nv_bfloat16* xa, int xa_cols, cudaStream_t s) {
+                           __nv_bfloat16* xa, int xa_cols, unsigned* status2, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  count_launch();
-  prenorm_kernel<<<T, kRowThreads, 0, s>>>(x, x_f32 ? 1 : 0, g_pre, D, eps, xa, xa_cols);
-  return cudaGetLastError();
+  return launch_pdl(prenorm_kernel, dim3(T), dim3(kRowThreads), 0, s, x, x_f32 ? 1 : 0, g_pre, D,
+                    eps, xa, xa_cols, status2);
 }
 
 cudaError_t launch_topk(const float* logits, int ld, const float* bias, const int32_t* forced,
@@ -788,33 +793,27 @@ cudaError_t launch_topk(const float* logits, int ld, const float* bias, const in
   if (T == 0) return cudaSuccess;
   const int blocks = (T + kTopkWarps - 1) / kTopkWarps;
   const size_t smem = static_cast<size_t>(kTopkWarps) * E * sizeof(float);
-  count_launch();
-  topk_kernel<<<blocks, kTopkWarps * 32, smem, s>>>(logits, ld, bias, forced, T, E, k, idx, w,
-                                                    near_tie, idx_copy, w_copy, err);
-  return cudaGetLastError();
+  return launch_pdl(topk_kernel, dim3(blocks), dim3(kTopkWarps * 32), smem, s, logits, ld, bias,
+                    forced, T, E, k, idx, w, near_tie, idx_copy, w_copy, err);
 }
 
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
                            int32_t* n_tiles, cudaStream_t s, int32_t* tile_base) {
   const int n = T * k;
-  count_launch();
-  expert_count_kernel<<<E, kPermThreads, 0, s>>>(idx, n, counts);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(expert_count_kernel, dim3(E), dim3(kPermThreads), 0, s, idx, n,
+                             counts);
   if (e != cudaSuccess) return e;
-  count_launch();
-  expert_scatter_kernel<<<E, kPermThreads, 0, s>>>(idx, n, k, E, counts, offsets, row_of, tok_of,
-                                                   tiles, n_tiles, tile_base);
-  return cudaGetLastError();
+  return launch_pdl(expert_scatter_kernel, dim3(E), dim3(kPermThreads), 0, s, idx, n, k, E, counts,
+                    offsets, row_of, tok_of, tiles, n_tiles, tile_base);
 }
 
 cudaError_t launch_poolnorm_scatter(const float* p, const float* ss_p, int ld_ss,
                                     const float* g_pool, const int32_t* row_of, int T, int L,
                                     int k, float eps, __nv_bfloat16* xe, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  count_launch();
-  poolnorm_scatter_kernel<<<T, kRowThreads, 0, s>>>(p, ss_p, ld_ss, g_pool, row_of, L, k, eps, xe);
-  return cudaGetLastError();
+  return launch_pdl(poolnorm_scatter_kernel, dim3(T), dim3(kRowThreads), 0, s, p, ss_p, ld_ss,
+                    g_pool, row_of, L, k, eps, xe);
 }
 
 cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
@@ -822,19 +821,16 @@ cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
                            const float* g_expert, int T, int L, int k, float eps,
                            __nv_bfloat16* c, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  count_launch();
-  combine_kernel<<<T, kRowThreads, 0, s>>>(y, ss_y, ld_ss, row_of, idx, w, g_expert, L, k, eps, c);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(T), dim3(kRowThreads), 0, s, y, ss_y, ld_ss, row_of, idx, w,
+                    g_expert, L, k, eps, c);
 }
 
 cudaError_t launch_postnorm_residual(const void* x, bool x_f32, const float* u,
                                      const float* ss_u, int ld_ss, const float* g_post, int T,
                                      int D, float eps, void* out, bool out_f32, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  count_launch();
-  postnorm_residual_kernel<<<T, kRowThreads, 0, s>>>(x, x_f32 ? 1 : 0, u, ss_u, ld_ss, g_post, D,
-                                                     eps, out, out_f32 ? 1 : 0);
-  return cudaGetLastError();
+  return launch_pdl(postnorm_residual_kernel, dim3(T), dim3(kRowThreads), 0, s, x, x_f32 ? 1 : 0, u,
+                    ss_u, ld_ss, g_post, D, eps, out, out_f32 ? 1 : 0);
 }
 
 cudaError_t launch_weight_split(const float* W, long long rows, int K, int parts,
@@ -842,9 +838,8 @@ cudaError_t launch_weight_split(const float* W, long long rows, int K, int parts
   const long long chunks = rows * (K / 8);
   if (chunks == 0) return cudaSuccess;
   const int blocks = static_cast<int>(std::min<long long>((chunks + 255) / 256, 152 * 16));
-  count_launch();
-  weight_split_kernel<<<blocks, 256, 0, s>>>(W, rows, K, parts, lo_mask, dst);
-  return cudaGetLastError();
+  return launch_pdl(weight_split_kernel, dim3(blocks), dim3(256), 0, s, W, rows, K, parts, lo_mask,
+                    dst);
 }
 
 }  // namespace lmoe
