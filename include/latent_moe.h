@@ -184,8 +184,9 @@ lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStrea
 /* Byte offsets of the intermediates inside the workspace, for inspection:
  *  xa (router/pooler input rows), logits [T,E] f32, topk_idx [T,k] i32, topk_w [T,k] f32,
  *  counts [E] i32, offsets [E+1] i32, row_of [T,k] i32, tok_of [T*k] i32,
- *  p [T,L] bf16, xe [T*k, L] (expert-contiguous expert inputs), h [T*k, I], y [T*k, L] bf16,
- *  ss_y [T*k, L/128] f32, c [T,L] bf16, u [T,D] bf16, err (u32).  Unused fields are -1. */
+ *  p [T,L] f32, xe [T*k, L] bf16 (expert-contiguous expert inputs), h [T*k, I] bf16,
+ *  y [T*k, L] f32, ss_y [T*k, L/BN] f32, c [T,L] bf16, u [T,D] f32, err (u32).
+ *  Unused fields are -1. */
 typedef struct {
   long long xa, logits, topk_idx, topk_w, counts, offsets, row_of, tok_of, tiles, n_tiles,
       p, ss_p, xe, xe_scale, h, y, ss_y, c, u, ss_u, err, total;
@@ -195,6 +196,9 @@ typedef struct {
    * codes [T*k, I/2]); c block scales [T, L/16] and row scales [T] (c holds codes [T, L/2]). */
   long long xq, xq_scale, xq_rowscale, xe_rowscale, h_scale, c_scale, c_rowscale;
   int xa_cols; /* columns of one xa row (2*D: xn_hi | xn_lo, or 3*D for fp32 weights) */
+  /* [2] int32: the split-K counts the grouped gate/up and down GEMMs used in the last call
+   * (chosen on the device from the live tile count; 1 = unsplit; NVFP4 weights only) */
+  long long grouped_splits;
 } lmoe_workspace_layout;
 lmoe_status lmoe_get_workspace_layout(const lmoe_config* cfg, lmoe_workspace_layout* layout);
 

@@ -61,7 +61,7 @@ _LAYOUT_FIELDS_NVFP4 = ["xq", "xq_scale", "xq_rowscale", "xe_rowscale", "h_scale
 
 class lmoe_workspace_layout(ctypes.Structure):
     _fields_ = ([(f, ctypes.c_longlong) for f in _LAYOUT_FIELDS + _LAYOUT_FIELDS_NVFP4]
-                + [("xa_cols", ctypes.c_int)])
+                + [("xa_cols", ctypes.c_int), ("grouped_splits", ctypes.c_longlong)])
 
 
 _P = ctypes.c_void_p
@@ -174,6 +174,7 @@ def lmoe_get_workspace_layout(cfg: Config) -> dict:
     _check(_lib().lmoe_get_workspace_layout(ctypes.byref(c), ctypes.byref(lay)), "lmoe_get_workspace_layout")
     d = {f: getattr(lay, f) for f in _LAYOUT_FIELDS + _LAYOUT_FIELDS_NVFP4}
     d["xa_cols"] = lay.xa_cols
+    d["grouped_splits"] = lay.grouped_splits
     return d
 
 

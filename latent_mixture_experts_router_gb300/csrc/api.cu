@@ -39,12 +39,23 @@ struct Layout {
   lmoe_workspace_layout pub;
   long long near_tie;
   long long tile_base;  // [E] first M tile of each expert
-  long long partial;    // split-K partial products of the dense GEMMs
+  long long partial;    // split-K partial products of the dense and grouped GEMMs
+  long long splits_dev; // [2] split counts the grouped NVFP4 GEMMs chose (gate/up, down)
   // fp32-weight mode: bf16 copies of the weights
   long long w_router, w_pool, w_gate, w_up, w_down, w_unpool;
   long long x_stage, out_stage, host_io_total;
   int ld_logits, ld_ss_p, ld_ss_y, ld_ss_u, max_tiles;
 };
+
+// Upper bound of the split count of the grouped NVFP4 GEMMs (the kernel picks the count from
+// the live tiles).  Split-K adds 8 bytes per partial element (write + read) on top of the
+// weight stream; with R = T k rows each expert row block reads at least k of the E experts'
+// weights, so the bound keeps the partial traffic a few percent of the weights'.
+int grouped_max_splits(const lmoe_config* c) {
+  if (c->weight_dtype != LMOE_NVFP4 || c->T <= 0) return 1;
+  const long long sp = (c->d_latent / 128) / c->T;
+  return sp >= 8 ? 8 : (sp < 1 ? 1 : static_cast<int>(sp));
+}
 
 // Split-K for dense GEMMs with few output tiles (small T): enough K ranges to give the 152
 // SMs of a GB300 work, at least `min_kb` K blocks each, at most 32.  A fixed SM count keeps
@@ -171,13 +182,18 @@ void make_layout(const lmoe_config* c, Layout* L) {
     L->w_down = take(E * Ld * 2 * I * 2);
     L->w_unpool = take(D * 2 * Ld * 2);
   }
-  {  // split-K partials: the largest of the dense GEMMs' [splits][T][N]
+  {  // split-K partials: the largest of the dense GEMMs' [splits][T][N] and the grouped
+     // GEMMs' [splits][R][2I] (gate | up) and [splits][R][L]
     const DenseSplits d = dense_split_plan(c);
     long long need = 0;
     if (d.router > 1) need = std::max(need, d.router * T * E);
     if (d.pooler > 1) need = std::max(need, d.pooler * T * Ld);
     if (d.unpool > 1) need = std::max(need, d.unpool * T * D);
+    const long long gs = grouped_max_splits(c);
+    if (gs > 1) need = std::max(need, gs * R * std::max(2 * I, Ld));
     L->partial = need > 0 ? take(need * 4) : -1;
+    L->splits_dev = take(2 * 4);
+    P.grouped_splits = c->weight_dtype == LMOE_NVFP4 ? L->splits_dev : -1;
   }
   P.total = static_cast<long long>(off);
   L->x_stage = take(T * D * (c->act_dtype == LMOE_F32 ? 4 : 2));
@@ -273,9 +289,13 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   a.ld_ss = ld_ss;
   a.err = err;
   a.budget = budget;
-  a.b_stream_once = rows_per_b <= kBM;
+  // evict-first only where (nearly) every B tile meets one M tile: at a mean near kBM rows
+  // per expert, many experts spill into a second M tile that re-reads B from L2
+  a.b_stream_once = rows_per_b <= kBM / 2;
   a.k_splits = splits > 1 ? splits : 1;
   a.partial = partial;
+  a.max_tiles = m_tiles;
+  a.n_groups = static_cast<int>(b_rows / N);
   LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s));
   if (splits > 1)
     LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
@@ -295,7 +315,7 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                          uint8_t* out_scales, float* ss, int ld_ss, const float* row_scale,
                          const float* ts, const float* ts2, unsigned* err, long long budget,
                          cudaStream_t s, long long rows_per_b, int splits = 1,
-                         float* partial = nullptr) {
+                         float* partial = nullptr, int* splits_dev = nullptr) {
   CUtensorMap maps[6];
   const unsigned long long kc = K / 2;
   const unsigned bn = kBNFp4;
@@ -323,13 +343,27 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
   a.b2_scales = B2 ? B2->scales : nullptr;
   a.err = err;
   a.budget = budget;
-  a.b_stream_once = rows_per_b <= kBM;
+  // evict-first only where (nearly) every B tile meets one M tile: at a mean near kBM rows
+  // per expert, many experts spill into a second M tile that re-reads B from L2
+  a.b_stream_once = rows_per_b <= kBM / 2;
   a.k_splits = splits > 1 ? splits : 1;
   a.partial = partial;
+  a.max_tiles = m_tiles;
+  a.n_groups = static_cast<int>(b_rows / N);
+  // grouped: `splits` bounds the count the kernel picks and leaves at splits_dev
+  const bool adaptive = tiles != nullptr && splits > 1;
+  a.adaptive_splits = adaptive ? 1 : 0;
+  a.splits_out = tiles != nullptr ? splits_dev : nullptr;
+  if (adaptive && (partial == nullptr || splits_dev == nullptr)) return LMOE_ERR_WORKSPACE;
   LMOE_CUDA(launch_gemm_fp4(epi, maps, a, m_tiles, s));
-  if (splits > 1)
-    LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
-                                   ldo, ss, ld_ss, kBNFp4, s));
+  if (splits > 1) {
+    if (epi == kFp4EpiSwiGLUQuant)
+      LMOE_CUDA(launch_swiglu_reduce_nvfp4(partial, splits_dev, static_cast<int>(a_rows), N, tiles,
+                                           n_tiles, m_tiles, static_cast<uint8_t*>(out), out_scales, s));
+    else
+      LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
+                                     ldo, ss, ld_ss, kBNFp4, s, adaptive ? splits_dev : nullptr));
+  }
   return LMOE_OK;
 }
 
@@ -492,17 +526,21 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                                             tile_base, T, Ld, k, eps, wsb + L.pub.xe,
                                             wsb + L.pub.xe_scale, xe_s, s));
     LMOE_MARK(LMOE_STAGE_GATE_UP);
-    // S7 grouped gate/up + SwiGLU, h requantised to NVFP4 (scale 1)
+    // S7 grouped gate/up + SwiGLU, h requantised to NVFP4 (scale 1); at small T split-K
+    // with the split count picked on the device from the live tiles
+    const int gsplit = grouped_max_splits(cfg);
+    int* splits_dev = static_cast<int*>(at(L.splits_dev));
     const Fp4Operand up = op(q4[2]);
     st = run_gemm_fp4(kFp4EpiSwiGLUQuant, xeq, R, Ld, op(q4[1]), 1LL * E * I, &up, I, tiles, n_tiles,
                       L.max_tiles, wsb + L.pub.h, I, wsb + L.pub.h_scale, nullptr, 0, xe_s,
-                      q4[1]->tensor_scale, q4[2]->tensor_scale, err, budget, s, R / E);
+                      q4[1]->tensor_scale, q4[2]->tensor_scale, err, budget, s, R / E, gsplit, partial,
+                      splits_dev);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_DOWN);
     // S8 grouped down (fp32 y) with per-row partial sums of squares
     st = run_gemm_fp4(kFp4EpiF32Ss, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
                       L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
-                      nullptr, err, budget, s, R / E);
+                      nullptr, err, budget, s, R / E, gsplit, partial, splits_dev + 1);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_COMBINE);
     // S9 combine, c quantised per token

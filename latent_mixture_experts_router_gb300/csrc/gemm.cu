@@ -63,15 +63,11 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* mma_done = acc_empty + 2;         // every MMA of this CTA has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
-  // A grouped GEMM takes its tile table from the previous kernel: wait for it before the walk.
-  // A dense GEMM's tiles are known up front, so it sets up and warms L2 with its first
-  // weight tile while the previous kernel finishes.
-  const bool grouped = args.tiles != nullptr;
-  if (grouped) griddep_wait();
-  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb);
-  if (static_cast<int>(blockIdx.x) >= walk.n_ids) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Set-up reads nothing an earlier kernel of the stream writes, so it runs before the wait,
+  // overlapping the end of that kernel, and so does an L2 prefetch of this CTA's first
+  // weight tile.
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -86,17 +82,13 @@ __global__ void __launch_bounds__(192, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     if (C::kDual) prefetch_tmap(&tmB2);
-    if (!grouped) {
-      // one CTA per raster group and N tile warms it (the group's M tiles share the tile)
-      int mt, expert, row0, nrows, ntile, kb0, kb1;
-      if (walk.at(blockIdx.x, mt, expert, row0, nrows, ntile) && mt % kRasterGroup == 0) {
-        walk.k_range(blockIdx.x, kb0, kb1);
-        const int brow = ntile * BN;
-        for (int kb = kb0; kb < min(kb1, kb0 + kPrefetchKb); ++kb) {
-          const int kbb = (kb % args.kb_period_b) * kBK;
-          prefetch_l2_tile_2d(&tmB, kbb, brow);
-          if (C::kDual) prefetch_l2_tile_2d(&tmB2, kbb, brow);
-        }
+    int brow, kb0, kb1;
+    if (first_tile_hint(args.tiles, args.n_tiles, args.max_tiles, args.n_groups, args.M, args.N, BN,
+                        args.k_splits, args.num_kb, false, brow, kb0, kb1)) {
+      for (int kb = kb0; kb < min(kb1, kb0 + kPrefetchKb); ++kb) {
+        const int kbb = (kb % args.kb_period_b) * kBK;
+        prefetch_l2_tile_2d(&tmB, kbb, brow);
+        if (C::kDual) prefetch_l2_tile_2d(&tmB2, kbb, brow);
       }
     }
   }
@@ -109,6 +101,8 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   griddep_enter();
+  // CTAs past the live tile ids walk nothing and go straight to the teardown
+  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb);
   const long long budget = args.budget;
 
   if (warp == 0) {
@@ -211,9 +205,9 @@ __global__ void __launch_bounds__(192, 1)
       const long long grow = static_cast<long long>(row0) + r;
       const int n0 = ntile * BN;
       const uint32_t tq = tmem + buf * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
-      if (EPI != kEpiSwiGLU && args.k_splits > 1) {
+      if (EPI != kEpiSwiGLU && walk.splits > 1) {
         // split-K: raw fp32 partial product of this K range; the reduction finishes the tile
-        float* prow = args.partial + (static_cast<long long>(id % args.k_splits) * args.M + grow) * args.N;
+        float* prow = args.partial + (static_cast<long long>(id % walk.splits) * args.M + grow) * args.N;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t v[32];

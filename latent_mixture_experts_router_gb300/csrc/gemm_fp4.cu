@@ -14,11 +14,14 @@
 // read through tcgen05.cp 32x128b (blocks of 32 lines x 16 bytes, line m0 holding the 4
 // scale bytes of rows m0, m0+32, m0+64, m0+96 — the "4x32 transpose" the pages apply before
 // the copy, done once when the scales are written), so a stage's scales are one bulk copy.
-// Roles (192 threads):
+// Roles (192 or 320 threads):
 //   warp 0 lane 0   TMA: A codes + B codes (+ B2 for gate/up) + bulk copies of their scales
 //   warp 1          TMEM allocation; lane 0 copies scale factors into TMEM (tcgen05.cp) and
 //                   issues tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
-//   warps 2..5      epilogue (warp w owns TMEM lanes 32*(w%4) ..)
+//   warps 2..        epilogue: warp w owns TMEM lanes 32*(w%4) ..; the gate/up kernel runs
+//                   8 epilogue warps, warp w also taking column half (w-2)/4, so each
+//                   scheduler runs two of them and a tile drains in half the time (its
+//                   single accumulator waits for that); the fp32 kernels run 4
 // The A box covers only the tile's live rows rounded up to 32 (a decode tile holds a few
 // rows of one expert), and the producer loads the next tile's table entry one tile ahead.
 // Epilogues: kFp4EpiF32Ss — alpha * acc as fp32 plus per-row partial sums of squares; two
@@ -101,6 +104,8 @@ struct Fp4Cfg {
   static constexpr int kSfCol0 = kAccBufs * kAccCols;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024 /*recip*/ + 256;
+  static constexpr int kEpiWarps = kDual ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static_assert(kSfCol0 + kStages * kSfCols <= 512, "tensor memory");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kStageBytes % 1024 == 0, "1024-byte aligned stages");
@@ -108,7 +113,7 @@ struct Fp4Cfg {
 };
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
     gemm_fp4_kernel(const __grid_constant__ CUtensorMap tmA32, const __grid_constant__ CUtensorMap tmA64,
                     const __grid_constant__ CUtensorMap tmA96, const __grid_constant__ CUtensorMap tmA128,
                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB2,
@@ -125,14 +130,10 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
-  // grouped: the tile table comes from the previous kernel; dense: warm L2 with the first
-  // weight tile (codes and scale blocks) while the previous kernel finishes
-  const bool grouped = args.tiles != nullptr;
-  if (grouped) griddep_wait();
-  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb);
-  if (static_cast<int>(blockIdx.x) >= walk.n_ids) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // Set-up reads nothing an earlier kernel of the stream writes: it runs before the wait,
+  // with an L2 prefetch of this CTA's first weight tile (codes and scale blocks).
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -140,28 +141,30 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], C::kEpiWarps);
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
     prefetch_tmap(&tmA128);
     prefetch_tmap(&tmB);
-    if (!grouped) {
-      int mt, expert, row0, nrows, ntile, kb0, kb1;
-      if (walk.at(blockIdx.x, mt, expert, row0, nrows, ntile) && mt % kRasterGroup == 0) {
-        walk.k_range(blockIdx.x, kb0, kb1);
-        kb1 = min(kb1, kb0 + kPrefetchKb);
-        const int brow = ntile * BN;
-        const uint8_t* sfb = args.b_scales + static_cast<size_t>(brow / BN) * args.num_kb * 4 * 512;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          prefetch_l2_tile_2d(&tmB, kb * 128, brow);
-          prefetch_l2_bulk(sfb + kb * 2048, 2048u);
+    if (C::kDual) prefetch_tmap(&tmB2);
+    int brow, kb0, kb1;
+    if (first_tile_hint(args.tiles, args.n_tiles, args.max_tiles, args.n_groups, args.M, args.N, BN,
+                        args.k_splits, args.num_kb, args.adaptive_splits != 0, brow, kb0, kb1)) {
+      kb1 = min(kb1, kb0 + kPrefetchKb);
+      const size_t sf0 = static_cast<size_t>(brow / BN) * args.num_kb * 4 * 512;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        prefetch_l2_tile_2d(&tmB, kb * 128, brow);
+        prefetch_l2_bulk(args.b_scales + sf0 + kb * 2048, 2048u);
+        if (C::kDual) {
+          prefetch_l2_tile_2d(&tmB2, kb * 128, brow);
+          prefetch_l2_bulk(args.b2_scales + sf0 + kb * 2048, 2048u);
         }
       }
     }
   }
-  if (warp >= 2 && warp <= 5) {
-    for (int i = threadIdx.x - 64; i < 256; i += 128) recip[i] = c_e4m3_recip.v[i];
+  if (warp >= 2) {
+    for (int i = threadIdx.x - 64; i < 256; i += 32 * C::kEpiWarps) recip[i] = c_e4m3_recip.v[i];
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -172,6 +175,11 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   griddep_enter();
+  // CTAs past the live tile ids walk nothing and go straight to the teardown
+  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb,
+                      args.adaptive_splits != 0);
+  if (args.splits_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
+    *args.splits_out = walk.splits;
   const long long budget = args.budget;
   const int nk = args.num_kb;  // stages of K = 256
 
@@ -284,9 +292,12 @@ __global__ void __launch_bounds__(192, 1)
       mma_commit(mma_done);
     }
   } else {
-    // ---- epilogue: warps 2..5
+    // ---- epilogue: lane quadrant warp % 4; with 8 warps, column half (warp - 2) / 4
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;
+    constexpr int kCols = BN * 4 / C::kEpiWarps;
+    const int c_lo = half * kCols, c_hi = c_lo + kCols;
     int tc = 0;
     for (int id = blockIdx.x; id < walk.n_ids; id += gridDim.x) {
       int mt, expert, row0, nrows, ntile;
@@ -305,12 +316,12 @@ __global__ void __launch_bounds__(192, 1)
       const float rs = (args.row_scale != nullptr && row_ok) ? args.row_scale[grow] : 1.f;
       if constexpr (EPI == kFp4EpiF32Ss) {
         const float alpha = rs * args.tensor_scale[args.tiles ? expert : 0];
-        const bool split = args.k_splits > 1;   // split-K: alpha * partial product, no ss
-        float* orow = split ? args.partial + (static_cast<long long>(id % args.k_splits) * args.M + grow) * args.N
+        const bool split = walk.splits > 1;   // split-K: alpha * partial product, no ss
+        float* orow = split ? args.partial + (static_cast<long long>(id % walk.splits) * args.M + grow) * args.N
                             : static_cast<float*>(args.out) + grow * args.ldo;
         float ss = 0.f;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32cols(tq + c0, v);
           tmem_ld_wait();
@@ -335,14 +346,30 @@ __global__ void __launch_bounds__(192, 1)
         const float ag = rs * args.tensor_scale[e], au = rs * args.tensor_scale2[e];
         uint8_t* crow = static_cast<uint8_t*>(args.out) + grow * (args.ldo / 2);
         const int K_h = static_cast<int>(args.ldo);   // h is the next GEMM's A: scales by M tile
+        // split-K: the scaled gate and up partial products, [splits][rows][2N] (gate | up)
+        float* prow = walk.splits > 1
+                          ? args.partial + (static_cast<long long>(id % walk.splits) * args.M + grow) * 2 * args.N
+                          : nullptr;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
           uint32_t g[32], u[32];
           tmem_ld_32cols(tq + c0, g);
           tmem_ld_32cols(tq + BN + c0, u);
           tmem_ld_wait();
           const int col = n0 + c0;
-          if (row_ok && col + 32 <= args.N) {
+          if (prow != nullptr) {
+            if (row_ok && col + 32 <= args.N) {
+              float4* og = reinterpret_cast<float4*>(prow + col);
+              float4* ou = reinterpret_cast<float4*>(prow + args.N + col);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                og[i] = make_float4(__uint_as_float(g[4 * i]) * ag, __uint_as_float(g[4 * i + 1]) * ag,
+                                    __uint_as_float(g[4 * i + 2]) * ag, __uint_as_float(g[4 * i + 3]) * ag);
+                ou[i] = make_float4(__uint_as_float(u[4 * i]) * au, __uint_as_float(u[4 * i + 1]) * au,
+                                    __uint_as_float(u[4 * i + 2]) * au, __uint_as_float(u[4 * i + 3]) * au);
+              }
+            }
+          } else if (row_ok && col + 32 <= args.N) {
             uint2 q[2];
             uint32_t sc[2];
 #pragma unroll
@@ -392,7 +419,7 @@ cudaError_t launch_fp4_one(const CUtensorMap* maps, const Fp4Args& a, int m_tile
   const long long ids = tile_id_bound(m_tiles, a.N, BN, a.k_splits > 1 ? a.k_splits : 1);
   if (ids == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
-  return launch_pdl(kern, dim3(grid), dim3(192), C::kSmemBytes, s, maps[0], maps[1], maps[2], maps[3],
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, maps[0], maps[1], maps[2], maps[3],
                     maps[4], maps[5], a);
 }
 

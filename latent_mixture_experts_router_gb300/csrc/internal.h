@@ -62,6 +62,8 @@ struct GemmArgs {
   int b_stream_once;       // B tiles are read by ~one M tile each: stream them evict-first
   int k_splits;            // > 1: split-K; the epilogue writes raw fp32 partial products
   float* partial;          // [k_splits][rows][N] (split-K), reduced by launch_splitk_reduce
+  int max_tiles;           // grouped: capacity of the tile table
+  int n_groups;            // grouped: experts (B holds n_groups * N rows)
 };
 
 struct Fp4Args {
@@ -86,6 +88,14 @@ struct Fp4Args {
   int b_stream_once;         // B tiles are read by ~one M tile each: stream them evict-first
   int k_splits;              // > 1: split-K; the epilogue writes alpha * partial products
   float* partial;            // [k_splits][rows][N] (split-K), reduced by launch_splitk_reduce
+  // Grouped GEMMs only: with adaptive_splits, k_splits is an upper bound and the kernel picks
+  // the split count from the live tile count (choose_splits, tiles.cuh); the count used is
+  // stored at splits_out (if set), where the reduce kernel reads it.  SwiGLU partials hold
+  // gate and up side by side: [splits][rows][2N].
+  int adaptive_splits;
+  int* splits_out;
+  int max_tiles;             // grouped: capacity of the tile table
+  int n_groups;              // grouped: experts (B holds n_groups * N rows)
 };
 
 // NVFP4 GEMM; maps = {A codes with boxes of 32, 64, 96, 128 rows, B codes, B2 codes}; scales
@@ -117,9 +127,19 @@ cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool 
 int sm_count();
 
 // Sums split-K partials [splits][rows][N] in split order into out [rows, ldo] (fp32) and, when
-// ss != nullptr, writes per-row partial sums of squares per group of `group` columns.
+// ss != nullptr, writes per-row partial sums of squares per group of `group` columns.  With
+// splits_dev != nullptr the split count is read there on the device (adaptive grouped GEMMs)
+// and `splits` is only its upper bound; a count of 1 means the GEMM wrote out itself.
 cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, float* out,
-                                 long long ldo, float* ss, int ld_ss, int group, cudaStream_t s);
+                                 long long ldo, float* ss, int ld_ss, int group, cudaStream_t s,
+                                 const int* splits_dev = nullptr);
+// Grouped SwiGLU after an adaptive split-K gate/up GEMM: sums the [splits][rows][2N] partials
+// (gate | up, already scaled), h = silu(gate) * up, quantised to NVFP4 with scale 1: codes
+// [rows, N/2] and E4M3 block scales in the block layout of M tile `mt` (the h operand of the
+// down GEMM).  Does nothing when the split count at splits_dev is 1.
+cudaError_t launch_swiglu_reduce_nvfp4(const float* partial, const int* splits_dev, int rows, int N,
+                                       const Tile* tiles, const int* n_tiles, int max_tiles,
+                                       uint8_t* codes, uint8_t* scales, cudaStream_t s);
 
 // Counts every kernel launch of the library (lmoe_kernel_launches).
 void count_launch();

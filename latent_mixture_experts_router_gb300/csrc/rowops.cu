@@ -664,8 +664,12 @@ __global__ void nvfp4_block_scales_kernel(const uint8_t* __restrict__ src, long 
 // result does not depend on scheduling) and writes the group's sum of squares.
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, int rows, int N,
                                      float* __restrict__ out, long long ldo, float* __restrict__ ss,
-                                     int ld_ss) {
+                                     int ld_ss, const int* __restrict__ splits_dev) {
   griddep_enter();
+  if (splits_dev != nullptr) {
+    splits = *splits_dev;
+    if (splits <= 1) return;   // the GEMM wrote out and ss itself
+  }
   __shared__ float red[33];
   const int r = blockIdx.x, grp = blockIdx.y;
   const int col = grp * blockDim.x + threadIdx.x;
@@ -677,6 +681,50 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int spli
   if (ss != nullptr) {
     const float t = block_sum(col < N ? v * v : 0.f, red);
     if (threadIdx.x == 0) ss[static_cast<long long>(r) * ld_ss + grp] = t;
+  }
+}
+
+// One CTA per (M tile, 4096 columns); a thread owns one 16-column block of h and walks the
+// tile's rows: sums the gate and up partials in split order, applies SwiGLU and quantises the
+// block (scale 1) exactly as the unsplit GEMM epilogue does.
+__global__ void __launch_bounds__(256) swiglu_reduce_nvfp4_kernel(
+    const float* __restrict__ partial, const int* __restrict__ splits_dev, int rows, int N,
+    const Tile* __restrict__ tiles, const int* __restrict__ n_tiles, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales) {
+  griddep_enter();
+  __shared__ float recip[256];
+  const int splits = *splits_dev;
+  const int mt = blockIdx.x;
+  if (splits <= 1 || mt >= *n_tiles) return;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) recip[i] = c_e4m3_recip.v[i];
+  __syncthreads();
+  const Tile t = tiles[mt];
+  const int cb = blockIdx.y * blockDim.x + threadIdx.x;   // 16-column block of h
+  if (cb * 16 >= N) return;
+  const long long plane = static_cast<long long>(rows) * 2 * N;   // one split's partials
+  for (int r = 0; r < t.nrows; ++r) {
+    const long long grow = static_cast<long long>(t.row0) + r;
+    const float* pg = partial + grow * 2 * N + cb * 16;
+    float g[16], u[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) g[i] = u[i] = 0.f;
+    for (int q = 0; q < splits; ++q) {
+      const float4* g4 = reinterpret_cast<const float4*>(pg + q * plane);
+      const float4* u4 = reinterpret_cast<const float4*>(pg + q * plane + N);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 a = g4[i], b = u4[i];
+        g[4 * i] += a.x; g[4 * i + 1] += a.y; g[4 * i + 2] += a.z; g[4 * i + 3] += a.w;
+        u[4 * i] += b.x; u[4 * i + 1] += b.y; u[4 * i + 2] += b.z; u[4 * i + 3] += b.w;
+      }
+    }
+    float h[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) h[i] = __fdividef(g[i], 1.f + __expf(-g[i])) * u[i];
+    uint2 q;
+    const uint32_t sc = nvfp4_quant16(h, 6.f, 1.f, recip, q);
+    *reinterpret_cast<uint2*>(codes + grow * (N / 2) + cb * 8) = q;
+    scales[blocked_sf_offset(mt, r, cb, N)] = static_cast<uint8_t>(sc);
   }
 }
 
@@ -769,11 +817,21 @@ cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K,
 }
 
 cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, float* out,
-                                 long long ldo, float* ss, int ld_ss, int group, cudaStream_t s) {
+                                 long long ldo, float* ss, int ld_ss, int group, cudaStream_t s,
+                                 const int* splits_dev) {
   if (rows == 0) return cudaSuccess;
   dim3 grid(rows, (N + group - 1) / group);
   return launch_pdl(splitk_reduce_kernel, dim3(grid), dim3(group), 0, s, partial, splits, rows, N,
-                    out, ldo, ss, ld_ss);
+                    out, ldo, ss, ld_ss, splits_dev);
+}
+
+cudaError_t launch_swiglu_reduce_nvfp4(const float* partial, const int* splits_dev, int rows, int N,
+                                       const Tile* tiles, const int* n_tiles, int max_tiles,
+                                       uint8_t* codes, uint8_t* scales, cudaStream_t s) {
+  if (rows == 0 || max_tiles == 0) return cudaSuccess;
+  dim3 grid(max_tiles, (N / 16 + 255) / 256);
+  return launch_pdl(swiglu_reduce_nvfp4_kernel, grid, dim3(256), 0, s, partial, splits_dev, rows, N,
+                    tiles, n_tiles, codes, scales);
 }
 
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s) {

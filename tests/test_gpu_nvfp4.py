@@ -68,6 +68,13 @@ SHAPES = [  # (T, D, L, E, I, k)
     (130, 256, 512, 16, 512, 4),
     (257, 512, 256, 6, 256, 6),
 ]
+# few rows and a long K: the grouped GEMMs split K (count picked on the device); gate/up
+# splits in the first two, down in the last
+SPLIT_SHAPES = [  # (T, D, L, E, I, k)
+    (2, 512, 4096, 8, 1024, 2),
+    (5, 256, 4096, 16, 512, 3),
+    (1, 256, 256, 4, 4096, 2),
+]
 
 
 @pytest.mark.parametrize("T,D,L,E,I,k", SHAPES)
@@ -82,6 +89,43 @@ def test_nvfp4_block_parity(cuda, T, D, L, E, I, k):
     ref = oracle.forward_batched(x, P, k, trace=tr)
     rep = compare_block(out.cpu().numpy(), idx.cpu().numpy(), x, P, k, TOL_NVFP4, tr=tr, ref=ref)
     print(w.name, rep)
+    assert rep.ok, str(rep)
+
+
+@pytest.mark.parametrize("T,D,L,E,I,k", SPLIT_SHAPES)
+def test_nvfp4_grouped_split_parity(cuda, T, D, L, E, I, k):
+    import latent_mixture_experts_router_gb300 as lm
+    w = workloads.Workload(f"fp4s_{T}_{D}_{L}_{E}_{I}_{k}", T=T, D=D, L=L, E=E, I=I, k=k,
+                           weights="nvfp4", seed=T)
+    inp = workloads.make_inputs(w, cuda)
+    out, idx, blk, cfg = run(inp)
+    lay = lm.lmoe_get_workspace_layout(cfg)
+    o = lay["grouped_splits"]
+    splits = blk._ws[o:o + 8].view(torch.int32).cpu().tolist()
+    n_tiles = int(blk._ws[lay["n_tiles"]:lay["n_tiles"] + 4].view(torch.int32).item())
+    # the device's choice against the rule: fill the last wave of the persistent grid best,
+    # with the smallest divisor of the K blocks that gains more than 2 %
+    grid = torch.cuda.get_device_properties(cuda).multi_processor_count
+    s_max = min(8, max(1, (L // 128) // T))
+
+    def rule(units, num_kb):
+        if s_max <= 1 or units >= 3 * grid:
+            return 1
+        best, best_eff = 1, units / (-(-units // grid) * grid)
+        for s in range(2, min(s_max, num_kb // 8) + 1):   # at least 8 K blocks per split
+            if num_kb % s == 0:
+                eff = units * s / (-(-units * s // grid) * grid)
+                if eff > best_eff + 0.02:
+                    best, best_eff = s, eff
+        return best
+    assert splits == [rule(n_tiles * (I // 128), L // 256), rule(n_tiles * (L // 128), I // 256)], splits
+    assert max(splits) > 1, splits   # a grouped GEMM took the split path
+    P = oracle.params_from_inputs(inp)
+    x = inp.x.double().cpu().numpy()
+    tr = oracle.Trace()
+    ref = oracle.forward_batched(x, P, k, trace=tr)
+    rep = compare_block(out.cpu().numpy(), idx.cpu().numpy(), x, P, k, TOL_NVFP4, tr=tr, ref=ref)
+    print(w.name, splits, rep)
     assert rep.ok, str(rep)
 
 
