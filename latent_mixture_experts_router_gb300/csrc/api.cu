@@ -20,6 +20,7 @@
 
 #include "../../include/latent_moe.h"
 #include "internal.h"
+#include "tiles.cuh"
 
 using namespace lmoe;
 
@@ -40,6 +41,7 @@ struct Layout {
   long long near_tie;
   long long tile_base;  // [E] first M tile of each expert
   long long partial;    // split-K partial products of the dense and grouped GEMMs
+  long long partial_pool;  // the pooler's own (it may run beside the router on a side stream)
   long long splits_dev; // [2] split counts the grouped NVFP4 GEMMs chose (gate/up, down)
   // fp32-weight mode: bf16 copies of the weights
   long long w_router, w_pool, w_gate, w_up, w_down, w_unpool;
@@ -61,10 +63,13 @@ int grouped_max_splits(const lmoe_config* c) {
 // SMs of a GB300 work, at least `min_kb` K blocks each, at most 32.  A fixed SM count keeps
 // the workspace layout independent of the device a call runs on.
 constexpr int kSplitSms = 152;
-int dense_splits(int T, int N, int bn, int num_kb, int min_kb) {
+// The pooler runs beside the router (side stream): at small T its split count is sized for
+// about two thirds of the SMs, so that the router's CTAs find SMs of their own.
+constexpr int kPoolerSms = 100;
+int dense_splits(int T, int N, int bn, int num_kb, int min_kb, int sms = kSplitSms) {
   const long long tiles = static_cast<long long>((T + kBM - 1) / kBM) * ((N + bn - 1) / bn);
-  if (tiles == 0 || tiles * 2 >= kSplitSms) return 1;
-  long long sp = kSplitSms / tiles;
+  if (tiles == 0 || tiles * 2 >= sms) return 1;
+  long long sp = sms / tiles;
   if (sp > num_kb / min_kb) sp = num_kb / min_kb;
   if (sp > 32) sp = 32;
   return sp < 1 ? 1 : static_cast<int>(sp);
@@ -80,10 +85,10 @@ DenseSplits dense_split_plan(const lmoe_config* c) {
   DenseSplits d;
   d.router = dense_splits(c->T, c->n_experts, kBNWide, xa_cols / kBK, 4);
   if (fp4) {
-    d.pooler = dense_splits(c->T, L, kBNFp4, D / 256, 2);
+    d.pooler = dense_splits(c->T, L, kBNFp4, D / 256, 2, kPoolerSms);
     d.unpool = dense_splits(c->T, D, kBNFp4, L / 256, 2);
   } else {
-    d.pooler = dense_splits(c->T, L, kBNWide, (f32w ? 3 * D : D) / kBK, 4);
+    d.pooler = dense_splits(c->T, L, kBNWide, (f32w ? 3 * D : D) / kBK, 4, kPoolerSms);
     d.unpool = dense_splits(c->T, D, kBNWide, wsplit * L / kBK, 4);
   }
   return d;
@@ -182,13 +187,13 @@ void make_layout(const lmoe_config* c, Layout* L) {
     L->w_down = take(E * Ld * 2 * I * 2);
     L->w_unpool = take(D * 2 * Ld * 2);
   }
-  {  // split-K partials: the largest of the dense GEMMs' [splits][T][N] and the grouped
-     // GEMMs' [splits][R][2I] (gate | up) and [splits][R][L]
+  {  // split-K partials: the largest of the router's and unpooler's [splits][T][N] and the
+     // grouped GEMMs' [splits][R][2I] (gate | up) and [splits][R][L]; the pooler's apart
     const DenseSplits d = dense_split_plan(c);
     long long need = 0;
     if (d.router > 1) need = std::max(need, d.router * T * E);
-    if (d.pooler > 1) need = std::max(need, d.pooler * T * Ld);
     if (d.unpool > 1) need = std::max(need, d.unpool * T * D);
+    L->partial_pool = d.pooler > 1 ? take(d.pooler * T * Ld * 4) : -1;
     const long long gs = grouped_max_splits(c);
     if (gs > 1) need = std::max(need, gs * R * std::max(2 * I, Ld));
     L->partial = need > 0 ? take(need * 4) : -1;
@@ -367,6 +372,33 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
   return LMOE_OK;
 }
 
+// ------------------------------------------------------------------ side stream
+// The pooler reads only the pre-norm output, so it runs on a side stream while the router,
+// top-k and permutation run on the caller's stream (all three are latency-bound at small T).
+// One side stream and one fork/join event pair per device; the mutex keeps a fork, the
+// pooler and the matching join of one call together when several host threads call at once.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+  bool ok = false;
+};
+constexpr int kMaxDevices = 64;
+
+SideStream* side_stream() {
+  static SideStream side[kMaxDevices];
+  static std::once_flag once[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  SideStream& ss = side[dev];
+  std::call_once(once[dev], [&ss] {
+    ss.ok = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) == cudaSuccess &&
+            cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) == cudaSuccess;
+  });
+  return ss.ok ? &ss : nullptr;
+}
+
 lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_router,
                          const void* W_pool, const float* g_pool, const void* W_gate,
                          const void* W_up, const void* W_down, const float* g_expert,
@@ -487,39 +519,96 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                                    status2, s));
   else
     LMOE_CUDA(launch_prenorm(x, x_f32, g_pre, T, D, eps, xa, xa_cols, status2, s));
+  const int m_tiles_T = cdiv(T, kBM);
+  // NVFP4 operands (offsets of fields a BF16 layout lacks are -1: null pointers then)
+  auto wsp = [&](long long off) -> uint8_t* { return off >= 0 ? wsb + off : nullptr; };
+  const Fp4Operand xq{wsp(L.pub.xq), wsp(L.pub.xq_scale)};
+  const Fp4Operand xeq{wsp(L.pub.xe), wsp(L.pub.xe_scale)};
+  const Fp4Operand hq{wsp(L.pub.h), wsp(L.pub.h_scale)};
+  const Fp4Operand cq{wsp(L.pub.c), wsp(L.pub.c_scale)};
+  float* xq_s = reinterpret_cast<float*>(wsp(L.pub.xq_rowscale));
+  float* xe_s = reinterpret_cast<float*>(wsp(L.pub.xe_rowscale));
+  float* c_s = reinterpret_cast<float*>(wsp(L.pub.c_rowscale));
+  auto op = [](const lmoe_nvfp4_weight* w) { return Fp4Operand{w->data, w->scales}; };
+  float* partial_pool = L.partial_pool >= 0 ? static_cast<float*>(at(L.partial_pool)) : nullptr;
+
+  // S5 pooler, enqueued on stream `ps`: NVFP4 p = s_x * s_W * (Q(xn) . W_pool^T) (block-scaled
+  // FP4 MMA), else p = xn_hi . W_pool^T; both with row partial sums of squares
+  auto pooler = [&](cudaStream_t ps) -> lmoe_status {
+    if (fp4)
+      return run_gemm_fp4(kFp4EpiF32Ss, xq, T, D, op(q4[0]), Ld, nullptr, Ld, nullptr, nullptr, m_tiles_T,
+                          p, Ld, nullptr, ss_p, L.ld_ss_p, xq_s, q4[0]->tensor_scale, nullptr, err, budget,
+                          ps, T, dsp.pooler, partial_pool);
+    const int pool_k = f32w ? 3 * D : D;
+    return run_gemm(kEpiF32Ss, xa, T, pool_k, xa_cols, wp, Ld, pool_k, nullptr, Ld, pool_k / kBK,
+                    nullptr, nullptr, m_tiles_T, p, Ld, ss_p, L.ld_ss_p, err, budget, ps, T, dsp.pooler,
+                    partial_pool);
+  };
+  // The pooler needs only xn: it runs on the side stream beside S2-S4 unless the caller
+  // times those stages (their events pin every stage to the caller's stream).
+  bool staged = false;
+  for (int i = LMOE_STAGE_PRENORM; ev != nullptr && i <= LMOE_STAGE_POOLNORM; ++i)
+    staged = staged || ev[i] != nullptr;
+  SideStream* side = staged ? nullptr : side_stream();
+  std::unique_lock<std::mutex> side_lock;
+  struct Join {  // the caller's stream waits for the side stream on every way out
+    cudaStream_t s;
+    SideStream* side;
+    bool join() {
+      SideStream* q = side;
+      side = nullptr;
+      return q == nullptr || cudaStreamWaitEvent(s, q->join, 0) == cudaSuccess;
+    }
+    ~Join() { join(); }
+  } joiner{s, nullptr};
+  if (side != nullptr) {
+    side_lock = std::unique_lock<std::mutex>(side->mu);
+    LMOE_CUDA(cudaEventRecord(side->fork, s));
+    LMOE_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));
+    joiner.side = side;
+    st = pooler(side->stream);
+    if (cudaEventRecord(side->join, side->stream) != cudaSuccess) {
+      joiner.side = nullptr;   // nothing to wait on; the error is reported
+      return LMOE_ERR_CUDA;
+    }
+    if (st != LMOE_OK) return st;
+  }
+
   LMOE_MARK(LMOE_STAGE_ROUTER);
   // S2 router logits = [xn_hi | xn_lo (| xn_hi)] . [W | W (| W_lo)]^T
-  const int m_tiles_T = cdiv(T, kBM);
   st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
                 xa_cols / kBK, nullptr, nullptr, m_tiles_T, logits, L.ld_logits, nullptr, 0, err,
                 budget, s, T, dsp.router, partial);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_TOPK);
-  // S3 top-k + softmax
-  LMOE_CUDA(launch_topk(logits, L.ld_logits, ex ? ex->router_bias : nullptr,
-                        ex ? ex->forced_idx : nullptr, T, E, k, tk_idx, tk_w, near_tie,
-                        ex ? ex->topk_idx_out : nullptr, ex ? ex->topk_w_out : nullptr, err, s));
+  // S3 top-k + softmax, S4 permutation (one kernel for few pairs unless S4 is timed apart)
+  const float* bias = ex ? ex->router_bias : nullptr;
+  const int32_t* forced = ex ? ex->forced_idx : nullptr;
+  int32_t* tile_base = static_cast<int32_t*>(at(L.tile_base));
+  const bool fused_route = route_small_fits(T, k, E) && (ev == nullptr || ev[LMOE_STAGE_PERMUTE] == nullptr);
+  if (fused_route) {
+    LMOE_CUDA(launch_route_small(logits, L.ld_logits, bias, forced, T, E, k, tk_idx, tk_w, near_tie,
+                                 ex ? ex->topk_idx_out : nullptr, ex ? ex->topk_w_out : nullptr, err,
+                                 counts, offsets, row_of, tok_of, tiles, n_tiles, tile_base, s));
+    LMOE_MARK(LMOE_STAGE_PERMUTE);
+  } else {
+    LMOE_CUDA(launch_topk(logits, L.ld_logits, bias, forced, T, E, k, tk_idx, tk_w, near_tie,
+                          ex ? ex->topk_idx_out : nullptr, ex ? ex->topk_w_out : nullptr, err, s));
+    LMOE_MARK(LMOE_STAGE_PERMUTE);
+    LMOE_CUDA(launch_permute(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, s,
+                             tile_base));
+  }
   if (ex && ex->near_tie_count_out)
     LMOE_CUDA(cudaMemcpyAsync(ex->near_tie_count_out, near_tie, 4, cudaMemcpyDeviceToDevice, s));
-  LMOE_MARK(LMOE_STAGE_PERMUTE);
-  // S4 permutation
-  int32_t* tile_base = static_cast<int32_t*>(at(L.tile_base));
-  LMOE_CUDA(launch_permute(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, s,
-                           tile_base));
-  if (fp4) {
-    const Fp4Operand xq{wsb + L.pub.xq, wsb + L.pub.xq_scale};
-    const Fp4Operand xeq{wsb + L.pub.xe, wsb + L.pub.xe_scale};
-    const Fp4Operand hq{wsb + L.pub.h, wsb + L.pub.h_scale};
-    const Fp4Operand cq{wsb + L.pub.c, wsb + L.pub.c_scale};
-    float* xq_s = reinterpret_cast<float*>(wsb + L.pub.xq_rowscale);
-    float* xe_s = reinterpret_cast<float*>(wsb + L.pub.xe_rowscale);
-    float* c_s = reinterpret_cast<float*>(wsb + L.pub.c_rowscale);
-    auto op = [](const lmoe_nvfp4_weight* w) { return Fp4Operand{w->data, w->scales}; };
+  if (side != nullptr) {
+    if (!joiner.join()) return LMOE_ERR_CUDA;
+    side_lock.unlock();
+  } else {
     LMOE_MARK(LMOE_STAGE_POOLER);
-    // S5 pooler p = s_x * s_W * (Q(xn) . W_pool^T), block-scaled FP4 MMA
-    st = run_gemm_fp4(kFp4EpiF32Ss, xq, T, D, op(q4[0]), Ld, nullptr, Ld, nullptr, nullptr, m_tiles_T,
-                      p, Ld, nullptr, ss_p, L.ld_ss_p, xq_s, q4[0]->tensor_scale, nullptr, err, budget, s, T, dsp.pooler, partial);
+    st = pooler(s);
     if (st != LMOE_OK) return st;
+  }
+  if (fp4) {
     LMOE_MARK(LMOE_STAGE_POOLNORM);
     // S6 pool norm, quantised per token, copied to the k expert rows
     LMOE_CUDA(launch_poolnorm_scatter_nvfp4(p, ss_p, L.ld_ss_p, g_pool, row_of, tk_idx, offsets,
@@ -528,19 +617,28 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     LMOE_MARK(LMOE_STAGE_GATE_UP);
     // S7 grouped gate/up + SwiGLU, h requantised to NVFP4 (scale 1); at small T split-K
     // with the split count picked on the device from the live tiles
-    const int gsplit = grouped_max_splits(cfg);
     int* splits_dev = static_cast<int*>(at(L.splits_dev));
+    // the live tile count lies in [max(k, R/128), max_tiles] (a token's k experts are
+    // distinct); where no count in that range splits, the GEMM runs unsplit with no reduce
+    const int lo_tiles = std::max(k, cdiv(R, kBM));
+    auto grouped_splits = [&](int N, int num_kb) -> int {
+      const int gs = grouped_max_splits(cfg);
+      if (gs <= 1) return 1;
+      const long long ids = tile_id_bound(L.max_tiles, N, kBNFp4, gs);
+      const int grid = static_cast<int>(std::min<long long>(ids, sm_count()));
+      return grouped_split_possible(lo_tiles, L.max_tiles, cdiv(N, kBNFp4), num_kb, grid, gs) ? gs : 1;
+    };
     const Fp4Operand up = op(q4[2]);
     st = run_gemm_fp4(kFp4EpiSwiGLUQuant, xeq, R, Ld, op(q4[1]), 1LL * E * I, &up, I, tiles, n_tiles,
                       L.max_tiles, wsb + L.pub.h, I, wsb + L.pub.h_scale, nullptr, 0, xe_s,
-                      q4[1]->tensor_scale, q4[2]->tensor_scale, err, budget, s, R / E, gsplit, partial,
-                      splits_dev);
+                      q4[1]->tensor_scale, q4[2]->tensor_scale, err, budget, s, R / E,
+                      grouped_splits(I, Ld / 256), partial, splits_dev);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_DOWN);
     // S8 grouped down (fp32 y) with per-row partial sums of squares
     st = run_gemm_fp4(kFp4EpiF32Ss, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
                       L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
-                      nullptr, err, budget, s, R / E, gsplit, partial, splits_dev + 1);
+                      nullptr, err, budget, s, R / E, grouped_splits(Ld, I / 256), partial, splits_dev + 1);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_COMBINE);
     // S9 combine, c quantised per token
@@ -552,12 +650,6 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                       D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s, T, dsp.unpool, partial);
     if (st != LMOE_OK) return st;
   } else {
-  LMOE_MARK(LMOE_STAGE_POOLER);
-  // S5 pooler p = xn_hi . W_pool^T, with row partial sums of squares
-  const int pool_k = f32w ? 3 * D : D;
-  st = run_gemm(kEpiF32Ss, xa, T, pool_k, xa_cols, wp, Ld, pool_k, nullptr, Ld, pool_k / kBK,
-                nullptr, nullptr, m_tiles_T, p, Ld, ss_p, L.ld_ss_p, err, budget, s, T, dsp.pooler, partial);
-  if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_POOLNORM);
   // S6 pool norm, scattered to the k expert-contiguous rows of each token
   LMOE_CUDA(launch_poolnorm_scatter(p, ss_p, L.ld_ss_p, g_pool, row_of, T, Ld, k, eps, xe, s));

@@ -144,7 +144,8 @@ cudaError_t launch_swiglu_reduce_nvfp4(const float* partial, const int* splits_d
 // Counts every kernel launch of the library (lmoe_kernel_launches).
 void count_launch();
 
-// Launches `kern` with programmatic stream serialisation and counts it.  The kernel must call
+// Launches `kern` with programmatic stream serialisation and counts it; with cluster > 1
+// also as clusters of `cluster` CTAs along x.  The kernel must call
 // griddep_wait() (ptx.cuh) before it reads anything an earlier kernel of the stream wrote.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
@@ -162,6 +163,26 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   count_launch();
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
+  count_launch();
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Launches one tcgen05 GEMM: out = A * B^T over grid (ceil(N/BN), m_tiles).
 cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
@@ -172,6 +193,14 @@ cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& 
 // status words at status2 (error word, near-tie count) when status2 != nullptr.
 cudaError_t launch_prenorm(const void* x, bool x_f32, const float* g_pre, int T, int D, float eps,
                            __nv_bfloat16* xa, int xa_cols, unsigned* status2, cudaStream_t s);
+// S3 and S4 in one CTA for few (token, slot) pairs (route_small_fits); same outputs as
+// launch_topk followed by launch_permute.
+bool route_small_fits(int T, int k, int E);
+cudaError_t launch_route_small(const float* logits, int ld, const float* bias, const int32_t* forced,
+                               int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
+                               int32_t* idx_copy, float* w_copy, unsigned* err, int32_t* counts,
+                               int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
+                               int32_t* n_tiles, int32_t* tile_base, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int ld, const float* bias, const int32_t* forced,
                         int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
                         int32_t* idx_copy, float* w_copy, unsigned* err, cudaStream_t s);

@@ -97,6 +97,75 @@ __device__ __forceinline__ void store8_bf16(__nv_bfloat16* p, const float (&v)[8
   *reinterpret_cast<uint4*>(p) = q;
 }
 __device__ __forceinline__ void load8_f32(const float* p, float (&v)[8]) { load8(p, true, 0, v); }
+__device__ __forceinline__ void store8_f32(float* p, const float (&v)[8]) {   // p 16-byte aligned
+  float4* q = reinterpret_cast<float4*>(p);
+  q[0] = make_float4(v[0], v[1], v[2], v[3]);
+  q[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    float t = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+    if (l == 0) red[32] = t;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+// ------------------------------------------------------------------ row slices
+// A row kernel runs C CTAs per token (C = 1, 2, 4 or 8, chosen by the launcher from T so
+// that a few tokens still spread over many SMs): CTA blockIdx.x = t * C + c handles the
+// columns [c N / C, (c + 1) N / C) of token t.  Kernels that reduce over the row are
+// launched as clusters of C CTAs and combine the CTAs' partial sums (maxima) through
+// distributed shared memory in rank order, so every CTA of the token gets the same value.
+struct RowSlice {
+  long long t;
+  int c, i0, i1;
+};
+__device__ __forceinline__ RowSlice row_slice(int N, int C) {
+  RowSlice r;
+  r.t = blockIdx.x / C;
+  r.c = static_cast<int>(blockIdx.x % C);
+  const int w = N / C;
+  r.i0 = r.c * w;
+  r.i1 = r.i0 + w;
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// A float of the shared memory of cluster CTA `rank` (same variable as *p in this CTA)
+__device__ __forceinline__ float dsmem_ld(const float* p, int rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+// Cluster-wide sum (is_max: maximum of non-negative values) of v, which every thread of a
+// CTA holds; `slot` is a __shared__ float used by this one reduction only.  Every thread of
+// every CTA of the cluster calls it.  A kernel that calls it ends with cluster_sync_all(),
+// so that no CTA leaves while another still reads its slot.
+__device__ __forceinline__ float cluster_combine(float v, float* slot, int C, bool is_max) {
+  if (C == 1) return v;
+  if (threadIdx.x == 0) *slot = v;
+  cluster_sync_all();
+  float r = 0.f;
+  for (int q = 0; q < C; ++q) {
+    const float o = dsmem_ld(slot, q);
+    r = is_max ? fmaxf(r, o) : r + o;
+  }
+  return r;
+}
 
 // ------------------------------------------------------------------ prenorm
 // One CTA per token.  xa row = [xn_hi | xn_lo] (or [hi | lo | hi] when xa_cols = 3D,
@@ -105,22 +174,25 @@ __global__ void __launch_bounds__(kRowThreads) prenorm_kernel(const void* __rest
                                                               const float* __restrict__ g,
                                                               int D, float eps,
                                                               __nv_bfloat16* __restrict__ xa,
-                                                              int xa_cols, unsigned* status2) {
+                                                              int xa_cols, unsigned* status2, int C) {
   griddep_enter();
   if (status2 != nullptr && blockIdx.x == 0 && threadIdx.x == 0) status2[0] = status2[1] = 0u;
   __shared__ float red[33];
-  const long long t = blockIdx.x;
+  __shared__ float slot_ss;
+  const RowSlice sl = row_slice(D, C);
+  const long long t = sl.t;
   const long long xoff = t * D;
   float ss = 0.f;
-  for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
+  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float v[8];
     load8(x, x_f32, xoff + i, v);
 #pragma unroll
     for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
   }
-  const float rs = rsqrtf(block_sum(ss, red) / static_cast<float>(D) + eps);
+  const float rs =
+      rsqrtf(cluster_combine(block_sum(ss, red), &slot_ss, C, false) / static_cast<float>(D) + eps);
   __nv_bfloat16* row = xa + t * xa_cols;
-  for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
+  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float v[8], gg[8], hi[8], lo[8];
     load8(x, x_f32, xoff + i, v);
     load8_f32(g + i, gg);
@@ -134,6 +206,7 @@ __global__ void __launch_bounds__(kRowThreads) prenorm_kernel(const void* __rest
     store8_bf16(row + D + i, lo);
     if (xa_cols == 3 * D) store8_bf16(row + 2 * D + i, hi);
   }
+  if (C > 1) cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ top-k + softmax
@@ -141,24 +214,18 @@ __global__ void __launch_bounds__(kRowThreads) prenorm_kernel(const void* __rest
 // index asc); the (k+1)-th round gives the margin for the near-tie count.
 constexpr int kTopkWarps = 4;
 
-__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
-    const float* __restrict__ logits, int ld, const float* __restrict__ bias,
-    const int32_t* __restrict__ forced, int T, int E, int k, int32_t* __restrict__ idx_out,
-    float* __restrict__ w_out, int32_t* __restrict__ near_tie, int32_t* __restrict__ idx_copy,
-    float* __restrict__ w_copy, unsigned* __restrict__ err) {
-  griddep_enter();
-  extern __shared__ float vals_all[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long t = static_cast<long long>(blockIdx.x) * kTopkWarps + warp;
-  if (t >= T) return;
-  float* vals = vals_all + warp * E;
-  for (int i = lane; i < E; i += 32) vals[i] = logits[t * ld + i] + (bias ? bias[i] : 0.f);
-  __syncwarp();
+// The top-k of one token, computed by one warp: vals[E] (shared memory, overwritten) holds
+// the token's logits (+ bias); forced_row, if set, holds its k experts.  Lane 0 writes the
+// experts (descending logit) and their softmax weights renormalised over the k.
+__device__ __forceinline__ void warp_topk(float* vals, const int32_t* forced_row, int E, int k,
+                                          long long t, int lane, int32_t* idx_out, float* w_out,
+                                          int32_t* near_tie, int32_t* idx_copy, float* w_copy,
+                                          unsigned* err) {
   int sel[16];
   float sval[16];
-  if (forced != nullptr) {
+  if (forced_row != nullptr) {
     for (int j = 0; j < k; ++j) {
-      int e = forced[t * k + j];
+      int e = forced_row[j];
       if (e < 0 || e >= E) {  // an id outside [0, E) would index out of bounds downstream
         if (lane == 0) atomicOr(err, kErrBadIndex);
         e = 0;
@@ -213,6 +280,23 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
       if (w_copy) w_copy[t * k + j] = ex[j] * inv;
     }
   }
+}
+
+__global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
+    const float* __restrict__ logits, int ld, const float* __restrict__ bias,
+    const int32_t* __restrict__ forced, int T, int E, int k, int32_t* __restrict__ idx_out,
+    float* __restrict__ w_out, int32_t* __restrict__ near_tie, int32_t* __restrict__ idx_copy,
+    float* __restrict__ w_copy, unsigned* __restrict__ err) {
+  griddep_enter();
+  extern __shared__ float vals_all[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long t = static_cast<long long>(blockIdx.x) * kTopkWarps + warp;
+  if (t >= T) return;
+  float* vals = vals_all + warp * E;
+  for (int i = lane; i < E; i += 32) vals[i] = logits[t * ld + i] + (bias ? bias[i] : 0.f);
+  __syncwarp();
+  warp_topk(vals, forced ? forced + t * k : nullptr, E, k, t, lane, idx_out, w_out, near_tie,
+            idx_copy, w_copy, err);
 }
 
 // ------------------------------------------------------------------ permutation
@@ -298,15 +382,129 @@ __global__ void __launch_bounds__(kPermThreads) expert_scatter_kernel(
   }
 }
 
+// ------------------------------------------------------------------ routing for few tokens
+// With few (token, slot) pairs one CTA performs S3 and S4 together, saving two launches on
+// the latency-bound chain: each warp selects the top-k of its tokens (warp_topk), then the
+// CTA counts the pairs per expert, scans the counts into offsets and first M tiles, writes
+// the tile table and gives pair i the row offsets[e] + #{j < i : idx[j] = e} (the stable
+// order of the expert_count / expert_scatter path, so both paths give identical results).
+constexpr int kRouteThreads = 512;
+constexpr int kRouteMaxPairs = 256;
+
+// Exclusive block scan of (a, b) over the threads' values, in thread order; returns the
+// totals through *ta, *tb.  Every thread of the block calls it.
+__device__ __forceinline__ void block_scan2(int& a, int& b, int* sh, int* ta, int* tb) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  int ia = a, ib = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ya = __shfl_up_sync(0xffffffffu, ia, o), yb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) {
+      ia += ya;
+      ib += yb;
+    }
+  }
+  __syncthreads();
+  if (lane == 31) {
+    sh[warp] = ia;
+    sh[32 + warp] = ib;
+  }
+  __syncthreads();
+  int pa = 0, pb = 0, sa = 0, sb = 0;
+  for (int q = 0; q < nw; ++q) {
+    if (q < warp) {
+      pa += sh[q];
+      pb += sh[32 + q];
+    }
+    sa += sh[q];
+    sb += sh[32 + q];
+  }
+  a = pa + ia - a;
+  b = pb + ib - b;
+  *ta = sa;
+  *tb = sb;
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_small_kernel(
+    const float* __restrict__ logits, int ld, const float* __restrict__ bias,
+    const int32_t* __restrict__ forced, int T, int E, int k, int32_t* __restrict__ idx_out,
+    float* __restrict__ w_out, int32_t* __restrict__ near_tie, int32_t* __restrict__ idx_copy,
+    float* __restrict__ w_copy, unsigned* __restrict__ err, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of,
+    Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles, int32_t* __restrict__ tile_base) {
+  griddep_enter();
+  extern __shared__ float route_sh[];
+  constexpr int nw = kRouteThreads / 32;
+  float* vals_all = route_sh;                                         // [nw][E]
+  int* cnt_s = reinterpret_cast<int*>(route_sh + nw * E);             // [E]
+  int* off_s = cnt_s + E;                                             // [E]
+  int* idx_s = off_s + E;                                             // [kRouteMaxPairs]
+  __shared__ int scan_sh[64];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = T * k;
+  // S3: a warp per token
+  for (int t = warp; t < T; t += nw) {
+    float* vals = vals_all + warp * E;
+    for (int i = lane; i < E; i += 32) vals[i] = logits[static_cast<long long>(t) * ld + i] + (bias ? bias[i] : 0.f);
+    __syncwarp();
+    warp_topk(vals, forced ? forced + static_cast<long long>(t) * k : nullptr, E, k, t, lane, idx_out, w_out,
+              near_tie, idx_copy, w_copy, err);
+    __syncwarp();
+  }
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) cnt_s[e] = 0;
+  __syncthreads();   // idx_out of every token written (global, this CTA) and counts zeroed
+  for (int i = threadIdx.x; i < n; i += kRouteThreads) {
+    const int e = idx_out[i];
+    idx_s[i] = e;
+    atomicAdd(&cnt_s[e], 1);
+  }
+  __syncthreads();
+  // S4: offsets and first M tiles by an exclusive scan over the experts (thread-contiguous
+  // runs of experts, so thread order is expert order)
+  const int per = (E + kRouteThreads - 1) / kRouteThreads;
+  const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
+  int a = 0, b = 0;
+  for (int e = e0; e < e1; ++e) {
+    a += cnt_s[e];
+    b += (cnt_s[e] + kBM - 1) / kBM;
+  }
+  int ta, tb;
+  block_scan2(a, b, scan_sh, &ta, &tb);
+  for (int e = e0; e < e1; ++e) {
+    const int c = cnt_s[e], nt = (c + kBM - 1) / kBM;
+    off_s[e] = a;
+    counts[e] = c;
+    offsets[e] = a;
+    if (tile_base != nullptr) tile_base[e] = b;
+    for (int m = 0; m < nt; ++m) tiles[b + m] = Tile{e, a + m * kBM, min(kBM, c - m * kBM), 0};
+    a += c;
+    b += nt;
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = ta;
+    *n_tiles = tb;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kRouteThreads) {
+    const int e = idx_s[i];
+    int rank = 0;
+    for (int j = 0; j < i; ++j) rank += (idx_s[j] == e);
+    const int r = off_s[e] + rank;
+    row_of[i] = r;
+    tok_of[r] = i / k;
+  }
+}
+
 // ------------------------------------------------------------------ pool norm + scatter
 __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
     const float* __restrict__ p, const float* __restrict__ ss_p, int ld_ss,
     const float* __restrict__ g, const int32_t* __restrict__ row_of, int L, int k, float eps,
-    __nv_bfloat16* __restrict__ xe) {
+    __nv_bfloat16* __restrict__ xe, int C) {
   griddep_enter();
   __shared__ float s_rs;
   __shared__ int s_rows[16];
-  const long long t = blockIdx.x;
+  const RowSlice sl = row_slice(L, C);
+  const long long t = sl.t;
   if (threadIdx.x == 0) {
     float ss = 0.f;
     for (int q = 0; q < ld_ss; ++q) ss += ss_p[t * ld_ss + q];
@@ -315,7 +513,7 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
   if (threadIdx.x < k) s_rows[threadIdx.x] = row_of[t * k + threadIdx.x];
   __syncthreads();
   const float rs = s_rs;
-  for (int i = threadIdx.x * 8; i < L; i += kRowThreads * 8) {
+  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float v[8], gg[8];
     load8_f32(p + t * L + i, v);
     load8_f32(g + i, gg);
@@ -330,11 +528,12 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx,
     const float* __restrict__ w, const float* __restrict__ g_expert, int L, int k, float eps,
-    __nv_bfloat16* __restrict__ c) {
+    __nv_bfloat16* __restrict__ c, int C) {
   griddep_enter();
   __shared__ float s_coef[16];
   __shared__ int s_row[16], s_e[16];
-  const long long t = blockIdx.x;
+  const RowSlice sl = row_slice(L, C);
+  const long long t = sl.t;
   if (threadIdx.x < k) {
     const int j = threadIdx.x;
     const int row = row_of[t * k + j];
@@ -345,7 +544,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     s_e[j] = idx[t * k + j];
   }
   __syncthreads();
-  for (int i = threadIdx.x * 8; i < L; i += kRowThreads * 8) {
+  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {  // slot order
       float v[8], gg[8];
@@ -362,10 +561,11 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
 __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
     const void* __restrict__ x, int x_f32, const float* __restrict__ u,
     const float* __restrict__ ss_u, int ld_ss, const float* __restrict__ g, int D, float eps,
-    void* __restrict__ out, int out_f32) {
+    void* __restrict__ out, int out_f32, int C) {
   griddep_enter();
   __shared__ float s_rs;
-  const long long t = blockIdx.x;
+  const RowSlice sl = row_slice(D, C);
+  const long long t = sl.t;
   if (threadIdx.x == 0) {
     float ss = 0.f;
     for (int q = 0; q < ld_ss; ++q) ss += ss_u[t * ld_ss + q];
@@ -373,7 +573,7 @@ __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
   }
   __syncthreads();
   const float rs = s_rs;
-  for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
+  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float xv[8], uv[8], gg[8];
     load8(x, x_f32, t * D + i, xv);
     load8_f32(u + t * D + i, uv);
@@ -413,22 +613,6 @@ __global__ void weight_split_kernel(const float* __restrict__ W, long long rows,
 }
 
 // ------------------------------------------------------------------ NVFP4 rows
-__device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) red[w] = v;
-  __syncthreads();
-  if (w == 0) {
-    float t = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
-    if (l == 0) red[32] = t;
-  }
-  __syncthreads();
-  return red[32];
-}
 
 __device__ __forceinline__ void load_recip(float* recip) {
   for (int i = threadIdx.x; i < 256; i += blockDim.x) recip[i] = c_e4m3_recip.v[i];
@@ -443,16 +627,23 @@ struct QDest {
   int m;
 };
 
-// Quantises the K values of `buf` (shared memory) with row scale s into `ndst` destination
-// rows.
-__device__ __forceinline__ void quantize_row_to(const float* buf, int K, float s, const float* recip,
-                                                uint8_t* codes, uint8_t* scales, const QDest* dst,
-                                                int ndst) {
+// Quantises columns [i0, i1) of a row of K values (buf, shared memory, holds columns i0..)
+// with row scale s into `ndst` destination rows.
+__device__ __forceinline__ void quantize_row_to(const float* buf, int K, int i0, int i1, float s,
+                                                const float* recip, uint8_t* codes, uint8_t* scales,
+                                                const QDest* dst, int ndst) {
   const float six_s = __fmul_rn(6.f, s), inv_s = __fdiv_rn(1.f, s);
-  for (int b = threadIdx.x; b < K / 16; b += blockDim.x) {
+  for (int b = i0 / 16 + threadIdx.x; b < i1 / 16; b += blockDim.x) {
     float v[16];
+    const float4* src = reinterpret_cast<const float4*>(buf + (b * 16 - i0));   // i0 % 16 == 0
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = buf[b * 16 + i];
+    for (int i = 0; i < 4; ++i) {
+      const float4 f = src[i];
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
     uint2 q;
     const uint32_t sc = nvfp4_quant16(v, six_s, inv_s, recip, q);
     for (int j = 0; j < ndst; ++j) {
@@ -470,49 +661,54 @@ __device__ __forceinline__ void quantize_row_to(const float* buf, int K, float s
 __global__ void __launch_bounds__(kRowThreads) prenorm_nvfp4_kernel(
     const void* __restrict__ x, int x_f32, const float* __restrict__ g, int D, float eps,
     __nv_bfloat16* __restrict__ xa, int xa_cols, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, float* __restrict__ s_row, unsigned* status2) {
+    uint8_t* __restrict__ scales, float* __restrict__ s_row, unsigned* status2, int C) {
   griddep_enter();
   if (status2 != nullptr && blockIdx.x == 0 && threadIdx.x == 0) status2[0] = status2[1] = 0u;
   extern __shared__ float dyn[];
-  float* buf = dyn;
-  float* recip = dyn + D;
+  const RowSlice sl = row_slice(D, C);
+  float* buf = dyn;                  // this CTA's columns
+  float* recip = dyn + (sl.i1 - sl.i0);
   __shared__ float red[33];
+  __shared__ float slot_ss, slot_amax;
   __shared__ QDest s_d;
   load_recip(recip);
-  const long long t = blockIdx.x;
+  const long long t = sl.t;
   const long long xoff = t * D;
   float ss = 0.f;
-  for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
+  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float v[8];
     load8(x, x_f32, xoff + i, v);
 #pragma unroll
     for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
   }
-  const float rs = rsqrtf(block_sum(ss, red) / static_cast<float>(D) + eps);
+  const float rs =
+      rsqrtf(cluster_combine(block_sum(ss, red), &slot_ss, C, false) / static_cast<float>(D) + eps);
   __nv_bfloat16* row = xa + t * xa_cols;
   float amax = 0.f;
-  for (int i = threadIdx.x * 8; i < D; i += kRowThreads * 8) {
+  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float v[8], gg[8], hi[8], lo[8];
     load8(x, x_f32, xoff + i, v);
     load8_f32(g + i, gg);
+    float xn[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float xn = v[j] * rs * gg[j];
-      buf[i + j] = xn;
-      amax = fmaxf(amax, fabsf(xn));
-      hi[j] = bf16_round(xn);
-      lo[j] = xn - hi[j];
+      xn[j] = v[j] * rs * gg[j];
+      amax = fmaxf(amax, fabsf(xn[j]));
+      hi[j] = bf16_round(xn[j]);
+      lo[j] = xn[j] - hi[j];
     }
+    store8_f32(buf + (i - sl.i0), xn);
     store8_bf16(row + i, hi);
     store8_bf16(row + D + i, lo);
   }
-  const float s = nvfp4_row_scale(block_max(amax, red));
+  const float s = nvfp4_row_scale(cluster_combine(block_max(amax, red), &slot_amax, C, true));
   if (threadIdx.x == 0) {
-    s_row[t] = s;
+    if (sl.c == 0) s_row[t] = s;
     s_d = QDest{t, t / kBM, static_cast<int>(t % kBM)};
   }
   __syncthreads();
-  quantize_row_to(buf, D, s, recip, codes, scales, &s_d, 1);
+  quantize_row_to(buf, D, sl.i0, sl.i1, s, recip, codes, scales, &s_d, 1);
+  if (C > 1) cluster_sync_all();
 }
 
 // Pool norm whose output is quantised once (row scale per token) and written to the token's
@@ -521,16 +717,17 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
     const float* __restrict__ p, const float* __restrict__ ss_p, int ld_ss, const float* __restrict__ g,
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
     const int32_t* __restrict__ tile_base, int L, int k, float eps, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, float* __restrict__ s_rows) {
+    uint8_t* __restrict__ scales, float* __restrict__ s_rows, int C) {
   griddep_enter();
   extern __shared__ float dyn[];
-  float* buf = dyn;
-  float* recip = dyn + L;
+  const RowSlice sl = row_slice(L, C);
+  float* buf = dyn;                  // this CTA's columns
+  float* recip = dyn + (sl.i1 - sl.i0);
   __shared__ float red[33];
-  __shared__ float s_rs;
+  __shared__ float s_rs, slot_amax;
   __shared__ QDest s_dst[16];
   load_recip(recip);
-  const long long t = blockIdx.x;
+  const long long t = sl.t;
   if (threadIdx.x == 0) {
     float ss = 0.f;
     for (int q = 0; q < ld_ss; ++q) ss += ss_p[t * ld_ss + q];
@@ -545,20 +742,21 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
   __syncthreads();
   const float rs = s_rs;
   float amax = 0.f;
-  for (int i = threadIdx.x * 8; i < L; i += kRowThreads * 8) {
+  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float v[8], gg[8];
     load8_f32(p + t * L + i, v);
     load8_f32(g + i, gg);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float h = v[j] * rs * gg[j];
-      buf[i + j] = h;
-      amax = fmaxf(amax, fabsf(h));
+      v[j] = v[j] * rs * gg[j];
+      amax = fmaxf(amax, fabsf(v[j]));
     }
+    store8_f32(buf + (i - sl.i0), v);
   }
-  const float s = nvfp4_row_scale(block_max(amax, red));
-  if (threadIdx.x < k) s_rows[s_dst[threadIdx.x].code_row] = s;
-  quantize_row_to(buf, L, s, recip, codes, scales, s_dst, k);
+  const float s = nvfp4_row_scale(cluster_combine(block_max(amax, red), &slot_amax, C, true));
+  if (sl.c == 0 && threadIdx.x < k) s_rows[s_dst[threadIdx.x].code_row] = s;
+  quantize_row_to(buf, L, sl.i0, sl.i1, s, recip, codes, scales, s_dst, k);
+  if (C > 1) cluster_sync_all();
 }
 
 // Combine whose output c is quantised (row scale per token) for the unpooler.
@@ -567,17 +765,18 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
     const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const float* __restrict__ w,
     const float* __restrict__ g_expert, int L, int k, float eps, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, float* __restrict__ s_row) {
+    uint8_t* __restrict__ scales, float* __restrict__ s_row, int C) {
   griddep_enter();
   extern __shared__ float dyn[];
-  float* buf = dyn;
-  float* recip = dyn + L;
+  const RowSlice sl = row_slice(L, C);
+  float* buf = dyn;                  // this CTA's columns
+  float* recip = dyn + (sl.i1 - sl.i0);
   __shared__ float red[33];
-  __shared__ float s_coef[16];
+  __shared__ float s_coef[16], slot_amax;
   __shared__ int s_rowj[16], s_e[16];
   __shared__ QDest s_d;
   load_recip(recip);
-  const long long t = blockIdx.x;
+  const long long t = sl.t;
   if (threadIdx.x < k) {
     const int j = threadIdx.x;
     const int row = row_of[t * k + j];
@@ -589,7 +788,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
   }
   __syncthreads();
   float amax = 0.f;
-  for (int i = threadIdx.x * 8; i < L; i += kRowThreads * 8) {
+  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
       float v[8], gg[8];
@@ -599,18 +798,17 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
       for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_coef[j], v[q] * gg[q], acc[q]);
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      buf[i + q] = acc[q];
-      amax = fmaxf(amax, fabsf(acc[q]));
-    }
+    for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(acc[q]));
+    store8_f32(buf + (i - sl.i0), acc);
   }
-  const float s = nvfp4_row_scale(block_max(amax, red));
+  const float s = nvfp4_row_scale(cluster_combine(block_max(amax, red), &slot_amax, C, true));
   if (threadIdx.x == 0) {
-    s_row[t] = s;
+    if (sl.c == 0) s_row[t] = s;
     s_d = QDest{t, t / kBM, static_cast<int>(t % kBM)};
   }
   __syncthreads();
-  quantize_row_to(buf, L, s, recip, codes, scales, &s_d, 1);
+  quantize_row_to(buf, L, sl.i0, sl.i1, s, recip, codes, scales, &s_d, 1);
+  if (C > 1) cluster_sync_all();
 }
 
 // Stand-alone quantiser: one CTA per row of src [rows, K] fp32.
@@ -638,7 +836,7 @@ __global__ void __launch_bounds__(kRowThreads) quantize_nvfp4_kernel(
     s_d = QDest{t, -1, 0};   // row-major scales
   }
   __syncthreads();
-  quantize_row_to(buf, K, s, recip, codes, scales, &s_d, 1);
+  quantize_row_to(buf, K, 0, K, s, recip, codes, scales, &s_d, 1);
 }
 
 // Row-major E4M3 scales [rows, K/16] -> block layout with blocks of block_rows rows (128, or
@@ -743,19 +941,28 @@ __global__ void wait_selftest_kernel(long long budget, unsigned* err) {
 }  // namespace
 
 // ------------------------------------------------------------------ launchers
+// CTAs per token of the row kernels: a few tokens are spread over about 128 CTAs or more
+// (at most 8 per token, each taking a multiple of 128 columns).
+int row_split(int T, int N) {
+  int C = 1;
+  while (C < 8 && static_cast<long long>(T) * C < 128 && N % (2 * C * 128) == 0) C *= 2;
+  return C;
+}
+
 cudaError_t launch_prenorm_nvfp4(const void* x, bool x_f32, const float* g_pre, int T, int D,
                                  float eps, __nv_bfloat16* xa, int xa_cols, uint8_t* codes,
                                  uint8_t* scales, float* s_row, unsigned* status2, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const size_t smem = (static_cast<size_t>(D) + 256) * sizeof(float);
+  const int C = row_split(T, D);
+  const size_t smem = (static_cast<size_t>(D / C) + 256) * sizeof(float);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(prenorm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(prenorm_nvfp4_kernel, dim3(T), dim3(kRowThreads), smem, s, x, x_f32 ? 1 : 0,
-                    g_pre, D, eps, xa, xa_cols, codes, scales, s_row, status2);
+  return launch_pdl_cluster(prenorm_nvfp4_kernel, dim3(T * C), dim3(kRowThreads), smem, s, C, x,
+                            x_f32 ? 1 : 0, g_pre, D, eps, xa, xa_cols, codes, scales, s_row, status2, C);
 }
 
 cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int ld_ss,
@@ -765,16 +972,17 @@ cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int
                                           uint8_t* codes, uint8_t* scales, float* s_rows,
                                           cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const size_t smem = (static_cast<size_t>(L) + 256) * sizeof(float);
+  const int C = row_split(T, L);
+  const size_t smem = (static_cast<size_t>(L / C) + 256) * sizeof(float);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(poolnorm_scatter_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(poolnorm_scatter_nvfp4_kernel, dim3(T), dim3(kRowThreads), smem, s, p, ss_p,
-                    ld_ss, g_pool, row_of, idx, offsets, tile_base, L, k, eps, codes, scales,
-                    s_rows);
+  return launch_pdl_cluster(poolnorm_scatter_nvfp4_kernel, dim3(T * C), dim3(kRowThreads), smem, s, C,
+                            p, ss_p, ld_ss, g_pool, row_of, idx, offsets, tile_base, L, k, eps, codes,
+                            scales, s_rows, C);
 }
 
 cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, const int32_t* row_of,
@@ -782,15 +990,16 @@ cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, c
                                  int L, int k, float eps, uint8_t* codes, uint8_t* scales,
                                  float* s_row, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  const size_t smem = (static_cast<size_t>(L) + 256) * sizeof(float);
+  const int C = row_split(T, L);
+  const size_t smem = (static_cast<size_t>(L / C) + 256) * sizeof(float);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(combine_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(combine_nvfp4_kernel, dim3(T), dim3(kRowThreads), smem, s, y, ss_y, ld_ss,
-                    row_of, idx, w, g_expert, L, k, eps, codes, scales, s_row);
+  return launch_pdl_cluster(combine_nvfp4_kernel, dim3(T * C), dim3(kRowThreads), smem, s, C, y, ss_y,
+                            ld_ss, row_of, idx, w, g_expert, L, k, eps, codes, scales, s_row, C);
 }
 
 cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool row_scale,
@@ -841,8 +1050,9 @@ cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s
 cudaError_t launch_prenorm(const void* x, bool x_f32, const float* g_pre, int T, int D, float eps,
                            __nv_bfloat16* xa, int xa_cols, unsigned* status2, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  return launch_pdl(prenorm_kernel, dim3(T), dim3(kRowThreads), 0, s, x, x_f32 ? 1 : 0, g_pre, D,
-                    eps, xa, xa_cols, status2);
+  const int C = row_split(T, D);
+  return launch_pdl_cluster(prenorm_kernel, dim3(T * C), dim3(kRowThreads), 0, s, C, x, x_f32 ? 1 : 0,
+                            g_pre, D, eps, xa, xa_cols, status2, C);
 }
 
 cudaError_t launch_topk(const float* logits, int ld, const float* bias, const int32_t* forced,
@@ -853,6 +1063,29 @@ cudaError_t launch_topk(const float* logits, int ld, const float* bias, const in
   const size_t smem = static_cast<size_t>(kTopkWarps) * E * sizeof(float);
   return launch_pdl(topk_kernel, dim3(blocks), dim3(kTopkWarps * 32), smem, s, logits, ld, bias,
                     forced, T, E, k, idx, w, near_tie, idx_copy, w_copy, err);
+}
+
+bool route_small_fits(int T, int k, int E) {
+  return T * k <= kRouteMaxPairs && E <= 1024;
+}
+
+cudaError_t launch_route_small(const float* logits, int ld, const float* bias, const int32_t* forced,
+                               int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
+                               int32_t* idx_copy, float* w_copy, unsigned* err, int32_t* counts,
+                               int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
+                               int32_t* n_tiles, int32_t* tile_base, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const size_t smem = (static_cast<size_t>(kRouteThreads / 32) * E + 2 * E + kRouteMaxPairs) * 4;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>((kRouteThreads / 32 * 1024 + 2 * 1024 + kRouteMaxPairs) * 4));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(route_small_kernel, dim3(1), dim3(kRouteThreads), smem, s, logits, ld, bias, forced, T, E,
+                    k, idx, w, near_tie, idx_copy, w_copy, err, counts, offsets, row_of, tok_of, tiles,
+                    n_tiles, tile_base);
 }
 
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
@@ -870,8 +1103,9 @@ cudaError_t launch_poolnorm_scatter(const float* p, const float* ss_p, int ld_ss
                                     const float* g_pool, const int32_t* row_of, int T, int L,
                                     int k, float eps, __nv_bfloat16* xe, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  return launch_pdl(poolnorm_scatter_kernel, dim3(T), dim3(kRowThreads), 0, s, p, ss_p, ld_ss,
-                    g_pool, row_of, L, k, eps, xe);
+  const int C = row_split(T, L);
+  return launch_pdl(poolnorm_scatter_kernel, dim3(T * C), dim3(kRowThreads), 0, s, p, ss_p, ld_ss,
+                    g_pool, row_of, L, k, eps, xe, C);
 }
 
 cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
@@ -879,16 +1113,18 @@ cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
                            const float* g_expert, int T, int L, int k, float eps,
                            __nv_bfloat16* c, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  return launch_pdl(combine_kernel, dim3(T), dim3(kRowThreads), 0, s, y, ss_y, ld_ss, row_of, idx, w,
-                    g_expert, L, k, eps, c);
+  const int C = row_split(T, L);
+  return launch_pdl(combine_kernel, dim3(T * C), dim3(kRowThreads), 0, s, y, ss_y, ld_ss, row_of, idx,
+                    w, g_expert, L, k, eps, c, C);
 }
 
 cudaError_t launch_postnorm_residual(const void* x, bool x_f32, const float* u,
                                      const float* ss_u, int ld_ss, const float* g_post, int T,
                                      int D, float eps, void* out, bool out_f32, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  return launch_pdl(postnorm_residual_kernel, dim3(T), dim3(kRowThreads), 0, s, x, x_f32 ? 1 : 0, u,
-                    ss_u, ld_ss, g_post, D, eps, out, out_f32 ? 1 : 0);
+  const int C = row_split(T, D);
+  return launch_pdl(postnorm_residual_kernel, dim3(T * C), dim3(kRowThreads), 0, s, x, x_f32 ? 1 : 0,
+                    u, ss_u, ld_ss, g_post, D, eps, out, out_f32 ? 1 : 0, C);
 }
 
 cudaError_t launch_weight_split(const float* W, long long rows, int K, int parts,

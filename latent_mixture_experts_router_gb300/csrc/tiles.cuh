@@ -12,7 +12,7 @@ namespace lmoe {
 // Split-K pays a partial write and a reduce pass, so it is offered only where the A rows are
 // few (the host bounds max_splits).
 constexpr int kMinSplitKb = 8;
-LMOE_DEV int choose_splits(int units, int num_kb, int grid, int max_splits) {
+__host__ __device__ inline int choose_splits(int units, int num_kb, int grid, int max_splits) {
   if (max_splits <= 1 || units <= 0 || units >= 3 * grid) return 1;
   const int w1 = (units + grid - 1) / grid;
   float best_eff = static_cast<float>(units) / static_cast<float>(w1 * grid);
@@ -140,6 +140,14 @@ LMOE_DEV bool first_tile_hint(const Tile* tiles, const int* n_tiles, int max_til
   w.k_range(blockIdx.x, kb0, kb1);
   brow = expert * N + nt_ * bn;
   return kb0 < kb1;
+}
+
+// Host side: whether a grouped GEMM whose live M-tile count lies in [lo, hi] can pick a split
+// count above 1 (if not, it runs unsplit and no reduce pass is launched).
+inline bool grouped_split_possible(int lo, int hi, int nt, int num_kb, int grid, int max_splits) {
+  for (int m = lo < 1 ? 1 : lo; m <= hi; ++m)
+    if (choose_splits(m * nt, num_kb, grid, max_splits) > 1) return true;
+  return false;
 }
 
 // Upper bound of the tile ids of a launch (host side): m_tiles M tiles of at most kBM rows.

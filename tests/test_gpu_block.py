@@ -86,6 +86,7 @@ SHAPES = [  # (T, D, L, E, I, k): ragged T, N tails of the 256-wide tiles, k = 1
     (257, 512, 256, 6, 128, 6),
     (200, 256, 128, 1, 256, 1),
     (64, 1024, 512, 64, 768, 8),
+    (2, 2048, 1024, 16, 512, 4),    # rows split over clusters of 8 CTAs
 ]
 
 
@@ -123,6 +124,28 @@ def test_deterministic_and_token_order_equivariant(cuda):
     perm = torch.randperm(w.T, generator=torch.Generator().manual_seed(0)).to(cuda)
     c, ic, _, _ = run(inp, blk=blk, x=inp.x[perm].contiguous())
     assert torch.equal(c, a[perm]) and torch.equal(ic, ia[perm])
+
+
+@pytest.mark.parametrize("T,k,routing", [(16, 4, "uniform"), (40, 6, "hot4"), (100, 3, "zipf")])
+def test_overlapped_and_serial_paths_agree(cuda, T, k, routing):
+    # Without stage events the pooler runs on the side stream and, for at most 256 (token,
+    # slot) pairs, top-k and the permutation run as one kernel; with every stage timed the
+    # call runs serially through separate kernels.  Both give bit-identical results.
+    import latent_mixture_experts_router_gb300 as lm
+    w = workloads.Workload(f"paths_{T}_{k}", T=T, D=512, L=256, E=32, I=256, k=k, routing=routing,
+                           seed=T)
+    inp = workloads.make_inputs(w, cuda)
+    blk = make_block(inp)
+    a, ia, _, cfg = run(inp, blk=blk)
+    a = a.clone()
+    va = views(blk, cfg)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(lm.NUM_STAGE_EVENTS)]
+    b, ib, _, _ = run(inp, blk=blk, stage_events=evs)
+    vb = views(blk, cfg)
+    assert torch.equal(a, b) and torch.equal(ia, ib)
+    for name in ("topk_w", "counts", "offsets", "row_of", "tok_of", "n_tiles", "p", "y", "u"):
+        assert np.array_equal(va[name], vb[name]), name
+    _check_permutation(va, ia.cpu().numpy(), w.E)
 
 
 def test_router_bias_and_forced_routing(cuda):
