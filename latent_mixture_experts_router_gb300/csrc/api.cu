@@ -43,10 +43,11 @@ struct Layout {
   long long partial;    // split-K partial products of the dense and grouped GEMMs
   long long partial_pool;  // the pooler's own (it may run beside the router on a side stream)
   long long splits_dev; // [2] split counts the grouped NVFP4 GEMMs chose (gate/up, down)
+  long long tiles2, n_tiles2;  // table of 256-row tiles (BF16 grouped GEMMs of many rows)
   // fp32-weight mode: bf16 copies of the weights
   long long w_router, w_pool, w_gate, w_up, w_down, w_unpool;
   long long x_stage, out_stage, host_io_total;
-  int ld_logits, ld_ss_p, ld_ss_y, ld_ss_u, max_tiles;
+  int ld_logits, ld_ss_p, ld_ss_y, ld_ss_u, max_tiles, max_tiles2;
 };
 
 // Upper bound of the split count of the grouped NVFP4 GEMMs (the kernel picks the count from
@@ -135,6 +136,7 @@ void make_layout(const lmoe_config* c, Layout* L) {
   L->ld_ss_y = cdiv(Ld, bn_ss);
   L->ld_ss_u = cdiv(D, bn_ss);
   L->max_tiles = cdiv(R, kBM) + static_cast<int>(E < R ? E : R);
+  L->max_tiles2 = cdiv(R, 2 * kBM) + static_cast<int>(E < R ? E : R);
   P.err = take(kAlign);  // error word; the near-tie counter shares this line
   L->near_tie = P.err + 4;
   P.xa = take(T * P.xa_cols * 2);
@@ -148,6 +150,8 @@ void make_layout(const lmoe_config* c, Layout* L) {
   P.tiles = take(static_cast<size_t>(L->max_tiles) * sizeof(Tile));
   P.n_tiles = take(4);
   L->tile_base = take(E * 4);
+  L->tiles2 = take(static_cast<size_t>(L->max_tiles2) * sizeof(Tile));
+  L->n_tiles2 = take(4);
   P.p = take(T * Ld * 4);
   P.ss_p = take(T * L->ld_ss_p * 4);
   const bool fp4 = c->weight_dtype == LMOE_NVFP4;
@@ -272,7 +276,7 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
                      const Tile* tiles, const int* n_tiles, int m_tiles, void* out,
                      long long ldo, float* ss, int ld_ss, unsigned* err, long long budget,
                      cudaStream_t s, long long rows_per_b, int splits = 1,
-                     float* partial = nullptr) {
+                     float* partial = nullptr, int m_halves = 1) {
   const unsigned bn = epi == kEpiSwiGLU ? kBNSwiGLU : kBNWide;
   CUtensorMap ta, tb, tb2;
   if (!encode_bf16_2d(&ta, A, a_cols_used, a_rows, a_row_stride_elems * 2, kBK, kBM))
@@ -301,7 +305,7 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   a.partial = partial;
   a.max_tiles = m_tiles;
   a.n_groups = static_cast<int>(b_rows / N);
-  LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s));
+  LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s, m_halves));
   if (splits > 1)
     LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
                                    ldo, ss, ld_ss, kBNWide, s));
@@ -534,6 +538,11 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
 
   // S5 pooler, enqueued on stream `ps`: NVFP4 p = s_x * s_W * (Q(xn) . W_pool^T) (block-scaled
   // FP4 MMA), else p = xn_hi . W_pool^T; both with row partial sums of squares
+  // BF16 GEMMs over many rows take 256-row tiles (two MMAs share each weight tile): dense
+  // ones from 512 rows when not split along K, grouped ones at >= 256 rows per expert on
+  // average (they then walk the table of 256-row tiles)
+  auto dense_mh = [&](int splits) { return splits <= 1 && T >= 4 * kBM ? 2 : 1; };
+  auto dense_mt = [&](int splits) { return cdiv(T, kBM * dense_mh(splits)); };
   auto pooler = [&](cudaStream_t ps) -> lmoe_status {
     if (fp4)
       return run_gemm_fp4(kFp4EpiF32Ss, xq, T, D, op(q4[0]), Ld, nullptr, Ld, nullptr, nullptr, m_tiles_T,
@@ -541,8 +550,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                           ps, T, dsp.pooler, partial_pool);
     const int pool_k = f32w ? 3 * D : D;
     return run_gemm(kEpiF32Ss, xa, T, pool_k, xa_cols, wp, Ld, pool_k, nullptr, Ld, pool_k / kBK,
-                    nullptr, nullptr, m_tiles_T, p, Ld, ss_p, L.ld_ss_p, err, budget, ps, T, dsp.pooler,
-                    partial_pool);
+                    nullptr, nullptr, dense_mt(dsp.pooler), p, Ld, ss_p, L.ld_ss_p, err, budget, ps, T,
+                    dsp.pooler, partial_pool, dense_mh(dsp.pooler));
   };
   // The pooler needs only xn: it runs on the side stream beside S2-S4 unless the caller
   // times those stages (their events pin every stage to the caller's stream).
@@ -577,26 +586,29 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   LMOE_MARK(LMOE_STAGE_ROUTER);
   // S2 router logits = [xn_hi | xn_lo (| xn_hi)] . [W | W (| W_lo)]^T
   st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
-                xa_cols / kBK, nullptr, nullptr, m_tiles_T, logits, L.ld_logits, nullptr, 0, err,
-                budget, s, T, dsp.router, partial);
+                xa_cols / kBK, nullptr, nullptr, dense_mt(dsp.router), logits, L.ld_logits, nullptr, 0, err,
+                budget, s, T, dsp.router, partial, dense_mh(dsp.router));
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_TOPK);
   // S3 top-k + softmax, S4 permutation (one kernel for few pairs unless S4 is timed apart)
   const float* bias = ex ? ex->router_bias : nullptr;
   const int32_t* forced = ex ? ex->forced_idx : nullptr;
   int32_t* tile_base = static_cast<int32_t*>(at(L.tile_base));
+  Tile* tiles2 = static_cast<Tile*>(at(L.tiles2));
+  int32_t* n_tiles2 = static_cast<int32_t*>(at(L.n_tiles2));
   const bool fused_route = route_small_fits(T, k, E) && (ev == nullptr || ev[LMOE_STAGE_PERMUTE] == nullptr);
   if (fused_route) {
     LMOE_CUDA(launch_route_small(logits, L.ld_logits, bias, forced, T, E, k, tk_idx, tk_w, near_tie,
                                  ex ? ex->topk_idx_out : nullptr, ex ? ex->topk_w_out : nullptr, err,
-                                 counts, offsets, row_of, tok_of, tiles, n_tiles, tile_base, s));
+                                 counts, offsets, row_of, tok_of, tiles, n_tiles, tile_base, tiles2,
+                                 n_tiles2, s));
     LMOE_MARK(LMOE_STAGE_PERMUTE);
   } else {
     LMOE_CUDA(launch_topk(logits, L.ld_logits, bias, forced, T, E, k, tk_idx, tk_w, near_tie,
                           ex ? ex->topk_idx_out : nullptr, ex ? ex->topk_w_out : nullptr, err, s));
     LMOE_MARK(LMOE_STAGE_PERMUTE);
     LMOE_CUDA(launch_permute(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, s,
-                             tile_base));
+                             tile_base, tiles2, n_tiles2));
   }
   if (ex && ex->near_tie_count_out)
     LMOE_CUDA(cudaMemcpyAsync(ex->near_tie_count_out, near_tie, 4, cudaMemcpyDeviceToDevice, s));
@@ -655,13 +667,19 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   LMOE_CUDA(launch_poolnorm_scatter(p, ss_p, L.ld_ss_p, g_pool, row_of, T, Ld, k, eps, xe, s));
   LMOE_MARK(LMOE_STAGE_GATE_UP);
   // S7 grouped gate/up + SwiGLU
+  const int gmh = R / E >= 2 * kBM ? 2 : 1;
+  const Tile* gtiles = gmh == 2 ? tiles2 : tiles;
+  const int* gn_tiles = gmh == 2 ? n_tiles2 : n_tiles;
+  const int gmax = gmh == 2 ? L.max_tiles2 : L.max_tiles;
   st = run_gemm(kEpiSwiGLU, xe, R, Ld, Ld, wg, 1LL * E * I, 1LL * wsplit * Ld, wu, I,
-                wsplit * Ld / kBK, tiles, n_tiles, L.max_tiles, h, I, nullptr, 0, err, budget, s, R / E);
+                wsplit * Ld / kBK, gtiles, gn_tiles, gmax, h, I, nullptr, 0, err, budget, s, R / E, 1,
+                nullptr, gmh);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_DOWN);
   // S8 grouped down (fp32 y), with per-row partial sums of squares
   st = run_gemm(kEpiF32Ss, h, R, I, I, wd, 1LL * E * Ld, 1LL * wsplit * I, nullptr, Ld,
-                wsplit * I / kBK, tiles, n_tiles, L.max_tiles, y, Ld, ss_y, L.ld_ss_y, err, budget, s, R / E);
+                wsplit * I / kBK, gtiles, gn_tiles, gmax, y, Ld, ss_y, L.ld_ss_y, err, budget, s, R / E, 1,
+                nullptr, gmh);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_COMBINE);
   // S9 combine: per-expert RMSNorm, routing weight, fp32 sum in slot order
@@ -669,7 +687,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   LMOE_MARK(LMOE_STAGE_UNPOOLER);
   // S10 unpooler u = c . W_unpool^T with row partial sums of squares
   st = run_gemm(kEpiF32Ss, c, T, Ld, Ld, wun, D, 1LL * wsplit * Ld, nullptr, D, wsplit * Ld / kBK,
-                nullptr, nullptr, m_tiles_T, u, D, ss_u, L.ld_ss_u, err, budget, s, T, dsp.unpool, partial);
+                nullptr, nullptr, dense_mt(dsp.unpool), u, D, ss_u, L.ld_ss_u, err, budget, s, T, dsp.unpool,
+                partial, dense_mh(dsp.unpool));
   if (st != LMOE_OK) return st;
   }
   LMOE_MARK(LMOE_STAGE_POSTNORM);

@@ -6,14 +6,18 @@
 // the other (K-concatenation without copying).  A and B are K-major bf16 staged in shared
 // memory by TMA (128-byte swizzle); fp32 accumulators live in tensor memory.
 //
-// One CTA per SM walks the 128 x BN output tiles in grouped order (groups of 16 M tiles,
-// M fastest inside a group, ids strided by the grid size), with three roles:
-//   warp 0, lane 0   TMA producer over a 4-deep ring of smem stages (the ring runs on
-//                    across tiles)
-//   warp 1, lane 0   tcgen05.mma issuer; warp 1 also owns the TMEM allocation (512 columns:
-//                    two accumulator buffers, so the next tile's MMAs run while the
-//                    epilogue drains the previous one)
+// One CTA per SM walks the (128 MH) x BN output tiles in grouped order (groups of 16 M
+// tiles, M fastest inside a group, ids strided by the grid size), with three roles:
+//   warp 0, lane 0   TMA producer over a ring of smem stages (the ring runs on across tiles)
+//   warp 1, lane 0   tcgen05.mma issuer; warp 1 also owns the TMEM allocation (512 columns)
 //   warps 2..5       epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (one row each)
+// MH = 1: 128-row tiles, 4 stages, two accumulator buffers (the next tile's MMAs run while
+// the epilogue drains the previous one) — the weight-streaming regime of few rows.
+// MH = 2: 256-row tiles (two M = 128 MMAs per K step share each B tile), 3 stages, one
+// accumulator buffer spanning the 512 columns.  A CTA can take in only about 100 GB/s of
+// operands from L2 or HBM; a 128 x 256 bf16 tile needs 48 KB per 2 x 128 x 256 x 64 FLOP,
+// which caps it near 70 % of the tensor rate, while the 256-row tile needs 64 KB per twice
+// the work — the many-row (prefill) regime.
 // Epilogues (one per use in the latent-MoE block):
 //   kEpiF32     fp32 logits (router)
 //   kEpiF32Ss   fp32 output plus, per row, the partial sum of squares of the values of
@@ -32,27 +36,32 @@
 
 namespace lmoe {
 
-template <int BN, int EPI>
+template <int BN, int EPI, int MH>
 struct GemmCfg {
   static constexpr bool kDual = (EPI == kEpiSwiGLU);
-  static constexpr int kStages = 4;
-  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kStages = MH == 2 ? 3 : 4;
+  static constexpr int kAHalf = kBM * kBK * 2;            // one 128-row half of A
+  static constexpr int kABytes = MH * kAHalf;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes * (kDual ? 2 : 1);
-  static constexpr int kAccCols = kDual ? 2 * BN : BN;   // one accumulator buffer
-  static constexpr uint32_t kTmemCols = 512;              // two buffers
+  static constexpr int kAccCols = kDual ? 2 * BN : BN;   // accumulator of one M half
+  static constexpr int kBufCols = MH * kAccCols;         // one accumulator buffer
+  static constexpr int kAccBufs = 512 / kBufCols >= 2 ? 2 : 1;
+  static constexpr int kTileRows = MH * kBM;
+  static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
-  static_assert(2 * kAccCols <= 512, "two accumulator buffers in tensor memory");
+  static_assert(kAccBufs * kBufCols <= 512, "accumulator buffers in tensor memory");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
+  static_assert(MH == 1 || MH == 2, "one or two M halves");
 };
 
-template <int BN, int EPI>
+template <int BN, int EPI, int MH>
 __global__ void __launch_bounds__(192, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
-  using C = GemmCfg<BN, EPI>;
+  using C = GemmCfg<BN, EPI, MH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -73,7 +82,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], 4);
     }
@@ -84,7 +93,7 @@ __global__ void __launch_bounds__(192, 1)
     if (C::kDual) prefetch_tmap(&tmB2);
     int brow, kb0, kb1;
     if (first_tile_hint(args.tiles, args.n_tiles, args.max_tiles, args.n_groups, args.M, args.N, BN,
-                        args.k_splits, args.num_kb, false, brow, kb0, kb1)) {
+                        args.k_splits, args.num_kb, false, brow, kb0, kb1, C::kTileRows)) {
       for (int kb = kb0; kb < min(kb1, kb0 + kPrefetchKb); ++kb) {
         const int kbb = (kb % args.kb_period_b) * kBK;
         prefetch_l2_tile_2d(&tmB, kbb, brow);
@@ -102,7 +111,8 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = *tmem_slot;
   griddep_enter();
   // CTAs past the live tile ids walk nothing and go straight to the teardown
-  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb);
+  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb, false,
+                      C::kTileRows);
   const long long budget = args.budget;
 
   if (warp == 0) {
@@ -115,6 +125,8 @@ __global__ void __launch_bounds__(192, 1)
         int expert, row0, nrows, ntile;
         if (!walk.at(id, expert, row0, nrows, ntile)) continue;
         const int brow = expert * args.N + ntile * BN;
+        const int halves = nrows > kBM ? 2 : 1;   // a 256-row tile with at most 128 live rows
+        const uint32_t tx = C::kStageBytes - (MH - halves) * C::kAHalf;   // skips its second half
         int kb0, kb1;
         walk.k_range(id, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -126,8 +138,10 @@ __global__ void __launch_bounds__(192, 1)
             break;
           }
           uint8_t* sa = smem + s * C::kStageBytes;
-          mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-          tma_load_2d(sa, &tmA, &full[s], (kb % args.kb_period_a) * kBK, row0);
+          mbar_arrive_expect_tx(&full[s], tx);
+          const int ka = (kb % args.kb_period_a) * kBK;
+          tma_load_2d(sa, &tmA, &full[s], ka, row0);
+          if (MH == 2 && halves == 2) tma_load_2d(sa + C::kAHalf, &tmA, &full[s], ka, row0 + kBM);
           const int kbb = (kb % args.kb_period_b) * kBK;
           tma_load_2d_hint(sa + C::kABytes, &tmB, &full[s], kbb, brow, pol_b);
           if (C::kDual) tma_load_2d_hint(sa + C::kABytes + C::kBBytes, &tmB2, &full[s], kbb, brow, pol_b);
@@ -149,14 +163,15 @@ __global__ void __launch_bounds__(192, 1)
       for (int id = blockIdx.x; ok && id < walk.n_ids; id += gridDim.x) {
         int expert, row0, nrows, ntile;
         if (!walk.at(id, expert, row0, nrows, ntile)) continue;
-        const int buf = tc & 1;
-        const uint32_t use = (tc >> 1) & 1;
+        const int halves = nrows > kBM ? 2 : 1;
+        const int buf = tc % C::kAccBufs;
+        const uint32_t use = (tc / C::kAccBufs) & 1;
         if (!mbar_wait(&acc_empty[buf], use ^ 1, budget)) {   // epilogue released this buffer
           atomicOr(args.err, kErrWaitMma);
           break;
         }
         tc_fence_after();
-        const uint32_t acc = tmem + buf * C::kAccCols;
+        const uint32_t acc = tmem + buf * C::kBufCols;
         int kb0, kb1;
         walk.k_range(id, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -172,11 +187,17 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t b0 = a0 + C::kABytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = sw128_kmajor_desc(a0 + kk * 32);
             const uint32_t accum = (kb > kb0 || kk > 0) ? 1u : 0u;
-            mma_bf16(acc, ad, sw128_kmajor_desc(b0 + kk * 32), idesc, accum);
-            if (C::kDual)
-              mma_bf16(acc + BN, ad, sw128_kmajor_desc(b0 + C::kBBytes + kk * 32), idesc, accum);
+            const uint64_t bd = sw128_kmajor_desc(b0 + kk * 32);
+            const uint64_t bd2 = sw128_kmajor_desc(b0 + C::kBBytes + kk * 32);
+#pragma unroll
+            for (int h = 0; h < MH; ++h) {
+              if (h >= halves) break;
+              const uint64_t ad = sw128_kmajor_desc(a0 + h * C::kAHalf + kk * 32);
+              const uint32_t dh = acc + h * C::kAccCols;
+              mma_bf16(dh, ad, bd, idesc, accum);
+              if (C::kDual) mma_bf16(dh + BN, ad, bd2, idesc, accum);
+            }
           }
           mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
           ++it;
@@ -194,17 +215,21 @@ __global__ void __launch_bounds__(192, 1)
     for (int id = blockIdx.x; id < walk.n_ids; id += gridDim.x) {
       int expert, row0, nrows, ntile;
       if (!walk.at(id, expert, row0, nrows, ntile)) continue;
-      const int buf = tc & 1;
-      const uint32_t use = (tc >> 1) & 1;
+      const int buf = tc % C::kAccBufs;
+      const uint32_t use = (tc / C::kAccBufs) & 1;
       if (!mbar_wait(&acc_full[buf], use, budget)) {
         atomicOr(args.err, kErrWaitEpilogue);
         break;
       }
       tc_fence_after();
-      const bool row_ok = r < nrows;
-      const long long grow = static_cast<long long>(row0) + r;
+      const int halves = nrows > kBM ? 2 : 1;
       const int n0 = ntile * BN;
-      const uint32_t tq = tmem + buf * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
+#pragma unroll 1
+      for (int h = 0; h < halves; ++h) {
+      const int rr = h * kBM + r;   // row within the tile
+      const bool row_ok = rr < nrows;
+      const long long grow = static_cast<long long>(row0) + rr;
+      const uint32_t tq = tmem + buf * C::kBufCols + h * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       if (EPI != kEpiSwiGLU && walk.splits > 1) {
         // split-K: raw fp32 partial product of this K range; the reduction finishes the tile
         float* prow = args.partial + (static_cast<long long>(id % walk.splits) * args.M + grow) * args.N;
@@ -294,6 +319,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      }  // M halves
       // every TMEM read of this buffer is complete: hand it back to the MMA issuer
       tc_fence_before();
       __syncwarp();
@@ -324,12 +350,12 @@ int sm_count() {
   return n;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int MH>
 static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
                               const CUtensorMap& tmB2, const GemmArgs& a, int m_tiles,
                               cudaStream_t s) {
-  using C = GemmCfg<BN, EPI>;
-  auto kern = gemm_tcgen05_kernel<BN, EPI>;
+  using C = GemmCfg<BN, EPI, MH>;
+  auto kern = gemm_tcgen05_kernel<BN, EPI, MH>;
   static bool attr_set = false;  // per process; the attribute is per function
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -346,11 +372,19 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
 
 cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         const CUtensorMap& tmB2, const GemmArgs& a, int m_tiles,
-                        cudaStream_t s) {
+                        cudaStream_t s, int m_halves) {
+  if (m_halves == 2) {
+    switch (epi) {
+      case kEpiF32: return launch_one<kBNWide, kEpiF32, 2>(tmA, tmB, tmB2, a, m_tiles, s);
+      case kEpiF32Ss: return launch_one<kBNWide, kEpiF32Ss, 2>(tmA, tmB, tmB2, a, m_tiles, s);
+      case kEpiSwiGLU: return launch_one<kBNSwiGLU, kEpiSwiGLU, 2>(tmA, tmB, tmB2, a, m_tiles, s);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (epi) {
-    case kEpiF32: return launch_one<kBNWide, kEpiF32>(tmA, tmB, tmB2, a, m_tiles, s);
-    case kEpiF32Ss: return launch_one<kBNWide, kEpiF32Ss>(tmA, tmB, tmB2, a, m_tiles, s);
-    case kEpiSwiGLU: return launch_one<kBNSwiGLU, kEpiSwiGLU>(tmA, tmB, tmB2, a, m_tiles, s);
+    case kEpiF32: return launch_one<kBNWide, kEpiF32, 1>(tmA, tmB, tmB2, a, m_tiles, s);
+    case kEpiF32Ss: return launch_one<kBNWide, kEpiF32Ss, 1>(tmA, tmB, tmB2, a, m_tiles, s);
+    case kEpiSwiGLU: return launch_one<kBNSwiGLU, kEpiSwiGLU, 1>(tmA, tmB, tmB2, a, m_tiles, s);
   }
   return cudaErrorInvalidValue;
 }

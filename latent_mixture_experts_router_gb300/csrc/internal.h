@@ -184,10 +184,12 @@ cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Launches one tcgen05 GEMM: out = A * B^T over grid (ceil(N/BN), m_tiles).
+// Launches one persistent tcgen05 GEMM: out = A * B^T over m_tiles M tiles (an upper bound
+// for grouped GEMMs) of 128 * m_halves rows (m_halves = 2: tiles of 256 rows, for many rows;
+// a grouped GEMM then takes a table of 256-row tiles).
 cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                         const CUtensorMap& tmB2, const GemmArgs& a, int m_tiles,
-                        cudaStream_t s);
+                        cudaStream_t s, int m_halves);
 
 // Row kernels (rowops.cu).  The pre-norm kernels, the first of a call, also zero the two
 // status words at status2 (error word, near-tie count) when status2 != nullptr.
@@ -200,14 +202,16 @@ cudaError_t launch_route_small(const float* logits, int ld, const float* bias, c
                                int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
                                int32_t* idx_copy, float* w_copy, unsigned* err, int32_t* counts,
                                int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
-                               int32_t* n_tiles, int32_t* tile_base, cudaStream_t s);
+                               int32_t* n_tiles, int32_t* tile_base, Tile* tiles2, int32_t* n_tiles2,
+                               cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int ld, const float* bias, const int32_t* forced,
                         int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
                         int32_t* idx_copy, float* w_copy, unsigned* err, cudaStream_t s);
 // tile_base (optional, [E]): first M tile of each expert in the tile table
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
-                           int32_t* n_tiles, cudaStream_t s, int32_t* tile_base = nullptr);
+                           int32_t* n_tiles, cudaStream_t s, int32_t* tile_base = nullptr,
+                           Tile* tiles2 = nullptr, int32_t* n_tiles2 = nullptr);
 cudaError_t launch_poolnorm_scatter(const float* p, const float* ss_p, int ld_ss,
                                     const float* g_pool, const int32_t* row_of, int T, int L,
                                     int k, float eps, __nv_bfloat16* xe, cudaStream_t s);

@@ -305,6 +305,37 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
 constexpr int kPermThreads = 256;
 constexpr int kPermPerThread = 16;
 
+// Order of the table of 256-row tiles (grouped BF16 GEMMs over many rows).  An expert's tiles
+// with more than 128 live rows ("full": MMA-bound, and those of one expert share its weights
+// in L2) and its last tile when it holds at most 128 rows ("light": it streams the expert's
+// weights for few rows) are interleaved in runs of kMixRun, so that every wave of the
+// persistent GEMM mixes tensor-bound and memory-bound tiles instead of alternating between
+// phases of each.  Full tile j (in expert order) and light tile i go to these places:
+constexpr int kMixRun = 8;
+__device__ __forceinline__ int mixed_pos_full(int j, int n_light) {
+  return j + min((j / kMixRun) * kMixRun, n_light);
+}
+__device__ __forceinline__ int mixed_pos_light(int i, int n_full) {
+  return i + min((i / kMixRun + 1) * kMixRun, n_full);
+}
+// (full, light) tile counts of an expert with c rows
+__device__ __forceinline__ void tile2_counts(int c, int& full, int& light) {
+  const int nt2 = (c + 2 * kBM - 1) / (2 * kBM), rem = c % (2 * kBM);
+  light = (rem > 0 && rem <= kBM) ? 1 : 0;
+  full = nt2 - light;
+}
+// writes the 256-row tiles of expert e (c rows from row `off`) given the full and light
+// tiles of the experts before it (f0, l0) and the totals (nf, nl)
+__device__ __forceinline__ void write_tiles2(Tile* tiles2, int e, int off, int c, int f0, int l0, int nf,
+                                             int nl, int first, int step) {
+  int full, light;
+  tile2_counts(c, full, light);
+  for (int m = first; m < full + light; m += step) {
+    const int pos = m < full ? mixed_pos_full(f0 + m, nl) : mixed_pos_light(l0, nf);
+    tiles2[pos] = Tile{e, off + m * 2 * kBM, min(2 * kBM, c - m * 2 * kBM), 0};
+  }
+}
+
 __global__ void __launch_bounds__(kPermThreads) expert_count_kernel(const int32_t* __restrict__ idx,
                                                                     int n, int32_t* counts) {
   griddep_enter();
@@ -319,19 +350,30 @@ __global__ void __launch_bounds__(kPermThreads) expert_count_kernel(const int32_
 __global__ void __launch_bounds__(kPermThreads) expert_scatter_kernel(
     const int32_t* __restrict__ idx, int n, int k, int E, const int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of,
-    Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles, int32_t* __restrict__ tile_base) {
+    Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles, int32_t* __restrict__ tile_base,
+    Tile* __restrict__ tiles2, int32_t* __restrict__ n_tiles2) {
   griddep_enter();
   __shared__ int wsum[kPermThreads / 32];
   __shared__ int red[33];
   const int e = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int my_off = 0, my_t0 = 0;
-  for (int q = threadIdx.x; q < e; q += kPermThreads) {
-    my_off += counts[q];
-    my_t0 += (counts[q] + kBM - 1) / kBM;
+  int my_off = 0, my_t0 = 0, my_f0 = 0, my_l0 = 0, my_nf = 0, my_nl = 0;
+  for (int q = threadIdx.x; q < E; q += kPermThreads) {
+    int f, l;
+    tile2_counts(counts[q], f, l);
+    my_nf += f;
+    my_nl += l;
+    if (q < e) {
+      my_off += counts[q];
+      my_t0 += (counts[q] + kBM - 1) / kBM;
+      my_f0 += f;
+      my_l0 += l;
+    }
   }
   const int off = block_sum_int(my_off, red);
   const int tile0 = block_sum_int(my_t0, red);
+  const int f0 = block_sum_int(my_f0, red), l0 = block_sum_int(my_l0, red);
+  const int nf = block_sum_int(my_nf, red), nl = block_sum_int(my_nl, red);
   const int cnt = counts[e];
   if (threadIdx.x == 0) {
     offsets[e] = off;
@@ -339,11 +381,13 @@ __global__ void __launch_bounds__(kPermThreads) expert_scatter_kernel(
     if (e == E - 1) {
       offsets[E] = off + cnt;
       *n_tiles = tile0 + (cnt + kBM - 1) / kBM;
+      if (n_tiles2 != nullptr) *n_tiles2 = nf + nl;
     }
   }
   const int ntile = (cnt + kBM - 1) / kBM;
   for (int m = threadIdx.x; m < ntile; m += kPermThreads)
     tiles[tile0 + m] = Tile{e, off + m * kBM, min(kBM, cnt - m * kBM), 0};
+  if (tiles2 != nullptr) write_tiles2(tiles2, e, off, cnt, f0, l0, nf, nl, threadIdx.x, kPermThreads);
   if (cnt == 0) return;
   int running = 0;
   for (int base = 0; base < n; base += kPermThreads * kPermPerThread) {
@@ -431,7 +475,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(
     float* __restrict__ w_out, int32_t* __restrict__ near_tie, int32_t* __restrict__ idx_copy,
     float* __restrict__ w_copy, unsigned* __restrict__ err, int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of,
-    Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles, int32_t* __restrict__ tile_base) {
+    Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles, int32_t* __restrict__ tile_base,
+    Tile* __restrict__ tiles2, int32_t* __restrict__ n_tiles2) {
   griddep_enter();
   extern __shared__ float route_sh[];
   constexpr int nw = kRouteThreads / 32;
@@ -463,26 +508,37 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(
   // runs of experts, so thread order is expert order)
   const int per = (E + kRouteThreads - 1) / kRouteThreads;
   const int e0 = threadIdx.x * per, e1 = min(E, e0 + per);
-  int a = 0, b = 0;
+  int a = 0, b = 0, f = 0, l = 0;
   for (int e = e0; e < e1; ++e) {
+    int fe, le;
+    tile2_counts(cnt_s[e], fe, le);
     a += cnt_s[e];
     b += (cnt_s[e] + kBM - 1) / kBM;
+    f += fe;
+    l += le;
   }
-  int ta, tb;
+  int ta, tb, nf, nl;
   block_scan2(a, b, scan_sh, &ta, &tb);
+  block_scan2(f, l, scan_sh, &nf, &nl);
   for (int e = e0; e < e1; ++e) {
     const int c = cnt_s[e], nt = (c + kBM - 1) / kBM;
+    int fe, le;
+    tile2_counts(c, fe, le);
     off_s[e] = a;
     counts[e] = c;
     offsets[e] = a;
     if (tile_base != nullptr) tile_base[e] = b;
     for (int m = 0; m < nt; ++m) tiles[b + m] = Tile{e, a + m * kBM, min(kBM, c - m * kBM), 0};
+    if (tiles2 != nullptr) write_tiles2(tiles2, e, a, c, f, l, nf, nl, 0, 1);
     a += c;
     b += nt;
+    f += fe;
+    l += le;
   }
   if (threadIdx.x == 0) {
     offsets[E] = ta;
     *n_tiles = tb;
+    if (n_tiles2 != nullptr) *n_tiles2 = nf + nl;
   }
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += kRouteThreads) {
@@ -1073,7 +1129,8 @@ cudaError_t launch_route_small(const float* logits, int ld, const float* bias, c
                                int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
                                int32_t* idx_copy, float* w_copy, unsigned* err, int32_t* counts,
                                int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
-                               int32_t* n_tiles, int32_t* tile_base, cudaStream_t s) {
+                               int32_t* n_tiles, int32_t* tile_base, Tile* tiles2, int32_t* n_tiles2,
+                               cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const size_t smem = (static_cast<size_t>(kRouteThreads / 32) * E + 2 * E + kRouteMaxPairs) * 4;
   static bool attr = false;
@@ -1085,18 +1142,19 @@ cudaError_t launch_route_small(const float* logits, int ld, const float* bias, c
   }
   return launch_pdl(route_small_kernel, dim3(1), dim3(kRouteThreads), smem, s, logits, ld, bias, forced, T, E,
                     k, idx, w, near_tie, idx_copy, w_copy, err, counts, offsets, row_of, tok_of, tiles,
-                    n_tiles, tile_base);
+                    n_tiles, tile_base, tiles2, n_tiles2);
 }
 
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
-                           int32_t* n_tiles, cudaStream_t s, int32_t* tile_base) {
+                           int32_t* n_tiles, cudaStream_t s, int32_t* tile_base, Tile* tiles2,
+                           int32_t* n_tiles2) {
   const int n = T * k;
   cudaError_t e = launch_pdl(expert_count_kernel, dim3(E), dim3(kPermThreads), 0, s, idx, n,
                              counts);
   if (e != cudaSuccess) return e;
   return launch_pdl(expert_scatter_kernel, dim3(E), dim3(kPermThreads), 0, s, idx, n, k, E, counts,
-                    offsets, row_of, tok_of, tiles, n_tiles, tile_base);
+                    offsets, row_of, tok_of, tiles, n_tiles, tile_base, tiles2, n_tiles2);
 }
 
 cudaError_t launch_poolnorm_scatter(const float* p, const float* ss_p, int ld_ss,

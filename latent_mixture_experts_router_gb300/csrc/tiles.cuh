@@ -35,17 +35,18 @@ __host__ __device__ inline int choose_splits(int units, int num_kb, int grid, in
 struct TileWalk {
   const Tile* tiles;
   int M, N, total_m, nt, n_ids, bn, splits, num_kb, kb_per_split;
+  int bm;   // rows of a dense M tile (a grouped table's tiles carry their own row counts)
   // splits > 1: every output tile is computed as `splits` partial products over disjoint K
   // ranges (split-K), consecutive ids taking the K ranges of one tile
   // adaptive (grouped only): splits_ is the upper bound, the count comes from choose_splits
   LMOE_DEV TileWalk(const Tile* tiles_, const int* n_tiles, int M_, int N_, int bn_, int splits_ = 1,
-                    int num_kb_ = 1, bool adaptive = false)
-      : TileWalk(tiles_, tiles_ != nullptr ? *n_tiles : (M_ + kBM - 1) / kBM, M_, N_, bn_, splits_,
-                 num_kb_, adaptive) {}
+                    int num_kb_ = 1, bool adaptive = false, int bm_ = kBM)
+      : TileWalk(tiles_, tiles_ != nullptr ? *n_tiles : (M_ + bm_ - 1) / bm_, M_, N_, bn_, splits_,
+                 num_kb_, adaptive, bm_) {}
   // same, with the live M-tile count given
   LMOE_DEV TileWalk(const Tile* tiles_, int total_m_, int M_, int N_, int bn_, int splits_, int num_kb_,
-                    bool adaptive)
-      : tiles(tiles_), M(M_), N(N_), bn(bn_), splits(splits_ < 1 ? 1 : splits_), num_kb(num_kb_) {
+                    bool adaptive, int bm_ = kBM)
+      : tiles(tiles_), M(M_), N(N_), bn(bn_), splits(splits_ < 1 ? 1 : splits_), num_kb(num_kb_), bm(bm_) {
     total_m = total_m_;
     nt = (N + bn - 1) / bn;
     if (adaptive && tiles != nullptr)
@@ -77,8 +78,8 @@ struct TileWalk {
       nrows = t.nrows;
     } else {
       expert = 0;
-      row0 = mt * kBM;
-      nrows = min(kBM, M - row0);
+      row0 = mt * bm;
+      nrows = min(bm, M - row0);
     }
     return nrows > 0;
   }
@@ -102,7 +103,7 @@ LMOE_DEV TileRef find_tile(const TileWalk& w, int from) {
 }
 LMOE_DEV Tile tile_of(const TileWalk& w, int mt) {
   if (w.tiles != nullptr) return w.tiles[mt];
-  return Tile{0, mt * kBM, min(kBM, w.M - mt * kBM), 0};
+  return Tile{0, mt * w.bm, min(w.bm, w.M - mt * w.bm), 0};
 }
 
 // This CTA's first weight tile, for an L2 prefetch issued before the CTA waits on the previous
@@ -117,14 +118,14 @@ LMOE_DEV int ld_relaxed_gpu(const int* p) {
 }
 LMOE_DEV bool first_tile_hint(const Tile* tiles, const int* n_tiles, int max_tiles, int n_groups, int M,
                               int N, int bn, int splits, int num_kb, bool adaptive, int& brow, int& kb0,
-                              int& kb1) {
+                              int& kb1, int bm = kBM) {
   int total_m;
   if (tiles != nullptr) {
     total_m = min(max(ld_relaxed_gpu(n_tiles), 0), max_tiles);
   } else {
-    total_m = (M + kBM - 1) / kBM;
+    total_m = (M + bm - 1) / bm;
   }
-  const TileWalk w(tiles, total_m, M, N, bn, splits, num_kb, adaptive);
+  const TileWalk w(tiles, total_m, M, N, bn, splits, num_kb, adaptive, bm);
   int mt, nt_;
   if (static_cast<int>(blockIdx.x) >= w.n_ids ||
       !grouped_tile(static_cast<int>(blockIdx.x) / w.splits, w.total_m, w.nt, kRasterGroup, mt, nt_))
