@@ -14,14 +14,19 @@
 // read through tcgen05.cp 32x128b (blocks of 32 lines x 16 bytes, line m0 holding the 4
 // scale bytes of rows m0, m0+32, m0+64, m0+96 — the "4x32 transpose" the pages apply before
 // the copy, done once when the scales are written), so a stage's scales are one bulk copy.
-// Roles (192 or 320 threads):
+// Roles (224 or 352 threads):
 //   warp 0 lane 0   TMA: A codes + B codes (+ B2 for gate/up) + bulk copies of their scales
-//   warp 1          TMEM allocation; lane 0 copies scale factors into TMEM (tcgen05.cp) and
-//                   issues tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//   warp 1          TMEM allocation; lane 0 issues tcgen05.mma.kind::mxf4nvf4.block_scale.
+//                   scale_vec::4X
 //   warps 2..        epilogue: warp w owns TMEM lanes 32*(w%4) ..; the gate/up kernel runs
 //                   8 epilogue warps, warp w also taking column half (w-2)/4, so each
 //                   scheduler runs two of them and a tile drains in half the time (its
 //                   single accumulator waits for that); the fp32 kernels run 4
+//   last warp lane 0  copies each stage's scale factors into tensor memory (tcgen05.cp) and
+//                   signals them ready through its own barrier.  A thread takes about as
+//                   long to issue one 512-byte scale copy as one MMA, so copies issued by
+//                   the MMA thread would double its time per stage; from a second thread
+//                   they overlap the MMAs of the previous stage.
 // The A box covers only the tile's live rows rounded up to 32 (a decode tile holds a few
 // rows of one expert), and the producer loads the next tile's table entry one tile ahead.
 // Epilogues: kFp4EpiF32Ss — alpha * acc as fp32 plus per-row partial sums of squares; two
@@ -105,7 +110,8 @@ struct Fp4Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024 /*recip*/ + 256;
   static constexpr int kEpiWarps = kDual ? 8 : 4;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kCopyWarp = 2 + kEpiWarps;             // scale-factor copies
+  static constexpr int kThreads = 32 * (kCopyWarp + 1);
   static_assert(kSfCol0 + kStages * kSfCols <= 512, "tensor memory");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(kStageBytes % 1024 == 0, "1024-byte aligned stages");
@@ -128,7 +134,8 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
   uint64_t* acc_full = empty + C::kStages;     // [kAccBufs]
   uint64_t* acc_empty = acc_full + 2;          // [kAccBufs], 4 epilogue warps arrive
   uint64_t* mma_done = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* sf_full = mma_done + 1;            // [kStages] scales of the stage are in TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + C::kStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -138,6 +145,7 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_full[s], 1);
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
       }
     }
   }
-  if (warp >= 2) {
+  if (warp >= 2 && warp < C::kCopyWarp) {
     for (int i = threadIdx.x - 64; i < 256; i += 32 * C::kEpiWarps) recip[i] = c_e4m3_recip.v[i];
   }
   if (warp == 1) {
@@ -256,7 +264,8 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
         for (int kb = kb0; kb < kb1; ++kb) {
           const int s = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
-          if (!mbar_wait(&full[s], ph, budget)) {
+          // the stage's codes have landed and the copier has put its scales in tensor memory
+          if (!mbar_wait(&full[s], ph, budget) || !mbar_wait(&sf_full[s], ph, budget)) {
             atomicOr(args.err, kErrWaitMma);
             ok = false;
             break;
@@ -265,14 +274,6 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
           const uint32_t st = smem_u32(smem + s * C::kStageBytes);
           const uint32_t sfa = tmem + C::kSfCol0 + s * C::kSfCols;
           const uint32_t sfb = sfa + C::kSfaCols;
-#pragma unroll
-          for (int j = 0; j < C::kKStep; ++j) {
-            tmem_cp_32x128b_x4(sfa + j * 4, sf_desc(st + C::kOffSfa + j * 512));
-#pragma unroll
-            for (int b = 0; b < C::kNB; ++b)
-              tmem_cp_32x128b_x4(sfb + b * C::kSfbColsOne + j * 4,
-                                 sf_desc(st + C::kOffSfb + b * C::kSfbBytes + j * 512));
-          }
 #pragma unroll
           for (int j = 0; j < C::kKStep; ++j) {
             const uint64_t ad = sw128_kmajor_desc(st + j * 32);
@@ -290,6 +291,47 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
         ++tc;
       }
       mma_commit(mma_done);
+    }
+  } else if (warp == C::kCopyWarp) {
+    if (lane == 0) {
+      // ---- scale-factor copier: the stage's A and B scale blocks into the stage's columns
+      // (the slot is free again once the stage has been refilled: its previous MMAs completed
+      // before the producer saw the stage empty)
+      int it = 0;
+      bool ok = true;
+      for (int id = blockIdx.x; ok && id < walk.n_ids; id += gridDim.x) {
+        int expert, row0, nrows, ntile;
+        if (!walk.at(id, expert, row0, nrows, ntile)) continue;
+        int kb0, kb1;
+        walk.k_range(id, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const int s = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (!mbar_wait(&full[s], ph, budget)) {
+            atomicOr(args.err, kErrWaitMma);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t sfa = tmem + C::kSfCol0 + s * C::kSfCols;
+          const uint32_t sfb = sfa + C::kSfaCols;
+#pragma unroll
+          for (int j = 0; j < C::kKStep; ++j) {
+            tmem_cp_32x128b_x4(sfa + j * 4, sf_desc(st + C::kOffSfa + j * 512));
+#pragma unroll
+            for (int b = 0; b < C::kNB; ++b)
+              tmem_cp_32x128b_x4(sfb + b * C::kSfbColsOne + j * 4,
+                                 sf_desc(st + C::kOffSfb + b * C::kSfbBytes + j * 512));
+          }
+          mma_commit(&sf_full[s]);
+          ++it;
+        }
+      }
+      // every copy this thread issued has completed before the CTA tears down
+      for (int j = max(0, it - C::kStages); j < it; ++j)
+        if (!mbar_wait(&sf_full[j % C::kStages], (j / C::kStages) & 1, kDrainBudget))
+          atomicOr(args.err, kErrDrain);
     }
   } else {
     // ---- epilogue: lane quadrant warp % 4; with 8 warps, column half (warp - 2) / 4
