@@ -181,9 +181,10 @@ def measured_traffic(stage: str, w: workloads.Workload, units: int):
     covers this kernel in this regime or the kernel source changed since it was taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path) or w.T > 512:   # captures cover the decode regime
+    if not os.path.exists(path):
         return None
-    rec = json.load(open(path)).get(f"{stage}/{w.weights}/decode")
+    regime = "decode" if w.T <= 512 else "prefill"
+    rec = json.load(open(path)).get(f"{stage}/{w.weights}/{regime}")
     if rec is None:
         return None
     src = os.path.join(ROOT, rec["kernel_source"])
