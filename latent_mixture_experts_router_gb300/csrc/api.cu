@@ -276,7 +276,7 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
                      const Tile* tiles, const int* n_tiles, int m_tiles, void* out,
                      long long ldo, float* ss, int ld_ss, unsigned* err, long long budget,
                      cudaStream_t s, long long rows_per_b, int splits = 1,
-                     float* partial = nullptr, int m_halves = 1) {
+                     float* partial = nullptr, int m_halves = 1, bool reduce = true) {
   const unsigned bn = epi == kEpiSwiGLU ? kBNSwiGLU : kBNWide;
   CUtensorMap ta, tb, tb2;
   if (!encode_bf16_2d(&ta, A, a_cols_used, a_rows, a_row_stride_elems * 2, kBK, kBM))
@@ -306,7 +306,7 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   a.max_tiles = m_tiles;
   a.n_groups = static_cast<int>(b_rows / N);
   LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s, m_halves));
-  if (splits > 1)
+  if (splits > 1 && reduce)   // else the consumer sums the partials
     LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
                                    ldo, ss, ld_ss, kBNWide, s));
   return LMOE_OK;
@@ -324,7 +324,8 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                          uint8_t* out_scales, float* ss, int ld_ss, const float* row_scale,
                          const float* ts, const float* ts2, unsigned* err, long long budget,
                          cudaStream_t s, long long rows_per_b, int splits = 1,
-                         float* partial = nullptr, int* splits_dev = nullptr) {
+                         float* partial = nullptr, int* splits_dev = nullptr,
+                         bool reduce = true) {
   CUtensorMap maps[6];
   const unsigned long long kc = K / 2;
   const unsigned bn = kBNFp4;
@@ -365,7 +366,7 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
   a.splits_out = tiles != nullptr ? splits_dev : nullptr;
   if (adaptive && (partial == nullptr || splits_dev == nullptr)) return LMOE_ERR_WORKSPACE;
   LMOE_CUDA(launch_gemm_fp4(epi, maps, a, m_tiles, s));
-  if (splits > 1) {
+  if (splits > 1 && reduce) {   // else the consumer sums the partials
     if (epi == kFp4EpiSwiGLUQuant)
       LMOE_CUDA(launch_swiglu_reduce_nvfp4(partial, splits_dev, static_cast<int>(a_rows), N, tiles,
                                            n_tiles, m_tiles, static_cast<uint8_t*>(out), out_scales, s));
@@ -585,9 +586,13 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
 
   LMOE_MARK(LMOE_STAGE_ROUTER);
   // S2 router logits = [xn_hi | xn_lo (| xn_hi)] . [W | W (| W_lo)]^T
+  // few pairs: top-k and the permutation run as one kernel, which also sums the router's
+  // split-K partials when they are few (one launch less on the chain)
+  const bool fused_route = route_small_fits(T, k, E) && (ev == nullptr || ev[LMOE_STAGE_PERMUTE] == nullptr);
+  const int rsplits = fused_route && dsp.router > 1 && 1LL * T * dsp.router * E <= 65536 ? dsp.router : 1;
   st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
                 xa_cols / kBK, nullptr, nullptr, dense_mt(dsp.router), logits, L.ld_logits, nullptr, 0, err,
-                budget, s, T, dsp.router, partial, dense_mh(dsp.router));
+                budget, s, T, dsp.router, partial, dense_mh(dsp.router), rsplits == 1);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_TOPK);
   // S3 top-k + softmax, S4 permutation (one kernel for few pairs unless S4 is timed apart)
@@ -596,9 +601,9 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   int32_t* tile_base = static_cast<int32_t*>(at(L.tile_base));
   Tile* tiles2 = static_cast<Tile*>(at(L.tiles2));
   int32_t* n_tiles2 = static_cast<int32_t*>(at(L.n_tiles2));
-  const bool fused_route = route_small_fits(T, k, E) && (ev == nullptr || ev[LMOE_STAGE_PERMUTE] == nullptr);
   if (fused_route) {
-    LMOE_CUDA(launch_route_small(logits, L.ld_logits, bias, forced, T, E, k, tk_idx, tk_w, near_tie,
+    LMOE_CUDA(launch_route_small(logits, L.ld_logits, partial, rsplits, bias, forced, T, E, k, tk_idx, tk_w,
+                                 near_tie,
                                  ex ? ex->topk_idx_out : nullptr, ex ? ex->topk_w_out : nullptr, err,
                                  counts, offsets, row_of, tok_of, tiles, n_tiles, tile_base, tiles2,
                                  n_tiles2, s));
@@ -659,7 +664,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     LMOE_MARK(LMOE_STAGE_UNPOOLER);
     // S10 unpooler u = s_c * s_W * (Q(c) . W_unpool^T)
     st = run_gemm_fp4(kFp4EpiF32Ss, cq, T, Ld, op(q4[4]), D, nullptr, D, nullptr, nullptr, m_tiles_T, u,
-                      D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s, T, dsp.unpool, partial);
+                      D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s, T, dsp.unpool,
+                      partial, nullptr, false);
     if (st != LMOE_OK) return st;
   } else {
   LMOE_MARK(LMOE_STAGE_POOLNORM);
@@ -688,13 +694,14 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   // S10 unpooler u = c . W_unpool^T with row partial sums of squares
   st = run_gemm(kEpiF32Ss, c, T, Ld, Ld, wun, D, 1LL * wsplit * Ld, nullptr, D, wsplit * Ld / kBK,
                 nullptr, nullptr, dense_mt(dsp.unpool), u, D, ss_u, L.ld_ss_u, err, budget, s, T, dsp.unpool,
-                partial, dense_mh(dsp.unpool));
+                partial, dense_mh(dsp.unpool), false);
   if (st != LMOE_OK) return st;
   }
   LMOE_MARK(LMOE_STAGE_POSTNORM);
   // S11 post-norm + residual
+  // S11 reads the unpooler's split-K partials itself when it ran split (no reduction launch)
   LMOE_CUDA(launch_postnorm_residual(x, x_f32, u, ss_u, L.ld_ss_u, g_post, T, D, eps, out,
-                                     cfg->out_dtype == LMOE_F32, s));
+                                     cfg->out_dtype == LMOE_F32, s, partial, dsp.unpool));
   LMOE_MARK(LMOE_STAGE_END);
 #undef LMOE_MARK
   return LMOE_OK;

@@ -198,7 +198,10 @@ cudaError_t launch_prenorm(const void* x, bool x_f32, const float* g_pre, int T,
 // S3 and S4 in one CTA for few (token, slot) pairs (route_small_fits); same outputs as
 // launch_topk followed by launch_permute.
 bool route_small_fits(int T, int k, int E);
-cudaError_t launch_route_small(const float* logits, int ld, const float* bias, const int32_t* forced,
+// rsplits > 1: the logits are summed here from the router's split-K partials rpart
+// [rsplits][T][E] (in split order, as the reduction kernel does) and written to `logits`.
+cudaError_t launch_route_small(float* logits, int ld, const float* rpart, int rsplits, const float* bias,
+                               const int32_t* forced,
                                int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
                                int32_t* idx_copy, float* w_copy, unsigned* err, int32_t* counts,
                                int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
@@ -219,9 +222,12 @@ cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
                            const int32_t* row_of, const int32_t* idx, const float* w,
                            const float* g_expert, int T, int L, int k, float eps,
                            __nv_bfloat16* c, cudaStream_t s);
-cudaError_t launch_postnorm_residual(const void* x, bool x_f32, const float* u,
+// usplits > 1: u is summed here from the unpooler's split-K partials upart [usplits][T][D] and
+// written to u, and the row's sum of squares is taken from it (ss_u is not read).
+cudaError_t launch_postnorm_residual(const void* x, bool x_f32, float* u,
                                      const float* ss_u, int ld_ss, const float* g_post, int T,
-                                     int D, float eps, void* out, bool out_f32, cudaStream_t s);
+                                     int D, float eps, void* out, bool out_f32, cudaStream_t s,
+                                     const float* upart = nullptr, int usplits = 1);
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s);
 // fp32 weight [rows, K] -> bf16 [rows, parts*K]: part q is W_hi when bit q of lo_mask is 0,
 // else W_lo = bf16(W - W_hi).  [hi | hi | lo] pairs with activations [x_hi | x_lo | x_hi];

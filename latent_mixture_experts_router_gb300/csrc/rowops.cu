@@ -470,7 +470,8 @@ __device__ __forceinline__ void block_scan2(int& a, int& b, int* sh, int* ta, in
 }
 
 __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(
-    const float* __restrict__ logits, int ld, const float* __restrict__ bias,
+    float* __restrict__ logits, int ld, const float* __restrict__ rpart, int rsplits,
+    const float* __restrict__ bias,
     const int32_t* __restrict__ forced, int T, int E, int k, int32_t* __restrict__ idx_out,
     float* __restrict__ w_out, int32_t* __restrict__ near_tie, int32_t* __restrict__ idx_copy,
     float* __restrict__ w_copy, unsigned* __restrict__ err, int32_t* __restrict__ counts,
@@ -488,6 +489,26 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = T * k;
   // S3: a warp per token
+  if (rsplits > 1) {
+    // the router's split-K partials [rsplits][T][E], summed in split order (as the reduction
+    // kernel does) by every thread of the CTA, loads issued eight at a time
+    for (int ti = threadIdx.x; ti < T * E; ti += kRouteThreads) {
+      const int t = ti / E, i = ti % E;
+      const float* src = rpart + static_cast<long long>(t) * E + i;
+      const long long plane = static_cast<long long>(T) * E;
+      float v = 0.f;
+      for (int q0 = 0; q0 < rsplits; q0 += 8) {
+        float pv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pv[j] = q0 + j < rsplits ? src[(q0 + j) * plane] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (q0 + j < rsplits) v += pv[j];
+      }
+      logits[static_cast<long long>(t) * ld + i] = v;
+    }
+    __syncthreads();
+  }
   for (int t = warp; t < T; t += nw) {
     float* vals = vals_all + warp * E;
     for (int i = lane; i < E; i += 32) vals[i] = logits[static_cast<long long>(t) * ld + i] + (bias ? bias[i] : 0.f);
@@ -615,24 +636,46 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
 
 // ------------------------------------------------------------------ post-norm + residual
 __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
-    const void* __restrict__ x, int x_f32, const float* __restrict__ u,
+    const void* __restrict__ x, int x_f32, float* __restrict__ u,
     const float* __restrict__ ss_u, int ld_ss, const float* __restrict__ g, int D, float eps,
-    void* __restrict__ out, int out_f32, int C) {
+    void* __restrict__ out, int out_f32, int C, const float* __restrict__ upart, int usplits, int T) {
   griddep_enter();
   __shared__ float s_rs;
+  __shared__ float red[33];
+  __shared__ float slot_ss;
   const RowSlice sl = row_slice(D, C);
   const long long t = sl.t;
-  if (threadIdx.x == 0) {
+  float rs;
+  if (usplits > 1) {
+    // u from the unpooler's split-K partials [usplits][T][D] (split order, as the reduction
+    // kernel sums them), written to u; the row's sum of squares over the cluster
     float ss = 0.f;
-    for (int q = 0; q < ld_ss; ++q) ss += ss_u[t * ld_ss + q];
-    s_rs = rsqrtf(ss / static_cast<float>(D) + eps);
+    for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
+      float uv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int q = 0; q < usplits; ++q) {
+        float pv[8];
+        load8_f32(upart + (static_cast<long long>(q) * T + t) * D + i, pv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) uv[j] += pv[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(uv[j], uv[j], ss);
+      store8_f32(u + t * D + i, uv);
+    }
+    rs = rsqrtf(cluster_combine(block_sum(ss, red), &slot_ss, C, false) / static_cast<float>(D) + eps);
+  } else {
+    if (threadIdx.x == 0) {
+      float ss = 0.f;
+      for (int q = 0; q < ld_ss; ++q) ss += ss_u[t * ld_ss + q];
+      s_rs = rsqrtf(ss / static_cast<float>(D) + eps);
+    }
+    __syncthreads();
+    rs = s_rs;
   }
-  __syncthreads();
-  const float rs = s_rs;
   for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float xv[8], uv[8], gg[8];
     load8(x, x_f32, t * D + i, xv);
-    load8_f32(u + t * D + i, uv);
+    load8_f32(u + t * D + i, uv);   // this thread's own stores when u came from the partials
     load8_f32(g + i, gg);
 #pragma unroll
     for (int j = 0; j < 8; ++j) xv[j] = xv[j] + uv[j] * rs * gg[j];
@@ -644,6 +687,7 @@ __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
       store8_bf16(static_cast<__nv_bfloat16*>(out) + t * D + i, xv);
     }
   }
+  if (usplits > 1 && C > 1) cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ fp32 weights -> bf16 hi/lo
@@ -1125,7 +1169,8 @@ bool route_small_fits(int T, int k, int E) {
   return T * k <= kRouteMaxPairs && E <= 1024;
 }
 
-cudaError_t launch_route_small(const float* logits, int ld, const float* bias, const int32_t* forced,
+cudaError_t launch_route_small(float* logits, int ld, const float* rpart, int rsplits, const float* bias,
+                               const int32_t* forced,
                                int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
                                int32_t* idx_copy, float* w_copy, unsigned* err, int32_t* counts,
                                int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
@@ -1140,7 +1185,8 @@ cudaError_t launch_route_small(const float* logits, int ld, const float* bias, c
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(route_small_kernel, dim3(1), dim3(kRouteThreads), smem, s, logits, ld, bias, forced, T, E,
+  return launch_pdl(route_small_kernel, dim3(1), dim3(kRouteThreads), smem, s, logits, ld, rpart, rsplits,
+                    bias, forced, T, E,
                     k, idx, w, near_tie, idx_copy, w_copy, err, counts, offsets, row_of, tok_of, tiles,
                     n_tiles, tile_base, tiles2, n_tiles2);
 }
@@ -1176,13 +1222,18 @@ cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
                     w, g_expert, L, k, eps, c, C);
 }
 
-cudaError_t launch_postnorm_residual(const void* x, bool x_f32, const float* u,
+cudaError_t launch_postnorm_residual(const void* x, bool x_f32, float* u,
                                      const float* ss_u, int ld_ss, const float* g_post, int T,
-                                     int D, float eps, void* out, bool out_f32, cudaStream_t s) {
+                                     int D, float eps, void* out, bool out_f32, cudaStream_t s,
+                                     const float* upart, int usplits) {
   if (T == 0) return cudaSuccess;
   const int C = row_split(T, D);
+  if (usplits > 1)   // the row's sum of squares is combined over a cluster of C CTAs
+    return launch_pdl_cluster(postnorm_residual_kernel, dim3(T * C), dim3(kRowThreads), 0, s, C, x,
+                              x_f32 ? 1 : 0, u, ss_u, ld_ss, g_post, D, eps, out, out_f32 ? 1 : 0, C, upart,
+                              usplits, T);
   return launch_pdl(postnorm_residual_kernel, dim3(T * C), dim3(kRowThreads), 0, s, x, x_f32 ? 1 : 0,
-                    u, ss_u, ld_ss, g_post, D, eps, out, out_f32 ? 1 : 0, C);
+                    u, ss_u, ld_ss, g_post, D, eps, out, out_f32 ? 1 : 0, C, upart, usplits, T);
 }
 
 cudaError_t launch_weight_split(const float* W, long long rows, int K, int parts,
