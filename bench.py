@@ -368,29 +368,29 @@ def run_ours(args, ws, rank, local):
     W = blk.W
 
     def step_io():
-        lm.latent_moe_forward_host_io(cfg, x_host, W["W_router"], W["W_pool"], W["g_pool"], W["W_gate"],
-                                      W["W_up"], W["W_down"], W["g_expert"], W["W_unpool"], W["g_pre"],
-                                      W["g_post"], w.k, out_host, ws_io)
+        lm.latent_moe_forward_host_io_ex(cfg, x_host, W["W_router"], W["W_pool"], W["g_pool"], W["W_gate"],
+                                         W["W_up"], W["W_down"], W["g_expert"], W["W_unpool"], W["g_pre"],
+                                         W["g_post"], w.k, out_host, ws_io, **ex)
 
-    e2e = None
-    if inp.router_bias is None and inp.forced_idx is None:
-        for _ in range(max(2, args.warmup // 2)):
-            step_io()
-        torch.cuda.synchronize()
-        barrier(ws)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step_io()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier(ws)
-        ms_io = allreduce_max(e0.elapsed_time(e1), ws)
-        e2e = {"value": round(ws * T * args.steps / (ms_io * 1e-3), 1), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
-               "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()),
-               "ms_per_step": round(ms_io / args.steps, 4), "path": "latent_moe_forward_host_io"}
+    # router bias and forced routing stay device-resident routing controls; x and out go
+    # through pinned host memory every step
+    for _ in range(max(2, args.warmup // 2)):
+        step_io()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step_io()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms_io = allreduce_max(e0.elapsed_time(e1), ws)
+    e2e = {"value": round(ws * T * args.steps / (ms_io * 1e-3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
+           "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()),
+           "ms_per_step": round(ms_io / args.steps, 4), "path": "latent_moe_forward_host_io_ex"}
 
     if rank != 0:
         return None

@@ -175,6 +175,16 @@ lmoe_status latent_moe_forward_host_io(const lmoe_config* cfg, const void* x_hos
                                        const float* g_post, int top_k, void* out_host,
                                        void* workspace, size_t workspace_bytes,
                                        cudaStream_t stream);
+/* latent_moe_forward_host_io with the extensions of `ex` (host pointer, may be NULL; the
+ * pointers inside it stay device pointers, as for latent_moe_forward_ex). */
+lmoe_status latent_moe_forward_host_io_ex(const lmoe_config* cfg, const void* x_host,
+                                          const void* W_router, const void* W_pool,
+                                          const float* g_pool, const void* W_gate, const void* W_up,
+                                          const void* W_down, const float* g_expert,
+                                          const void* W_unpool, const float* g_pre,
+                                          const float* g_post, int top_k, void* out_host,
+                                          void* workspace, size_t workspace_bytes,
+                                          cudaStream_t stream, const lmoe_ex* ex);
 
 /* Reads (synchronising `stream`) and clears the device error word of `workspace`.
  * Returns LMOE_OK or LMOE_ERR_TIMEOUT; *detail (host, may be NULL) receives the raw word. */

@@ -20,7 +20,8 @@ import torch
 
 from ._lib import (Config, LmoeError, lmoe_workspace_size, lmoe_workspace_size_host_io,  # noqa: F401
                    lmoe_get_workspace_layout, latent_moe_forward, latent_moe_forward_ex,
-                   latent_moe_forward_host_io, lmoe_check_status, lmoe_wait_selftest, load,
+                   latent_moe_forward_host_io, latent_moe_forward_host_io_ex, lmoe_check_status,
+                   lmoe_wait_selftest, load,
                    LIB_PATH, STAGES, NUM_STAGE_EVENTS, lmoe_kernel_launches,
                    lmoe_quantize_nvfp4, lmoe_nvfp4_block_scales)
 

@@ -89,6 +89,8 @@ def _lib():
         L.latent_moe_forward_ex.restype = ctypes.c_int
         L.latent_moe_forward_host_io.argtypes = _FWD_ARGS
         L.latent_moe_forward_host_io.restype = ctypes.c_int
+        L.latent_moe_forward_host_io_ex.argtypes = _FWD_ARGS + [ctypes.POINTER(lmoe_ex)]
+        L.latent_moe_forward_host_io_ex.restype = ctypes.c_int
         L.lmoe_check_status.argtypes = [ctypes.POINTER(lmoe_config), _P, _P, ctypes.POINTER(ctypes.c_uint32)]
         L.lmoe_check_status.restype = ctypes.c_int
         L.lmoe_wait_selftest.argtypes = [ctypes.POINTER(lmoe_config), _P, ctypes.c_longlong, _P]
@@ -227,6 +229,17 @@ def latent_moe_forward_host_io(cfg, x_host, W_router, W_pool, g_pool, W_gate, W_
     args = _fwd_args(cfg, x_host, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool,
                      g_pre, g_post, top_k, out_host, workspace, stream, keep)
     _check(_lib().latent_moe_forward_host_io(*args), "latent_moe_forward_host_io")
+
+
+def latent_moe_forward_host_io_ex(cfg, x_host, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert,
+                                  W_unpool, g_pre, g_post, top_k, out_host, workspace, stream=None,
+                                  router_bias=None, forced_idx=None):
+    """latent_moe_forward_host_io with the device-resident routing extensions of lmoe_ex."""
+    keep = []
+    args = _fwd_args(cfg, x_host, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool,
+                     g_pre, g_post, top_k, out_host, workspace, stream, keep)
+    ex = lmoe_ex(_ptr(router_bias), _ptr(forced_idx), None, None, None, 0, None)
+    _check(_lib().latent_moe_forward_host_io_ex(*args, ctypes.byref(ex)), "latent_moe_forward_host_io_ex")
 
 
 def lmoe_check_status(cfg, workspace, stream=None) -> tuple[int, int]:

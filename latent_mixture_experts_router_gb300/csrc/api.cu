@@ -761,14 +761,14 @@ lmoe_status latent_moe_forward_ex(const lmoe_config* cfg, const void* x, const v
                       g_pre, g_post, top_k, out, workspace, workspace_bytes, stream, ex);
 }
 
-lmoe_status latent_moe_forward_host_io(const lmoe_config* cfg, const void* x_host,
-                                       const void* W_router, const void* W_pool,
-                                       const float* g_pool, const void* W_gate, const void* W_up,
-                                       const void* W_down, const float* g_expert,
-                                       const void* W_unpool, const float* g_pre,
-                                       const float* g_post, int top_k, void* out_host,
-                                       void* workspace, size_t workspace_bytes,
-                                       cudaStream_t stream) {
+lmoe_status latent_moe_forward_host_io_ex(const lmoe_config* cfg, const void* x_host,
+                                          const void* W_router, const void* W_pool,
+                                          const float* g_pool, const void* W_gate, const void* W_up,
+                                          const void* W_down, const float* g_expert,
+                                          const void* W_unpool, const float* g_pre,
+                                          const float* g_post, int top_k, void* out_host,
+                                          void* workspace, size_t workspace_bytes,
+                                          cudaStream_t stream, const lmoe_ex* ex) {
   const lmoe_status st = check_config(cfg);
   if (st != LMOE_OK) return st;
   if (x_host == nullptr || out_host == nullptr) return LMOE_ERR_ARG;
@@ -785,11 +785,24 @@ lmoe_status latent_moe_forward_host_io(const lmoe_config* cfg, const void* x_hos
   const lmoe_status s2 =
       forward_impl(cfg, ws + L.x_stage, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert,
                    W_unpool, g_pre, g_post, top_k, ws + L.out_stage, workspace,
-                   static_cast<size_t>(L.pub.total), stream, nullptr);
+                   static_cast<size_t>(L.pub.total), stream, ex);
   if (s2 != LMOE_OK) return s2;
   if (cudaMemcpyAsync(out_host, ws + L.out_stage, ob, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return LMOE_ERR_CUDA;
   return LMOE_OK;
+}
+
+lmoe_status latent_moe_forward_host_io(const lmoe_config* cfg, const void* x_host,
+                                       const void* W_router, const void* W_pool,
+                                       const float* g_pool, const void* W_gate, const void* W_up,
+                                       const void* W_down, const float* g_expert,
+                                       const void* W_unpool, const float* g_pre,
+                                       const float* g_post, int top_k, void* out_host,
+                                       void* workspace, size_t workspace_bytes,
+                                       cudaStream_t stream) {
+  return latent_moe_forward_host_io_ex(cfg, x_host, W_router, W_pool, g_pool, W_gate, W_up, W_down,
+                                       g_expert, W_unpool, g_pre, g_post, top_k, out_host, workspace,
+                                       workspace_bytes, stream, nullptr);
 }
 
 lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStream_t stream,

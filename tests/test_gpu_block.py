@@ -185,6 +185,26 @@ def test_bf16_output_and_host_io(cuda):
     assert torch.equal(oh, out32.cpu())
 
 
+@pytest.mark.parametrize("routing", ["zipf", "hot4"])
+def test_host_io_with_routing_controls(cuda, routing):
+    # x in and out back through pinned host memory, with the router bias (Zipf) or forced
+    # routing (hot experts) of lmoe_ex: the same result as the device-resident call
+    import latent_mixture_experts_router_gb300 as lm
+    w = workloads.Workload(f"io_{routing}", T=40, D=256, L=256, E=16, I=128, k=4, routing=routing)
+    inp = workloads.make_inputs(w, cuda)
+    out, _, blk, _ = run(inp)
+    cfg = blk.config(w.T, "bf16", "f32")
+    ws = torch.zeros(lm.lmoe_workspace_size_host_io(cfg), dtype=torch.uint8, device=cuda)
+    xh = inp.x.cpu().pin_memory()
+    oh = torch.empty(w.T, w.D, dtype=torch.float32).pin_memory()
+    W = blk.W
+    lm.latent_moe_forward_host_io_ex(cfg, xh, W["W_router"], W["W_pool"], W["g_pool"], W["W_gate"], W["W_up"],
+                                     W["W_down"], W["g_expert"], W["W_unpool"], W["g_pre"], W["g_post"], w.k,
+                                     oh, ws, router_bias=inp.router_bias, forced_idx=inp.forced_idx)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, out.cpu())
+
+
 def test_out_of_range_forced_id_is_flagged(cuda):
     import latent_mixture_experts_router_gb300 as lm
     w = workloads.Workload("badidx", T=8, D=256, L=128, E=8, I=128, k=2)
