@@ -131,7 +131,7 @@ void make_layout(const lmoe_config* c, Layout* L) {
   lmoe_workspace_layout& P = L->pub;
   P.xa_cols = static_cast<int>((f32w ? 3 : 2) * D);
   L->ld_logits = static_cast<int>(align_up(E, 32));
-  const int bn_ss = c->weight_dtype == LMOE_NVFP4 ? kBNFp4 : kBNWide;  // N of the GEMM tiles
+  const int bn_ss = 128;   // the GEMM epilogues write one row sum of squares per 128 columns
   L->ld_ss_p = cdiv(Ld, bn_ss);
   L->ld_ss_y = cdiv(Ld, bn_ss);
   L->ld_ss_u = cdiv(D, bn_ss);
@@ -308,7 +308,7 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s, m_halves));
   if (splits > 1 && reduce)   // else the consumer sums the partials
     LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
-                                   ldo, ss, ld_ss, kBNWide, s));
+                                   ldo, ss, ld_ss, 128, s));
   return LMOE_OK;
 }
 
@@ -372,7 +372,7 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                                            n_tiles, m_tiles, static_cast<uint8_t*>(out), out_scales, s));
     else
       LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
-                                     ldo, ss, ld_ss, kBNFp4, s, adaptive ? splits_dev : nullptr));
+                                     ldo, ss, ld_ss, 128, s, adaptive ? splits_dev : nullptr));
   }
   return LMOE_OK;
 }

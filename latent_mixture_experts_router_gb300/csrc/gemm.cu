@@ -10,7 +10,9 @@
 // tiles, M fastest inside a group, ids strided by the grid size), with three roles:
 //   warp 0, lane 0   TMA producer over a ring of smem stages (the ring runs on across tiles)
 //   warp 1, lane 0   tcgen05.mma issuer; warp 1 also owns the TMEM allocation (512 columns)
-//   warps 2..5       epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (one row each)
+//   warps 2..5       epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (one row each).  (Eight
+//                    epilogue warps on half the columns each measured slower here: the
+//                    waiting warps take issue slots from the producer and the MMA issuer.)
 // MH = 1: 128-row tiles, 4 stages, two accumulator buffers (the next tile's MMAs run while
 // the epilogue drains the previous one) — the weight-streaming regime of few rows.
 // MH = 2: 256-row tiles (two M = 128 MMAs per K step share each B tile), 3 stages, one
@@ -49,6 +51,8 @@ struct GemmCfg {
   static constexpr int kAccBufs = 512 / kBufCols >= 2 ? 2 : 1;
   static constexpr int kTileRows = MH * kBM;
   static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
   static_assert(kAccBufs * kBufCols <= 512, "accumulator buffers in tensor memory");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
@@ -57,7 +61,7 @@ struct GemmCfg {
 };
 
 template <int BN, int EPI, int MH>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(GemmCfg<BN, EPI, MH>::kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmB2, const GemmArgs args) {
@@ -84,7 +88,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
       mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 4);
+      mbar_init(&acc_empty[b], C::kEpiWarps);
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -208,9 +212,12 @@ __global__ void __launch_bounds__(192, 1)
       mma_commit(mma_done);
     }
   } else {
-    // ---- epilogue: warps 2..5 ; TMEM lane quadrant = warp % 4
+    // ---- epilogue: TMEM lane quadrant = warp % 4; with 8 warps, column half (warp - 2) / 4
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;
+    constexpr int kCols = BN * 4 / C::kEpiWarps;
+    const int c_lo = half * kCols, c_hi = c_lo + kCols;
     int tc = 0;
     for (int id = blockIdx.x; id < walk.n_ids; id += gridDim.x) {
       int expert, row0, nrows, ntile;
@@ -234,7 +241,7 @@ __global__ void __launch_bounds__(192, 1)
         // split-K: raw fp32 partial product of this K range; the reduction finishes the tile
         float* prow = args.partial + (static_cast<long long>(id % walk.splits) * args.M + grow) * args.N;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32cols(tq + c0, v);
           tmem_ld_wait();
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(192, 1)
       } else if constexpr (EPI == kEpiF32) {
         float* orow = static_cast<float*>(args.out) + grow * args.ldo;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32cols(tq + c0, v);
           tmem_ld_wait();
@@ -272,33 +279,41 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       } else if constexpr (EPI == kEpiF32Ss) {
+        // row sums of squares per 128 columns ([rows, N/128]; the consumer adds them in order)
         float* orow = static_cast<float*>(args.out) + grow * args.ldo;
-        float ss = 0.f;
+        float ss0 = 0.f, ss1 = 0.f;   // columns [c_lo, c_lo + 128), [c_lo + 128, c_hi)
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32cols(tq + c0, v);
           tmem_ld_wait();
           const int col = n0 + c0;
           if (row_ok && col + 32 <= args.N) {
             float4* o = reinterpret_cast<float4*>(orow + col);
+            float sp = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                            __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-              ss = fmaf(f.x, f.x, ss);
-              ss = fmaf(f.y, f.y, ss);
-              ss = fmaf(f.z, f.z, ss);
-              ss = fmaf(f.w, f.w, ss);
+              sp = fmaf(f.x, f.x, sp);
+              sp = fmaf(f.y, f.y, sp);
+              sp = fmaf(f.z, f.z, sp);
+              sp = fmaf(f.w, f.w, sp);
               o[i] = f;
             }
+            if (c0 - c_lo < 128) ss0 += sp;
+            else ss1 += sp;
           }
         }
-        if (row_ok) args.ss[grow * args.ld_ss + ntile] = ss;
+        if (row_ok) {
+          float* srow = args.ss + grow * args.ld_ss + (n0 + c_lo) / 128;
+          srow[0] = ss0;
+          if (c_hi - c_lo > 128 && n0 + c_lo + 128 < args.N) srow[1] = ss1;
+        }
       } else {  // kEpiSwiGLU
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
           uint32_t g[32], u[32];
           tmem_ld_32cols(tq + c0, g);
           tmem_ld_32cols(tq + BN + c0, u);
@@ -367,7 +382,7 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
   const long long ids = tile_id_bound(m_tiles, a.N, BN, a.k_splits > 1 ? a.k_splits : 1);
   if (ids == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
-  return launch_pdl(kern, dim3(grid), dim3(192), C::kSmemBytes, s, tmA, tmB, tmB2, a);
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, tmA, tmB, tmB2, a);
 }
 
 cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& tmB,

@@ -44,12 +44,26 @@ LMOE_DEV bool mbar_try_wait(uint32_t addr, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same with a suspend-time hint: a waiting thread may sleep up to `ns` nanoseconds and
+// resumes as soon as the phase completes, so waiting warps issue few instructions.
+LMOE_DEV bool mbar_try_wait_sleep(uint32_t addr, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kWaitSleepNs = 20000;
 // Waits for the phase of parity `parity` to complete; false once `budget` cycles pass.
 LMOE_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, long long budget) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(a, parity)) {
+  while (!mbar_try_wait_sleep(a, parity, kWaitSleepNs)) {
     if (clock64() - t0 > budget) return false;
   }
   return true;
