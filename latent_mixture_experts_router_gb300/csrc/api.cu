@@ -172,10 +172,7 @@ void make_layout(const lmoe_config* c, Layout* L) {
     P.xe = take(R * Ld * 2);
     P.h = take(R * I * 2);
   }
-  // y: bf16 for BF16 weights (its row sums of squares are of the fp32 values); fp32 for fp32
-  // weights, whose error budget needs it, and for NVFP4, whose combine requantises c to E2M1 —
-  // a bf16-rounded y moves c across code boundaries there, each flip a whole E2M1 step
-  P.y = take(R * Ld * (c->weight_dtype == LMOE_BF16 ? 2 : 4));
+  P.y = take(R * Ld * 4);
   P.ss_y = take(R * L->ld_ss_y * 4);
   if (fp4) {
     P.c = take(T * Ld / 2);
@@ -279,8 +276,7 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
                      const Tile* tiles, const int* n_tiles, int m_tiles, void* out,
                      long long ldo, float* ss, int ld_ss, unsigned* err, long long budget,
                      cudaStream_t s, long long rows_per_b, int splits = 1,
-                     float* partial = nullptr, int m_halves = 1, bool reduce = true,
-                     bool out_bf16 = false) {
+                     float* partial = nullptr, int m_halves = 1, bool reduce = true) {
   const unsigned bn = epi == kEpiSwiGLU ? kBNSwiGLU : kBNWide;
   CUtensorMap ta, tb, tb2;
   if (!encode_bf16_2d(&ta, A, a_cols_used, a_rows, a_row_stride_elems * 2, kBK, kBM))
@@ -309,11 +305,10 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   a.partial = partial;
   a.max_tiles = m_tiles;
   a.n_groups = static_cast<int>(b_rows / N);
-  a.out_bf16 = out_bf16 ? 1 : 0;
   LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s, m_halves));
   if (splits > 1 && reduce)   // else the consumer sums the partials
     LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
-                                   ldo, ss, ld_ss, 128, s, nullptr, out_bf16));
+                                   ldo, ss, ld_ss, 128, s));
   return LMOE_OK;
 }
 
@@ -330,7 +325,7 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                          const float* ts, const float* ts2, unsigned* err, long long budget,
                          cudaStream_t s, long long rows_per_b, int splits = 1,
                          float* partial = nullptr, int* splits_dev = nullptr,
-                         bool reduce = true, bool out_bf16 = false) {
+                         bool reduce = true) {
   CUtensorMap maps[6];
   const unsigned long long kc = K / 2;
   const unsigned bn = kBNFp4;
@@ -365,7 +360,6 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
   a.partial = partial;
   a.max_tiles = m_tiles;
   a.n_groups = static_cast<int>(b_rows / N);
-  a.out_bf16 = out_bf16 ? 1 : 0;
   // grouped: `splits` bounds the count the kernel picks and leaves at splits_dev
   const bool adaptive = tiles != nullptr && splits > 1;
   a.adaptive_splits = adaptive ? 1 : 0;
@@ -378,7 +372,7 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                                            n_tiles, m_tiles, static_cast<uint8_t*>(out), out_scales, s));
     else
       LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
-                                     ldo, ss, ld_ss, 128, s, adaptive ? splits_dev : nullptr, out_bf16));
+                                     ldo, ss, ld_ss, 128, s, adaptive ? splits_dev : nullptr));
   }
   return LMOE_OK;
 }
@@ -479,8 +473,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   float* ss_p = static_cast<float*>(at(L.pub.ss_p));
   __nv_bfloat16* xe = static_cast<__nv_bfloat16*>(at(L.pub.xe));
   __nv_bfloat16* h = static_cast<__nv_bfloat16*>(at(L.pub.h));
-  void* y = at(L.pub.y);   // bf16 for BF16 weights, else fp32
-  const bool y_bf16 = cfg->weight_dtype == LMOE_BF16;
+  float* y = static_cast<float*>(at(L.pub.y));
   float* ss_y = static_cast<float*>(at(L.pub.ss_y));
   __nv_bfloat16* c = static_cast<__nv_bfloat16*>(at(L.pub.c));
   float* u = static_cast<float*>(at(L.pub.u));
@@ -662,12 +655,11 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     // S8 grouped down (fp32 y) with per-row partial sums of squares
     st = run_gemm_fp4(kFp4EpiF32Ss, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
                       L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
-                      nullptr, err, budget, s, R / E, grouped_splits(Ld, I / 256), partial, splits_dev + 1,
-                      true, y_bf16);
+                      nullptr, err, budget, s, R / E, grouped_splits(Ld, I / 256), partial, splits_dev + 1);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_COMBINE);
     // S9 combine, c quantised per token
-    LMOE_CUDA(launch_combine_nvfp4(y, y_bf16, ss_y, L.ld_ss_y, row_of, tk_idx, tk_w, g_expert, T, Ld, k, eps,
+    LMOE_CUDA(launch_combine_nvfp4(y, ss_y, L.ld_ss_y, row_of, tk_idx, tk_w, g_expert, T, Ld, k, eps,
                                    wsb + L.pub.c, wsb + L.pub.c_scale, c_s, s));
     LMOE_MARK(LMOE_STAGE_UNPOOLER);
     // S10 unpooler u = s_c * s_W * (Q(c) . W_unpool^T)
@@ -690,15 +682,14 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                 nullptr, gmh);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_DOWN);
-  // S8 grouped down (bf16 y; fp32 for fp32 weights), with per-row partial sums of squares of
-  // the fp32 values
+  // S8 grouped down (fp32 y), with per-row partial sums of squares
   st = run_gemm(kEpiF32Ss, h, R, I, I, wd, 1LL * E * Ld, 1LL * wsplit * I, nullptr, Ld,
                 wsplit * I / kBK, gtiles, gn_tiles, gmax, y, Ld, ss_y, L.ld_ss_y, err, budget, s, R / E, 1,
-                nullptr, gmh, true, y_bf16);
+                nullptr, gmh);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_COMBINE);
   // S9 combine: per-expert RMSNorm, routing weight, fp32 sum in slot order
-  LMOE_CUDA(launch_combine(y, y_bf16, ss_y, L.ld_ss_y, row_of, tk_idx, tk_w, g_expert, T, Ld, k, eps, c, s));
+  LMOE_CUDA(launch_combine(y, ss_y, L.ld_ss_y, row_of, tk_idx, tk_w, g_expert, T, Ld, k, eps, c, s));
   LMOE_MARK(LMOE_STAGE_UNPOOLER);
   // S10 unpooler u = c . W_unpool^T with row partial sums of squares
   st = run_gemm(kEpiF32Ss, c, T, Ld, Ld, wun, D, 1LL * wsplit * Ld, nullptr, D, wsplit * Ld / kBK,

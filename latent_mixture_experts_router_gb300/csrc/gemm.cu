@@ -279,9 +279,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, MH>::kThreads, 1)
           }
         }
       } else if constexpr (EPI == kEpiF32Ss) {
-        // row sums of squares per 128 columns ([rows, N/128]; the consumer adds them in order),
-        // of the fp32 values whether the output is stored fp32 or bf16
-        float* orow = static_cast<float*>(args.out) + grow * args.ldo;   // (fp32 output)
+        // row sums of squares per 128 columns ([rows, N/128]; the consumer adds them in order)
+        float* orow = static_cast<float*>(args.out) + grow * args.ldo;
         float ss0 = 0.f, ss1 = 0.f;   // columns [c_lo, c_lo + 128), [c_lo + 128, c_hi)
 #pragma unroll 1
         for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
@@ -290,23 +289,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, MH>::kThreads, 1)
           tmem_ld_wait();
           const int col = n0 + c0;
           if (row_ok && col + 32 <= args.N) {
+            float4* o = reinterpret_cast<float4*>(orow + col);
             float sp = 0.f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sp = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), sp);
-            if (args.out_bf16) {
-              uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo + col);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                o[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
-                                  pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
-                                  pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
-                                  pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
-            } else {
-              float4* o = reinterpret_cast<float4*>(orow + col);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                o[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            for (int i = 0; i < 8; ++i) {
+              const float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                           __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+              sp = fmaf(f.x, f.x, sp);
+              sp = fmaf(f.y, f.y, sp);
+              sp = fmaf(f.z, f.z, sp);
+              sp = fmaf(f.w, f.w, sp);
+              o[i] = f;
             }
             if (c0 - c_lo < 128) ss0 += sp;
             else ss1 += sp;

@@ -361,7 +361,6 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
         const bool split = walk.splits > 1;   // split-K: alpha * partial product, no ss
         float* orow = split ? args.partial + (static_cast<long long>(id % walk.splits) * args.M + grow) * args.N
                             : static_cast<float*>(args.out) + grow * args.ldo;
-        const bool bf16_out = args.out_bf16 && !split;   // ss of the fp32 values either way
         float ss = 0.f;
 #pragma unroll 1
         for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
@@ -370,22 +369,16 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
           tmem_ld_wait();
           const int col = n0 + c0;
           if (row_ok && col + 32 <= args.N) {
-            float f[32];
+            float4* o = reinterpret_cast<float4*>(orow + col);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              f[i] = __uint_as_float(v[i]) * alpha;
-              ss = fmaf(f[i], f[i], ss);
-            }
-            if (bf16_out) {
-              uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo + col);
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                o[i] = make_uint4(pack_bf16x2(f[8 * i], f[8 * i + 1]), pack_bf16x2(f[8 * i + 2], f[8 * i + 3]),
-                                  pack_bf16x2(f[8 * i + 4], f[8 * i + 5]), pack_bf16x2(f[8 * i + 6], f[8 * i + 7]));
-            } else {
-              float4* o = reinterpret_cast<float4*>(orow + col);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) o[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            for (int i = 0; i < 8; ++i) {
+              const float4 f = make_float4(__uint_as_float(v[4 * i]) * alpha, __uint_as_float(v[4 * i + 1]) * alpha,
+                                           __uint_as_float(v[4 * i + 2]) * alpha, __uint_as_float(v[4 * i + 3]) * alpha);
+              ss = fmaf(f.x, f.x, ss);
+              ss = fmaf(f.y, f.y, ss);
+              ss = fmaf(f.z, f.z, ss);
+              ss = fmaf(f.w, f.w, ss);
+              o[i] = f;
             }
           }
         }

@@ -64,7 +64,6 @@ struct GemmArgs {
   float* partial;          // [k_splits][rows][N] (split-K), reduced by launch_splitk_reduce
   int max_tiles;           // grouped: capacity of the tile table
   int n_groups;            // grouped: experts (B holds n_groups * N rows)
-  int out_bf16;            // kEpiF32Ss: store bf16 (the sums of squares stay of the fp32 values)
 };
 
 struct Fp4Args {
@@ -97,7 +96,6 @@ struct Fp4Args {
   int* splits_out;
   int max_tiles;             // grouped: capacity of the tile table
   int n_groups;              // grouped: experts (B holds n_groups * N rows)
-  int out_bf16;              // kFp4EpiF32Ss: store bf16 (sums of squares of the fp32 values)
 };
 
 // NVFP4 GEMM; maps = {A codes with boxes of 32, 64, 96, 128 rows, B codes, B2 codes}; scales
@@ -118,7 +116,7 @@ cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int
 // row-major E4M3 scales [rows, K/16] -> block layout with blocks of block_rows (64 or 128) rows
 cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K, int block_rows,
                                       uint8_t* dst, cudaStream_t s);
-cudaError_t launch_combine_nvfp4(const void* y, bool y_bf16, const float* ss_y, int ld_ss, const int32_t* row_of,
+cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, const int32_t* row_of,
                                  const int32_t* idx, const float* w, const float* g_expert, int T,
                                  int L, int k, float eps, uint8_t* codes, uint8_t* scales,
                                  float* s_row, cudaStream_t s);
@@ -132,9 +130,9 @@ int sm_count();
 // ss != nullptr, writes per-row partial sums of squares per group of `group` columns.  With
 // splits_dev != nullptr the split count is read there on the device (adaptive grouped GEMMs)
 // and `splits` is only its upper bound; a count of 1 means the GEMM wrote out itself.
-cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, void* out,
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, float* out,
                                  long long ldo, float* ss, int ld_ss, int group, cudaStream_t s,
-                                 const int* splits_dev = nullptr, bool out_bf16 = false);
+                                 const int* splits_dev = nullptr);
 // Grouped SwiGLU after an adaptive split-K gate/up GEMM: sums the [splits][rows][2N] partials
 // (gate | up, already scaled), h = silu(gate) * up, quantised to NVFP4 with scale 1: codes
 // [rows, N/2] and E4M3 block scales in the block layout of M tile `mt` (the h operand of the
@@ -220,7 +218,7 @@ cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* cou
 cudaError_t launch_poolnorm_scatter(const float* p, const float* ss_p, int ld_ss,
                                     const float* g_pool, const int32_t* row_of, int T, int L,
                                     int k, float eps, __nv_bfloat16* xe, cudaStream_t s);
-cudaError_t launch_combine(const void* y, bool y_bf16, const float* ss_y, int ld_ss,
+cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
                            const int32_t* row_of, const int32_t* idx, const float* w,
                            const float* g_expert, int T, int L, int k, float eps,
                            __nv_bfloat16* c, cudaStream_t s);

@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
 
 // ------------------------------------------------------------------ combine
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(
-    const void* __restrict__ y, int y_bf16, const float* __restrict__ ss_y, int ld_ss,
+    const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx,
     const float* __restrict__ w, const float* __restrict__ g_expert, int L, int k, float eps,
     __nv_bfloat16* __restrict__ c, int C) {
@@ -625,7 +625,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {  // slot order
       float v[8], gg[8];
-      load8(y, !y_bf16, static_cast<long long>(s_row[j]) * L + i, v);
+      load8_f32(y + static_cast<long long>(s_row[j]) * L + i, v);
       load8_f32(g_expert + static_cast<long long>(s_e[j]) * L + i, gg);
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_coef[j], v[q] * gg[q], acc[q]);
@@ -862,7 +862,7 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
 // Combine whose output c is quantised (row scale per token) for the unpooler.
 // Dynamic smem: L + 256 floats.
 __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
-    const void* __restrict__ y, int y_bf16, const float* __restrict__ ss_y, int ld_ss,
+    const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const float* __restrict__ w,
     const float* __restrict__ g_expert, int L, int k, float eps, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, float* __restrict__ s_row, int C) {
@@ -892,7 +892,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < k; ++j) {
       float v[8], gg[8];
-      load8(y, !y_bf16, static_cast<long long>(s_rowj[j]) * L + i, v);
+      load8_f32(y + static_cast<long long>(s_rowj[j]) * L + i, v);
       load8_f32(g_expert + static_cast<long long>(s_e[j]) * L + i, gg);
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_coef[j], v[q] * gg[q], acc[q]);
@@ -961,8 +961,8 @@ __global__ void nvfp4_block_scales_kernel(const uint8_t* __restrict__ src, long 
 // One CTA of `group` threads per (row, column group): sums the partials in split order (the
 // result does not depend on scheduling) and writes the group's sum of squares.
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, int rows, int N,
-                                     void* __restrict__ out, long long ldo, float* __restrict__ ss,
-                                     int ld_ss, const int* __restrict__ splits_dev, int out_bf16) {
+                                     float* __restrict__ out, long long ldo, float* __restrict__ ss,
+                                     int ld_ss, const int* __restrict__ splits_dev) {
   griddep_enter();
   if (splits_dev != nullptr) {
     splits = *splits_dev;
@@ -974,10 +974,7 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int spli
   float v = 0.f;
   if (col < N) {
     for (int q = 0; q < splits; ++q) v += partial[(static_cast<long long>(q) * rows + r) * N + col];
-    if (out_bf16)
-      static_cast<__nv_bfloat16*>(out)[static_cast<long long>(r) * ldo + col] = __float2bfloat16_rn(v);
-    else
-      static_cast<float*>(out)[static_cast<long long>(r) * ldo + col] = v;
+    out[static_cast<long long>(r) * ldo + col] = v;
   }
   if (ss != nullptr) {
     const float t = block_sum(col < N ? v * v : 0.f, red);
@@ -1088,7 +1085,7 @@ cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int
                             scales, s_rows, C);
 }
 
-cudaError_t launch_combine_nvfp4(const void* y, bool y_bf16, const float* ss_y, int ld_ss, const int32_t* row_of,
+cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, const int32_t* row_of,
                                  const int32_t* idx, const float* w, const float* g_expert, int T,
                                  int L, int k, float eps, uint8_t* codes, uint8_t* scales,
                                  float* s_row, cudaStream_t s) {
@@ -1101,7 +1098,7 @@ cudaError_t launch_combine_nvfp4(const void* y, bool y_bf16, const float* ss_y, 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl_cluster(combine_nvfp4_kernel, dim3(T * C), dim3(kRowThreads), smem, s, C, y, y_bf16 ? 1 : 0, ss_y,
+  return launch_pdl_cluster(combine_nvfp4_kernel, dim3(T * C), dim3(kRowThreads), smem, s, C, y, ss_y,
                             ld_ss, row_of, idx, w, g_expert, L, k, eps, codes, scales, s_row, C);
 }
 
@@ -1128,13 +1125,13 @@ cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K,
                     block_rows, dst);
 }
 
-cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, void* out,
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, float* out,
                                  long long ldo, float* ss, int ld_ss, int group, cudaStream_t s,
-                                 const int* splits_dev, bool out_bf16) {
+                                 const int* splits_dev) {
   if (rows == 0) return cudaSuccess;
   dim3 grid(rows, (N + group - 1) / group);
   return launch_pdl(splitk_reduce_kernel, dim3(grid), dim3(group), 0, s, partial, splits, rows, N,
-                    out, ldo, ss, ld_ss, splits_dev, out_bf16 ? 1 : 0);
+                    out, ldo, ss, ld_ss, splits_dev);
 }
 
 cudaError_t launch_swiglu_reduce_nvfp4(const float* partial, const int* splits_dev, int rows, int N,
@@ -1215,13 +1212,13 @@ cudaError_t launch_poolnorm_scatter(const float* p, const float* ss_p, int ld_ss
                     g_pool, row_of, L, k, eps, xe, C);
 }
 
-cudaError_t launch_combine(const void* y, bool y_bf16, const float* ss_y, int ld_ss,
+cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
                            const int32_t* row_of, const int32_t* idx, const float* w,
                            const float* g_expert, int T, int L, int k, float eps,
                            __nv_bfloat16* c, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int C = row_split(T, L);
-  return launch_pdl(combine_kernel, dim3(T * C), dim3(kRowThreads), 0, s, y, y_bf16 ? 1 : 0, ss_y, ld_ss, row_of, idx,
+  return launch_pdl(combine_kernel, dim3(T * C), dim3(kRowThreads), 0, s, y, ss_y, ld_ss, row_of, idx,
                     w, g_expert, L, k, eps, c, C);
 }
 
