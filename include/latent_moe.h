@@ -195,7 +195,8 @@ lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStrea
  *  xa (router/pooler input rows), logits [T,E] f32, topk_idx [T,k] i32, topk_w [T,k] f32,
  *  counts [E] i32, offsets [E+1] i32, row_of [T,k] i32, tok_of [T*k] i32,
  *  p [T,L] f32, xe [T*k, L] bf16 (expert-contiguous expert inputs), h [T*k, I] bf16,
- *  y [T*k, L] f32, ss_y [T*k, L/BN] f32, c [T,L] bf16, u [T,D] f32, err (u32).
+ *  y [T*k, L] f32, ss_y [T*k, L/128] f32, c [T,L] bf16, u [T,D] f32, ss_p / ss_u
+ *  [rows, N/128] f32 (row sums of squares per 128 columns), err (u32).
  *  Unused fields are -1. */
 typedef struct {
   long long xa, logits, topk_idx, topk_w, counts, offsets, row_of, tok_of, tiles, n_tiles,
