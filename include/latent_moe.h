@@ -117,6 +117,11 @@ enum {
  *  topk_w_out        [T, k] fp32 device: their routing weights
  *  near_tie_count_out  [1] int32 device: tokens whose k-th and (k+1)-th logits differ by < 1e-3
  *  wait_budget_cycles  SM clock cycles a device wait may spin before it gives up (0: default)
+ *  next_norm_gamma   [D] fp32 device, with next_norm_out [T, D] device (out_dtype): S11 also
+ *                    writes RMSNorm(out) * next_norm_gamma — the next layer's pre-norm taken
+ *                    from the same row in the same kernel (LMSYS Muse Spark Open post,
+ *                    § "Kernel optimizations": FFN post-norm, residual add and the next
+ *                    pre-norm as one kernel).  Both NULL: not written.  One alone: ERR_ARG.
  *  stage_events      host array of LMOE_NUM_STAGE_EVENTS caller-created cudaEvent_t, or NULL:
  *                    recorded on the stream at the stage boundaries above (timing only);
  *                    a NULL entry is skipped.  Kernels of one call are launched with
@@ -130,6 +135,8 @@ typedef struct {
   int32_t* near_tie_count_out;
   long long wait_budget_cycles;
   cudaEvent_t* stage_events;
+  const float* next_norm_gamma;
+  void* next_norm_out;
 } lmoe_ex;
 
 /* Bytes of device workspace a call with this config needs (host out-parameter). */

@@ -44,7 +44,8 @@ class lmoe_ex(ctypes.Structure):
     _fields_ = [("router_bias", ctypes.c_void_p), ("forced_idx", ctypes.c_void_p),
                 ("topk_idx_out", ctypes.c_void_p), ("topk_w_out", ctypes.c_void_p),
                 ("near_tie_count_out", ctypes.c_void_p), ("wait_budget_cycles", ctypes.c_longlong),
-                ("stage_events", ctypes.c_void_p)]
+                ("stage_events", ctypes.c_void_p), ("next_norm_gamma", ctypes.c_void_p),
+                ("next_norm_out", ctypes.c_void_p)]
 
 STAGES = ["prenorm", "router", "topk", "permute", "pooler", "poolnorm", "gate_up", "down", "combine",
           "unpooler", "postnorm"]
@@ -201,7 +202,7 @@ def latent_moe_forward(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g
 def latent_moe_forward_ex(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool,
                           g_pre, g_post, top_k, out, workspace, stream=None, router_bias=None,
                           forced_idx=None, topk_idx_out=None, topk_w_out=None, near_tie_count_out=None,
-                          wait_budget_cycles=0, stage_events=None):
+                          wait_budget_cycles=0, stage_events=None, next_norm_gamma=None, next_norm_out=None):
     """``stage_events``: a list of NUM_STAGE_EVENTS torch.cuda.Event(enable_timing=True) or None,
     recorded by the library at the stage boundaries (for per-stage timing; None entries are
     skipped)."""
@@ -219,7 +220,8 @@ def latent_moe_forward_ex(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down
         keep.append(evs)
     ex = lmoe_ex(_ptr(router_bias), _ptr(forced_idx), _ptr(topk_idx_out), _ptr(topk_w_out),
                  _ptr(near_tie_count_out), int(wait_budget_cycles),
-                 ctypes.cast(evs, ctypes.c_void_p) if evs is not None else None)
+                 ctypes.cast(evs, ctypes.c_void_p) if evs is not None else None,
+                 _ptr(next_norm_gamma), _ptr(next_norm_out))
     _check(_lib().latent_moe_forward_ex(*args, ctypes.byref(ex)), "latent_moe_forward_ex")
 
 
@@ -238,7 +240,7 @@ def latent_moe_forward_host_io_ex(cfg, x_host, W_router, W_pool, g_pool, W_gate,
     keep = []
     args = _fwd_args(cfg, x_host, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool,
                      g_pre, g_post, top_k, out_host, workspace, stream, keep)
-    ex = lmoe_ex(_ptr(router_bias), _ptr(forced_idx), None, None, None, 0, None)
+    ex = lmoe_ex(_ptr(router_bias), _ptr(forced_idx), None, None, None, 0, None, None, None)
     _check(_lib().latent_moe_forward_host_io_ex(*args, ctypes.byref(ex)), "latent_moe_forward_host_io_ex")
 
 

@@ -413,6 +413,10 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   lmoe_status st = check_config(cfg);
   if (st != LMOE_OK) return st;
   if (top_k != cfg->top_k) return LMOE_ERR_ARG;
+  if (ex != nullptr && (ex->next_norm_gamma == nullptr) != (ex->next_norm_out == nullptr)) return LMOE_ERR_ARG;
+  if (ex != nullptr && ex->next_norm_out != nullptr &&
+      (!aligned16(ex->next_norm_out) || !aligned16(ex->next_norm_gamma)))
+    return LMOE_ERR_ALIGN;
   if (cfg->T == 0) {  // no rows: nothing is read; only the error word is cleared
     Layout L0;
     make_layout(cfg, &L0);
@@ -701,7 +705,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   // S11 post-norm + residual
   // S11 reads the unpooler's split-K partials itself when it ran split (no reduction launch)
   LMOE_CUDA(launch_postnorm_residual(x, x_f32, u, ss_u, L.ld_ss_u, g_post, T, D, eps, out,
-                                     cfg->out_dtype == LMOE_F32, s, partial, dsp.unpool));
+                                     cfg->out_dtype == LMOE_F32, s, partial, dsp.unpool,
+                                     ex ? ex->next_norm_gamma : nullptr, ex ? ex->next_norm_out : nullptr));
   LMOE_MARK(LMOE_STAGE_END);
 #undef LMOE_MARK
   return LMOE_OK;

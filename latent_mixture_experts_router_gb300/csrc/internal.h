@@ -223,11 +223,13 @@ cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
                            const float* g_expert, int T, int L, int k, float eps,
                            __nv_bfloat16* c, cudaStream_t s);
 // usplits > 1: u is summed here from the unpooler's split-K partials upart [usplits][T][D] and
-// written to u, and the row's sum of squares is taken from it (ss_u is not read).
+// written to u, and the row's sum of squares is taken from it (ss_u is not read).  g_next:
+// also next_out = RMSNorm(out) * g_next (out as stored), the next layer's pre-norm.
 cudaError_t launch_postnorm_residual(const void* x, bool x_f32, float* u,
                                      const float* ss_u, int ld_ss, const float* g_post, int T,
                                      int D, float eps, void* out, bool out_f32, cudaStream_t s,
-                                     const float* upart = nullptr, int usplits = 1);
+                                     const float* upart = nullptr, int usplits = 1,
+                                     const float* g_next = nullptr, void* next_out = nullptr);
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s);
 // fp32 weight [rows, K] -> bf16 [rows, parts*K]: part q is W_hi when bit q of lo_mask is 0,
 // else W_lo = bf16(W - W_hi).  [hi | hi | lo] pairs with activations [x_hi | x_lo | x_hi];

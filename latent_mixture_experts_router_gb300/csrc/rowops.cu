@@ -638,11 +638,12 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
 __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
     const void* __restrict__ x, int x_f32, float* __restrict__ u,
     const float* __restrict__ ss_u, int ld_ss, const float* __restrict__ g, int D, float eps,
-    void* __restrict__ out, int out_f32, int C, const float* __restrict__ upart, int usplits, int T) {
+    void* __restrict__ out, int out_f32, int C, const float* __restrict__ upart, int usplits, int T,
+    const float* __restrict__ g_next, void* __restrict__ next_out) {
   griddep_enter();
   __shared__ float s_rs;
   __shared__ float red[33];
-  __shared__ float slot_ss;
+  __shared__ float slot_ss, slot_ss2;
   const RowSlice sl = row_slice(D, C);
   const long long t = sl.t;
   float rs;
@@ -672,22 +673,49 @@ __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
     __syncthreads();
     rs = s_rs;
   }
-  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
-    float xv[8], uv[8], gg[8];
-    load8(x, x_f32, t * D + i, xv);
+  // out = x + u rs g_post, as stored (bf16 out rounds); with g_next the stored rows also feed
+  // the next layer's pre-norm, a second row reduction over the same cluster
+  auto out_row = [&](int i, float (&o)[8]) {
+    float uv[8], gg[8];
+    load8(x, x_f32, t * D + i, o);
     load8_f32(u + t * D + i, uv);   // this thread's own stores when u came from the partials
     load8_f32(g + i, gg);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) xv[j] = xv[j] + uv[j] * rs * gg[j];
+    for (int j = 0; j < 8; ++j) o[j] = o[j] + uv[j] * rs * gg[j];
+    if (!out_f32) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] = bf16_round(o[j]);
+    }
+  };
+  float ss2 = 0.f;
+  for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
+    float o[8];
+    out_row(i, o);
     if (out_f32) {
-      float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + t * D + i);
-      o[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
-      o[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+      store8_f32(static_cast<float*>(out) + t * D + i, o);
     } else {
-      store8_bf16(static_cast<__nv_bfloat16*>(out) + t * D + i, xv);
+      store8_bf16(static_cast<__nv_bfloat16*>(out) + t * D + i, o);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss2 = fmaf(o[j], o[j], ss2);
+  }
+  if (g_next != nullptr) {
+    const float rs2 =
+        rsqrtf(cluster_combine(block_sum(ss2, red), &slot_ss2, C, false) / static_cast<float>(D) + eps);
+    for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
+      float o[8], gg[8];
+      out_row(i, o);
+      load8_f32(g_next + i, gg);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] = o[j] * rs2 * gg[j];
+      if (out_f32) {
+        store8_f32(static_cast<float*>(next_out) + t * D + i, o);
+      } else {
+        store8_bf16(static_cast<__nv_bfloat16*>(next_out) + t * D + i, o);
+      }
     }
   }
-  if (usplits > 1 && C > 1) cluster_sync_all();
+  if (C > 1 && (usplits > 1 || g_next != nullptr)) cluster_sync_all();
 }
 
 // ------------------------------------------------------------------ fp32 weights -> bf16 hi/lo
@@ -1225,15 +1253,17 @@ cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
 cudaError_t launch_postnorm_residual(const void* x, bool x_f32, float* u,
                                      const float* ss_u, int ld_ss, const float* g_post, int T,
                                      int D, float eps, void* out, bool out_f32, cudaStream_t s,
-                                     const float* upart, int usplits) {
+                                     const float* upart, int usplits, const float* g_next,
+                                     void* next_out) {
   if (T == 0) return cudaSuccess;
   const int C = row_split(T, D);
-  if (usplits > 1)   // the row's sum of squares is combined over a cluster of C CTAs
+  if (usplits > 1 || g_next != nullptr)   // row sums of squares combined over a cluster of C CTAs
     return launch_pdl_cluster(postnorm_residual_kernel, dim3(T * C), dim3(kRowThreads), 0, s, C, x,
                               x_f32 ? 1 : 0, u, ss_u, ld_ss, g_post, D, eps, out, out_f32 ? 1 : 0, C, upart,
-                              usplits, T);
+                              usplits, T, g_next, next_out);
   return launch_pdl(postnorm_residual_kernel, dim3(T * C), dim3(kRowThreads), 0, s, x, x_f32 ? 1 : 0,
-                    u, ss_u, ld_ss, g_post, D, eps, out, out_f32 ? 1 : 0, C, upart, usplits, T);
+                    u, ss_u, ld_ss, g_post, D, eps, out, out_f32 ? 1 : 0, C, upart, usplits, T, g_next,
+                    next_out);
 }
 
 cudaError_t launch_weight_split(const float* W, long long rows, int K, int parts,

@@ -86,3 +86,18 @@ def test_forward_rejects_bad_pointers_without_launching(lm):
     st = lib.latent_moe_forward(*args, 2, fake + 4096, fake, 16, None)
     assert st == -4
     assert isinstance(lmoe_config, type)
+
+
+def test_next_norm_arguments_checked_without_launching(lm):
+    # the fused next-layer pre-norm needs both its gamma and its output, 16-byte aligned
+    lib = lm.load()
+    from latent_mixture_experts_router_gb300._lib import lmoe_ex
+    c = lm.Config(8, 256, 128, 8, 128, 2).c()
+    fake = 1 << 20   # never dereferenced: validation fails first
+    args = [ctypes.byref(c)] + [fake] * 11 + [2, fake, fake, 1 << 30, None]
+    only_gamma = lmoe_ex(None, None, None, None, None, 0, None, fake, None)
+    assert lib.latent_moe_forward_ex(*args, ctypes.byref(only_gamma)) == -1
+    only_out = lmoe_ex(None, None, None, None, None, 0, None, None, fake)
+    assert lib.latent_moe_forward_ex(*args, ctypes.byref(only_out)) == -1
+    misaligned = lmoe_ex(None, None, None, None, None, 0, None, fake, fake + 4)
+    assert lib.latent_moe_forward_ex(*args, ctypes.byref(misaligned)) == -3

@@ -205,6 +205,26 @@ def test_host_io_with_routing_controls(cuda, routing):
     assert torch.equal(oh, out.cpu())
 
 
+@pytest.mark.parametrize("T,out_dtype", [(40, "f32"), (40, "bf16"), (300, "f32")])
+def test_next_layer_pre_norm(cuda, T, out_dtype):
+    # S11 also writing RMSNorm(out) * g_next (the next layer's pre-norm from the same row; at
+    # T = 40 the row is split over a cluster of 4 CTAs): out itself is unchanged, and the extra
+    # output is the RMSNorm of out as stored, within fp32 rounding
+    w = workloads.Workload(f"next_{T}", T=T, D=1024, L=256, E=8, I=256, k=2, seed=3)
+    inp = workloads.make_inputs(w, cuda)
+    blk = make_block(inp)
+    base, _, _, _ = run(inp, blk=blk, out_dtype=out_dtype)
+    base = base.clone()
+    g_next = (1.0 + 0.1 * torch.randn(w.D, generator=torch.Generator().manual_seed(5), dtype=torch.float64)
+              ).to(torch.float32).to(cuda)
+    nxt = torch.empty(w.T, w.D, dtype=base.dtype, device=cuda)
+    out, _, _, _ = run(inp, blk=blk, out_dtype=out_dtype, next_norm_gamma=g_next, next_norm_out=nxt)
+    assert torch.equal(out, base)
+    ref = oracle.rms_norm(out.double().cpu().numpy(), g_next.double().cpu().numpy(), w.eps)
+    err = np.abs(nxt.double().cpu().numpy() - ref).max() / np.sqrt(np.mean(ref ** 2))
+    assert err < (4e-6 if out_dtype == "f32" else 1.6e-2), err   # fp32 rounding; bf16 half-ulp at |v| <= 4 RMS
+
+
 def test_out_of_range_forced_id_is_flagged(cuda):
     import latent_mixture_experts_router_gb300 as lm
     w = workloads.Workload("badidx", T=8, D=256, L=128, E=8, I=128, k=2)
