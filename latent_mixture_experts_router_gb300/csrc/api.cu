@@ -546,8 +546,13 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   // BF16 GEMMs over many rows take 256-row tiles (two MMAs share each weight tile): dense
   // ones from 512 rows when not split along K, grouped ones at >= 256 rows per expert on
   // average (they then walk the table of 256-row tiles)
-  auto dense_mh = [&](int splits) { return splits <= 1 && T >= 4 * kBM ? 2 : 1; };
-  auto dense_mt = [&](int splits) { return cdiv(T, kBM * dense_mh(splits)); };
+  // (256-row tiles only where they still give every SM a tile: the router's single N tile
+  // at T = 16384 would leave 88 of 152 SMs idle)
+  auto dense_mh_n = [&](int splits, int n_tiles) {
+    return splits <= 1 && T >= 4 * kBM && 1LL * cdiv(T, 2 * kBM) * n_tiles >= kSplitSms ? 2 : 1;
+  };
+  const int pool_mh = dense_mh_n(dsp.pooler, cdiv(Ld, kBNWide));
+  const int unpool_mh = dense_mh_n(dsp.unpool, cdiv(D, kBNWide));
   auto pooler = [&](cudaStream_t ps) -> lmoe_status {
     if (fp4)
       return run_gemm_fp4(kFp4EpiF32Ss, xq, T, D, op(q4[0]), Ld, nullptr, Ld, nullptr, nullptr, m_tiles_T,
@@ -555,8 +560,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                           ps, T, dsp.pooler, partial_pool);
     const int pool_k = f32w ? 3 * D : D;
     return run_gemm(kEpiF32Ss, xa, T, pool_k, xa_cols, wp, Ld, pool_k, nullptr, Ld, pool_k / kBK,
-                    nullptr, nullptr, dense_mt(dsp.pooler), p, Ld, ss_p, L.ld_ss_p, err, budget, ps, T,
-                    dsp.pooler, partial_pool, dense_mh(dsp.pooler));
+                    nullptr, nullptr, cdiv(T, kBM * pool_mh), p, Ld, ss_p, L.ld_ss_p, err, budget, ps, T,
+                    dsp.pooler, partial_pool, pool_mh);
   };
   // The pooler needs only xn: it runs on the side stream beside S2-S4 unless the caller
   // times those stages (their events pin every stage to the caller's stream).
@@ -594,9 +599,10 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   // split-K partials when they are few (one launch less on the chain)
   const bool fused_route = route_small_fits(T, k, E) && (ev == nullptr || ev[LMOE_STAGE_PERMUTE] == nullptr);
   const int rsplits = fused_route && dsp.router > 1 && 1LL * T * dsp.router * E <= 65536 ? dsp.router : 1;
+  const int router_mh = dense_mh_n(dsp.router, cdiv(E, kBNWide));
   st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
-                xa_cols / kBK, nullptr, nullptr, dense_mt(dsp.router), logits, L.ld_logits, nullptr, 0, err,
-                budget, s, T, dsp.router, partial, dense_mh(dsp.router), rsplits == 1);
+                xa_cols / kBK, nullptr, nullptr, cdiv(T, kBM * router_mh), logits, L.ld_logits, nullptr, 0,
+                err, budget, s, T, dsp.router, partial, router_mh, rsplits == 1);
   if (st != LMOE_OK) return st;
   LMOE_MARK(LMOE_STAGE_TOPK);
   // S3 top-k + softmax, S4 permutation (one kernel for few pairs unless S4 is timed apart)
@@ -697,8 +703,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   LMOE_MARK(LMOE_STAGE_UNPOOLER);
   // S10 unpooler u = c . W_unpool^T with row partial sums of squares
   st = run_gemm(kEpiF32Ss, c, T, Ld, Ld, wun, D, 1LL * wsplit * Ld, nullptr, D, wsplit * Ld / kBK,
-                nullptr, nullptr, dense_mt(dsp.unpool), u, D, ss_u, L.ld_ss_u, err, budget, s, T, dsp.unpool,
-                partial, dense_mh(dsp.unpool), false);
+                nullptr, nullptr, cdiv(T, kBM * unpool_mh), u, D, ss_u, L.ld_ss_u, err, budget, s, T,
+                dsp.unpool, partial, unpool_mh, false);
   if (st != LMOE_OK) return st;
   }
   LMOE_MARK(LMOE_STAGE_POSTNORM);
