@@ -112,7 +112,9 @@ enum {
 /* Optional extensions of one call (host struct; every member may be NULL/0).
  *  router_bias       [E] fp32 device: added to the router logits before softmax/top-k
  *  forced_idx        [T, k] int32 device: use these experts (distinct per row) instead of
- *                    the top-k; weights are the softmax of the logits renormalised over them
+ *                    the top-k; weights are the softmax of the logits renormalised over them.
+ *                    An id outside [0, E) or repeated within a row is flagged on the
+ *                    device (lmoe_check_status then returns LMOE_ERR_ARG).
  *  topk_idx_out      [T, k] int32 device: selected experts, descending logit
  *  topk_w_out        [T, k] fp32 device: their routing weights
  *  near_tie_count_out  [1] int32 device: tokens whose k-th and (k+1)-th logits differ by < 1e-3

@@ -230,6 +230,9 @@ __device__ __forceinline__ void warp_topk(float* vals, const int32_t* forced_row
         if (lane == 0) atomicOr(err, kErrBadIndex);
         e = 0;
       }
+      // a repeated id breaks the one-row-per-token-and-expert bound the GEMM tiles rely on
+      for (int i = 0; i < j; ++i)
+        if (sel[i] == e && lane == 0) atomicOr(err, kErrBadIndex);
       sel[j] = e;
       sval[j] = vals[e];
     }

@@ -225,12 +225,13 @@ def test_next_layer_pre_norm(cuda, T, out_dtype):
     assert err < (4e-6 if out_dtype == "f32" else 1.6e-2), err   # fp32 rounding; bf16 half-ulp at |v| <= 4 RMS
 
 
-def test_out_of_range_forced_id_is_flagged(cuda):
+@pytest.mark.parametrize("bad_row", [[3, 99], [5, 5]], ids=["out_of_range", "repeated"])
+def test_bad_forced_id_is_flagged(cuda, bad_row):
     import latent_mixture_experts_router_gb300 as lm
     w = workloads.Workload("badidx", T=8, D=256, L=128, E=8, I=128, k=2)
     inp = workloads.make_inputs(w, cuda)
     blk = make_block(inp)
-    forced = torch.tensor([[0, 1]] * 7 + [[3, 99]], dtype=torch.int32, device=cuda)
+    forced = torch.tensor([[0, 1]] * 7 + [bad_row], dtype=torch.int32, device=cuda)
     blk.forward(inp.x, forced_idx=forced)
     st, word = lm.lmoe_check_status(blk.config(w.T), blk._ws)
     assert st == -1 and word & (1 << 3)
