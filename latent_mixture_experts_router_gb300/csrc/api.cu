@@ -67,6 +67,11 @@ constexpr int kSplitSms = 152;
 // The pooler runs beside the router (side stream): at small T its split count is sized for
 // about two thirds of the SMs, so that the router's CTAs find SMs of their own.
 constexpr int kPoolerSms = 100;
+// BF16 GEMMs with fp32 outputs store them through the epilogue's transpose tiles (whole-line
+// stores) from this many rows per weight matrix (T for the dense GEMMs, R/E for the grouped
+// ones); below it the tiles hold few rows and the smaller shared-memory footprint lets the next
+// kernel's CTAs become resident beside the GEMM's
+constexpr long long kXposeRows = 64;
 int dense_splits(int T, int N, int bn, int num_kb, int min_kb, int sms = kSplitSms) {
   const long long tiles = static_cast<long long>((T + kBM - 1) / kBM) * ((N + bn - 1) / bn);
   if (tiles == 0 || tiles * 2 >= sms) return 1;
@@ -305,6 +310,7 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   a.partial = partial;
   a.max_tiles = m_tiles;
   a.n_groups = static_cast<int>(b_rows / N);
+  a.xpose = rows_per_b >= kXposeRows ? 1 : 0;
   LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s, m_halves));
   if (splits > 1 && reduce)   // else the consumer sums the partials
     LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),

@@ -53,7 +53,9 @@ struct GemmCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kEpiWarps = 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int kXposeOff = kStages * kStageBytes + 256;   // after the barriers
+  static constexpr int kXposeBytes = kEpiWarps * 32 * 33 * 4;      // reserved when args.xpose
+  static constexpr int kSmemBytes = kXposeOff + kXposeBytes + 1024 /*align*/;
   static_assert(kAccBufs * kBufCols <= 512, "accumulator buffers in tensor memory");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "tile N");
@@ -77,6 +79,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, MH>::kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // epilogue warp w's transpose tile for coalesced fp32 stores
+  float* xpose = reinterpret_cast<float*>(smem + C::kXposeOff) + (warp >= 2 ? (warp - 2) * 32 * 33 : 0);
 
   // Set-up reads nothing an earlier kernel of the stream writes, so it runs before the wait,
   // overlapping the end of that kernel, and so does an L2 prefetch of this CTA's first
@@ -236,22 +240,24 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, MH>::kThreads, 1)
       const int rr = h * kBM + r;   // row within the tile
       const bool row_ok = rr < nrows;
       const long long grow = static_cast<long long>(row0) + rr;
+      // this warp's 32 rows: the first of them, and how many hold live rows
+      const long long wrow = static_cast<long long>(row0) + h * kBM + quad * 32;
+      const int wvalid = min(32, max(0, nrows - (h * kBM + quad * 32)));
       const uint32_t tq = tmem + buf * C::kBufCols + h * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       if (EPI != kEpiSwiGLU && walk.splits > 1) {
         // split-K: raw fp32 partial product of this K range; the reduction finishes the tile
-        float* prow = args.partial + (static_cast<long long>(id % walk.splits) * args.M + grow) * args.N;
+        const long long pbase = static_cast<long long>(id % walk.splits) * args.M;
+        float* prow = args.partial + (pbase + grow) * args.N;
 #pragma unroll 1
         for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32cols(tq + c0, v);
           tmem_ld_wait();
           const int col = n0 + c0;
-          if (row_ok && col + 32 <= args.N) {
-            float4* o = reinterpret_cast<float4*>(prow + col);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          if (args.xpose && col + 32 <= args.N) {   // warp-uniform
+            warp_store_32x32_f32(xpose, v, args.partial + (pbase + wrow) * args.N + col, args.N, wvalid, lane);
+          } else if (row_ok && col + 32 <= args.N) {
+            store_row32_f32(prow + col, v);
           } else if (row_ok && col < args.N) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -260,18 +266,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, MH>::kThreads, 1)
         }
       } else if constexpr (EPI == kEpiF32) {
         float* orow = static_cast<float*>(args.out) + grow * args.ldo;
+        float* wout = static_cast<float*>(args.out) + wrow * args.ldo;
 #pragma unroll 1
         for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
           uint32_t v[32];
           tmem_ld_32cols(tq + c0, v);
           tmem_ld_wait();
           const int col = n0 + c0;
-          if (row_ok && col + 32 <= args.N) {
-            float4* o = reinterpret_cast<float4*>(orow + col);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          if (args.xpose && col + 32 <= args.N) {   // warp-uniform
+            warp_store_32x32_f32(xpose, v, wout + col, args.ldo, wvalid, lane);
+          } else if (row_ok && col + 32 <= args.N) {
+            store_row32_f32(orow + col, v);
           } else if (row_ok && col < args.N) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -281,6 +286,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, MH>::kThreads, 1)
       } else if constexpr (EPI == kEpiF32Ss) {
         // row sums of squares per 128 columns ([rows, N/128]; the consumer adds them in order)
         float* orow = static_cast<float*>(args.out) + grow * args.ldo;
+        float* wout = static_cast<float*>(args.out) + wrow * args.ldo;
         float ss0 = 0.f, ss1 = 0.f;   // columns [c_lo, c_lo + 128), [c_lo + 128, c_hi)
 #pragma unroll 1
         for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
@@ -288,22 +294,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, MH>::kThreads, 1)
           tmem_ld_32cols(tq + c0, v);
           tmem_ld_wait();
           const int col = n0 + c0;
-          if (row_ok && col + 32 <= args.N) {
-            float4* o = reinterpret_cast<float4*>(orow + col);
-            float sp = 0.f;
+          if (col + 32 > args.N) continue;   // (N is a multiple of 128 here)
+          float sp = 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                           __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-              sp = fmaf(f.x, f.x, sp);
-              sp = fmaf(f.y, f.y, sp);
-              sp = fmaf(f.z, f.z, sp);
-              sp = fmaf(f.w, f.w, sp);
-              o[i] = f;
-            }
-            if (c0 - c_lo < 128) ss0 += sp;
-            else ss1 += sp;
-          }
+          for (int i = 0; i < 32; ++i) sp = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), sp);
+          if (c0 - c_lo < 128) ss0 += sp;
+          else ss1 += sp;
+          if (args.xpose) warp_store_32x32_f32(xpose, v, wout + col, args.ldo, wvalid, lane);
+          else if (row_ok) store_row32_f32(orow + col, v);
         }
         if (row_ok) {
           float* srow = args.ss + grow * args.ld_ss + (n0 + c_lo) / 128;
@@ -382,7 +380,8 @@ static cudaError_t launch_one(const CUtensorMap& tmA, const CUtensorMap& tmB,
   const long long ids = tile_id_bound(m_tiles, a.N, BN, a.k_splits > 1 ? a.k_splits : 1);
   if (ids == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
-  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, tmA, tmB, tmB2, a);
+  const int smem = C::kSmemBytes - (a.xpose ? 0 : C::kXposeBytes);
+  return launch_pdl(kern, dim3(grid), dim3(C::kThreads), smem, s, tmA, tmB, tmB2, a);
 }
 
 cudaError_t launch_gemm(EpiKind epi, const CUtensorMap& tmA, const CUtensorMap& tmB,

@@ -64,6 +64,8 @@ struct GemmArgs {
   float* partial;          // [k_splits][rows][N] (split-K), reduced by launch_splitk_reduce
   int max_tiles;           // grouped: capacity of the tile table
   int n_groups;            // grouped: experts (B holds n_groups * N rows)
+  int xpose;               // fp32 stores through a per-warp transpose tile (many rows per tile;
+                           // the launch then reserves the tile's shared memory)
 };
 
 struct Fp4Args {

@@ -191,6 +191,38 @@ LMOE_DEV void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]) {
 }
 LMOE_DEV void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------------------ epilogue stores
+// One thread's 32 consecutive fp32 values (a row segment, 16-byte aligned), as 8 vector stores.
+LMOE_DEV void store_row32_f32(float* g, const uint32_t (&v)[32]) {
+  float4* o = reinterpret_cast<float4*>(g);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    o[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                       __uint_as_float(v[4 * i + 3]));
+}
+// A warp's 32 x 32 fp32 block, read from tensor memory with one row per thread (thread i
+// holds row i's 32 columns in v).  Stored straight from those registers, every store
+// instruction would touch 32 rows, 16 bytes each; instead the block passes through this warp's
+// padded shared tile (32 x 33 floats: the odd pitch keeps the row writes and the column reads
+// free of bank conflicts) and each store instruction writes four whole 128-byte row segments.
+// Rows [0, nvalid) are stored at g + row * ld (g and ld * 4 bytes 16-byte aligned).
+LMOE_DEV void warp_store_32x32_f32(float* xp, const uint32_t (&v)[32], float* g, long long ld,
+                                   int nvalid, int lane) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) xp[lane * 33 + c] = __uint_as_float(v[c]);
+  __syncwarp();
+  const int sub = lane >> 3, c4 = (lane & 7) * 4;
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    const int r = 4 * st + sub;
+    if (r < nvalid) {
+      const float* q = xp + r * 33 + c4;
+      *reinterpret_cast<float4*>(g + r * ld + c4) = make_float4(q[0], q[1], q[2], q[3]);
+    }
+  }
+  __syncwarp();
+}
+
 // ------------------------------------------------------------------ programmatic dependent launch
 // Every kernel of the library is launched with programmatic stream serialisation: its CTAs
 // may become resident while the previous kernel of the stream is still finishing, and they
