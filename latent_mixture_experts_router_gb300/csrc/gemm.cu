@@ -51,7 +51,7 @@ struct GemmCfg {
   static constexpr int kAccBufs = 512 / kBufCols >= 2 ? 2 : 1;
   static constexpr int kTileRows = MH * kBM;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiWarps = MH == 2 ? 8 : 4;   // 256-row tiles: twice the rows to drain
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kXposeOff = kStages * kStageBytes + 256;   // after the barriers
   static constexpr int kXposeBytes = kEpiWarps * 32 * 33 * 4;      // reserved when args.xpose

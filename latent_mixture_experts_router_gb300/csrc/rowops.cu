@@ -472,6 +472,38 @@ __device__ __forceinline__ void block_scan2(int& a, int& b, int* sh, int* ta, in
   *tb = sb;
 }
 
+// logits[t][i] = sum over q in split order of part[q][t][i]; element ti = t * E + i; M logits per
+// thread and J splits per round of loads
+template <int M, int J>
+__device__ __forceinline__ void route_sum_partials(const float* __restrict__ part, int splits, int te, int E,
+                                                   float* __restrict__ logits, int ld) {
+  for (int g0 = 0; g0 < te; g0 += M * kRouteThreads) {
+    float v[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) v[m] = 0.f;
+    for (int q0 = 0; q0 < splits; q0 += J) {
+      float pv[M][J];
+#pragma unroll
+      for (int m = 0; m < M; ++m) {
+        const int ti = g0 + m * kRouteThreads + threadIdx.x;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+          pv[m][j] = (ti < te && q0 + j < splits) ? part[static_cast<long long>(q0 + j) * te + ti] : 0.f;
+      }
+#pragma unroll
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+          if (q0 + j < splits) v[m] += pv[m][j];
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+      const int ti = g0 + m * kRouteThreads + threadIdx.x;
+      if (ti < te) logits[static_cast<long long>(ti / E) * ld + ti % E] = v[m];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(
     float* __restrict__ logits, int ld, const float* __restrict__ rpart, int rsplits,
     const float* __restrict__ bias,
@@ -494,22 +526,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(
   // S3: a warp per token
   if (rsplits > 1) {
     // the router's split-K partials [rsplits][T][E], summed in split order (as the reduction
-    // kernel does) by every thread of the CTA, loads issued eight at a time
-    for (int ti = threadIdx.x; ti < T * E; ti += kRouteThreads) {
-      const int t = ti / E, i = ti % E;
-      const float* src = rpart + static_cast<long long>(t) * E + i;
-      const long long plane = static_cast<long long>(T) * E;
-      float v = 0.f;
-      for (int q0 = 0; q0 < rsplits; q0 += 8) {
-        float pv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) pv[j] = q0 + j < rsplits ? src[(q0 + j) * plane] : 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (q0 + j < rsplits) v += pv[j];
-      }
-      logits[static_cast<long long>(t) * ld + i] = v;
-    }
+    // kernel does) by every thread of the CTA: a chain of dependent L2 round trips, so each
+    // thread keeps 32 loads in flight per round (fewer logits per thread, more splits a round)
+    const int te = T * E;
+    if (te <= kRouteThreads) route_sum_partials<1, 32>(rpart, rsplits, te, E, logits, ld);
+    else if (te <= 2 * kRouteThreads) route_sum_partials<2, 16>(rpart, rsplits, te, E, logits, ld);
+    else route_sum_partials<4, 8>(rpart, rsplits, te, E, logits, ld);
     __syncthreads();
   }
   for (int t = warp; t < T; t += nw) {
