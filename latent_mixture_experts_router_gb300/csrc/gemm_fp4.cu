@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
     }
   }
   if (warp >= 2 && warp < C::kCopyWarp) {
-    for (int i = threadIdx.x - 64; i < 256; i += 32 * C::kEpiWarps) recip[i] = c_e4m3_recip.v[i];
+    for (int i = threadIdx.x - 64; i < 256; i += 32 * C::kEpiWarps) recip[i] = g_e4m3_recip.v[i];
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);

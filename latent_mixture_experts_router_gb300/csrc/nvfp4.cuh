@@ -44,8 +44,10 @@ struct E4M3RecipTable {
   }
 };
 
-// The table lives in constant memory of each translation unit that includes this header.
-static __constant__ E4M3RecipTable c_e4m3_recip = E4M3RecipTable();
+// The table lives in global memory of each translation unit that includes this header: kernels
+// copy it to shared memory with one coalesced load per thread (constant memory would serialise
+// the 32 distinct addresses of each warp's load).
+static __device__ const E4M3RecipTable g_e4m3_recip = E4M3RecipTable();
 
 // ---- hardware conversions (round to nearest even, saturate to the largest finite)
 // one byte holding E2M1(hi) in the high nibble and E2M1(lo) in the low nibble

@@ -103,6 +103,44 @@ __device__ __forceinline__ void store8_f32(float* p, const float (&v)[8]) {   //
   q[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
+// acc[0, 8) += sum over slots j (in slot order) of coef[j] * y[row[j]][i, i+8) * g[e[j]][i, i+8).
+// The loads of NB slots are issued together, before their multiply-adds.  NB = 4 for few
+// tokens, where the combine is a chain of round trips and more loads in flight shorten it;
+// NB = 1 for many, where the registers NB = 4 takes would halve the CTAs an SM holds.
+constexpr int kCombineBatch = 4;          // slots per batch of loads at few tokens
+constexpr int kCombineBatchMaxT = 512;    // "few": a token per CTA (or per cluster) fills no GPU
+template <int NB>
+__device__ __forceinline__ void combine_cols8(const float* __restrict__ y, const float* __restrict__ g_expert,
+                                              int L, int i, int k, const int* rows, const int* es,
+                                              const float* coef, float (&acc)[8]) {
+  for (int j0 = 0; j0 < k; j0 += NB) {
+    float v[NB][8], gg[NB][8];
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj)
+      if (j0 + jj < k) {
+        load8_f32(y + static_cast<long long>(rows[j0 + jj]) * L + i, v[jj]);
+        load8_f32(g_expert + static_cast<long long>(es[j0 + jj]) * L + i, gg[jj]);
+      }
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj)
+      if (j0 + jj < k) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(coef[j0 + jj], v[jj][q] * gg[jj][q], acc[q]);
+      }
+  }
+}
+
+// Sum of the n partials p[0, n) by one warp: lane-strided loads (one round trip for n <= 32),
+// then a shuffle tree; lane 0's result, broadcast, so every lane returns the same value and
+// the order is the same on every call.
+__device__ __forceinline__ float warp_sum_partials(const float* __restrict__ p, int n, int lane) {
+  float v = 0.f;
+  for (int q = lane; q < n; q += 32) v += p[q];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return __shfl_sync(0xffffffffu, v, 0);
+}
+
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -607,10 +645,9 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
   __shared__ int s_rows[16];
   const RowSlice sl = row_slice(L, C);
   const long long t = sl.t;
-  if (threadIdx.x == 0) {
-    float ss = 0.f;
-    for (int q = 0; q < ld_ss; ++q) ss += ss_p[t * ld_ss + q];
-    s_rs = rsqrtf(ss / static_cast<float>(L) + eps);
+  if (threadIdx.x < 32) {
+    const float ss = warp_sum_partials(ss_p + t * ld_ss, ld_ss, threadIdx.x);
+    if (threadIdx.x == 0) s_rs = rsqrtf(ss / static_cast<float>(L) + eps);
   }
   if (threadIdx.x < k) s_rows[threadIdx.x] = row_of[t * k + threadIdx.x];
   __syncthreads();
@@ -626,6 +663,7 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
 }
 
 // ------------------------------------------------------------------ combine
+template <int NB>
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx,
@@ -636,25 +674,20 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
   __shared__ int s_row[16], s_e[16];
   const RowSlice sl = row_slice(L, C);
   const long long t = sl.t;
-  if (threadIdx.x < k) {
-    const int j = threadIdx.x;
+  for (int j = threadIdx.x >> 5; j < k; j += kRowThreads / 32) {   // a warp per slot
+    const int lane = threadIdx.x & 31;
     const int row = row_of[t * k + j];
-    float ss = 0.f;
-    for (int q = 0; q < ld_ss; ++q) ss += ss_y[static_cast<long long>(row) * ld_ss + q];
-    s_coef[j] = w[t * k + j] * rsqrtf(ss / static_cast<float>(L) + eps);
-    s_row[j] = row;
-    s_e[j] = idx[t * k + j];
+    const float ss = warp_sum_partials(ss_y + static_cast<long long>(row) * ld_ss, ld_ss, lane);
+    if (lane == 0) {
+      s_coef[j] = w[t * k + j] * rsqrtf(ss / static_cast<float>(L) + eps);
+      s_row[j] = row;
+      s_e[j] = idx[t * k + j];
+    }
   }
   __syncthreads();
   for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {  // slot order
-      float v[8], gg[8];
-      load8_f32(y + static_cast<long long>(s_row[j]) * L + i, v);
-      load8_f32(g_expert + static_cast<long long>(s_e[j]) * L + i, gg);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_coef[j], v[q] * gg[q], acc[q]);
-    }
+    combine_cols8<NB>(y, g_expert, L, i, k, s_row, s_e, s_coef, acc);   // slot order
     store8_bf16(c + t * L + i, acc);
   }
 }
@@ -690,10 +723,9 @@ __global__ void __launch_bounds__(kRowThreads) postnorm_residual_kernel(
     }
     rs = rsqrtf(cluster_combine(block_sum(ss, red), &slot_ss, C, false) / static_cast<float>(D) + eps);
   } else {
-    if (threadIdx.x == 0) {
-      float ss = 0.f;
-      for (int q = 0; q < ld_ss; ++q) ss += ss_u[t * ld_ss + q];
-      s_rs = rsqrtf(ss / static_cast<float>(D) + eps);
+    if (threadIdx.x < 32) {
+      const float ss = warp_sum_partials(ss_u + t * ld_ss, ld_ss, threadIdx.x);
+      if (threadIdx.x == 0) s_rs = rsqrtf(ss / static_cast<float>(D) + eps);
     }
     __syncthreads();
     rs = s_rs;
@@ -768,7 +800,7 @@ __global__ void weight_split_kernel(const float* __restrict__ W, long long rows,
 // ------------------------------------------------------------------ NVFP4 rows
 
 __device__ __forceinline__ void load_recip(float* recip) {
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) recip[i] = c_e4m3_recip.v[i];
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) recip[i] = g_e4m3_recip.v[i];
 }
 
 // Destination row of a quantised row: codes at row `code_row` (pitch K/2 bytes); scales
@@ -881,10 +913,9 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
   __shared__ QDest s_dst[16];
   load_recip(recip);
   const long long t = sl.t;
-  if (threadIdx.x == 0) {
-    float ss = 0.f;
-    for (int q = 0; q < ld_ss; ++q) ss += ss_p[t * ld_ss + q];
-    s_rs = rsqrtf(ss / static_cast<float>(L) + eps);
+  if (threadIdx.x < 32) {
+    const float ss = warp_sum_partials(ss_p + t * ld_ss, ld_ss, threadIdx.x);
+    if (threadIdx.x == 0) s_rs = rsqrtf(ss / static_cast<float>(L) + eps);
   }
   if (threadIdx.x < k) {   // the expert row, and its M tile (the scale block) and place in it
     const int row = row_of[t * k + threadIdx.x];
@@ -914,6 +945,7 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
 
 // Combine whose output c is quantised (row scale per token) for the unpooler.
 // Dynamic smem: L + 256 floats.
+template <int NB>
 __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
     const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const float* __restrict__ w,
@@ -930,26 +962,21 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
   __shared__ QDest s_d;
   load_recip(recip);
   const long long t = sl.t;
-  if (threadIdx.x < k) {
-    const int j = threadIdx.x;
+  for (int j = threadIdx.x >> 5; j < k; j += kRowThreads / 32) {   // a warp per slot
+    const int lane = threadIdx.x & 31;
     const int row = row_of[t * k + j];
-    float ss = 0.f;
-    for (int q = 0; q < ld_ss; ++q) ss += ss_y[static_cast<long long>(row) * ld_ss + q];
-    s_coef[j] = w[t * k + j] * rsqrtf(ss / static_cast<float>(L) + eps);
-    s_rowj[j] = row;
-    s_e[j] = idx[t * k + j];
+    const float ss = warp_sum_partials(ss_y + static_cast<long long>(row) * ld_ss, ld_ss, lane);
+    if (lane == 0) {
+      s_coef[j] = w[t * k + j] * rsqrtf(ss / static_cast<float>(L) + eps);
+      s_rowj[j] = row;
+      s_e[j] = idx[t * k + j];
+    }
   }
   __syncthreads();
   float amax = 0.f;
   for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      float v[8], gg[8];
-      load8_f32(y + static_cast<long long>(s_rowj[j]) * L + i, v);
-      load8_f32(g_expert + static_cast<long long>(s_e[j]) * L + i, gg);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(s_coef[j], v[q] * gg[q], acc[q]);
-    }
+    combine_cols8<NB>(y, g_expert, L, i, k, s_rowj, s_e, s_coef, acc);   // slot order
 #pragma unroll
     for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(acc[q]));
     store8_f32(buf + (i - sl.i0), acc);
@@ -1047,7 +1074,7 @@ __global__ void __launch_bounds__(256) swiglu_reduce_nvfp4_kernel(
   const int splits = *splits_dev;
   const int mt = blockIdx.x;
   if (splits <= 1 || mt >= *n_tiles) return;
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) recip[i] = c_e4m3_recip.v[i];
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) recip[i] = g_e4m3_recip.v[i];
   __syncthreads();
   const Tile t = tiles[mt];
   const int cb = blockIdx.y * blockDim.x + threadIdx.x;   // 16-column block of h
@@ -1147,12 +1174,15 @@ cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, c
   const size_t smem = (static_cast<size_t>(L / C) + 256) * sizeof(float);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(combine_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
-    if (e != cudaSuccess) return e;
+    for (auto kern : {combine_nvfp4_kernel<1>, combine_nvfp4_kernel<kCombineBatch>}) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+      if (e != cudaSuccess) return e;
+    }
     attr = true;
   }
-  return launch_pdl_cluster(combine_nvfp4_kernel, dim3(T * C), dim3(kRowThreads), smem, s, C, y, ss_y,
-                            ld_ss, row_of, idx, w, g_expert, L, k, eps, codes, scales, s_row, C);
+  return launch_pdl_cluster(T <= kCombineBatchMaxT ? combine_nvfp4_kernel<kCombineBatch> : combine_nvfp4_kernel<1>,
+                            dim3(T * C), dim3(kRowThreads), smem, s, C, y, ss_y, ld_ss, row_of, idx, w,
+                            g_expert, L, k, eps, codes, scales, s_row, C);
 }
 
 cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool row_scale,
@@ -1271,8 +1301,8 @@ cudaError_t launch_combine(const float* y, const float* ss_y, int ld_ss,
                            __nv_bfloat16* c, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int C = row_split(T, L);
-  return launch_pdl(combine_kernel, dim3(T * C), dim3(kRowThreads), 0, s, y, ss_y, ld_ss, row_of, idx,
-                    w, g_expert, L, k, eps, c, C);
+  return launch_pdl(T <= kCombineBatchMaxT ? combine_kernel<kCombineBatch> : combine_kernel<1>, dim3(T * C),
+                    dim3(kRowThreads), 0, s, y, ss_y, ld_ss, row_of, idx, w, g_expert, L, k, eps, c, C);
 }
 
 cudaError_t launch_postnorm_residual(const void* x, bool x_f32, float* u,
