@@ -103,29 +103,40 @@ __device__ __forceinline__ void store8_f32(float* p, const float (&v)[8]) {   //
   q[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// acc[0, 8) += sum over slots j (in slot order) of coef[j] * y[row[j]][i, i+8) * g[e[j]][i, i+8).
-// The loads of NB slots are issued together, before their multiply-adds.  NB = 4 for few
-// tokens, where the combine is a chain of round trips and more loads in flight shorten it;
-// NB = 1 for many, where the registers NB = 4 takes would halve the CTAs an SM holds.
-constexpr int kCombineBatch = 4;          // slots per batch of loads at few tokens
+constexpr int kCombineBatch = 4;          // slots per batch of loads at few tokens (8 columns)
 constexpr int kCombineBatchMaxT = 512;    // "few": a token per CTA (or per cluster) fills no GPU
-template <int NB>
-__device__ __forceinline__ void combine_cols8(const float* __restrict__ y, const float* __restrict__ g_expert,
-                                              int L, int i, int k, const int* rows, const int* es,
-                                              const float* coef, float (&acc)[8]) {
+
+// acc[0, NC) += sum over slots j (in slot order) of coef[j] * y[row[j]][i, i+NC) * g[e[j]][i, i+NC)
+// (NC = 8 or 16).  The loads of NB slots are issued together, before their multiply-adds.
+// NB > 1 for few tokens, where the combine is a chain of round trips and more loads in
+// flight shorten it; NB = 1 for many, where the registers would halve the CTAs an SM holds.
+template <int NC, int NB>
+__device__ __forceinline__ void combine_cols(const float* __restrict__ y, const float* __restrict__ g_expert,
+                                             int L, int i, int k, const int* rows, const int* es,
+                                             const float* coef, float (&acc)[NC]) {
+  static_assert(NC == 8 || NC == 16, "columns per thread");
   for (int j0 = 0; j0 < k; j0 += NB) {
-    float v[NB][8], gg[NB][8];
+    float v[NB][NC], gg[NB][NC];
 #pragma unroll
     for (int jj = 0; jj < NB; ++jj)
       if (j0 + jj < k) {
-        load8_f32(y + static_cast<long long>(rows[j0 + jj]) * L + i, v[jj]);
-        load8_f32(g_expert + static_cast<long long>(es[j0 + jj]) * L + i, gg[jj]);
+#pragma unroll
+        for (int h = 0; h < NC / 8; ++h) {
+          float a[8], b[8];
+          load8_f32(y + static_cast<long long>(rows[j0 + jj]) * L + i + 8 * h, a);
+          load8_f32(g_expert + static_cast<long long>(es[j0 + jj]) * L + i + 8 * h, b);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            v[jj][8 * h + q] = a[q];
+            gg[jj][8 * h + q] = b[q];
+          }
+        }
       }
 #pragma unroll
     for (int jj = 0; jj < NB; ++jj)
       if (j0 + jj < k) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = fmaf(coef[j0 + jj], v[jj][q] * gg[jj][q], acc[q]);
+        for (int q = 0; q < NC; ++q) acc[q] = fmaf(coef[j0 + jj], v[jj][q] * gg[jj][q], acc[q]);
       }
   }
 }
@@ -687,7 +698,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
   __syncthreads();
   for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    combine_cols8<NB>(y, g_expert, L, i, k, s_row, s_e, s_coef, acc);   // slot order
+    combine_cols<8, NB>(y, g_expert, L, i, k, s_row, s_e, s_coef, acc);   // slot order
     store8_bf16(c + t * L + i, acc);
   }
 }
@@ -976,7 +987,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
   float amax = 0.f;
   for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    combine_cols8<NB>(y, g_expert, L, i, k, s_rowj, s_e, s_coef, acc);   // slot order
+    combine_cols<8, NB>(y, g_expert, L, i, k, s_rowj, s_e, s_coef, acc);   // slot order
 #pragma unroll
     for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(acc[q]));
     store8_f32(buf + (i - sl.i0), acc);
@@ -988,6 +999,275 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
   }
   __syncthreads();
   quantize_row_to(buf, L, sl.i0, sl.i1, s, recip, codes, scales, &s_d, 1);
+  if (C > 1) cluster_sync_all();
+}
+
+// ------------------------------------------------------------------ NVFP4 rows from registers
+// The rows are read and written as float4 chunks spread over the CTA (a warp's loads and
+// stores are contiguous): thread x of TPB handles, for m < NCH, columns
+// i0 + 4 TPB m + 4x .. +3, so the four lanes 4g .. 4g+3 hold one 16-column quantisation block.
+// The row is normalised, reduced and quantised from registers (one pass over the inputs, no
+// shared-memory staging).  Same rule and per-element arithmetic as the staged kernels above;
+// the row reductions run in another order.
+
+// This lane's 4 values of a block held by lanes 4g .. 4g+3 (block positions 4 (lane % 4) ..):
+// the block's E4M3 scale code (in every lane of the group, as in nvfp4_quant16) and this
+// lane's two code bytes (block bytes 2 (lane % 4), +1), low byte first.
+__device__ __forceinline__ uint32_t quant4_group(const float (&v)[4], float six_s, float inv_s, uint32_t& sc) {
+  float a = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  sc = cvt_e4m3(__fdiv_rn(a, six_s));
+  const float r = g_e4m3_recip.v[sc];
+  const uint32_t b0 = cvt_e2m1x2(__fmul_rn(__fmul_rn(v[1], r), inv_s), __fmul_rn(__fmul_rn(v[0], r), inv_s));
+  const uint32_t b1 = cvt_e2m1x2(__fmul_rn(__fmul_rn(v[3], r), inv_s), __fmul_rn(__fmul_rn(v[2], r), inv_s));
+  return b0 | (b1 << 8);
+}
+
+// Stores block b (this lane's group's) into destination row d: the lane's two code bytes, and
+// the scales of the warp's 8 consecutive blocks (lane 0's block a multiple of 8) as two words,
+// from lanes 0 and 16 (four adjacent bytes in both scale layouts).
+__device__ __forceinline__ void store_group(uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                            const QDest& d, int K, int b, uint32_t bytes2, uint32_t sc, int lane) {
+  *reinterpret_cast<uint16_t*>(codes + d.code_row * (K / 2) + b * 8 + 2 * (lane & 3)) = static_cast<uint16_t>(bytes2);
+  uint32_t w = 0u;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) w |= (__shfl_sync(0xffffffffu, sc, (lane & 16) + 4 * q) & 0xffu) << (8 * q);
+  if ((lane & 15) == 0) {
+    const size_t so = d.blk < 0 ? static_cast<size_t>(d.code_row) * (K / 16) + b : blocked_sf_offset(d.blk, d.m, b, K);
+    *reinterpret_cast<uint32_t*>(scales + so) = w;
+  }
+}
+
+// TPB and NCH for a row slice of n columns: 256 threads with n / 1024 chunks each (1, 2, 4 or
+// 8), else one chunk per thread for n = 128, 256 or 512; false when neither fits.
+bool qgroup_shape(int n, int& tpb, int& nch) {
+  if (n % 1024 == 0 && n / 1024 <= 8 && ((n / 1024) & (n / 1024 - 1)) == 0) {
+    tpb = 256;
+    nch = n / 1024;
+    return true;
+  }
+  if (n == 128 || n == 256 || n == 512) {
+    tpb = n / 4;
+    nch = 1;
+    return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void load4(const void* base, bool f32, long long i, float (&v)[4]) {
+  if (f32) {
+    const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  } else {
+    const uint2 q = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + i);
+    const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.x));
+    const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.y));
+    v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+  }
+}
+
+template <int TPB, int NCH>
+__global__ void __launch_bounds__(TPB) prenorm_nvfp4_q_kernel(
+    const void* __restrict__ x, int x_f32, const float* __restrict__ g, int D, float eps,
+    __nv_bfloat16* __restrict__ xa, int xa_cols, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ s_row, unsigned* status2, int C) {
+  griddep_enter();
+  if (status2 != nullptr && blockIdx.x == 0 && threadIdx.x == 0) status2[0] = status2[1] = 0u;
+  __shared__ float red[33];
+  __shared__ float slot_ss, slot_amax;
+  const RowSlice sl = row_slice(D, C);
+  const long long t = sl.t;
+  const int lane = threadIdx.x & 31;
+  float v[NCH][4];
+  float ss = 0.f;
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) load4(x, x_f32, t * D + sl.i0 + 4 * (TPB * m + threadIdx.x), v[m]);
+#pragma unroll
+  for (int m = 0; m < NCH; ++m)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) ss = fmaf(v[m][q], v[m][q], ss);
+  const float rs =
+      rsqrtf(cluster_combine(block_sum(ss, red), &slot_ss, C, false) / static_cast<float>(D) + eps);
+  __nv_bfloat16* row = xa + t * xa_cols;
+  float amax = 0.f;
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    const int e = sl.i0 + 4 * (TPB * m + threadIdx.x);
+    const float4 gg = *reinterpret_cast<const float4*>(g + e);
+    const float gv[4] = {gg.x, gg.y, gg.z, gg.w};
+    float hi[4], lo[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      v[m][q] = v[m][q] * rs * gv[q];
+      amax = fmaxf(amax, fabsf(v[m][q]));
+      hi[q] = bf16_round(v[m][q]);
+      lo[q] = v[m][q] - hi[q];
+    }
+    *reinterpret_cast<uint2*>(row + e) = make_uint2(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]));
+    *reinterpret_cast<uint2*>(row + D + e) = make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
+  }
+  const float s = nvfp4_row_scale(cluster_combine(block_max(amax, red), &slot_amax, C, true));
+  if (sl.c == 0 && threadIdx.x == 0) s_row[t] = s;
+  const float six_s = __fmul_rn(6.f, s), inv_s = __fdiv_rn(1.f, s);
+  const QDest d{t, t / kBM, static_cast<int>(t % kBM)};
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    uint32_t sc;
+    const uint32_t b2 = quant4_group(v[m], six_s, inv_s, sc);
+    store_group(codes, scales, d, D, (sl.i0 + 4 * (TPB * m + threadIdx.x)) / 16, b2, sc, lane);
+  }
+  if (C > 1) cluster_sync_all();
+}
+
+// The pool norm writes each quantised row to k destinations, so its stores dominate: here a
+// thread owns one whole 16-column block (TPB = columns / 16) and stores its 8 code bytes per
+// destination at once; lanes 4i .. 4i+3 hold consecutive blocks, whose scales lane 4i stores as
+// one word.
+__device__ __forceinline__ void store_qblock(uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                             const QDest& d, int K, int b, uint2 q, uint32_t sc, int lane) {
+  *reinterpret_cast<uint2*>(codes + d.code_row * (K / 2) + b * 8) = q;
+  uint32_t w = sc & 0xffu;
+  w |= (__shfl_down_sync(0xffffffffu, sc, 1) & 0xffu) << 8;
+  w |= (__shfl_down_sync(0xffffffffu, sc, 2) & 0xffu) << 16;
+  w |= (__shfl_down_sync(0xffffffffu, sc, 3) & 0xffu) << 24;
+  if ((lane & 3) == 0) {
+    const size_t so = d.blk < 0 ? static_cast<size_t>(d.code_row) * (K / 16) + b : blocked_sf_offset(d.blk, d.m, b, K);
+    *reinterpret_cast<uint32_t*>(scales + so) = w;
+  }
+}
+
+// TPB for a slice of n columns with one block per thread, or 0 when that does not fit.
+int qblock_threads(int n) {
+  if (n % 16) return 0;
+  const int tpb = n / 16;
+  return (tpb == 32 || tpb == 64 || tpb == 128 || tpb == 256 || tpb == 512) ? tpb : 0;
+}
+
+template <int TPB>
+__global__ void __launch_bounds__(TPB) poolnorm_scatter_nvfp4_q_kernel(
+    const float* __restrict__ p, const float* __restrict__ ss_p, int ld_ss, const float* __restrict__ g,
+    const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const int32_t* __restrict__ offsets,
+    const int32_t* __restrict__ tile_base, int L, int k, float eps, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ s_rows, int C) {
+  griddep_enter();
+  __shared__ float red[33];
+  __shared__ float s_rs, slot_amax;
+  __shared__ QDest s_dst[16];
+  const RowSlice sl = row_slice(L, C);
+  const long long t = sl.t;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    const float ss = warp_sum_partials(ss_p + t * ld_ss, ld_ss, lane);
+    if (lane == 0) s_rs = rsqrtf(ss / static_cast<float>(L) + eps);
+  }
+  constexpr int kDstWarp = TPB >= 64 ? 1 : 0;   // the destinations in a second warp when there is one
+  if (threadIdx.x >= 32 * kDstWarp && threadIdx.x < 32 * kDstWarp + k) {
+    const int j = threadIdx.x - 32 * kDstWarp;
+    const int row = row_of[t * k + j];
+    const int e = idx[t * k + j];
+    const int pos = row - offsets[e];
+    s_dst[j] = QDest{row, tile_base[e] + pos / kBM, pos % kBM};
+  }
+  const int i = sl.i0 + threadIdx.x * 16;
+  float v[16], gg[16];
+  {
+    float a[8], b[8];
+    load8_f32(p + t * L + i, a);
+    load8_f32(p + t * L + i + 8, b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      v[j] = a[j];
+      v[8 + j] = b[j];
+    }
+    load8_f32(g + i, a);
+    load8_f32(g + i + 8, b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      gg[j] = a[j];
+      gg[8 + j] = b[j];
+    }
+  }
+  __syncthreads();
+  const float rs = s_rs;
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    v[j] = v[j] * rs * gg[j];
+    amax = fmaxf(amax, fabsf(v[j]));
+  }
+  const float s = nvfp4_row_scale(cluster_combine(block_max(amax, red), &slot_amax, C, true));
+  if (sl.c == 0 && threadIdx.x < k) s_rows[s_dst[threadIdx.x].code_row] = s;
+  uint2 q;
+  const uint32_t sc = nvfp4_quant16(v, __fmul_rn(6.f, s), __fdiv_rn(1.f, s), g_e4m3_recip.v, q);
+  for (int j = 0; j < k; ++j) store_qblock(codes, scales, s_dst[j], L, i / 16, q, sc, lane);
+  if (C > 1) cluster_sync_all();
+}
+
+template <int TPB, int NCH, int NB>
+__global__ void __launch_bounds__(TPB) combine_nvfp4_q_kernel(
+    const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
+    const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const float* __restrict__ w,
+    const float* __restrict__ g_expert, int L, int k, float eps, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, float* __restrict__ s_row, int C) {
+  griddep_enter();
+  __shared__ float red[33];
+  __shared__ float s_coef[16], slot_amax;
+  __shared__ int s_rowj[16], s_e[16];
+  const RowSlice sl = row_slice(L, C);
+  const long long t = sl.t;
+  const int lane = threadIdx.x & 31;
+  for (int j = threadIdx.x >> 5; j < k; j += TPB / 32) {   // a warp per slot
+    const int row = row_of[t * k + j];
+    const float ss = warp_sum_partials(ss_y + static_cast<long long>(row) * ld_ss, ld_ss, lane);
+    if (lane == 0) {
+      s_coef[j] = w[t * k + j] * rsqrtf(ss / static_cast<float>(L) + eps);
+      s_rowj[j] = row;
+      s_e[j] = idx[t * k + j];
+    }
+  }
+  __syncthreads();
+  float acc[NCH][4];
+#pragma unroll
+  for (int m = 0; m < NCH; ++m)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
+  for (int j0 = 0; j0 < k; j0 += NB) {   // slot order; the loads of NB slots issued together
+    float yv[NB][NCH][4], gv[NB][NCH][4];
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj)
+      if (j0 + jj < k) {
+#pragma unroll
+        for (int m = 0; m < NCH; ++m) {
+          const int e = sl.i0 + 4 * (TPB * m + threadIdx.x);
+          load4(y, true, static_cast<long long>(s_rowj[j0 + jj]) * L + e, yv[jj][m]);
+          load4(g_expert, true, static_cast<long long>(s_e[j0 + jj]) * L + e, gv[jj][m]);
+        }
+      }
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj)
+      if (j0 + jj < k) {
+#pragma unroll
+        for (int m = 0; m < NCH; ++m)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[m][q] = fmaf(s_coef[j0 + jj], yv[jj][m][q] * gv[jj][m][q], acc[m][q]);
+      }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int m = 0; m < NCH; ++m)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) amax = fmaxf(amax, fabsf(acc[m][q]));
+  const float s = nvfp4_row_scale(cluster_combine(block_max(amax, red), &slot_amax, C, true));
+  if (sl.c == 0 && threadIdx.x == 0) s_row[t] = s;
+  const float six_s = __fmul_rn(6.f, s), inv_s = __fdiv_rn(1.f, s);
+  const QDest d{t, t / kBM, static_cast<int>(t % kBM)};
+#pragma unroll
+  for (int m = 0; m < NCH; ++m) {
+    uint32_t sc;
+    const uint32_t b2 = quant4_group(acc[m], six_s, inv_s, sc);
+    store_group(codes, scales, d, L, (sl.i0 + 4 * (TPB * m + threadIdx.x)) / 16, b2, sc, lane);
+  }
   if (C > 1) cluster_sync_all();
 }
 
@@ -1134,6 +1414,15 @@ cudaError_t launch_prenorm_nvfp4(const void* x, bool x_f32, const float* g_pre, 
                                  uint8_t* scales, float* s_row, unsigned* status2, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int C = row_split(T, D);
+  int tpb = 0, nch = 0;
+  if (qgroup_shape(D / C, tpb, nch)) {   // rows from registers, coalesced chunks
+#define LMOE_Q(TPB, NCH)                                                                                \
+  if (tpb == TPB && nch == NCH)                                                                         \
+    return launch_pdl_cluster(prenorm_nvfp4_q_kernel<TPB, NCH>, dim3(T * C), dim3(TPB), 0, s, C, x,     \
+                              x_f32 ? 1 : 0, g_pre, D, eps, xa, xa_cols, codes, scales, s_row, status2, C);
+    LMOE_Q(256, 1) LMOE_Q(256, 2) LMOE_Q(256, 4) LMOE_Q(256, 8) LMOE_Q(128, 1) LMOE_Q(64, 1) LMOE_Q(32, 1)
+#undef LMOE_Q
+  }
   const size_t smem = (static_cast<size_t>(D / C) + 256) * sizeof(float);
   static bool attr = false;
   if (!attr) {
@@ -1153,6 +1442,16 @@ cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int
                                           cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int C = row_split(T, L);
+  switch (qblock_threads(L / C)) {   // one quantisation block per thread, from registers
+#define LMOE_Q(TPB)                                                                                     \
+  case TPB:                                                                                             \
+    return launch_pdl_cluster(poolnorm_scatter_nvfp4_q_kernel<TPB>, dim3(T * C), dim3(TPB), 0, s, C, p, \
+                              ss_p, ld_ss, g_pool, row_of, idx, offsets, tile_base, L, k, eps, codes,   \
+                              scales, s_rows, C);
+    LMOE_Q(32) LMOE_Q(64) LMOE_Q(128) LMOE_Q(256) LMOE_Q(512)
+#undef LMOE_Q
+    default: break;
+  }
   const size_t smem = (static_cast<size_t>(L / C) + 256) * sizeof(float);
   static bool attr = false;
   if (!attr) {
@@ -1171,6 +1470,17 @@ cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, c
                                  float* s_row, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int C = row_split(T, L);
+  const bool few = T <= kCombineBatchMaxT;
+  int tpb = 0, nch = 0;
+  if (qgroup_shape(L / C, tpb, nch)) {   // rows from registers, coalesced chunks
+#define LMOE_Q(TPB, NCH)                                                                                \
+  if (tpb == TPB && nch == NCH)                                                                         \
+    return launch_pdl_cluster(few ? combine_nvfp4_q_kernel<TPB, NCH, 2> : combine_nvfp4_q_kernel<TPB, NCH, 1>, \
+                              dim3(T * C), dim3(TPB), 0, s, C, y, ss_y, ld_ss, row_of, idx, w, g_expert, \
+                              L, k, eps, codes, scales, s_row, C);
+    LMOE_Q(256, 1) LMOE_Q(256, 2) LMOE_Q(256, 4) LMOE_Q(256, 8) LMOE_Q(128, 1) LMOE_Q(64, 1) LMOE_Q(32, 1)
+#undef LMOE_Q
+  }
   const size_t smem = (static_cast<size_t>(L / C) + 256) * sizeof(float);
   static bool attr = false;
   if (!attr) {
@@ -1180,7 +1490,7 @@ cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, c
     }
     attr = true;
   }
-  return launch_pdl_cluster(T <= kCombineBatchMaxT ? combine_nvfp4_kernel<kCombineBatch> : combine_nvfp4_kernel<1>,
+  return launch_pdl_cluster(few ? combine_nvfp4_kernel<kCombineBatch> : combine_nvfp4_kernel<1>,
                             dim3(T * C), dim3(kRowThreads), smem, s, C, y, ss_y, ld_ss, row_of, idx, w,
                             g_expert, L, k, eps, codes, scales, s_row, C);
 }

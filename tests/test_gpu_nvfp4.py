@@ -68,6 +68,7 @@ SHAPES = [  # (T, D, L, E, I, k)
     (130, 256, 512, 16, 512, 4),
     (257, 512, 256, 6, 256, 6),
     (2, 2048, 1024, 8, 512, 2),     # rows split over clusters of 8 CTAs
+    (20, 4096, 4096, 4, 256, 2),    # clusters of 8, one quantisation block per thread
 ]
 # few rows and a long K: the grouped GEMMs split K (count picked on the device); gate/up
 # splits in the first two, down in the last
