@@ -72,8 +72,8 @@ constexpr int kPoolerSms = 100;
 // ones); below it the tiles hold few rows and the smaller shared-memory footprint lets the next
 // kernel's CTAs become resident beside the GEMM's
 constexpr long long kXposeRows = 64;
-int dense_splits(int T, int N, int bn, int num_kb, int min_kb, int sms = kSplitSms) {
-  const long long tiles = static_cast<long long>((T + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+int dense_splits(int T, int N, int bn, int num_kb, int min_kb, int sms = kSplitSms, int tile_rows = kBM) {
+  const long long tiles = static_cast<long long>((T + tile_rows - 1) / tile_rows) * ((N + bn - 1) / bn);
   if (tiles == 0 || tiles * 2 >= sms) return 1;
   long long sp = sms / tiles;
   if (sp > num_kb / min_kb) sp = num_kb / min_kb;
@@ -83,13 +83,21 @@ int dense_splits(int T, int N, int bn, int num_kb, int min_kb, int sms = kSplitS
 
 struct DenseSplits {
   int router, pooler, unpool;
+  int router_mh;   // M halves of the router's tiles
 };
+// The router's B (all experts' rows, K = 2D or 3D) is re-read by every M tile, so its tiles are
+// bound by what an SM can take in; 256-row tiles, split along K to keep every SM busy, halve
+// that traffic per row.  Measured on GB300 (E = 256, D = 8192): faster at 4096 tokens (the
+// router stage 58 -> 52 us), slower at 1024 (more splits than K blocks allow) and at 16384
+// (2 splits: the partials' round trip costs more than the tiles save).
+constexpr int kRouterWideMinT = 2048, kRouterWideMaxT = 8192;
 DenseSplits dense_split_plan(const lmoe_config* c) {
   const bool f32w = c->weight_dtype == LMOE_F32, fp4 = c->weight_dtype == LMOE_NVFP4;
   const int D = c->d_model, L = c->d_latent;
   const int xa_cols = (f32w ? 3 : 2) * D, wsplit = f32w ? 2 : 1;
   DenseSplits d;
-  d.router = dense_splits(c->T, c->n_experts, kBNWide, xa_cols / kBK, 4);
+  d.router_mh = c->T >= kRouterWideMinT && c->T <= kRouterWideMaxT ? 2 : 1;
+  d.router = dense_splits(c->T, c->n_experts, kBNWide, xa_cols / kBK, 4, kSplitSms, kBM * d.router_mh);
   if (fp4) {
     d.pooler = dense_splits(c->T, L, kBNFp4, D / 256, 2, kPoolerSms);
     d.unpool = dense_splits(c->T, D, kBNFp4, L / 256, 2);
@@ -549,11 +557,10 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
 
   // S5 pooler, enqueued on stream `ps`: NVFP4 p = s_x * s_W * (Q(xn) . W_pool^T) (block-scaled
   // FP4 MMA), else p = xn_hi . W_pool^T; both with row partial sums of squares
-  // BF16 GEMMs over many rows take 256-row tiles (two MMAs share each weight tile): dense
-  // ones from 512 rows when not split along K, grouped ones at >= 256 rows per expert on
-  // average (they then walk the table of 256-row tiles)
-  // (256-row tiles only where they still give every SM a tile: the router's single N tile
-  // at T = 16384 would leave 88 of 152 SMs idle)
+  // BF16 GEMMs over many rows take 256-row tiles (two MMAs share each weight tile): the
+  // pooler and unpooler from 512 rows when not split along K and where the 256-row tiles
+  // still give every SM one, grouped ones at >= 256 rows per expert on average (they then
+  // walk the table of 256-row tiles); the router has its own plan (dense_split_plan)
   auto dense_mh_n = [&](int splits, int n_tiles) {
     return splits <= 1 && T >= 4 * kBM && 1LL * cdiv(T, 2 * kBM) * n_tiles >= kSplitSms ? 2 : 1;
   };
@@ -605,7 +612,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   // split-K partials when they are few (one launch less on the chain)
   const bool fused_route = route_small_fits(T, k, E) && (ev == nullptr || ev[LMOE_STAGE_PERMUTE] == nullptr);
   const int rsplits = fused_route && dsp.router > 1 && 1LL * T * dsp.router * E <= 65536 ? dsp.router : 1;
-  const int router_mh = dense_mh_n(dsp.router, cdiv(E, kBNWide));
+  const int router_mh = dsp.router_mh;
   st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
                 xa_cols / kBK, nullptr, nullptr, cdiv(T, kBM * router_mh), logits, L.ld_logits, nullptr, 0,
                 err, budget, s, T, dsp.router, partial, router_mh, rsplits == 1);

@@ -88,6 +88,7 @@ SHAPES = [  # (T, D, L, E, I, k): ragged T, N tails of the 256-wide tiles, k = 1
     (64, 1024, 512, 64, 768, 8),
     (2, 2048, 1024, 16, 512, 4),    # rows split over clusters of 8 CTAs
     (600, 512, 256, 4, 384, 2),     # 256-row tiles, dense and grouped, ragged last tiles
+    (2100, 512, 256, 8, 256, 2),    # router in 256-row tiles split along K, ragged last tile
 ]
 
 
