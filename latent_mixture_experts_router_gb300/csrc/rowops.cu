@@ -355,7 +355,6 @@ __global__ void __launch_bounds__(kTopkWarps * 32) topk_kernel(
 // Pairs (t, j) are numbered i = t*k + j.  Expert e owns rows [off[e], off[e] + cnt[e])
 // of the expert-contiguous matrices, in increasing i (stable, so deterministic).
 constexpr int kPermThreads = 256;
-constexpr int kPermPerThread = 16;
 
 // Order of the table of 256-row tiles (grouped BF16 GEMMs over many rows).  An expert's tiles
 // with more than 128 live rows ("full": MMA-bound, and those of one expert share its weights
@@ -441,40 +440,54 @@ __global__ void __launch_bounds__(kPermThreads) expert_scatter_kernel(
     tiles[tile0 + m] = Tile{e, off + m * kBM, min(kBM, cnt - m * kBM), 0};
   if (tiles2 != nullptr) write_tiles2(tiles2, e, off, cnt, f0, l0, nf, nl, threadIdx.x, kPermThreads);
   if (cnt == 0) return;
-  int running = 0;
-  for (int base = 0; base < n; base += kPermThreads * kPermPerThread) {
-    const int i0 = base + threadIdx.x * kPermPerThread;
-    uint32_t mask = 0;
+  // The pairs split into one contiguous segment per warp (a multiple of 128 pairs, so that a
+  // lane reads four at a time): a first pass counts the segment's pairs of expert e, a scan
+  // over the warps gives each segment its first row, and a second pass ranks the pairs in
+  // order (lane-major, four per lane) within each 128-pair chunk; one block barrier in all.
+  constexpr int kWarps = kPermThreads / 32;
+  const int seg = (n + kWarps * 128 - 1) / (kWarps * 128) * 128;
+  const int s0 = warp * seg, s1 = min(n, s0 + seg);
+  const bool vec = (reinterpret_cast<uintptr_t>(idx) & 15u) == 0;   // idx may come from a caller
+  auto match4 = [&](int c) {   // bit q: pair c + 4 lane + q belongs to expert e
+    const int i = c + 4 * lane;
+    uint32_t m = 0;
+    if (vec && i + 3 < n) {
+      const int4 v = *reinterpret_cast<const int4*>(idx + i);
+      m = (v.x == e ? 1u : 0u) | (v.y == e ? 2u : 0u) | (v.z == e ? 4u : 0u) | (v.w == e ? 8u : 0u);
+    } else {
 #pragma unroll
-    for (int q = 0; q < kPermPerThread; ++q) {
-      const int i = i0 + q;
-      if (i < n && idx[i] == e) mask |= 1u << q;
+      for (int q = 0; q < 4; ++q)
+        if (i + q < n && idx[i + q] == e) m |= 1u << q;
     }
-    const int mine = __popc(mask);
-    int incl = mine;  // inclusive warp scan
+    return m;
+  };
+  int c_w = 0;
+  for (int c = s0; c < s1; c += 128) c_w += __popc(match4(c));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c_w += __shfl_xor_sync(0xffffffffu, c_w, o);
+  if (lane == 0) wsum[warp] = c_w;
+  __syncthreads();
+  int r0 = off;
+  for (int q = 0; q < warp; ++q) r0 += wsum[q];
+  for (int c = s0; c < s1; c += 128) {
+    uint32_t m = match4(c);
+    const int mine = __popc(m);
+    int incl = mine;   // inclusive scan over the lanes
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    int before = 0, total = 0;
-    for (int q = 0; q < kPermThreads / 32; ++q) {
-      before += (q < warp) ? wsum[q] : 0;
-      total += wsum[q];
-    }
-    int r = off + running + before + incl - mine;
-    while (mask) {
-      const int q = __ffs(mask) - 1;
-      mask &= mask - 1;
-      const int i = i0 + q;
+    int r = r0 + incl - mine;
+    while (m) {
+      const int q = __ffs(m) - 1;
+      m &= m - 1;
+      const int i = c + 4 * lane + q;
       row_of[i] = r;
       tok_of[r] = i / k;
       ++r;
     }
-    running += total;
-    __syncthreads();
+    r0 += __shfl_sync(0xffffffffu, incl, 31);
   }
 }
 

@@ -115,6 +115,33 @@ def test_zero_tokens(cuda):
     assert lm.lmoe_check_status(blk.config(0), blk._ws)[0] == 0
 
 
+@pytest.mark.parametrize("weights,T", [("bf16", 8), ("nvfp4", 8), ("nvfp4", 300)])
+def test_capturable_in_cuda_graph(cuda, weights, T):
+    # the forward enqueues work only (no host synchronisation, no allocation), side stream
+    # included, so it can be captured once and replayed, as a decode loop does
+    w = workloads.Workload(f"graph_{weights}_{T}", T=T, D=512, L=256, E=16, I=256, k=4, weights=weights,
+                           routing="hot4")
+    inp = workloads.make_inputs(w, cuda)
+    blk = make_block(inp)
+    out = torch.empty(T, w.D, dtype=torch.float32, device=cuda)
+    ex = {"forced_idx": inp.forced_idx} if inp.forced_idx is not None else {}
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        blk.forward(inp.x, out=out, **ex)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        blk.forward(inp.x, out=out, **ex)
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    import latent_mixture_experts_router_gb300 as lm
+    assert lm.lmoe_check_status(blk.config(T, w.act, "f32"), blk._ws)[0] == 0
+
+
 def test_deterministic_and_token_order_equivariant(cuda):
     w = workloads.Workload("det", T=300, D=512, L=256, E=16, I=256, k=4)
     inp = workloads.make_inputs(w, cuda)

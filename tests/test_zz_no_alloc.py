@@ -60,6 +60,25 @@ def test_no_alloc_permutation_matches_forward(lm, shapes):
         assert np.array_equal(tok_of, v["tok_of"])
 
 
+@pytest.mark.parametrize("misaligned", [False, True], ids=["aligned", "4-byte-aligned"])
+def test_no_alloc_permutation_many_pairs(lm, misaligned):
+    # 24000 pairs: several 128-pair chunks per warp segment and a ragged tail; an id array
+    # that is only 4-byte aligned takes the scalar loads
+    from gpu_util import expected_permutation
+    T, k, E = 3000, 8, 64
+    g = torch.Generator().manual_seed(11)
+    ids = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).to(torch.int32)
+    buf = torch.empty(T * k + 1, dtype=torch.int32, device="cuda:0")
+    idx = (buf[1:] if misaligned else buf[:-1]).view(T, k)
+    idx.copy_(ids.to("cuda:0"))
+    assert (idx.data_ptr() % 16 != 0) == misaligned
+    counts, offsets_ref, row_ref, tok_ref = expected_permutation(ids.numpy(), E)
+    offsets, row_of, tok_of = _noalloc_call(lm, idx, E)
+    assert np.array_equal(offsets, offsets_ref)
+    assert np.array_equal(row_of, row_ref)
+    assert np.array_equal(tok_of, tok_ref)
+
+
 def test_no_alloc_rejects_sizes_beyond_its_scratch(lm):
     idx = torch.zeros((70000, 1), dtype=torch.int32, device="cuda:0")
     with pytest.raises(lm.LmoeError) as ei:
