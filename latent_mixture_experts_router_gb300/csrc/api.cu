@@ -44,6 +44,7 @@ struct Layout {
   long long partial_pool;  // the pooler's own (it may run beside the router on a side stream)
   long long splits_dev; // [2] split counts the grouped NVFP4 GEMMs chose (gate/up, down)
   long long tiles2, n_tiles2;  // table of 256-row tiles (BF16 grouped GEMMs of many rows)
+  long long perm_hist, perm_base;  // [chunks][E] each: the chunked permutation of many pairs
   // fp32-weight mode: bf16 copies of the weights
   long long w_router, w_pool, w_gate, w_up, w_down, w_unpool;
   long long x_stage, out_stage, host_io_total;
@@ -165,6 +166,8 @@ void make_layout(const lmoe_config* c, Layout* L) {
   L->tile_base = take(E * 4);
   L->tiles2 = take(static_cast<size_t>(L->max_tiles2) * sizeof(Tile));
   L->n_tiles2 = take(4);
+  L->perm_hist = take(static_cast<size_t>(perm_chunks(R)) * E * 4);
+  L->perm_base = take(static_cast<size_t>(perm_chunks(R)) * E * 4);
   P.p = take(T * Ld * 4);
   P.ss_p = take(T * L->ld_ss_p * 4);
   const bool fp4 = c->weight_dtype == LMOE_NVFP4;
@@ -636,7 +639,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                           ex ? ex->topk_idx_out : nullptr, ex ? ex->topk_w_out : nullptr, err, s));
     LMOE_MARK(LMOE_STAGE_PERMUTE);
     LMOE_CUDA(launch_permute(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, s,
-                             tile_base, tiles2, n_tiles2));
+                             tile_base, tiles2, n_tiles2, static_cast<int32_t*>(at(L.perm_hist)),
+                             static_cast<int32_t*>(at(L.perm_base))));
   }
   if (ex && ex->near_tie_count_out)
     LMOE_CUDA(cudaMemcpyAsync(ex->near_tie_count_out, near_tie, 4, cudaMemcpyDeviceToDevice, s));

@@ -213,10 +213,16 @@ cudaError_t launch_topk(const float* logits, int ld, const float* bias, const in
                         int T, int E, int k, int32_t* idx, float* w, int32_t* near_tie,
                         int32_t* idx_copy, float* w_copy, unsigned* err, cudaStream_t s);
 // tile_base (optional, [E]): first M tile of each expert in the tile table
+// chunk_hist / chunk_base: [perm_chunks(T k)][E] int32 scratch; with them, from
+// kPermChunkedMinPairs pairs the permutation runs chunked (histogram, scan, rank kernels)
+// instead of one CTA per expert reading every id
+constexpr int kPermChunkedMinPairs = 16384;   // below: too few chunks for the GPU (measured at 8192: slower)
+int perm_chunks(long long pairs);
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
                            int32_t* n_tiles, cudaStream_t s, int32_t* tile_base = nullptr,
-                           Tile* tiles2 = nullptr, int32_t* n_tiles2 = nullptr);
+                           Tile* tiles2 = nullptr, int32_t* n_tiles2 = nullptr,
+                           int32_t* chunk_hist = nullptr, int32_t* chunk_base = nullptr);
 cudaError_t launch_poolnorm_scatter(const float* p, const float* ss_p, int ld_ss,
                                     const float* g_pool, const int32_t* row_of, int T, int L,
                                     int k, float eps, __nv_bfloat16* xe, cudaStream_t s);

@@ -659,6 +659,127 @@ __global__ void __launch_bounds__(kRouteThreads) route_small_kernel(
   }
 }
 
+// ------------------------------------------------------------------ permutation of many pairs
+// With many pairs the per-expert CTAs above all read the whole id array at once.  Instead the
+// pairs are cut into chunks of kPermChunk: each chunk CTA histograms its ids in shared memory
+// (perm_hist), one CTA turns the chunk histograms into per-chunk bases and the expert offsets
+// and tile tables (perm_scan), and each chunk CTA ranks its pairs (perm_rank): warp w of the
+// chunk takes 32 consecutive pairs at a time, ranks them among the warp's pairs of the same
+// expert by match-any ballots, and adds the counts of the earlier warps, earlier chunks and
+// earlier experts.  Same (expert, pair index) order, so the same outputs as the path above.
+constexpr int kPermChunk = 2048;           // 8 warps x 8 rounds x 32 pairs
+constexpr int kPermScanThreads = 1024;
+
+__global__ void __launch_bounds__(kPermThreads) perm_hist_kernel(const int32_t* __restrict__ idx, int n, int E,
+                                                                 int32_t* __restrict__ hist) {
+  griddep_enter();
+  extern __shared__ int h_sh[];   // [E]
+  for (int e = threadIdx.x; e < E; e += kPermThreads) h_sh[e] = 0;
+  __syncthreads();
+  const long long c0 = static_cast<long long>(blockIdx.x) * kPermChunk;
+#pragma unroll
+  for (int j = 0; j < kPermChunk / kPermThreads; ++j) {
+    const long long i = c0 + j * kPermThreads + threadIdx.x;
+    if (i < n) atomicAdd(&h_sh[idx[i]], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kPermThreads) hist[static_cast<long long>(blockIdx.x) * E + e] = h_sh[e];
+}
+
+__global__ void __launch_bounds__(kPermScanThreads) perm_scan_kernel(
+    const int32_t* __restrict__ hist, int chunks, int E, int32_t* __restrict__ base,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, Tile* __restrict__ tiles,
+    int32_t* __restrict__ n_tiles, int32_t* __restrict__ tile_base, Tile* __restrict__ tiles2,
+    int32_t* __restrict__ n_tiles2) {
+  griddep_enter();
+  __shared__ int scan_sh[64];
+  // thread-contiguous runs of experts, so that thread order is expert order in the scans
+  const int per = (E + kPermScanThreads - 1) / kPermScanThreads;
+  const int e0 = min(E, static_cast<int>(threadIdx.x) * per), e1 = min(E, e0 + per);
+  int a = 0, b = 0, f = 0, l = 0;
+  for (int e = e0; e < e1; ++e) {
+    int run = 0;   // chunk bases of expert e: pairs of e in the earlier chunks
+    for (int g = 0; g < chunks; ++g) {
+      const long long q = static_cast<long long>(g) * E + e;
+      const int c = hist[q];
+      base[q] = run;
+      run += c;
+    }
+    counts[e] = run;
+    int fe, le;
+    tile2_counts(run, fe, le);
+    a += run;
+    b += (run + kBM - 1) / kBM;
+    f += fe;
+    l += le;
+  }
+  int ta, tb, nf, nl;
+  block_scan2(a, b, scan_sh, &ta, &tb);
+  block_scan2(f, l, scan_sh, &nf, &nl);
+  for (int e = e0; e < e1; ++e) {
+    const int c = counts[e], nt = (c + kBM - 1) / kBM;   // this thread's own store above
+    int fe, le;
+    tile2_counts(c, fe, le);
+    offsets[e] = a;
+    if (tile_base != nullptr) tile_base[e] = b;
+    for (int m = 0; m < nt; ++m) tiles[b + m] = Tile{e, a + m * kBM, min(kBM, c - m * kBM), 0};
+    if (tiles2 != nullptr) write_tiles2(tiles2, e, a, c, f, l, nf, nl, 0, 1);
+    a += c;
+    b += nt;
+    f += fe;
+    l += le;
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = ta;
+    *n_tiles = tb;
+    if (n_tiles2 != nullptr) *n_tiles2 = nf + nl;
+  }
+}
+
+__global__ void __launch_bounds__(kPermThreads) perm_rank_kernel(
+    const int32_t* __restrict__ idx, int n, int k, int E, const int32_t* __restrict__ base,
+    const int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, int32_t* __restrict__ tok_of) {
+  griddep_enter();
+  extern __shared__ int wc_sh[];   // [8 warps][E]: pairs of each expert the warp has ranked
+  constexpr int kWarps = kPermThreads / 32, kRounds = kPermChunk / kPermThreads;
+  for (int q = threadIdx.x; q < kWarps * E; q += kPermThreads) wc_sh[q] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long c0 = static_cast<long long>(blockIdx.x) * kPermChunk + warp * (kPermChunk / kWarps);
+  int* wc = wc_sh + warp * E;
+  int rank[kRounds], ex[kRounds];
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const long long i = c0 + r * 32 + lane;
+    const int e = i < n ? idx[i] : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    rank[r] = (e >= 0 ? wc[e] : 0) + __popc(peers & ((1u << lane) - 1u));
+    ex[r] = e;
+    __syncwarp();   // every lane has read the count before the group's first lane adds to it
+    if (e >= 0 && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kPermThreads) {   // exclusive prefix over the warps
+    int run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wc_sh[w * E + e];
+      wc_sh[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int e = ex[r];
+    if (e < 0) continue;
+    const long long i = c0 + r * 32 + lane;
+    const int row = offsets[e] + base[static_cast<long long>(blockIdx.x) * E + e] + wc[e] + rank[r];
+    row_of[i] = row;
+    tok_of[row] = static_cast<int32_t>(i / k);
+  }
+}
+
 // ------------------------------------------------------------------ pool norm + scatter
 __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_kernel(
     const float* __restrict__ p, const float* __restrict__ ss_p, int ld_ss,
@@ -1597,11 +1718,25 @@ cudaError_t launch_route_small(float* logits, int ld, const float* rpart, int rs
                     n_tiles, tile_base, tiles2, n_tiles2);
 }
 
+int perm_chunks(long long pairs) { return static_cast<int>((pairs + kPermChunk - 1) / kPermChunk); }
+
 cudaError_t launch_permute(const int32_t* idx, int T, int k, int E, int32_t* counts,
                            int32_t* offsets, int32_t* row_of, int32_t* tok_of, Tile* tiles,
                            int32_t* n_tiles, cudaStream_t s, int32_t* tile_base, Tile* tiles2,
-                           int32_t* n_tiles2) {
+                           int32_t* n_tiles2, int32_t* chunk_hist, int32_t* chunk_base) {
   const int n = T * k;
+  if (chunk_hist != nullptr && chunk_base != nullptr && n >= kPermChunkedMinPairs) {
+    const int chunks = perm_chunks(n);
+    const size_t smem_h = static_cast<size_t>(E) * 4, smem_r = static_cast<size_t>(kPermThreads / 32) * E * 4;
+    cudaError_t e = launch_pdl(perm_hist_kernel, dim3(chunks), dim3(kPermThreads), smem_h, s, idx, n, E,
+                               chunk_hist);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(perm_scan_kernel, dim3(1), dim3(kPermScanThreads), 0, s, chunk_hist, chunks, E,
+                   chunk_base, counts, offsets, tiles, n_tiles, tile_base, tiles2, n_tiles2);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(perm_rank_kernel, dim3(chunks), dim3(kPermThreads), smem_r, s, idx, n, k, E,
+                      chunk_base, offsets, row_of, tok_of);
+  }
   cudaError_t e = launch_pdl(expert_count_kernel, dim3(E), dim3(kPermThreads), 0, s, idx, n,
                              counts);
   if (e != cudaSuccess) return e;

@@ -89,6 +89,7 @@ SHAPES = [  # (T, D, L, E, I, k): ragged T, N tails of the 256-wide tiles, k = 1
     (2, 2048, 1024, 16, 512, 4),    # rows split over clusters of 8 CTAs
     (600, 512, 256, 4, 384, 2),     # 256-row tiles, dense and grouped, ragged last tiles
     (2100, 512, 256, 8, 256, 2),    # router in 256-row tiles split along K, ragged last tile
+    (2100, 512, 256, 64, 256, 8),   # 16800 pairs: the chunked permutation
 ]
 
 
