@@ -321,7 +321,7 @@ lmoe_status run_gemm(EpiKind epi, const void* A, long long a_rows, long long a_c
   a.partial = partial;
   a.max_tiles = m_tiles;
   a.n_groups = static_cast<int>(b_rows / N);
-  a.xpose = rows_per_b >= kXposeRows ? 1 : 0;
+  a.xpose = epi != kEpiSwiGLU && rows_per_b >= kXposeRows ? 1 : 0;   // fp32 outputs only
   LMOE_CUDA(launch_gemm(epi, ta, tb, tb2, a, m_tiles, s, m_halves));
   if (splits > 1 && reduce)   // else the consumer sums the partials
     LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
