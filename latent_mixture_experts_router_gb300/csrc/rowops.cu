@@ -11,7 +11,8 @@
 //   topk               softmax over all experts, top-k (ties -> lower index),
 //                      weights renormalised over the k
 //   permute            expert-contiguous order of the (token, slot) pairs:
-//                      per-expert histogram, exclusive scan, stable scatter
+//                      per-expert histogram, exclusive scan, stable scatter (one CTA
+//                      per expert, or chunked for many pairs; same order either way)
 //   poolnorm_scatter   h0 = p / sqrt(mean(p^2) + eps) * g_pool, copied to the
 //                      k expert-contiguous rows of the token
 //   combine            c = sum_j w_j * g_expert[e_j] * y_j / sqrt(mean(y_j^2) + eps)
