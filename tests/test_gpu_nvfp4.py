@@ -94,6 +94,22 @@ def test_nvfp4_block_parity(cuda, T, D, L, E, I, k):
     assert rep.ok, str(rep)
 
 
+@pytest.mark.parametrize("T,D,L,E,I,k", [(130, 1024, 512, 8, 256, 2), (5, 2048, 1024, 8, 512, 2)])
+def test_nvfp4_f32_activations(cuda, T, D, L, E, I, k):
+    # fp32 x into the NVFP4 path: the pre-norm reads float4 chunks instead of bf16 ones
+    w = workloads.Workload(f"fp4x32_{T}_{D}", T=T, D=D, L=L, E=E, I=I, k=k, weights="nvfp4", act="f32",
+                           seed=T % 5)
+    inp = workloads.make_inputs(w, cuda)
+    assert inp.x.dtype == torch.float32
+    out, idx, blk, cfg = run(inp)
+    P = oracle.params_from_inputs(inp)
+    x = inp.x.double().cpu().numpy()
+    tr = oracle.Trace()
+    ref = oracle.forward_batched(x, P, k, trace=tr)
+    rep = compare_block(out.cpu().numpy(), idx.cpu().numpy(), x, P, k, TOL_NVFP4, tr=tr, ref=ref)
+    assert rep.ok, str(rep)
+
+
 @pytest.mark.parametrize("T,D,L,E,I,k", SPLIT_SHAPES)
 def test_nvfp4_grouped_split_parity(cuda, T, D, L, E, I, k):
     import latent_mixture_experts_router_gb300 as lm
