@@ -351,6 +351,7 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
         break;
       }
       tc_fence_after();
+      bool released = false;   // the accumulator buffer handed back before the stores
       const bool row_ok = r < nrows;
       const long long grow = static_cast<long long>(row0) + r;
       const int n0 = ntile * BN;
@@ -392,6 +393,44 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
         float* prow = walk.splits > 1
                           ? args.partial + (static_cast<long long>(id % walk.splits) * args.M + grow) * 2 * args.N
                           : nullptr;
+        if (prow == nullptr) {
+          // The whole accumulator slice is read first and the buffer handed back to the MMA
+          // issuer before the SwiGLU, the requantisation and the stores: there is one gate+up
+          // buffer, so the next tile's MMAs would otherwise wait for all of that (measured at
+          // prefill: gate/up 0.90 ms, 0.78 ms in a timing build without the epilogue's work).
+          constexpr int kCh = kCols / 32;
+          uint32_t g[kCh][32], u[kCh][32];
+#pragma unroll
+          for (int ch = 0; ch < kCh; ++ch) {
+            tmem_ld_32cols(tq + c_lo + 32 * ch, g[ch]);
+            tmem_ld_32cols(tq + BN + c_lo + 32 * ch, u[ch]);
+          }
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          released = true;
+#pragma unroll
+          for (int ch = 0; ch < kCh; ++ch) {
+            const int col = n0 + c_lo + 32 * ch;
+            if (!(row_ok && col + 32 <= args.N)) continue;
+            uint2 q[2];
+            uint32_t sc[2];
+#pragma unroll
+            for (int blk = 0; blk < 2; ++blk) {
+              float h[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float a = __uint_as_float(g[ch][blk * 16 + i]) * ag;
+                h[i] = __fdividef(a, 1.f + __expf(-a)) * (__uint_as_float(u[ch][blk * 16 + i]) * au);  // silu(a) * b
+              }
+              sc[blk] = nvfp4_quant16(h, 6.f, 1.f, recip, q[blk]);
+            }
+            *reinterpret_cast<uint4*>(crow + col / 2) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
+            *reinterpret_cast<uint16_t*>(args.out_scales + blocked_sf_offset(mt, r, col / 16, K_h)) =
+                static_cast<uint16_t>(sc[0] | (sc[1] << 8));
+          }
+        } else {
 #pragma unroll 1
         for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
           uint32_t g[32], u[32];
@@ -399,7 +438,7 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
           tmem_ld_32cols(tq + BN + c0, u);
           tmem_ld_wait();
           const int col = n0 + c0;
-          if (prow != nullptr) {
+          {
             if (row_ok && col + 32 <= args.N) {
               float4* og = reinterpret_cast<float4*>(prow + col);
               float4* ou = reinterpret_cast<float4*>(prow + args.N + col);
@@ -411,28 +450,15 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
                                     __uint_as_float(u[4 * i + 2]) * au, __uint_as_float(u[4 * i + 3]) * au);
               }
             }
-          } else if (row_ok && col + 32 <= args.N) {
-            uint2 q[2];
-            uint32_t sc[2];
-#pragma unroll
-            for (int blk = 0; blk < 2; ++blk) {
-              float h[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float a = __uint_as_float(g[blk * 16 + i]) * ag;
-                h[i] = __fdividef(a, 1.f + __expf(-a)) * (__uint_as_float(u[blk * 16 + i]) * au);  // silu(a) * b
-              }
-              sc[blk] = nvfp4_quant16(h, 6.f, 1.f, recip, q[blk]);
-            }
-            *reinterpret_cast<uint4*>(crow + col / 2) = make_uint4(q[0].x, q[0].y, q[1].x, q[1].y);
-            *reinterpret_cast<uint16_t*>(args.out_scales + blocked_sf_offset(mt, r, col / 16, K_h)) =
-                static_cast<uint16_t>(sc[0] | (sc[1] << 8));
           }
         }
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (!released) {   // every TMEM read of this buffer is complete: hand it back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      }
       ++tc;
     }
   }
