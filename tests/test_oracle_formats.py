@@ -105,3 +105,95 @@ def test_activation_rule_error_bound_and_zero_rows():
     # scale-1 rows (the SwiGLU output between the expert GEMMs)
     deq1 = F.fake_quantize_activation(v / np.maximum(np.abs(v).max(axis=1, keepdims=True), 1e-30), row_scale=False)
     assert np.isfinite(deq1).all()
+
+
+# ------------------------------------------------------------------ the rule vs its fp64 form
+# The oracle applies the activation rule with each rounding decision in fp32 (the precision
+# the kernels use).  Its plain definition (LMSYS Muse Spark Open post, "NVFP4 as a third MMA
+# type": E2M1 values with one UE4M3 scale per 16 elements and an FP32 per-token scale) is, in
+# exact arithmetic:
+#     s  = amax(row) / (6 * 448)      sc = E4M3_RNE(amax(block) / (6 s))
+#     q  = E2M1_RNE_sat(v / (sc * s)), q = 0 where sc = 0
+# The fp32 sequence may differ from it only where the exact quotient lies within a few fp32
+# rounding errors of an E4M3 or E2M1 rounding boundary.
+_E2M1_MID = (F.E2M1_TABLE[:7] + F.E2M1_TABLE[1:8]) / 2
+_E4M3_MID = (F.E4M3_TABLE[:126] + F.E4M3_TABLE[1:127]) / 2
+
+
+def _near(a, mids, rel):
+    a = np.abs(np.asarray(a, dtype=np.float64))
+    d = np.min(np.abs(a[..., None] - mids), axis=-1)
+    return d <= rel * np.maximum(a, 1e-300)
+
+
+def _rule_fp64(v, row_scale):
+    rows, K = v.shape
+    amax = np.max(np.abs(v), axis=1)
+    s = np.where(amax > 0, amax / (6.0 * 448.0), 1.0) if row_scale else np.ones(rows)
+    blocks = v.reshape(rows, K // 16, 16)
+    ratio = np.max(np.abs(blocks), axis=2) / (6.0 * s[:, None])
+    sc = F.e4m3_encode(ratio)
+    scv = F.E4M3_TABLE[sc]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = np.where(scv[:, :, None] > 0, blocks / (scv[:, :, None] * s[:, None, None]), 0.0)
+    return F.e2m1_encode(t).reshape(rows, K), sc, s, ratio, t.reshape(rows, K)
+
+
+@pytest.mark.parametrize("row_scale", [True, False])
+def test_activation_rule_matches_its_fp64_definition(row_scale):
+    rng = np.random.default_rng(7 + row_scale)
+    rows, K = 512, 512
+    v = rng.standard_normal((rows, K)) * np.exp2(rng.integers(-30, 30, size=(rows, 1)))
+    v[::7, :16] *= 1e3            # outlier blocks: the row scale comes from them
+    v[5] = 0.0
+    v[9, 32:48] = 0.0
+    if not row_scale:             # scale-1 rows (the SwiGLU output): keep the block scales in range
+        v = v / np.max(np.abs(v), axis=1, keepdims=True).clip(1e-300) * rng.uniform(0.01, 2000, size=(rows, 1))
+    v = v.astype(np.float32).astype(np.float64)   # both sides see the same fp32 inputs
+    q, sc, s = F.quantize_activation(v, row_scale=row_scale)
+    q64, sc64, s64, ratio, t = _rule_fp64(v, row_scale)
+    # row scales: fp32 rounding of the exact quotient
+    assert np.all(np.abs(s.astype(np.float64) - s64) <= 2.0 ** -24 * s64)
+    # block scales: equal except within a few fp32 roundings of an E4M3 midpoint
+    sc_diff = sc != sc64
+    assert np.all(_near(ratio[sc_diff], _E4M3_MID, 1e-6)), ratio[sc_diff][:8]
+    assert sc_diff.mean() < 1e-3
+    # codes of blocks whose scale agrees: equal as values except near an E2M1 midpoint
+    same_blk = np.repeat(~sc_diff, 16, axis=1)
+    q_diff = (F.E2M1_TABLE[q] != F.E2M1_TABLE[q64]) & same_blk
+    assert np.all(_near(t[q_diff], _E2M1_MID, 1e-6)), t[q_diff][:8]
+    assert q_diff.mean() < 1e-4, q_diff.mean()
+    # and the dequantised values agree to one E2M1 step where anything differs at all
+    deq = F.dequantize_activation(q, sc, s)
+    deq64 = F.E2M1_TABLE[q64] * np.repeat(F.E4M3_TABLE[sc64], 16, axis=1) * s64[:, None]
+    amax_b = np.repeat(np.abs(v).reshape(rows, K // 16, 16).max(axis=2), 16, axis=1)
+    assert np.all(np.abs(deq - deq64) <= amax_b / 3 + 1e-300)
+
+
+@pytest.mark.parametrize("mistake", ["scale_without_row_scale", "multiplies_swapped_to_divide",
+                                     "row_scale_6_only", "block_amax_over_4"])
+def test_fp64_definition_sees_plausible_mistakes(mistake):
+    # the comparison above is sharp enough to catch a plausible slip in the fp32 sequence
+    rng = np.random.default_rng(11)
+    rows, K = 64, 256
+    v = (rng.standard_normal((rows, K)) * np.exp2(rng.integers(-20, 20, size=(rows, 1))))
+    v = v.astype(np.float32).astype(np.float64)
+    f32 = np.float32
+    amax = np.max(np.abs(v), axis=1).astype(f32)
+    s = (amax / f32(2688.0) if mistake != "row_scale_6_only" else amax / f32(6.0)).astype(f32)
+    blocks = v.astype(f32).reshape(rows, K // 16, 16)
+    amax_b = np.max(np.abs(blocks), axis=2)
+    if mistake == "block_amax_over_4":
+        amax_b = amax_b * f32(1.5)
+    den = (f32(6.0) * s).astype(f32) if mistake != "scale_without_row_scale" else np.full(rows, f32(6.0))
+    sc = F.e4m3_encode((amax_b / den[:, None]).astype(f32))
+    scv = F.E4M3_TABLE[sc]
+    r = np.where(scv > 0, 1.0 / np.where(scv > 0, scv, 1.0), 0.0).astype(f32)
+    if mistake == "multiplies_swapped_to_divide":
+        scaled = (blocks / r[:, :, None].clip(1e-30)).astype(f32) / s[:, None, None]
+    else:
+        scaled = (blocks * r[:, :, None]).astype(f32) * (f32(1.0) / s)[:, None, None]
+    q_bad = F.e2m1_encode(scaled.astype(f32)).reshape(rows, K)
+    q64, sc64, *_ = _rule_fp64(v, True)
+    differs = (F.E2M1_TABLE[q_bad] != F.E2M1_TABLE[q64]).mean() + (sc != sc64).mean()
+    assert differs > 1e-2, (mistake, differs)
