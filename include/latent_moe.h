@@ -263,11 +263,16 @@ lmoe_status lmoe_wait_selftest(const lmoe_config* cfg, void* workspace, long lon
  * The scratch (per-expert counts, M-tile table) is a fixed 64 KiB __device__ array inside
  * the library, held by every GPU that loads the library until the process exits.  Limits:
  * E <= 1024 and T*k <= 65536; larger sizes return LMOE_ERR_UNSUPPORTED before any launch.
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- * the current device, which must be the stream's device; make that first call before any
- * stream capture.  All calls on a device share the one array and nothing in it needs to
- * start at zero (each call overwrites what it reads), but calls that overlap on the GPU
- * (unordered streams) race on it: order them. */
+ * The four arrays must be 4-byte aligned (else LMOE_ERR_ALIGN) device memory of the current
+ * device, and the stream must belong to that device (else LMOE_ERR_ARG), both checked before
+ * any launch.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it; make that first call before
+ * any stream capture.  Calls after a cudaDeviceReset of the device are not supported (the
+ * cached address is then stale).  All calls on a device share the one array and nothing in it
+ * needs to start at zero (each call overwrites what it reads), but calls that overlap on the
+ * GPU (unordered streams) race on it: order them.  This is the per-expert-scan form of the
+ * permutation (each of E CTAs reads every id), whose cost grows as E x T*k: at many pairs it
+ * is slower than the chunked permutation the forward call runs from its workspace. */
 lmoe_status lmoe_permute_noalloc(const int32_t* topk_idx, int T, int k, int E, int32_t* offsets,
                                  int32_t* row_of, int32_t* tok_of, cudaStream_t stream);
 

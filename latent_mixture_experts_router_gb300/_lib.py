@@ -273,8 +273,12 @@ def lmoe_permute_noalloc(topk_idx, E: int, offsets, row_of, tok_of, stream=None)
     fn.argtypes = [_P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P]
     fn.restype = ctypes.c_int
     T, k = topk_idx.shape
-    _check(fn(_ptr(topk_idx), T, k, int(E), _ptr(offsets), _ptr(row_of), _ptr(tok_of), _stream(stream)),
-           "lmoe_permute_noalloc")
+    # the library looks its scratch up for the current device: make the ids' device current
+    # and take the stream from it
+    with torch.cuda.device(topk_idx.device):
+        st = _stream(stream if stream is not None else torch.cuda.current_stream(topk_idx.device))
+        _check(fn(_ptr(topk_idx), T, k, int(E), _ptr(offsets), _ptr(row_of), _ptr(tok_of), st),
+               "lmoe_permute_noalloc")
 
 
 def lmoe_quantize_nvfp4(src, codes, scales, s_row=None, row_scale=True, stream=None):

@@ -12,7 +12,12 @@
 // The array is a file-scope __device__ object: every GPU that loads this library holds its
 // 64 KiB until the process exits.  Host code cannot use the symbol as a device address, so
 // the first call on each device looks the address up with cudaGetSymbolAddress (that
-// device current) and caches it; later calls reuse it.
+// device current) and caches it; later calls reuse it.  A cudaDeviceReset unloads the module
+// and leaves the cached address stale: calls after a reset of the device are not supported.
+//
+// This is the per-expert-scan form of the permutation (one CTA per expert, each reading every
+// id twice), so its cost grows as E x T*k; the block's own forward switches to a chunked
+// histogram/scan/rank form from 16384 pairs, whose per-chunk tables need workspace.
 #include <mutex>
 
 #include "../../include/latent_moe.h"
@@ -55,6 +60,19 @@ cudaError_t scratch_address(void** out) {
   return cudaSuccess;
 }
 
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// True when `p` is device (or managed) memory that device `dev` can use as its own.
+bool on_device(const void* p, int dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();   // an unknown pointer must not leave an error behind
+    return false;
+  }
+  if (a.type == cudaMemoryTypeManaged) return true;
+  return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
 }  // namespace
 
 extern "C" lmoe_status lmoe_permute_noalloc(const int32_t* topk_idx, int T, int k, int E,
@@ -64,6 +82,18 @@ extern "C" lmoe_status lmoe_permute_noalloc(const int32_t* topk_idx, int T, int 
   if (E > kNoAllocMaxExperts || static_cast<long long>(T) * k > kNoAllocMaxPairs)
     return LMOE_ERR_UNSUPPORTED;  // beyond the fixed scratch array
   if (offsets == nullptr || (T > 0 && (topk_idx == nullptr || row_of == nullptr || tok_of == nullptr)))
+    return LMOE_ERR_ARG;
+  // the kernels do plain int32 loads and stores on these arrays
+  if (!aligned4(offsets) || (T > 0 && (!aligned4(topk_idx) || !aligned4(row_of) || !aligned4(tok_of))))
+    return LMOE_ERR_ALIGN;
+  // The scratch address is looked up for the current device and the kernels run on the
+  // stream's device: they must be the same device, and so must the arrays' device.
+  int dev = 0, sdev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamGetDevice(stream, &sdev) != cudaSuccess)
+    return LMOE_ERR_CUDA;
+  if (sdev != dev) return LMOE_ERR_ARG;
+  if (!on_device(offsets, dev) ||
+      (T > 0 && (!on_device(topk_idx, dev) || !on_device(row_of, dev) || !on_device(tok_of, dev))))
     return LMOE_ERR_ARG;
   void* base = nullptr;
   if (scratch_address(&base) != cudaSuccess) return LMOE_ERR_CUDA;

@@ -101,3 +101,28 @@ def test_next_norm_arguments_checked_without_launching(lm):
     assert lib.latent_moe_forward_ex(*args, ctypes.byref(only_out)) == -1
     misaligned = lmoe_ex(None, None, None, None, None, 0, None, fake, fake + 4)
     assert lib.latent_moe_forward_ex(*args, ctypes.byref(misaligned)) == -3
+
+
+def _noalloc_fn(lm):
+    fn = lm.load().lmoe_permute_noalloc
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+@pytest.mark.parametrize("which", range(4))
+def test_no_alloc_rejects_misaligned_arrays_without_launching(lm, which):
+    # the allocation-free permutation does int32 loads and stores on its four arrays: a
+    # pointer that is not 4-byte aligned is refused on the host (no GPU touched)
+    fake = [1 << 20, 1 << 21, 1 << 22, 1 << 23]   # never dereferenced
+    fake[which] += 2
+    idx, offsets, row_of, tok_of = fake
+    assert _noalloc_fn(lm)(idx, 8, 2, 16, offsets, row_of, tok_of, None) == -3
+
+
+@pytest.mark.parametrize("T,k,E,status", [(8, 2, 1025, -2), (32769, 2, 64, -2), (8, 0, 16, -1),
+                                          (8, 17, 32, -1), (8, 4, 2, -1)])
+def test_no_alloc_rejects_sizes_without_launching(lm, T, k, E, status):
+    fake = 1 << 20
+    assert _noalloc_fn(lm)(fake, T, k, E, fake, fake, fake, None) == status

@@ -86,3 +86,32 @@ def test_no_alloc_rejects_sizes_beyond_its_scratch(lm):
         o = torch.empty(9, dtype=torch.int32, device="cuda:0")
         lmoe_permute_noalloc(idx, 8, o, idx, idx.view(-1))
     assert ei.value.status == -2
+
+
+def test_no_alloc_permutation_at_its_limits(lm):
+    # T*k = 65536 pairs over E = 1024 experts: the fixed tile table at full capacity
+    from gpu_util import expected_permutation
+    T, k, E = 8192, 8, 1024
+    g = torch.Generator().manual_seed(12)
+    ids = torch.argsort(torch.rand(T, E, generator=g), dim=1)[:, :k].to(torch.int32)
+    ids[:64] = torch.arange(k, dtype=torch.int32)      # a crowded expert or two as well
+    idx = ids.to("cuda:0")
+    counts, offsets_ref, row_ref, tok_ref = expected_permutation(ids.numpy(), E)
+    for _ in range(2):
+        offsets, row_of, tok_of = _noalloc_call(lm, idx, E)
+        assert np.array_equal(offsets, offsets_ref)
+        assert np.array_equal(row_of, row_ref)
+        assert np.array_equal(tok_of, tok_ref)
+
+
+def test_no_alloc_refuses_host_memory_before_launching(lm):
+    # an output array in (pinned) host memory is not device memory of the current device
+    from latent_mixture_experts_router_gb300._lib import lmoe_permute_noalloc
+    idx = torch.zeros((4, 2), dtype=torch.int32, device="cuda:0")
+    idx[:, 1] = 1
+    host = torch.empty(9, dtype=torch.int32).pin_memory()
+    row_of = torch.empty((4, 2), dtype=torch.int32, device="cuda:0")
+    tok_of = torch.empty(8, dtype=torch.int32, device="cuda:0")
+    with pytest.raises(lm.LmoeError) as ei:
+        lmoe_permute_noalloc(idx, 8, host, row_of, tok_of)
+    assert ei.value.status == -1
