@@ -86,3 +86,24 @@ def test_shapes_match_published_weight_budget():
     # active parameters with top-8: experts + latent + router per layer, plus attention
     active = layers * (w.k * 3 * w.L * w.I + 2 * w.D * w.L + w.E * w.D) / 1e9 + g["attention_B"]
     assert abs(active - g["active_B"]) < 1.0
+
+
+def test_gaussian_is_standard_normal():
+    # x and the gammas: Box-Muller deviates checked against scipy's normal distribution
+    # (Kolmogorov-Smirnov), its fourth moment and its tails (which an Irwin-Hall sum lacks)
+    import scipy.stats as st
+    z = rng.gaussian(0, 1, 0, 1_000_000, 1.0).numpy()
+    assert abs(z.mean()) < 3e-3 and abs(z.std() - 1.0) < 3e-3
+    assert abs(st.kurtosis(z, fisher=False) - 3.0) < 0.03
+    tail = np.mean(np.abs(z) > 3.5)
+    assert abs(tail - 2 * st.norm.sf(3.5)) < 1.5e-4            # 4.65e-4 expected
+    assert st.kstest(z[:200_000], "norm").pvalue > 1e-3
+    part = rng.gaussian(0, 1, 5000, 100, 2.0)
+    assert torch.equal(part, 2.0 * rng.gaussian(0, 1, 0, 6000, 1.0)[5000:5100])
+
+
+def test_x_rows_of_one_long_sequence():
+    w = workloads.WORKLOADS["tiny_fp32"].with_tokens(6)
+    x = workloads.x_tensor(w)
+    assert torch.equal(workloads.x_tensor(w.with_tokens(3), first_token=3), x[3:6])
+    assert torch.equal(workloads.x_tensor(w, rows=[5, 1]), x[[5, 1]])

@@ -2,4 +2,4 @@
 benchmark and the smoke check; holds none of the block's arithmetic)."""
 from .configs import (WORKLOADS, DECODE_SWEEP_T, Workload, BlockInputs, make_inputs,  # noqa: F401
                       dense_weight, nvfp4_weight, gammas, x_tensor, zipf_bias,
-                      forced_routing, hot_experts, nvfp4_tensor_scale)
+                      forced_routing, hot_experts, nvfp4_tensor_scale, to_device)

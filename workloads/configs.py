@@ -5,11 +5,12 @@ Shapes follow the Muse Spark Open layer: d_model 8192, pooled width 4096,
 expert; 256 experts x 62 layers = 799B, the weight budget of the vLLM day-0
 post, "Model architecture" table), top-8 routing.  Distributions: x ~ N(0,1);
 every W ~ N(0, 1/fan_in); RMSNorm gammas 1 + 0.1*N(0,1) in fp32; eps 1e-6.
-"N(0,1)" is the standardised Irwin-Hall(4) deviate of ``workloads.rng``.
-
-Tensors are generated on any torch device, slice by slice, with bit-identical
-values: a test can rebuild on the host exactly the expert slices one token
-touches.  Nothing here computes any part of the block.
+x and the gammas are true Gaussians (``rng.gaussian``, Box-Muller, drawn on the
+host and copied); the weights use the standardised Irwin-Hall(4) deviate of
+``rng.normal`` (variance 1, support +-2*sqrt(3)), drawn on the device with
+bit-identical values on any device, so a test can rebuild on the host exactly
+the expert slices one token touches.  Nothing here computes any part of the
+block.
 """
 from __future__ import annotations
 
@@ -80,16 +81,24 @@ def normal_tensor(w: Workload, stream: int, shape, std: float, dtype: str, devic
 
 def gamma_tensor(w: Workload, stream: int, shape, device="cpu", start: int = 0) -> torch.Tensor:
     n = math.prod(shape)
-    z = rng.normal(w.seed, stream, start, n, 1.0, device)
-    return (1.0 + z * 0.1).to(torch.float32).reshape(shape)
+    z = rng.gaussian(w.seed, stream, start, n, 1.0)
+    return (1.0 + z * 0.1).to(torch.float32).reshape(shape).to(device)
 
 
-def x_tensor(w: Workload, device="cpu", rows=None) -> torch.Tensor:
-    """x [T, D]; ``rows`` selects a subset of tokens (same values as in the full tensor)."""
+def x_tensor(w: Workload, device="cpu", rows=None, first_token: int = 0) -> torch.Tensor:
+    """x [T, D] ~ N(0,1) (Box-Muller on the host, rounded fp64 -> fp32 (-> bf16), then copied):
+    tokens first_token .. first_token+T-1 of one long seeded sequence; ``rows`` selects a
+    subset of tokens instead (same values as in the full tensor)."""
     if rows is None:
-        return normal_tensor(w, S_X, (w.T, w.D), 1.0, w.act, device)
-    return torch.stack([normal_tensor(w, S_X, (w.D,), 1.0, w.act, device, start=int(t) * w.D)
-                        for t in rows])
+        n = w.T * w.D
+        out = torch.empty(n, dtype=torch.float32 if w.act == "f32" else torch.bfloat16)
+        c = 1 << 22
+        for s0 in range(0, n, c):   # converted chunk by chunk (one fp64 chunk live at a time)
+            m = min(c, n - s0)
+            out[s0:s0 + m] = _to_dtype(rng.gaussian(w.seed, S_X, first_token * w.D + s0, m, 1.0), w.act)
+        return out.reshape(w.T, w.D).to(device)
+    return torch.stack([_to_dtype(rng.gaussian(w.seed, S_X, int(t) * w.D, w.D, 1.0), w.act)
+                        for t in rows]).to(device)
 
 
 def dense_weight_dtype(w: Workload) -> str:
@@ -252,3 +261,16 @@ def make_inputs(w: Workload, device="cpu") -> BlockInputs:
         router_bias=zipf_bias(w, device) if w.routing == "zipf" else None,
         forced_idx=forced_routing(w, device) if w.routing == "hot4" else None,
     )
+
+
+def to_device(inp: BlockInputs, device) -> BlockInputs:
+    """The same inputs copied to ``device`` (tensors, and the tensors of NVFP4 triples)."""
+    import dataclasses
+
+    def mv(v):
+        if isinstance(v, tuple):
+            return tuple(t.to(device) for t in v)
+        return v.to(device) if isinstance(v, torch.Tensor) else v
+    return dataclasses.replace(inp, **{f.name: mv(getattr(inp, f.name)) for f in dataclasses.fields(inp)
+                                       if f.name not in ("w", "extra")})
+

@@ -9,11 +9,18 @@ same call gives bit-identical results on a CPU tensor and on a CUDA tensor.
 That is what lets a test regenerate, on the host, exactly the slice of a
 weight tensor that a sampled token touches on the GPU.
 
-"Normal" deviates are standardised Irwin-Hall(4) sums of the four 16-bit
-fields of one hash: mean 0, variance 1 (to 1 part in 2^32), support (-2√3,
-2√3).  Only exact operations (integer sum, power-of-two scaling) and one
-correctly rounded multiply are used, so they too are bit-identical across
-devices.  This module holds no arithmetic of the latent-MoE block.
+Two kinds of normal deviates:
+  * ``normal``: standardised Irwin-Hall(4) sums of the four 16-bit fields of one
+    hash: mean 0, variance 1 (to 1 part in 2^32), support (-2√3, 2√3).  Only
+    exact operations (integer sum, power-of-two scaling) and one correctly
+    rounded multiply are used, so they are bit-identical across devices; the
+    weights are drawn this way, on the device.
+  * ``gaussian``: Box-Muller (Box & Muller, "A note on the generation of random
+    normal deviates", Ann. Math. Statist. 1958) on the two 32-bit halves of one
+    hash, in fp64 on the host: a true N(0,1) with tails to about 6.8 sigma.  Its
+    log/cos/sqrt are the host's, so it is always computed on the CPU and copied
+    to where it is needed; x and the RMSNorm gammas are drawn this way.
+This module holds no arithmetic of the latent-MoE block.
 """
 from __future__ import annotations
 
@@ -86,6 +93,21 @@ def normal(seed: int, stream: int, start: int, count: int, std: float,
         idx = torch.arange(start + s0, start + s0 + n, dtype=torch.int64, device=device)
         u = _irwin_hall4(hash64(seed, stream, idx))
         out[s0:s0 + n] = u * (math.sqrt(3.0) * std)  # one correctly rounded multiply
+    return out
+
+
+def gaussian(seed: int, stream: int, start: int, count: int, std: float) -> torch.Tensor:
+    """fp64 N(0, std^2) deviates (host) for indices [start, start+count): Box-Muller on the hash,
+    u1 = (hi32 + 0.5) / 2^32 and u2 = (lo32 + 0.5) / 2^32, z = sqrt(-2 ln u1) cos(2 pi u2)."""
+    out = torch.empty(count, dtype=torch.float64)
+    c = _chunk("cpu")
+    for s0 in range(0, count, c):
+        n = min(c, count - s0)
+        idx = torch.arange(start + s0, start + s0 + n, dtype=torch.int64)
+        h = hash64(seed, stream, idx)
+        u1 = (_lsr(h, 32).to(torch.float64) + 0.5) * (1.0 / 4294967296.0)
+        u2 = ((h & 0xFFFFFFFF).to(torch.float64) + 0.5) * (1.0 / 4294967296.0)
+        out[s0:s0 + n] = torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2) * std
     return out
 
 
