@@ -36,8 +36,9 @@ ties; the slot order is descending logit and the sum runs in slot order.
 NVFP4 mode: each GEMM input activation (xn into the pooler, h0 into gate/up,
 h into down, c into the unpooler) is replaced by its fake-quantised value
 under the activation rule of ``oracle.formats`` (row scale for xn, h0, c;
-scale 1 for h); weights are the dequantised packed weights; the router stays
-at full precision on xn.
+scale 1 for h); weights are the dequantised packed weights; each expert output
+y is rounded to bfloat16 before its norm (the BF16 values the pages' fused
+per-expert post-norm squares); the router stays at full precision on xn.
 """
 from __future__ import annotations
 
@@ -159,12 +160,17 @@ def _q(v: np.ndarray, nvfp4: bool, row_scale: bool = True) -> np.ndarray:
 
 
 def expert_ffn(P: BlockParams, e: int, h0: np.ndarray) -> np.ndarray:
-    """SwiGLU expert e on rows h0 [n, L] -> y [n, L] (before the per-expert norm)."""
+    """SwiGLU expert e on rows h0 [n, L] -> y [n, L] (before the per-expert norm).  In NVFP4
+    mode y is rounded to bfloat16: the down projection's tiles hold y as BF16 values and the
+    per-expert norm squares those values (LMSYS Muse Spark Open post, "Fused per-expert
+    post-norm"), and c is quantised again after the weighted sum, so the rounding of y decides
+    E2M1 codes downstream."""
     a_in = _q(h0, P.nvfp4)
     a = a_in @ P.W_gate[e].T
     b = a_in @ P.W_up[e].T
     h = silu(a) * b
-    return _q(h, P.nvfp4, row_scale=False) @ P.W_down[e].T
+    y = _q(h, P.nvfp4, row_scale=False) @ P.W_down[e].T
+    return formats.bf16_round(y) if P.nvfp4 else y
 
 
 # ------------------------------------------------------------------ forward
@@ -258,3 +264,66 @@ def forward_norm_after_sum(x: np.ndarray, P: BlockParams, k: int):
         c = rms_norm(s, g, P.eps)
         out[t] = x[t] + rms_norm(P.W_unpool @ c, P.g_post, P.eps)
     return out
+
+
+def forward_token_choices(x_t: np.ndarray, P: BlockParams, k: int, forced_row: Optional[np.ndarray] = None,
+                          band: float = formats.QUANT_BAND):
+    """NVFP4 mode: the outputs one token may legitimately have when a rounding decision of the
+    activation rule is undecided (formats.activation_choices: the exact value within `band` of
+    a rounding boundary).  The first entry is the rule's own output (forward_per_token); each
+    further entry takes one near-boundary decision of one quantised activation (xn into the
+    pooler, h0 into gate/up, the h row of one routed expert into down, c into the unpooler)
+    the other way, everything else as the rule decides."""
+    assert P.nvfp4
+    x_t = np.asarray(x_t, dtype=F64).reshape(-1)
+    xn = rms_norm(x_t, P.g_pre, P.eps)
+    l = P.W_router @ xn
+    if P.router_bias is not None:
+        l = l + P.router_bias
+    fr = None if forced_row is None else np.asarray(forced_row).reshape(1, -1)
+    idx, w, _ = route(l[None, :], k, fr)
+    idx, w = idx[0], w[0]
+
+    def quant(v, row_scale=True):
+        return formats.activation_choices(v, row_scale, band)
+
+    def expert_h(e, h0q):
+        a = h0q @ P.W_gate[int(e)].T
+        b = h0q @ P.W_up[int(e)].T
+        return silu(a) * b
+
+    def y_of(e, hq):
+        return formats.bf16_round(hq @ P.W_down[int(e)].T)
+
+    def c_of(ys):
+        c = np.zeros(P.g_pool.shape[0], dtype=F64)
+        for j in range(k):
+            c = c + w[j] * rms_norm(ys[j], P.g_expert[int(idx[j])], P.eps)
+        return c
+
+    def out_of(cq):
+        return x_t + rms_norm(cq @ P.W_unpool.T, P.g_post, P.eps)
+
+    def from_ys(ys):
+        return out_of(quant(c_of(ys))[0])
+
+    def from_h0q(h0q):
+        return from_ys([y_of(idx[j], quant(expert_h(idx[j], h0q), False)[0]) for j in range(k)])
+
+    def from_xnq(xnq):
+        return from_h0q(quant(rms_norm(xnq @ P.W_pool.T, P.g_pool, P.eps))[0])
+
+    xn_ch = quant(xn)
+    h0_ch = quant(rms_norm(xn_ch[0] @ P.W_pool.T, P.g_pool, P.eps))
+    hs = [expert_h(idx[j], h0_ch[0]) for j in range(k)]
+    h_ch = [quant(h, False) for h in hs]
+    ys = [y_of(idx[j], h_ch[j][0]) for j in range(k)]
+    c_ch = quant(c_of(ys))
+    outs = [out_of(c_ch[0])]
+    outs += [out_of(cq) for cq in c_ch[1:]]
+    for j in range(k):
+        for hq in h_ch[j][1:]:
+            outs.append(from_ys(ys[:j] + [y_of(idx[j], hq)] + ys[j + 1:]))
+    outs += [from_h0q(h0q) for h0q in h0_ch[1:]]
+    outs += [from_xnq(xnq) for xnq in xn_ch[1:]]
+    return outs

@@ -90,6 +90,17 @@ def nvfp4_dequantize(codes: np.ndarray, scales: np.ndarray, tensor_scale: float)
     return q * np.repeat(sc, 16, axis=-1) * float(tensor_scale)
 
 
+# ------------------------------------------------------------------ bf16
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """Round to the nearest bfloat16 value (8 significant bits, ties to even), in fp64.
+    bfloat16 keeps fp32's exponent range; the values rounded here (expert outputs) lie far
+    inside it, so only the significand is rounded: v = m * 2^e with m in [0.5, 1), and m is
+    rounded to a multiple of 2^-8 (numpy's rint rounds halves to even)."""
+    v = np.asarray(v, dtype=np.float64)
+    m, e = np.frexp(v)
+    return np.ldexp(np.rint(m * 256.0) / 256.0, e)
+
+
 # ------------------------------------------------------------------ activations
 # The activation rule (one fp32 scale per row, an E4M3 scale per 16-block,
 # E2M1 codes) takes each rounding decision in fp32, the precision of the
@@ -133,3 +144,108 @@ def dequantize_activation(q: np.ndarray, sc_code: np.ndarray, s: np.ndarray) -> 
 def fake_quantize_activation(v: np.ndarray, row_scale: bool = True) -> np.ndarray:
     """Q(v): the fp64 value the NVFP4 GEMM sees in place of the activation rows v."""
     return dequantize_activation(*quantize_activation(v, row_scale))
+
+
+# ------------------------------------------------------------------ weights
+def quantize_weight(W: np.ndarray):
+    """Dense weight rows [rows, K] -> packed NVFP4 (codes [rows, K/2] u8, low nibble = even k;
+    E4M3 block-scale codes [rows, K/16]; fp32 tensor scale), by the plain definition in fp64:
+        s  = fp32(amax(W) / (6 * 448))          one second-level scale for the matrix
+        sc = E4M3_RNE(amax(block) / (6 s))      one scale per 16 consecutive k
+        q  = E2M1_RNE_sat(w / (sc s))           (q = 0 where sc = 0)
+    (LMSYS Muse Spark Open post, "NVFP4 as a third MMA type": E2M1 values, a UE4M3 scale per
+    16 elements, an FP32 tensor-level scale).  Used to pack test weights drawn from a Gaussian."""
+    W = np.asarray(W, dtype=np.float64)
+    rows, K = W.shape
+    assert K % 16 == 0
+    amax = float(np.max(np.abs(W)))
+    s = float(np.float32(amax / 2688.0)) if amax > 0 else 1.0
+    blocks = W.reshape(rows, K // 16, 16)
+    sc = e4m3_encode(np.max(np.abs(blocks), axis=2) / (6.0 * s))
+    scv = E4M3_TABLE[sc]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = np.where(scv[:, :, None] > 0, blocks / (scv[:, :, None] * s), 0.0)
+    q = e2m1_encode(t).reshape(rows, K)
+    codes = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    return codes, sc, np.float32(s)
+
+
+# ------------------------------------------------------------------ near-boundary decisions
+# The activation rule rounds in fp32.  The GPU and the oracle feed it values computed in
+# different orders (fp32 sums on the GPU, fp64 here), which agree to ~1e-7 relative; where
+# the exact value lies that close to an E4M3 or E2M1 rounding boundary, either side of the
+# boundary is a legitimate result of the rule, as either expert is at a top-k near tie.
+QUANT_BAND = 1e-5   # relative distance to a rounding boundary treated as undecided
+
+
+def _other_neighbour(code_mag: int, a: float, pos: np.ndarray) -> int:
+    """The magnitude index on the other side of a's rounding boundary from code_mag."""
+    if a >= pos[code_mag]:
+        return min(code_mag + 1, len(pos) - 1)
+    return max(code_mag - 1, 0)
+
+
+def _rule_row(v32: np.ndarray, row_scale: bool, sc_override=None, code_override=None):
+    """The rule on one fp32 row (same fp32 steps as quantize_activation), optionally with some
+    block-scale codes (dict block -> E4M3 code) or element codes (dict i -> E2M1 code) forced.
+    Returns the dequantised fp64 row."""
+    K = v32.shape[0]
+    amax = np.max(np.abs(v32))
+    s = (amax / _F(2688.0)).astype(_F) if (row_scale and amax > 0) else _F(1.0)
+    six_s, inv_s = _F(_F(6.0) * s), _F(_F(1.0) / s)
+    blocks = v32.reshape(K // 16, 16)
+    sc = e4m3_encode((np.max(np.abs(blocks), axis=1) / six_s).astype(_F))
+    for b, c in (sc_override or {}).items():
+        sc[b] = c
+    scv = E4M3_TABLE[sc]
+    r = np.where(scv > 0, 1.0 / np.where(scv > 0, scv, 1.0), 0.0).astype(_F)
+    q = e2m1_encode(((blocks * r[:, None]).astype(_F) * inv_s).astype(_F)).reshape(K)
+    for i, c in (code_override or {}).items():
+        q[i] = c
+    return E2M1_TABLE[q] * np.repeat(scv, 16) * float(s)
+
+
+def activation_choices(v: np.ndarray, row_scale: bool = True, band: float = QUANT_BAND, max_choices: int = 8):
+    """Q(v) of one row, followed by the rows obtained by taking one near-boundary rounding
+    decision the other way: a block scale whose exact ratio amax_b / (6 s) lies within `band`
+    (relative) of an E4M3 midpoint, or an element whose exact v / (sc s) lies within `band` of
+    an E2M1 midpoint (one decision per variant; at most max_choices - 1 variants, nearest
+    first).  Exactness here means fp64 on the oracle's own values."""
+    v = np.asarray(v, dtype=np.float64)
+    v32 = v.astype(_F)
+    K = v.shape[0]
+    base = _rule_row(v32, row_scale)
+    amax = float(np.max(np.abs(v)))
+    s64 = amax / 2688.0 if (row_scale and amax > 0) else 1.0
+    blocks = v.reshape(K // 16, 16)
+    ratio = np.max(np.abs(blocks), axis=1) / (6.0 * s64)
+    sc = e4m3_encode(ratio.astype(_F))
+    cand = []   # (relative distance, kind, index, code)
+    mid4 = (_E4M3_POS[:-1] + _E4M3_POS[1:]) / 2
+    for b in range(K // 16):
+        if ratio[b] <= 0:
+            continue
+        d = np.min(np.abs(mid4 - ratio[b])) / ratio[b]
+        if d <= band:
+            alt = _other_neighbour(int(sc[b] & 0x7F), ratio[b], _E4M3_POS)
+            cand.append((d, "sc", b, alt))
+    mid2 = (_E2M1_POS[:-1] + _E2M1_POS[1:]) / 2
+    scv = E4M3_TABLE[sc]
+    for i in range(K):
+        if scv[i // 16] <= 0:
+            continue
+        t = abs(v[i]) / (scv[i // 16] * s64)
+        if t <= 0 or t >= _E2M1_POS[-1]:
+            continue
+        d = np.min(np.abs(mid2 - t)) / t
+        if d <= band:
+            q0 = int(e2m1_encode(np.array([t]))[0] & 7)
+            alt = _other_neighbour(q0, t, _E2M1_POS) | (8 if np.signbit(v[i]) else 0)
+            cand.append((d, "q", i, alt))
+    out = [base]
+    for d, kind, i, code in sorted(cand)[:max_choices - 1]:
+        if kind == "sc":
+            out.append(_rule_row(v32, row_scale, sc_override={i: code}))
+        else:
+            out.append(_rule_row(v32, row_scale, code_override={i: code}))
+    return out

@@ -15,7 +15,9 @@ from . import formats
 
 
 def _np(t: torch.Tensor) -> np.ndarray:
-    return t.detach().to("cpu").to(torch.float64).numpy()
+    # widening bf16/fp32 -> fp64 is exact, so it may run where the tensor lives (a device-side
+    # widening of a 100 MB expert matrix is much faster than the host's)
+    return t.detach().to(torch.float64).to("cpu").numpy()
 
 
 def _host_u8(t) -> np.ndarray:

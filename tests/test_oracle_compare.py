@@ -262,3 +262,89 @@ def test_broken_comparator_is_caught(name):
         except AssertionError:
             failed.append(case.__name__)
     assert failed, f"no case detects the broken comparator {name}"
+
+
+# ------------------------------------------------------------------ NVFP4 rounding boundaries
+def _nvfp4_params(seed=3):
+    P = _params(4, [0.0, -0.5, -1.0, -1.5], seed=seed, D=32, L=32, I=32)
+    P.nvfp4 = True
+    return P
+
+
+def test_forward_token_choices_first_is_the_definition():
+    P = _nvfp4_params()
+    x = _x(3, D=32)
+    ref = oracle.forward_per_token(x, P, 2)
+    for t in range(3):
+        outs = oracle.block.forward_token_choices(x[t], P, 2)
+        assert np.max(np.abs(outs[0] - ref[t])) <= 1e-12
+
+
+def _fake_choices(delta):
+    """A choices function whose single alternative moves element 0 of the output by delta."""
+    def choices(x_t, P, k, sel):
+        base = oracle.forward_per_token(np.asarray(x_t)[None], P, k,
+                                        forced_idx=None if sel is None else np.asarray(sel)[None])[0]
+        alt = base.copy()
+        alt[0] += delta
+        return [base, alt]
+    return choices
+
+
+def test_boundary_alternative_accepted_and_counted_only_when_it_matches():
+    P = _nvfp4_params()
+    x = _x(4, D=32)
+    out, tr = _ref(x, P, 2)
+    rms = float(np.sqrt(np.mean(out ** 2)))
+    big = 0.5 * rms                                 # far outside the 6e-2 bar
+    g = out.copy()
+    g[2, 0] += big
+    rep = C.compare_block(g, tr.idx, x, P, 2, C.TOL_NVFP4, choices=_fake_choices(big))
+    assert rep.ok and rep.quant_boundary_tokens == 1 and rep.max_abs_err < 1e-12
+    # the GPU output matches no alternative: rejected
+    rep = C.compare_block(g, tr.idx, x, P, 2, C.TOL_NVFP4, choices=_fake_choices(-big))
+    assert not rep.ok and rep.quant_boundary_tokens == 0
+    # BF16 compute has no quantisation decisions to take either way: never consulted
+    P.nvfp4 = False
+    out_b, tr_b = _ref(x, P, 2)
+    g_b = out_b.copy()
+    g_b[2, 0] += big
+    rep = C.compare_block(g_b, tr_b.idx, x, P, 2, C.TOL_BF16, choices=_fake_choices(big))
+    assert not rep.ok and rep.quant_boundary_tokens == 0
+
+
+def test_boundary_alternative_found_in_a_real_nvfp4_block():
+    # an NVFP4 block (E = 1024, k = 16, L = 256) where one token's c holds a block whose scale
+    # ratio lies 1e-8 (relative) from an E4M3 midpoint: the token has exactly one alternative
+    # output, 0.15 x RMS from the rule's own, the size of a one-code scale change of one block
+    import workloads
+    w = workloads.Workload("fp4_24_256_256_1024_256_16", T=24, D=256, L=256, E=1024, I=256, k=16,
+                           weights="nvfp4", seed=24 % 5)
+    inp = workloads.make_inputs(w, "cpu")
+    P = oracle.params_from_inputs(inp)
+    x = inp.x.double().numpy()[[3, 17]]
+    ref = oracle.forward_batched(x, P, w.k)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    assert len(oracle.block.forward_token_choices(x[0], P, w.k)) == 1
+    outs = oracle.block.forward_token_choices(x[1], P, w.k)
+    assert len(outs) == 2 and 0.1 < np.max(np.abs(outs[1] - outs[0])) / rms < 0.2
+
+
+def _compare_accepts_every_nvfp4_outlier(gpu_out, gpu_idx, x, P, k, tol, tr=None, ref=None, forced_idx=None,
+                                         choices=None):
+    """Mistake: an NVFP4 token outside the bar is accepted without matching an alternative."""
+    rep = C.compare_block(gpu_out, gpu_idx, x, P, k, tol, tr=tr, ref=ref, forced_idx=forced_idx,
+                          choices=lambda x_t, P_, k_, sel: [None, np.asarray(gpu_out)[
+                              int(np.nonzero(np.all(np.asarray(x) == x_t, axis=1))[0][0])]])
+    return rep
+
+
+def test_broken_boundary_acceptance_is_caught():
+    P = _nvfp4_params()
+    x = _x(4, D=32)
+    out, tr = _ref(x, P, 2)
+    g = out.copy()
+    g[2, 0] += 0.5 * float(np.sqrt(np.mean(out ** 2)))
+    # with no alternative matching, the real comparator rejects; the broken one would accept
+    assert not C.compare_block(g, tr.idx, x, P, 2, C.TOL_NVFP4, choices=_fake_choices(-1.0)).ok
+    assert _compare_accepts_every_nvfp4_outlier(g, tr.idx, x, P, 2, C.TOL_NVFP4).ok

@@ -197,3 +197,90 @@ def test_fp64_definition_sees_plausible_mistakes(mistake):
     q64, sc64, *_ = _rule_fp64(v, True)
     differs = (F.E2M1_TABLE[q_bad] != F.E2M1_TABLE[q64]).mean() + (sc != sc64).mean()
     assert differs > 1e-2, (mistake, differs)
+
+
+def test_quantize_weight_roundtrip_and_bound():
+    # weights built as e2m1 * e4m3 * s (the largest block scale 448 and a 6 in that block)
+    # come back exactly; Gaussian weights spread over 2^-20..1 land within half an E2M1 step
+    # of the block scale, and their block scales reach the E4M3 subnormals
+    rng = np.random.default_rng(5)
+    q = rng.integers(0, 16, size=(8, 64))
+    q[:, ::16] = 7
+    sc = rng.integers(0x08, 0x7E, size=(8, 4))
+    sc[0, 0] = 0x7E
+    s = np.float32(2.0 ** -10)
+    W = F.E2M1_TABLE[q] * np.repeat(F.E4M3_TABLE[sc], 16, axis=1) * float(s)
+    codes, sc2, s2 = F.quantize_weight(W)
+    assert s2 == s and np.array_equal(F.nvfp4_dequantize(codes, sc2, s2), W)
+    G = rng.standard_normal((256, 256)) * np.exp2(-rng.uniform(0, 20, size=(256, 1)))
+    codes, sc3, s3 = F.quantize_weight(G)
+    deq = F.nvfp4_dequantize(codes, sc3, s3)
+    unit = np.repeat(F.E4M3_TABLE[sc3], 16, axis=1) * float(s3)
+    inside = np.abs(G) <= 6 * unit
+    # in range: at most half of the largest E2M1 step (2 units); beyond 6 units (the block
+    # scale rounded down): saturated at 6 units with the sign kept
+    assert np.all(np.abs(deq - G)[inside] <= 1.0 * unit[inside] + 1e-300)
+    assert np.array_equal(deq[~inside], np.sign(G[~inside]) * 6 * unit[~inside])
+    assert np.any((sc3 & 0x78) == 0) and np.any(sc3 >= 0x70)  # subnormal and large scales
+
+
+def test_bf16_round_matches_torch_and_ties_to_even():
+    # fp32-representable inputs: torch's float32 -> bfloat16 conversion (round to nearest even)
+    rng = np.random.default_rng(9)
+    v = (rng.standard_normal(200_000) * np.exp2(rng.integers(-60, 60, 200_000))).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(F.bf16_round(v.astype(np.float64)), ref)
+    # exact halfway cases go to the even significand; one ulp either side goes the near way
+    one = 1.0 + 2.0 ** -8                 # halfway between 1 and 1 + 2^-7
+    assert F.bf16_round(np.array([one, 1.0 + 3 * 2.0 ** -8, -one]))[[0, 1, 2]].tolist() == \
+        [1.0, 1.0 + 2 * 2.0 ** -7, -1.0]
+    assert F.bf16_round(np.array([np.nextafter(one, 2.0)]))[0] == 1.0 + 2.0 ** -7
+    assert F.bf16_round(np.array([0.0, -0.0]))[1] == 0.0
+
+
+def _clean_row(rng, blocks=4):
+    # a row whose blocks hold a 6 (block max) and whose first block scale is 448: Q(v) = v
+    q = rng.integers(0, 16, size=(blocks * 16,))
+    q[::16] = 7
+    sc = rng.integers(0x30, 0x50, size=(blocks,))
+    sc[0] = 0x7E
+    return F.E2M1_TABLE[q] * np.repeat(F.E4M3_TABLE[sc], 16) * 0.25, sc
+
+
+def test_activation_choices_far_from_boundaries_is_the_rule():
+    rng = np.random.default_rng(12)
+    for _ in range(20):
+        v = rng.standard_normal(256) * np.exp2(rng.uniform(-10, 10))
+        ch = F.activation_choices(v)
+        assert len(ch) == 1 and np.array_equal(ch[0], F.fake_quantize_activation(v[None])[0])
+
+
+@pytest.mark.parametrize("rel,expect", [(1e-7, 2), (-1e-7, 2), (1e-3, 1)])
+def test_activation_choices_flip_one_element_at_an_e2m1_midpoint(rel, expect):
+    rng = np.random.default_rng(13)
+    v, sc = _clean_row(rng)
+    unit = F.E4M3_TABLE[sc[1]] * 0.25             # block 1's scale unit (row scale 0.25 exactly)
+    v[16 + 5] = 1.25 * unit * (1 + rel)           # between 1 and 1.5, just off the midpoint
+    ch = F.activation_choices(v)
+    assert len(ch) == expect
+    assert np.array_equal(ch[0], F.fake_quantize_activation(v[None])[0])
+    if expect == 2:
+        d = np.nonzero(ch[1] != ch[0])[0]
+        assert d.tolist() == [21] and abs(abs(ch[1][21] - ch[0][21]) - 0.5 * unit) < 1e-12 * unit
+        assert {ch[0][21], ch[1][21]} == {unit, 1.5 * unit}
+
+
+def test_activation_choices_flip_one_block_scale_at_an_e4m3_midpoint():
+    rng = np.random.default_rng(14)
+    v, sc = _clean_row(rng)
+    s = 0.25
+    lo, hi = F.E4M3_TABLE[0x44], F.E4M3_TABLE[0x45]
+    ratio = (lo + hi) / 2 * (1 + 1e-8)            # block 2's amax / (6 s), just above a midpoint
+    v[32:48] = v[32:48] / np.max(np.abs(v[32:48])) * ratio * 6 * s
+    ch = F.activation_choices(v)
+    assert len(ch) == 2
+    diff_blocks = sorted({int(i) // 16 for i in np.nonzero(ch[1] != ch[0])[0]})
+    assert diff_blocks == [2]
+    # the two scales are the midpoint's neighbours: block max at 6 units of one or the other
+    m0, m1 = np.max(np.abs(ch[0][32:48])), np.max(np.abs(ch[1][32:48]))
+    assert sorted([m0, m1]) == pytest.approx(sorted([6 * lo * s, 6 * hi * s]), rel=0, abs=1e-12)
