@@ -75,20 +75,32 @@ typedef struct {
   lmoe_dtype act_dtype, weight_dtype, out_dtype;
 } lmoe_config;
 
+/* Layouts of the E4M3 block scales of an NVFP4 weight (lmoe_nvfp4_weight.scale_layout). */
+typedef enum {
+  /* [rows, K/16] row-major, one scale per 16 consecutive k: the plain layout.  The forward
+   * entry points do not read it (they return LMOE_ERR_UNSUPPORTED before any launch):
+   * convert it once with lmoe_nvfp4_block_scales() and pass LMOE_NVFP4_SCALES_BLOCKED.     */
+  LMOE_NVFP4_SCALES_ROW_MAJOR = 0,
+  /* the tensor cores' block layout: 512-byte blocks of 128 rows x 64 k, ordered
+   * [rows/128][K/64]; inside a block the scale of row m = m0 + 32*m1 and 16-wide group kk
+   * sits at byte 16*m0 + 4*m1 + kk (what lmoe_nvfp4_block_scales() writes).                */
+  LMOE_NVFP4_SCALES_BLOCKED = 1
+} lmoe_nvfp4_scale_layout;
+
 /* One NVFP4-packed weight (host struct holding device pointers), "out x in" [rows, K]:
  *  data          [rows, K/2] bytes, two E2M1 codes per byte, the low nibble holds the even k
- *  scales        E4M3 block-scale codes (one per 16 consecutive k) in the tensor cores' block
- *                layout: 512-byte blocks of 128 rows x 64 k, ordered [rows/128][K/64]; inside
- *                a block the scale of row m = m0 + 32*m1 and 16-wide group kk sits at byte
- *                16*m0 + 4*m1 + kk.
- *                lmoe_nvfp4_block_scales() converts the row-major [rows, K/16] array once
- *                (for expert stacks, rows = E*rows_per_expert).
+ *  scales        E4M3 block-scale codes (one per 16 consecutive k), in `scale_layout`
+ *                (for expert stacks, rows = E*rows_per_expert)
  *  tensor_scale  fp32 second-level scale: 1 value, or one per expert for expert stacks
+ *  scale_layout  an lmoe_nvfp4_scale_layout; a zero-initialised struct declares row-major
+ *                scales, which the forward refuses, so scales in the wrong layout are never
+ *                read as if they were blocked
  *  value = e2m1(code) * e4m3(scale) * tensor_scale.                                    */
 typedef struct {
   const uint8_t* data;
   const uint8_t* scales;
   const float* tensor_scale;
+  int scale_layout;
 } lmoe_nvfp4_weight;
 
 /* Stage boundaries of one call, for stage_events (see lmoe_ex).  Event i is recorded on
@@ -148,9 +160,10 @@ lmoe_status lmoe_workspace_size(const lmoe_config* cfg, size_t* bytes);
  *  x         [T, D]   act_dtype
  *  W_router  [E, D]   fp32 when weight_dtype is LMOE_F32, else bf16
  *  W_pool    [L, D]   } bf16/fp32 per weight_dtype, or, for LMOE_NVFP4, a HOST pointer to
- *  W_gate    [E, I, L]}  an lmoe_nvfp4_weight (expert stacks: data [E, rows, K/2], scales
- *  W_up      [E, I, L]}  [E, rows, K/16], tensor_scale [E]; W_gate and W_up may use
- *  W_down    [E, L, I]}  different scales)
+ *  W_gate    [E, I, L]}  an lmoe_nvfp4_weight (expert stacks: data [E, rows, K/2], scales of
+ *  W_up      [E, I, L]}  E*rows rows, tensor_scale [E]; W_gate and W_up may use different
+ *  W_down    [E, L, I]}  scales; scale_layout must be LMOE_NVFP4_SCALES_BLOCKED, else
+ *                        LMOE_ERR_UNSUPPORTED)
  *  W_unpool  [D, L]   }
  *  g_pool [L], g_expert [E, L], g_pre [D], g_post [D]   fp32 RMSNorm gammas
  *  top_k     must equal cfg->top_k
@@ -196,7 +209,10 @@ lmoe_status latent_moe_forward_host_io_ex(const lmoe_config* cfg, const void* x_
                                           cudaStream_t stream, const lmoe_ex* ex);
 
 /* Reads (synchronising `stream`) and clears the device error word of `workspace`.
- * Returns LMOE_OK or LMOE_ERR_TIMEOUT; *detail (host, may be NULL) receives the raw word. */
+ * Returns LMOE_OK, LMOE_ERR_TIMEOUT (a device wait gave up: bits 0x1, 0x2, 0x4, 0x10) or
+ * LMOE_ERR_ARG (a forced expert id out of range or repeated: bit 0x8; routing structures
+ * that failed lmoe_validate_routing: bit 0x20); *detail (host, may be NULL) receives the raw
+ * word. */
 lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStream_t stream,
                               uint32_t* detail);
 
@@ -204,7 +220,8 @@ lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStrea
  *  xa (router/pooler input rows), logits [T,E] f32, topk_idx [T,k] i32, topk_w [T,k] f32,
  *  counts [E] i32, offsets [E+1] i32, row_of [T,k] i32, tok_of [T*k] i32,
  *  p [T,L] f32, xe [T*k, L] bf16 (expert-contiguous expert inputs), h [T*k, I] bf16,
- *  y [T*k, L] f32, ss_y [T*k, L/128] f32, c [T,L] bf16, u [T,D] f32, ss_p / ss_u
+ *  y [T*k, L] f32 (bf16 with NVFP4 weights), ss_y [T*k, L/128] f32 (sums of squares of the
+ *  stored y values), c [T,L] bf16, u [T,D] f32, ss_p / ss_u
  *  [rows, N/128] f32 (row sums of squares per 128 columns), err (u32).
  *  Unused fields are -1. */
 typedef struct {
@@ -275,6 +292,34 @@ lmoe_status lmoe_wait_selftest(const lmoe_config* cfg, void* workspace, long lon
  * is slower than the chunked permutation the forward call runs from its workspace. */
 lmoe_status lmoe_permute_noalloc(const int32_t* topk_idx, int T, int k, int E, int32_t* offsets,
                                  int32_t* row_of, int32_t* tok_of, cudaStream_t stream);
+
+/* Guard bands of the workspace, for memory-safety checks (no counterpart on the pages: a
+ * stand-in for a race/bounds sanitiser).  Every sub-buffer of the workspace is followed by
+ * LMOE_GUARD_BYTES bytes that no call reads or writes.  Writes *count (host) = the number of
+ * bands of a workspace for `cfg` (host_io != 0: the larger host-I/O workspace of
+ * lmoe_workspace_size_host_io()) and, when offsets != NULL (host array of `capacity`), the
+ * byte offset of each band from the start of the workspace.  A caller (a test) fills the
+ * workspace with a known byte pattern, runs the block, and checks that every band still
+ * holds it: a changed band is a write past the end of a sub-buffer.                    */
+#define LMOE_GUARD_BYTES 256
+lmoe_status lmoe_workspace_guards(const lmoe_config* cfg, int host_io, long long* offsets,
+                                  int capacity, int* count);
+
+/* Checks the routing structures the last call left in `workspace` (device, as for
+ * latent_moe_forward; asynchronous on `stream`) — the structures every later kernel indexes
+ * with: expert ids in [0, E); offsets starting at 0, non-decreasing, ending at T*k and
+ * equal to the per-expert counts' prefix sums; each (token, slot) pair's row (row_of, the
+ * scatter target of the pool norm and the source row of the combine) inside its expert's
+ * range, and each row the row of exactly one pair (tok_of); every 128-row and 256-row M tile
+ * inside its expert's rows with 1..128 (256) rows, the tiles covering T*k rows, the tile
+ * counts within their tables, each expert's first tile a tile of that expert.  Every value is
+ * bounds-checked before it is followed.  A violation sets bit 0x20 of the error word
+ * (lmoe_check_status then returns LMOE_ERR_ARG).  A library built with
+ * -DLMOE_BOUNDS_CHECKS=1 runs this check inside every forward call, right after the
+ * permutation, and on a violation also replaces the call's routing by one that the later
+ * kernels read in bounds (the output is then meaningless and the status says so).  No
+ * counterpart on the pages: a stand-in for a device bounds sanitiser.                   */
+lmoe_status lmoe_validate_routing(const lmoe_config* cfg, void* workspace, cudaStream_t stream);
 
 /* Number of kernels this library has launched in this process (all devices, all calls). */
 unsigned long long lmoe_kernel_launches(void);

@@ -23,7 +23,8 @@ from ._lib import (Config, LmoeError, lmoe_workspace_size, lmoe_workspace_size_h
                    latent_moe_forward_host_io, latent_moe_forward_host_io_ex, lmoe_check_status,
                    lmoe_wait_selftest, load,
                    LIB_PATH, STAGES, NUM_STAGE_EVENTS, lmoe_kernel_launches,
-                   lmoe_quantize_nvfp4, lmoe_nvfp4_block_scales)
+                   lmoe_quantize_nvfp4, lmoe_nvfp4_block_scales, SCALES_ROW_MAJOR, SCALES_BLOCKED,
+                   GUARD_BYTES, lmoe_workspace_guards, lmoe_validate_routing)
 
 load()
 
@@ -41,8 +42,8 @@ class LatentMoEBlock:
                  g_post, top_k: int, eps: float = 1e-6, weight_dtype: str = "bf16"):
         if weight_dtype == "nvfp4":   # (codes, row-major scales, s) -> scales in block layout
             def blocked(w, block_rows=128):
-                codes, scales, s = w
-                return codes, lmoe_nvfp4_block_scales(scales, codes.shape[-1] * 2, block_rows), s
+                codes, scales, s = w[:3]
+                return codes, lmoe_nvfp4_block_scales(scales, codes.shape[-1] * 2, block_rows), s, SCALES_BLOCKED
             W_pool, W_gate, W_up, W_down, W_unpool = map(blocked, (W_pool, W_gate, W_up, W_down, W_unpool))
         self.W = dict(W_router=W_router, W_pool=W_pool, g_pool=g_pool, W_gate=W_gate, W_up=W_up,
                       W_down=W_down, g_expert=g_expert, W_unpool=W_unpool, g_pre=g_pre, g_post=g_post)

@@ -36,8 +36,12 @@ class lmoe_config(ctypes.Structure):
                 ("out_dtype", ctypes.c_int)]
 
 
+SCALES_ROW_MAJOR, SCALES_BLOCKED = 0, 1   # lmoe_nvfp4_scale_layout
+
+
 class lmoe_nvfp4_weight(ctypes.Structure):
-    _fields_ = [("data", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p)]
+    _fields_ = [("data", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("tensor_scale", ctypes.c_void_p),
+                ("scale_layout", ctypes.c_int)]
 
 
 class lmoe_ex(ctypes.Structure):
@@ -140,10 +144,13 @@ def _ptr(t) -> int:
 
 
 def _weight_arg(w, keep: list):
-    """A dense tensor -> its pointer; an NVFP4 (codes, scales, tensor_scale) triple -> a pointer
-    to a host lmoe_nvfp4_weight (kept alive in ``keep``)."""
+    """A dense tensor -> its pointer; an NVFP4 (codes, scales, tensor_scale[, scale_layout])
+    tuple -> a pointer to a host lmoe_nvfp4_weight (kept alive in ``keep``).  Without a fourth
+    element the scales are declared row-major (which the forward refuses: convert them with
+    lmoe_nvfp4_block_scales and pass SCALES_BLOCKED)."""
     if isinstance(w, tuple):
-        s = lmoe_nvfp4_weight(_ptr(w[0]), _ptr(w[1]), _ptr(w[2]))
+        layout = w[3] if len(w) > 3 else SCALES_ROW_MAJOR
+        s = lmoe_nvfp4_weight(_ptr(w[0]), _ptr(w[1]), _ptr(w[2]), int(layout))
         keep.append(s)
         return ctypes.addressof(s)
     return _ptr(w)
@@ -257,6 +264,35 @@ def lmoe_wait_selftest(cfg, workspace, budget_cycles: int, stream=None):
     c = cfg.c()
     _check(_lib().lmoe_wait_selftest(ctypes.byref(c), _ptr(workspace), int(budget_cycles), _stream(stream)),
            "lmoe_wait_selftest")
+
+
+GUARD_BYTES = 256   # LMOE_GUARD_BYTES
+
+
+def lmoe_workspace_guards(cfg, host_io: bool = False, lib=None) -> list:
+    """Byte offsets of the workspace's guard bands (each GUARD_BYTES long)."""
+    L = lib or _lib()
+    fn = L.lmoe_workspace_guards
+    fn.argtypes = [ctypes.POINTER(lmoe_config), ctypes.c_int, _P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    fn.restype = ctypes.c_int
+    c = cfg.c()
+    n = ctypes.c_int()
+    _check(fn(ctypes.byref(c), 1 if host_io else 0, None, 0, ctypes.byref(n)), "lmoe_workspace_guards")
+    arr = (ctypes.c_longlong * max(n.value, 1))()
+    _check(fn(ctypes.byref(c), 1 if host_io else 0, ctypes.cast(arr, _P), n.value, ctypes.byref(n)),
+           "lmoe_workspace_guards")
+    return list(arr[:n.value])
+
+
+def lmoe_validate_routing(cfg, workspace, stream=None, lib=None):
+    """Check the routing structures the last call left in ``workspace``; a violation shows in
+    lmoe_check_status (LMOE_ERR_ARG, bit 0x20 of the error word)."""
+    L = lib or _lib()
+    fn = L.lmoe_validate_routing
+    fn.argtypes = [ctypes.POINTER(lmoe_config), _P, _P]
+    fn.restype = ctypes.c_int
+    c = cfg.c()
+    _check(fn(ctypes.byref(c), _ptr(workspace), _stream(stream)), "lmoe_validate_routing")
 
 
 def lmoe_kernel_launches() -> int:

@@ -3,6 +3,11 @@
 Each translation unit compiles in its own nvcc process, in parallel; objects go
 to ``_build/`` next to this file.  A unit is recompiled when it or any header
 under csrc/ or include/ is newer than its object.
+
+``build(checked=True)`` makes the checked variant liblatent_moe_checked.so (objects
+in ``_build_checked/``): the same sources with -DLMOE_BOUNDS_CHECKS=1, whose forward
+validates the routing structures before any kernel indexes with them.  It is off by
+default; the tests that exercise it build it on demand.
 """
 from __future__ import annotations
 
@@ -17,6 +22,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblatent_moe.so")
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "liblatent_moe_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -47,8 +54,13 @@ def _newer(src: str, obj: str, deps) -> bool:
     return os.path.getmtime(src) > t or any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    """Build (or reuse) the shared library and return its path."""
+def build(verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    """Build (or reuse) the shared library and return its path (checked: the bounds-checked
+    variant)."""
+    BUILD = BUILD_CHECKED if checked else globals()["BUILD"]
+    LIB = LIB_CHECKED if checked else globals()["LIB"]
+    if checked:
+        extra_flags = tuple(extra_flags) + ("-DLMOE_BOUNDS_CHECKS=1",)
     os.makedirs(BUILD, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     deps = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \

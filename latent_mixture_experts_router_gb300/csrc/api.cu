@@ -32,6 +32,11 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 namespace {
 
 constexpr size_t kAlign = 256;
+// Every workspace sub-buffer is followed by a guard band of LMOE_GUARD_BYTES that no kernel
+// writes (lmoe_workspace_guards lists them): a write past the end of a sub-buffer lands there
+// and shows as a changed canary.
+constexpr size_t kGuard = LMOE_GUARD_BYTES;
+constexpr int kMaxGuards = 64;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 int cdiv(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
@@ -49,6 +54,8 @@ struct Layout {
   long long w_router, w_pool, w_gate, w_up, w_down, w_unpool;
   long long x_stage, out_stage, host_io_total;
   int ld_logits, ld_ss_p, ld_ss_y, ld_ss_u, max_tiles, max_tiles2;
+  long long guards[kMaxGuards];   // start of the guard band after each sub-buffer
+  int n_guards;
 };
 
 // Upper bound of the split count of the grouped NVFP4 GEMMs (the kernel picks the count from
@@ -136,12 +143,15 @@ void make_layout(const lmoe_config* c, Layout* L) {
                   k = c->top_k, R = T * k;
   const bool f32w = c->weight_dtype == LMOE_F32;
   size_t off = 0;
+  memset(L, 0xff, sizeof(*L));
+  L->n_guards = 0;
   auto take = [&](size_t bytes) -> long long {
     const long long o = static_cast<long long>(off);
     off = align_up(off + bytes, kAlign);
+    if (L->n_guards < kMaxGuards) L->guards[L->n_guards++] = static_cast<long long>(off);
+    off += kGuard;
     return o;
   };
-  memset(L, 0xff, sizeof(*L));
   lmoe_workspace_layout& P = L->pub;
   P.xa_cols = static_cast<int>((f32w ? 3 : 2) * D);
   L->ld_logits = static_cast<int>(align_up(E, 32));
@@ -188,7 +198,7 @@ void make_layout(const lmoe_config* c, Layout* L) {
     P.xe = take(R * Ld * 2);
     P.h = take(R * I * 2);
   }
-  P.y = take(R * Ld * 4);
+  P.y = take(R * Ld * (fp4 ? 2 : 4));   // bf16 with NVFP4 weights, fp32 otherwise
   P.ss_y = take(R * L->ld_ss_y * 4);
   if (fp4) {
     P.c = take(T * Ld / 2);
@@ -388,8 +398,8 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
       LMOE_CUDA(launch_swiglu_reduce_nvfp4(partial, splits_dev, static_cast<int>(a_rows), N, tiles,
                                            n_tiles, m_tiles, static_cast<uint8_t*>(out), out_scales, s));
     else
-      LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, static_cast<float*>(out),
-                                     ldo, ss, ld_ss, 128, s, adaptive ? splits_dev : nullptr));
+      LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, out, ldo, ss, ld_ss, 128, s,
+                                     adaptive ? splits_dev : nullptr, epi == kFp4EpiBf16Ss));
   }
   return LMOE_OK;
 }
@@ -453,6 +463,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     for (int i = 0; i < 5; ++i) {
       q4[i] = static_cast<const lmoe_nvfp4_weight*>(wv[i]);
       if (!q4[i]->data || !q4[i]->scales || !q4[i]->tensor_scale) return LMOE_ERR_ARG;
+      // the kernels read the block layout only: row-major scales must be converted first
+      if (q4[i]->scale_layout != LMOE_NVFP4_SCALES_BLOCKED) return LMOE_ERR_UNSUPPORTED;
       if (!aligned16(q4[i]->data) || !aligned16(q4[i]->scales) || !aligned16(q4[i]->tensor_scale))
         return LMOE_ERR_ALIGN;
     }
@@ -569,9 +581,15 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   };
   const int pool_mh = dense_mh_n(dsp.pooler, cdiv(Ld, kBNWide));
   const int unpool_mh = dense_mh_n(dsp.unpool, cdiv(D, kBNWide));
+  // NVFP4 dense GEMMs of many rows (unsplit, at least two waves of 128 x 256 tiles) take the
+  // 256-wide tiles: the A tile is then read once per 256 output columns
+  auto fp4_dense_epi = [&](int splits, int N) {
+    return splits <= 1 && N % 256 == 0 && 1LL * m_tiles_T * (N / 256) >= 2 * kSplitSms ? kFp4EpiF32SsWide
+                                                                                         : kFp4EpiF32Ss;
+  };
   auto pooler = [&](cudaStream_t ps) -> lmoe_status {
     if (fp4)
-      return run_gemm_fp4(kFp4EpiF32Ss, xq, T, D, op(q4[0]), Ld, nullptr, Ld, nullptr, nullptr, m_tiles_T,
+      return run_gemm_fp4(fp4_dense_epi(dsp.pooler, Ld), xq, T, D, op(q4[0]), Ld, nullptr, Ld, nullptr, nullptr, m_tiles_T,
                           p, Ld, nullptr, ss_p, L.ld_ss_p, xq_s, q4[0]->tensor_scale, nullptr, err, budget,
                           ps, T, dsp.pooler, partial_pool);
     const int pool_k = f32w ? 3 * D : D;
@@ -642,6 +660,12 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                              tile_base, tiles2, n_tiles2, static_cast<int32_t*>(at(L.perm_hist)),
                              static_cast<int32_t*>(at(L.perm_base))));
   }
+#if LMOE_BOUNDS_CHECKS
+  // checked build: the routing structures are validated before any kernel follows them; on a
+  // violation the error word says so and the rest of the call runs on a harmless routing
+  LMOE_CUDA(launch_validate_routing(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, L.max_tiles,
+                                    tile_base, tiles2, n_tiles2, L.max_tiles2, err, true, s));
+#endif
   if (ex && ex->near_tie_count_out)
     LMOE_CUDA(cudaMemcpyAsync(ex->near_tie_count_out, near_tie, 4, cudaMemcpyDeviceToDevice, s));
   if (side != nullptr) {
@@ -679,18 +703,18 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                       grouped_splits(I, Ld / 256), partial, splits_dev);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_DOWN);
-    // S8 grouped down (fp32 y) with per-row partial sums of squares
-    st = run_gemm_fp4(kFp4EpiF32Ss, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
+    // S8 grouped down: y rounded to bf16, with per-row partial sums of squares of those values
+    st = run_gemm_fp4(kFp4EpiBf16Ss, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
                       L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
                       nullptr, err, budget, s, R / E, grouped_splits(Ld, I / 256), partial, splits_dev + 1);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_COMBINE);
     // S9 combine, c quantised per token
-    LMOE_CUDA(launch_combine_nvfp4(y, ss_y, L.ld_ss_y, row_of, tk_idx, tk_w, g_expert, T, Ld, k, eps,
+    LMOE_CUDA(launch_combine_nvfp4(y, true, ss_y, L.ld_ss_y, row_of, tk_idx, tk_w, g_expert, T, Ld, k, eps,
                                    wsb + L.pub.c, wsb + L.pub.c_scale, c_s, s));
     LMOE_MARK(LMOE_STAGE_UNPOOLER);
     // S10 unpooler u = s_c * s_W * (Q(c) . W_unpool^T)
-    st = run_gemm_fp4(kFp4EpiF32Ss, cq, T, Ld, op(q4[4]), D, nullptr, D, nullptr, nullptr, m_tiles_T, u,
+    st = run_gemm_fp4(fp4_dense_epi(dsp.unpool, D), cq, T, Ld, op(q4[4]), D, nullptr, D, nullptr, nullptr, m_tiles_T, u,
                       D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s, T, dsp.unpool,
                       partial, nullptr, false);
     if (st != LMOE_OK) return st;
@@ -848,7 +872,43 @@ lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStrea
   if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return LMOE_ERR_CUDA;
   if (detail) *detail = word;
   if (word & (kErrWaitProducer | kErrWaitMma | kErrWaitEpilogue | kErrDrain)) return LMOE_ERR_TIMEOUT;
-  if (word & kErrBadIndex) return LMOE_ERR_ARG;
+  if (word & (kErrBadIndex | kErrBounds)) return LMOE_ERR_ARG;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_workspace_guards(const lmoe_config* cfg, int host_io, long long* offsets, int capacity,
+                                  int* count) {
+  const lmoe_status st = check_config(cfg);
+  if (st != LMOE_OK) return st;
+  if (count == nullptr || capacity < 0) return LMOE_ERR_ARG;
+  Layout L;
+  make_layout(cfg, &L);
+  // the bands after the two host-I/O staging buffers are the last two
+  const int n = host_io ? L.n_guards : L.n_guards - 2;
+  *count = n;
+  if (offsets != nullptr)
+    for (int i = 0; i < n && i < capacity; ++i) offsets[i] = L.guards[i];
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_validate_routing(const lmoe_config* cfg, void* workspace, cudaStream_t stream) {
+  const lmoe_status st = check_config(cfg);
+  if (st != LMOE_OK) return st;
+  if (workspace == nullptr) return LMOE_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) != 0) return LMOE_ERR_ALIGN;
+  Layout L;
+  make_layout(cfg, &L);
+  char* ws = static_cast<char*>(workspace);
+  auto at = [&](long long o) { return static_cast<void*>(ws + o); };
+  if (launch_validate_routing(static_cast<int32_t*>(at(L.pub.topk_idx)), cfg->T, cfg->top_k, cfg->n_experts,
+                              static_cast<const int32_t*>(at(L.pub.counts)), static_cast<int32_t*>(at(L.pub.offsets)),
+                              static_cast<int32_t*>(at(L.pub.row_of)), static_cast<const int32_t*>(at(L.pub.tok_of)),
+                              static_cast<const Tile*>(at(L.pub.tiles)), static_cast<int32_t*>(at(L.pub.n_tiles)),
+                              L.max_tiles, static_cast<int32_t*>(at(L.tile_base)),
+                              static_cast<const Tile*>(at(L.tiles2)),
+                              static_cast<int32_t*>(at(L.n_tiles2)), L.max_tiles2,
+                              static_cast<unsigned*>(at(L.pub.err)), false, stream) != cudaSuccess)
+    return LMOE_ERR_CUDA;
   return LMOE_OK;
 }
 

@@ -30,7 +30,13 @@
 // The A box covers only the tile's live rows rounded up to 32 (a decode tile holds a few
 // rows of one expert), and the producer loads the next tile's table entry one tile ahead.
 // Epilogues: kFp4EpiF32Ss — alpha * acc as fp32 plus per-row partial sums of squares; two
-// accumulator buffers, so the next tile's MMAs overlap this tile's epilogue.
+// accumulator buffers, so the next tile's MMAs overlap this tile's epilogue.  kFp4EpiBf16Ss —
+// the same with the values rounded to bf16 and the sums of squares taken of the rounded values
+// (the expert down projection: each tile's partial sum of squares of the bf16 values it holds).
+// kFp4EpiF32SsWide — the fp32 epilogue on 128 x 256 tiles for dense GEMMs of many rows: a stage
+// loads the two 128-row halves of the tile's weights (as gate/up loads its two weights), so
+// the A tile is read once per 256 output columns (the operand intake of an SM, ~97 GB/s
+// measured, bounds these GEMMs); one accumulator buffer of 256 columns.
 // kFp4EpiSwiGLUQuant — gate and up tiles of the same columns, h = silu(alpha_g acc_g) *
 // (alpha_u acc_u) requantised to NVFP4 with scale 1 (block scales only, through the
 // reciprocal table) for the down projection; one accumulator buffer (two would leave no
@@ -83,7 +89,11 @@ LMOE_DEV void mma_nvf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint3
 
 template <int BN, int EPI>
 struct Fp4Cfg {
-  static constexpr bool kDual = (EPI == kFp4EpiSwiGLUQuant);
+  // kDual: two B boxes per stage into two accumulators of BN columns — gate and up tiles of the
+  // same columns (SwiGLU), or the two BN-row halves of one 2*BN-wide output tile (kWide)
+  static constexpr bool kWide = (EPI == kFp4EpiF32SsWide);
+  static constexpr bool kDual = (EPI == kFp4EpiSwiGLUQuant) || kWide;
+  static constexpr int kTileN = kWide ? 2 * BN : BN;   // output columns of one tile
   static constexpr int kNB = kDual ? 2 : 1;
   static constexpr int kStages = kDual ? 4 : 6;
   static constexpr int kKStep = 4;                 // MMAs (K = 64 each) per stage
@@ -157,14 +167,17 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
     prefetch_tmap(&tmB);
     if (C::kDual) prefetch_tmap(&tmB2);
     int brow, kb0, kb1;
-    if (first_tile_hint(args.tiles, args.n_tiles, args.max_tiles, args.n_groups, args.M, args.N, BN,
+    if (first_tile_hint(args.tiles, args.n_tiles, args.max_tiles, args.n_groups, args.M, args.N, C::kTileN,
                         args.k_splits, args.num_kb, args.adaptive_splits != 0, brow, kb0, kb1)) {
       kb1 = min(kb1, kb0 + kPrefetchKb);
       const size_t sf0 = static_cast<size_t>(brow / BN) * args.num_kb * 4 * 512;
       for (int kb = kb0; kb < kb1; ++kb) {
         prefetch_l2_tile_2d(&tmB, kb * 128, brow);
         prefetch_l2_bulk(args.b_scales + sf0 + kb * 2048, 2048u);
-        if (C::kDual) {
+        if (C::kWide) {   // the tile's second BN-row half of the same weights
+          prefetch_l2_tile_2d(&tmB, kb * 128, brow + BN);
+          prefetch_l2_bulk(args.b_scales + sf0 + static_cast<size_t>(args.num_kb) * 4 * 512 + kb * 2048, 2048u);
+        } else if (C::kDual) {
           prefetch_l2_tile_2d(&tmB2, kb * 128, brow);
           prefetch_l2_bulk(args.b2_scales + sf0 + kb * 2048, 2048u);
         }
@@ -184,7 +197,7 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   griddep_enter();
   // CTAs past the live tile ids walk nothing and go straight to the teardown
-  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, BN, args.k_splits, args.num_kb,
+  const TileWalk walk(args.tiles, args.n_tiles, args.M, args.N, C::kTileN, args.k_splits, args.num_kb,
                       args.adaptive_splits != 0);
   if (args.splits_out != nullptr && blockIdx.x == 0 && threadIdx.x == 0)
     *args.splits_out = walk.splits;
@@ -206,13 +219,18 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
         const TileRef nxt = find_tile(walk, cur.id + gridDim.x);
         const Tile nt = nxt.valid ? tile_of(walk, nxt.mt) : Tile{0, 0, 0, 0};
         const int row0 = ct.row0;
-        const int brow = ct.expert * args.N + cur.ntile * BN;
+        const int brow = ct.expert * args.N + cur.ntile * C::kTileN;
         const int abox = min(4, (ct.nrows + 31) / 32);   // A rows past the live ones are not read
         const CUtensorMap* tA = amap[abox - 1];
         const uint32_t tx = C::tx_bytes(abox * 32);
         const uint8_t* sfa_src = args.a_scales + static_cast<size_t>(cur.mt) * kblk * 512;
         const uint8_t* sfb_src = args.b_scales + static_cast<size_t>(brow / BN) * kblk * 512;
-        const uint8_t* sfb2_src = C::kDual ? args.b2_scales + static_cast<size_t>(brow / BN) * kblk * 512 : nullptr;
+        // second B box: the next BN rows of the same weights (wide tile), or the up weights
+        const uint8_t* sfb2_src = C::kWide ? sfb_src + static_cast<size_t>(kblk) * 512
+                                  : C::kDual ? args.b2_scales + static_cast<size_t>(brow / BN) * kblk * 512
+                                             : nullptr;
+        const CUtensorMap* tB2 = C::kWide ? &tmB : &tmB2;
+        const int brow2 = C::kWide ? brow + BN : brow;
         int kb0, kb1;
         walk.k_range(cur.id, kb0, kb1);
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -230,7 +248,7 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
           tma_load_2d_hint(st + C::kOffB, &tmB, &full[s], kb * 128, brow, pol_b);
           bulk_load(st + C::kOffSfb, sfb_src + kb * 2048, C::kSfbBytes, &full[s]);
           if (C::kDual) {
-            tma_load_2d_hint(st + C::kOffB + C::kBBytes, &tmB2, &full[s], kb * 128, brow, pol_b);
+            tma_load_2d_hint(st + C::kOffB + C::kBBytes, tB2, &full[s], kb * 128, brow2, pol_b);
             bulk_load(st + C::kOffSfb + C::kSfbBytes, sfb2_src + kb * 2048, C::kSfbBytes, &full[s]);
           }
           ++it;
@@ -354,14 +372,54 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
       bool released = false;   // the accumulator buffer handed back before the stores
       const bool row_ok = r < nrows;
       const long long grow = static_cast<long long>(row0) + r;
-      const int n0 = ntile * BN;
+      const int n0 = ntile * C::kTileN;
       const uint32_t tq = tmem + buf * C::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
       const float rs = (args.row_scale != nullptr && row_ok) ? args.row_scale[grow] : 1.f;
-      if constexpr (EPI == kFp4EpiF32Ss) {
-        const float alpha = rs * args.tensor_scale[args.tiles ? expert : 0];
-        const bool split = walk.splits > 1;   // split-K: alpha * partial product, no ss
+      if constexpr (C::kWide) {
+        // warp half h takes accumulator columns [h BN, (h+1) BN) = output columns n0 + h BN ..:
+        // all of them are read into registers and the single accumulator buffer is handed back
+        // to the MMA issuer before the scaling and the stores
+        const float alpha = rs * args.tensor_scale[0];
+        const bool split = walk.splits > 1;
+        constexpr int kCh = BN / 32;
+        uint32_t v[kCh][32];
+#pragma unroll
+        for (int ch = 0; ch < kCh; ++ch) tmem_ld_32cols(tq + half * BN + 32 * ch, v[ch]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        released = true;
+        const int cbase = n0 + half * BN;
         float* orow = split ? args.partial + (static_cast<long long>(id % walk.splits) * args.M + grow) * args.N
                             : static_cast<float*>(args.out) + grow * args.ldo;
+        float ss = 0.f;
+        if (row_ok && cbase + BN <= args.N) {
+#pragma unroll
+          for (int ch = 0; ch < kCh; ++ch) {
+            float4* o = reinterpret_cast<float4*>(orow + cbase + 32 * ch);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 f = make_float4(__uint_as_float(v[ch][4 * i]) * alpha, __uint_as_float(v[ch][4 * i + 1]) * alpha,
+                                           __uint_as_float(v[ch][4 * i + 2]) * alpha, __uint_as_float(v[ch][4 * i + 3]) * alpha);
+              ss = fmaf(f.x, f.x, ss);
+              ss = fmaf(f.y, f.y, ss);
+              ss = fmaf(f.z, f.z, ss);
+              ss = fmaf(f.w, f.w, ss);
+              o[i] = f;
+            }
+          }
+          if (!split) args.ss[grow * args.ld_ss + cbase / BN] = ss;   // one sum per 128 columns
+        }
+      } else if constexpr (EPI == kFp4EpiF32Ss || EPI == kFp4EpiBf16Ss) {
+        const float alpha = rs * args.tensor_scale[args.tiles ? expert : 0];
+        const bool split = walk.splits > 1;   // split-K: alpha * partial product (fp32), no ss
+        // bf16 output (unsplit): the values are rounded and the sum of squares is taken of
+        // the rounded values (LMSYS Muse Spark Open post, "Fused per-expert post-norm")
+        const bool bf = EPI == kFp4EpiBf16Ss && !split;
+        float* orow = split ? args.partial + (static_cast<long long>(id % walk.splits) * args.M + grow) * args.N
+                            : static_cast<float*>(args.out) + grow * args.ldo;
+        __nv_bfloat16* brow = static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo;
         float ss = 0.f;
 #pragma unroll 1
         for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
@@ -370,16 +428,33 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
           tmem_ld_wait();
           const int col = n0 + c0;
           if (row_ok && col + 32 <= args.N) {
-            float4* o = reinterpret_cast<float4*>(orow + col);
+            if (bf) {
+              uint4* o = reinterpret_cast<uint4*>(brow + col);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 f = make_float4(__uint_as_float(v[4 * i]) * alpha, __uint_as_float(v[4 * i + 1]) * alpha,
-                                           __uint_as_float(v[4 * i + 2]) * alpha, __uint_as_float(v[4 * i + 3]) * alpha);
-              ss = fmaf(f.x, f.x, ss);
-              ss = fmaf(f.y, f.y, ss);
-              ss = fmaf(f.z, f.z, ss);
-              ss = fmaf(f.w, f.w, ss);
-              o[i] = f;
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  const float a = bf16_round(__uint_as_float(v[8 * i + 2 * h]) * alpha);
+                  const float b = bf16_round(__uint_as_float(v[8 * i + 2 * h + 1]) * alpha);
+                  ss = fmaf(a, a, ss);
+                  ss = fmaf(b, b, ss);
+                  w4[h] = pack_bf16x2(a, b);
+                }
+                o[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
+            } else {
+              float4* o = reinterpret_cast<float4*>(orow + col);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 f = make_float4(__uint_as_float(v[4 * i]) * alpha, __uint_as_float(v[4 * i + 1]) * alpha,
+                                             __uint_as_float(v[4 * i + 2]) * alpha, __uint_as_float(v[4 * i + 3]) * alpha);
+                ss = fmaf(f.x, f.x, ss);
+                ss = fmaf(f.y, f.y, ss);
+                ss = fmaf(f.z, f.z, ss);
+                ss = fmaf(f.w, f.w, ss);
+                o[i] = f;
+              }
             }
           }
         }
@@ -484,7 +559,7 @@ cudaError_t launch_fp4_one(const CUtensorMap* maps, const Fp4Args& a, int m_tile
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const long long ids = tile_id_bound(m_tiles, a.N, BN, a.k_splits > 1 ? a.k_splits : 1);
+  const long long ids = tile_id_bound(m_tiles, a.N, C::kTileN, a.k_splits > 1 ? a.k_splits : 1);
   if (ids == 0) return cudaSuccess;
   const unsigned grid = static_cast<unsigned>(ids < sm_count() ? ids : sm_count());
   return launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, s, maps[0], maps[1], maps[2], maps[3],
@@ -498,6 +573,8 @@ cudaError_t launch_gemm_fp4(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Ar
   switch (epi) {
     case kFp4EpiF32Ss: return launch_fp4_one<kBNFp4, kFp4EpiF32Ss>(maps, a, m_tiles, s);
     case kFp4EpiSwiGLUQuant: return launch_fp4_one<kBNFp4, kFp4EpiSwiGLUQuant>(maps, a, m_tiles, s);
+    case kFp4EpiBf16Ss: return launch_fp4_one<kBNFp4, kFp4EpiBf16Ss>(maps, a, m_tiles, s);
+    case kFp4EpiF32SsWide: return launch_fp4_one<kBNFp4, kFp4EpiF32SsWide>(maps, a, m_tiles, s);
   }
   return cudaErrorInvalidValue;
 }

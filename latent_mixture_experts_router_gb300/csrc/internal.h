@@ -27,6 +27,7 @@ enum : uint32_t {
   kErrWaitEpilogue = 1u << 2,
   kErrBadIndex = 1u << 3,
   kErrDrain = 1u << 4,
+  kErrBounds = 1u << 5,   // routing structures failed validation (launch_validate_routing)
 };
 
 enum EpiKind : int {
@@ -38,6 +39,10 @@ enum EpiKind : int {
 enum Fp4EpiKind : int {
   kFp4EpiF32Ss = 0,         // alpha * acc as fp32 + per-row partial sums of squares
   kFp4EpiSwiGLUQuant = 1,   // silu(alpha_g a) * (alpha_u b), requantised to NVFP4 (scale 1)
+  kFp4EpiBf16Ss = 2,        // alpha * acc rounded to bf16 + partial sums of squares of the
+                            // rounded values (the expert down projection's y)
+  kFp4EpiF32SsWide = 3,     // as kFp4EpiF32Ss, with 128 x 256 output tiles (dense GEMMs of many
+                            // rows: the two 128-row halves of the tile's weights per stage)
 };
 
 // One M tile of a grouped GEMM: rows [row0, row0 + nrows) of A, all of expert `expert`.
@@ -77,7 +82,7 @@ struct Fp4Args {
   void* out;                 // fp32 [rows, ldo] (kFp4EpiF32Ss) or codes [rows, ldo/2] (quant)
   long long ldo;             // output row length in elements
   uint8_t* out_scales;       // quant: E4M3 block scales [rows, ldo/16]
-  float* ss;                 // kFp4EpiF32Ss: [rows, ld_ss] partial sums of squares
+  float* ss;                 // kFp4Epi*Ss: [rows, ld_ss] partial sums of squares
   int ld_ss;
   const float* row_scale;    // per A row fp32 scale, or nullptr (1)
   const float* tensor_scale; // per expert (grouped) or [0]: scale of B
@@ -118,23 +123,25 @@ cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int
 // row-major E4M3 scales [rows, K/16] -> block layout with blocks of block_rows (64 or 128) rows
 cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K, int block_rows,
                                       uint8_t* dst, cudaStream_t s);
-cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, const int32_t* row_of,
-                                 const int32_t* idx, const float* w, const float* g_expert, int T,
-                                 int L, int k, float eps, uint8_t* codes, uint8_t* scales,
-                                 float* s_row, cudaStream_t s);
+// y: [T*k, L] bf16 (y_bf16) or fp32
+cudaError_t launch_combine_nvfp4(const void* y, bool y_bf16, const float* ss_y, int ld_ss,
+                                 const int32_t* row_of, const int32_t* idx, const float* w,
+                                 const float* g_expert, int T, int L, int k, float eps, uint8_t* codes,
+                                 uint8_t* scales, float* s_row, cudaStream_t s);
 cudaError_t launch_quantize_nvfp4(const float* src, long long rows, int K, bool row_scale,
                                   uint8_t* codes, uint8_t* scales, float* s_row, cudaStream_t s);
 
 // Streaming multiprocessors of the current device (persistent grids).
 int sm_count();
 
-// Sums split-K partials [splits][rows][N] in split order into out [rows, ldo] (fp32) and, when
+// Sums split-K partials [splits][rows][N] in split order into out [rows, ldo] (fp32, or bf16
+// when out_bf16: then the sums of squares are those of the rounded values) and, when
 // ss != nullptr, writes per-row partial sums of squares per group of `group` columns.  With
 // splits_dev != nullptr the split count is read there on the device (adaptive grouped GEMMs)
 // and `splits` is only its upper bound; a count of 1 means the GEMM wrote out itself.
-cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, float* out,
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, void* out,
                                  long long ldo, float* ss, int ld_ss, int group, cudaStream_t s,
-                                 const int* splits_dev = nullptr);
+                                 const int* splits_dev = nullptr, bool out_bf16 = false);
 // Grouped SwiGLU after an adaptive split-K gate/up GEMM: sums the [splits][rows][2N] partials
 // (gate | up, already scaled), h = silu(gate) * up, quantised to NVFP4 with scale 1: codes
 // [rows, N/2] and E4M3 block scales in the block layout of M tile `mt` (the h operand of the
@@ -239,6 +246,18 @@ cudaError_t launch_postnorm_residual(const void* x, bool x_f32, float* u,
                                      const float* upart = nullptr, int usplits = 1,
                                      const float* g_next = nullptr, void* next_out = nullptr);
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s);
+// Checks the routing structures one call left in its workspace: ids in [0, E); offsets start
+// at 0, never decrease, end at R = T k and agree with counts; every pair's row lies in its
+// expert's range and every row is the row of exactly one pair (row_of / tok_of: the scatter
+// targets); every M tile (and 256-row tile) lies inside its expert's rows with 1..128 (256)
+// rows, the tiles cover R rows, the tile counts are within the tables, and each expert's first
+// tile (tile_base) is a tile of that expert.  A violation sets kErrBounds in *err; with
+// `sanitize` the call's routing is also replaced by one that every later kernel reads in bounds
+// (no tiles; every pair to row 0 of expert 0), so the rest of the call runs harmlessly.
+cudaError_t launch_validate_routing(int32_t* idx, int T, int k, int E, const int32_t* counts, int32_t* offsets,
+                                    int32_t* row_of, const int32_t* tok_of, const Tile* tiles, int32_t* n_tiles,
+                                    int max_tiles, int32_t* tile_base, const Tile* tiles2, int32_t* n_tiles2,
+                                    int max_tiles2, unsigned* err, bool sanitize, cudaStream_t s);
 // fp32 weight [rows, K] -> bf16 [rows, parts*K]: part q is W_hi when bit q of lo_mask is 0,
 // else W_lo = bf16(W - W_hi).  [hi | hi | lo] pairs with activations [x_hi | x_lo | x_hi];
 // [hi | lo] pairs with one activation read twice.

@@ -108,11 +108,11 @@ constexpr int kCombineBatch = 4;          // slots per batch of loads at few tok
 constexpr int kCombineBatchMaxT = 512;    // "few": a token per CTA (or per cluster) fills no GPU
 
 // acc[0, NC) += sum over slots j (in slot order) of coef[j] * y[row[j]][i, i+NC) * g[e[j]][i, i+NC)
-// (NC = 8 or 16).  The loads of NB slots are issued together, before their multiply-adds.
+// (NC = 8 or 16; y fp32, or bf16 when !YF32).  The loads of NB slots are issued together, before their multiply-adds.
 // NB > 1 for few tokens, where the combine is a chain of round trips and more loads in
 // flight shorten it; NB = 1 for many, where the registers would halve the CTAs an SM holds.
-template <int NC, int NB>
-__device__ __forceinline__ void combine_cols(const float* __restrict__ y, const float* __restrict__ g_expert,
+template <int NC, int NB, bool YF32 = true>
+__device__ __forceinline__ void combine_cols(const void* __restrict__ y, const float* __restrict__ g_expert,
                                              int L, int i, int k, const int* rows, const int* es,
                                              const float* coef, float (&acc)[NC]) {
   static_assert(NC == 8 || NC == 16, "columns per thread");
@@ -124,7 +124,7 @@ __device__ __forceinline__ void combine_cols(const float* __restrict__ y, const 
 #pragma unroll
         for (int h = 0; h < NC / 8; ++h) {
           float a[8], b[8];
-          load8_f32(y + static_cast<long long>(rows[j0 + jj]) * L + i + 8 * h, a);
+          load8(y, YF32, static_cast<long long>(rows[j0 + jj]) * L + i + 8 * h, a);
           load8_f32(g_expert + static_cast<long long>(es[j0 + jj]) * L + i + 8 * h, b);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -287,13 +287,20 @@ __device__ __forceinline__ void warp_topk(float* vals, const int32_t* forced_row
       sval[j] = vals[e];
     }
   } else {
+    // A NaN logit (a NaN or infinity in the token's input) orders below every number, as -inf;
+    // an expert already selected is marked NaN and skipped, so every round picks a valid index
+    // distinct from the earlier ones even when all logits are -inf or NaN.
+    for (int i = lane; i < E; i += 32)
+      if (vals[i] != vals[i]) vals[i] = -INFINITY;
+    __syncwarp();
     const int rounds = (k < E) ? k + 1 : k;
     for (int j = 0; j < rounds; ++j) {
       float best = -INFINITY;
       int bi = 0x7fffffff;
       for (int i = lane; i < E; i += 32) {
         const float v = vals[i];
-        if (v > best || (v == best && i < bi)) {
+        if (v != v) continue;   // selected in an earlier round
+        if (bi == 0x7fffffff || v > best || (v == best && i < bi)) {
           best = v;
           bi = i;
         }
@@ -310,7 +317,7 @@ __device__ __forceinline__ void warp_topk(float* vals, const int32_t* forced_row
       if (j < k) {
         sel[j] = bi;
         sval[j] = best;
-        if (lane == 0) vals[bi] = -INFINITY;
+        if (lane == 0) vals[bi] = __int_as_float(0x7fc00000);   // NaN: taken
         __syncwarp();
       } else if (lane == 0 && near_tie != nullptr && (sval[k - 1] - best) < 1e-3f) {
         atomicAdd(near_tie, 1);
@@ -1091,9 +1098,9 @@ __global__ void __launch_bounds__(kRowThreads) poolnorm_scatter_nvfp4_kernel(
 
 // Combine whose output c is quantised (row scale per token) for the unpooler.
 // Dynamic smem: L + 256 floats.
-template <int NB>
+template <int NB, bool YF32>
 __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
-    const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
+    const void* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const float* __restrict__ w,
     const float* __restrict__ g_expert, int L, int k, float eps, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, float* __restrict__ s_row, int C) {
@@ -1122,7 +1129,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
   float amax = 0.f;
   for (int i = sl.i0 + threadIdx.x * 8; i < sl.i1; i += kRowThreads * 8) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    combine_cols<8, NB>(y, g_expert, L, i, k, s_rowj, s_e, s_coef, acc);   // slot order
+    combine_cols<8, NB, YF32>(y, g_expert, L, i, k, s_rowj, s_e, s_coef, acc);   // slot order
 #pragma unroll
     for (int q = 0; q < 8; ++q) amax = fmaxf(amax, fabsf(acc[q]));
     store8_f32(buf + (i - sl.i0), acc);
@@ -1339,9 +1346,9 @@ __global__ void __launch_bounds__(TPB) poolnorm_scatter_nvfp4_q_kernel(
   if (C > 1) cluster_sync_all();
 }
 
-template <int TPB, int NCH, int NB>
+template <int TPB, int NCH, int NB, bool YF32>
 __global__ void __launch_bounds__(TPB) combine_nvfp4_q_kernel(
-    const float* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
+    const void* __restrict__ y, const float* __restrict__ ss_y, int ld_ss,
     const int32_t* __restrict__ row_of, const int32_t* __restrict__ idx, const float* __restrict__ w,
     const float* __restrict__ g_expert, int L, int k, float eps, uint8_t* __restrict__ codes,
     uint8_t* __restrict__ scales, float* __restrict__ s_row, int C) {
@@ -1375,7 +1382,7 @@ __global__ void __launch_bounds__(TPB) combine_nvfp4_q_kernel(
 #pragma unroll
         for (int m = 0; m < NCH; ++m) {
           const int e = sl.i0 + 4 * (TPB * m + threadIdx.x);
-          load4(y, true, static_cast<long long>(s_rowj[j0 + jj]) * L + e, yv[jj][m]);
+          load4(y, YF32, static_cast<long long>(s_rowj[j0 + jj]) * L + e, yv[jj][m]);
           load4(g_expert, true, static_cast<long long>(s_e[j0 + jj]) * L + e, gv[jj][m]);
         }
       }
@@ -1456,8 +1463,8 @@ __global__ void nvfp4_block_scales_kernel(const uint8_t* __restrict__ src, long 
 // One CTA of `group` threads per (row, column group): sums the partials in split order (the
 // result does not depend on scheduling) and writes the group's sum of squares.
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, int rows, int N,
-                                     float* __restrict__ out, long long ldo, float* __restrict__ ss,
-                                     int ld_ss, const int* __restrict__ splits_dev) {
+                                     void* __restrict__ out, long long ldo, float* __restrict__ ss,
+                                     int ld_ss, const int* __restrict__ splits_dev, int out_bf16) {
   griddep_enter();
   if (splits_dev != nullptr) {
     splits = *splits_dev;
@@ -1469,7 +1476,13 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int spli
   float v = 0.f;
   if (col < N) {
     for (int q = 0; q < splits; ++q) v += partial[(static_cast<long long>(q) * rows + r) * N + col];
-    out[static_cast<long long>(r) * ldo + col] = v;
+    if (out_bf16) {   // stored rounded; the sum of squares is that of the stored value
+      const __nv_bfloat16 b = __float2bfloat16_rn(v);
+      static_cast<__nv_bfloat16*>(out)[static_cast<long long>(r) * ldo + col] = b;
+      v = __bfloat162float(b);
+    } else {
+      static_cast<float*>(out)[static_cast<long long>(r) * ldo + col] = v;
+    }
   }
   if (ss != nullptr) {
     const float t = block_sum(col < N ? v * v : 0.f, red);
@@ -1518,6 +1531,101 @@ __global__ void __launch_bounds__(256) swiglu_reduce_nvfp4_kernel(
     const uint32_t sc = nvfp4_quant16(h, 6.f, 1.f, recip, q);
     *reinterpret_cast<uint2*>(codes + grow * (N / 2) + cb * 8) = q;
     scales[blocked_sf_offset(mt, r, cb, N)] = static_cast<uint8_t>(sc);
+  }
+}
+
+// ------------------------------------------------------------------ routing validation
+// One CTA.  Every read of a value under test is bounds-checked first, so corrupted structures
+// are reported, never followed.
+constexpr int kValidateThreads = 1024;
+
+__device__ __forceinline__ bool tile_ok(const Tile& t, int E, const int32_t* offsets, int max_rows) {
+  if (t.expert < 0 || t.expert >= E || t.nrows < 1 || t.nrows > max_rows) return false;
+  return t.row0 >= offsets[t.expert] && t.row0 + t.nrows <= offsets[t.expert + 1];
+}
+
+__global__ void __launch_bounds__(kValidateThreads) validate_routing_kernel(
+    int32_t* __restrict__ idx, int T, int k, int E, const int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ row_of, const int32_t* __restrict__ tok_of,
+    const Tile* __restrict__ tiles, int32_t* __restrict__ n_tiles, int max_tiles,
+    int32_t* __restrict__ tile_base, const Tile* __restrict__ tiles2, int32_t* __restrict__ n_tiles2,
+    int max_tiles2, unsigned* __restrict__ err, int sanitize) {
+  griddep_enter();
+  __shared__ int bad, offsets_ok;
+  __shared__ int red[33];
+  const long long R = static_cast<long long>(T) * k;
+  if (threadIdx.x == 0) {
+    bad = 0;
+    offsets_ok = offsets[0] == 0 && offsets[E] == R;
+  }
+  __syncthreads();
+  // offsets and counts
+  for (int e = threadIdx.x; e < E; e += kValidateThreads)
+    if (offsets[e + 1] < offsets[e] || counts[e] != offsets[e + 1] - offsets[e]) offsets_ok = 0;
+  __syncthreads();
+  if (!offsets_ok) {
+    bad = 1;
+  } else {
+    // every pair: its expert, its row inside the expert's range, the row's token
+    for (long long i = threadIdx.x; i < R; i += kValidateThreads) {
+      const int e = idx[i], r = row_of[i];
+      if (e < 0 || e >= E || r < offsets[e] || r >= offsets[e + 1] || tok_of[r] != static_cast<int>(i / k))
+        bad = 1;
+    }
+    // every row is the row of one of its token's pairs (with the above: a bijection)
+    for (long long r = threadIdx.x; r < R; r += kValidateThreads) {
+      const int t = tok_of[r];
+      bool found = false;
+      if (t >= 0 && t < T)
+        for (int j = 0; j < k; ++j) found = found || row_of[static_cast<long long>(t) * k + j] == r;
+      if (!found) bad = 1;
+    }
+    // the tile tables
+    const int nt = *n_tiles;
+    if (nt < 0 || nt > max_tiles) bad = 1;
+    int rows = 0;
+    for (int m = threadIdx.x; m < min(max(nt, 0), max_tiles); m += kValidateThreads) {
+      const Tile t = tiles[m];
+      if (!tile_ok(t, E, offsets, kBM)) bad = 1;
+      else rows += t.nrows;
+    }
+    if (block_sum_int(rows, red) != R) bad = 1;
+    if (tiles2 != nullptr) {
+      const int nt2 = *n_tiles2;
+      if (nt2 < 0 || nt2 > max_tiles2) bad = 1;
+      int rows2 = 0;
+      for (int m = threadIdx.x; m < min(max(nt2, 0), max_tiles2); m += kValidateThreads) {
+        const Tile t = tiles2[m];
+        if (!tile_ok(t, E, offsets, 2 * kBM)) bad = 1;
+        else rows2 += t.nrows;
+      }
+      if (block_sum_int(rows2, red) != R) bad = 1;
+    }
+    if (tile_base != nullptr)
+      for (int e = threadIdx.x; e < E; e += kValidateThreads)
+        if (counts[e] > 0) {
+          const int b = tile_base[e];
+          if (b < 0 || b >= min(max(nt, 0), max_tiles) || tiles[b].expert != e || tiles[b].row0 != offsets[e])
+            bad = 1;
+        }
+  }
+  __syncthreads();
+  if (!bad) return;
+  if (threadIdx.x == 0) atomicOr(err, kErrBounds);
+  if (!sanitize) return;
+  // a routing every later kernel of the call reads in bounds: no tiles (the grouped GEMMs do
+  // nothing), every pair to expert 0 and row 0, every expert starting at row 0 and tile 0
+  for (long long i = threadIdx.x; i < R; i += kValidateThreads) {
+    idx[i] = 0;
+    row_of[i] = 0;
+  }
+  for (int e = threadIdx.x; e <= E; e += kValidateThreads) {
+    offsets[e] = 0;
+    if (tile_base != nullptr && e < E) tile_base[e] = 0;
+  }
+  if (threadIdx.x == 0) {
+    *n_tiles = 0;
+    if (n_tiles2 != nullptr) *n_tiles2 = 0;
   }
 }
 
@@ -1599,34 +1707,38 @@ cudaError_t launch_poolnorm_scatter_nvfp4(const float* p, const float* ss_p, int
                             scales, s_rows, C);
 }
 
-cudaError_t launch_combine_nvfp4(const float* y, const float* ss_y, int ld_ss, const int32_t* row_of,
-                                 const int32_t* idx, const float* w, const float* g_expert, int T,
-                                 int L, int k, float eps, uint8_t* codes, uint8_t* scales,
-                                 float* s_row, cudaStream_t s) {
+cudaError_t launch_combine_nvfp4(const void* y, bool y_bf16, const float* ss_y, int ld_ss,
+                                 const int32_t* row_of, const int32_t* idx, const float* w,
+                                 const float* g_expert, int T, int L, int k, float eps, uint8_t* codes,
+                                 uint8_t* scales, float* s_row, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int C = row_split(T, L);
   const bool few = T <= kCombineBatchMaxT;
   int tpb = 0, nch = 0;
   if (qgroup_shape(L / C, tpb, nch)) {   // rows from registers, coalesced chunks
 #define LMOE_Q(TPB, NCH)                                                                                \
-  if (tpb == TPB && nch == NCH)                                                                         \
-    return launch_pdl_cluster(few ? combine_nvfp4_q_kernel<TPB, NCH, 2> : combine_nvfp4_q_kernel<TPB, NCH, 1>, \
-                              dim3(T * C), dim3(TPB), 0, s, C, y, ss_y, ld_ss, row_of, idx, w, g_expert, \
-                              L, k, eps, codes, scales, s_row, C);
+  if (tpb == TPB && nch == NCH) {                                                                       \
+    auto kern = few ? (y_bf16 ? combine_nvfp4_q_kernel<TPB, NCH, 2, false> : combine_nvfp4_q_kernel<TPB, NCH, 2, true>) \
+                    : (y_bf16 ? combine_nvfp4_q_kernel<TPB, NCH, 1, false> : combine_nvfp4_q_kernel<TPB, NCH, 1, true>); \
+    return launch_pdl_cluster(kern, dim3(T * C), dim3(TPB), 0, s, C, y, ss_y, ld_ss, row_of, idx, w,    \
+                              g_expert, L, k, eps, codes, scales, s_row, C);                             \
+  }
     LMOE_Q(256, 1) LMOE_Q(256, 2) LMOE_Q(256, 4) LMOE_Q(256, 8) LMOE_Q(128, 1) LMOE_Q(64, 1) LMOE_Q(32, 1)
 #undef LMOE_Q
   }
   const size_t smem = (static_cast<size_t>(L / C) + 256) * sizeof(float);
   static bool attr = false;
   if (!attr) {
-    for (auto kern : {combine_nvfp4_kernel<1>, combine_nvfp4_kernel<kCombineBatch>}) {
+    for (auto kern : {combine_nvfp4_kernel<1, true>, combine_nvfp4_kernel<kCombineBatch, true>,
+                      combine_nvfp4_kernel<1, false>, combine_nvfp4_kernel<kCombineBatch, false>}) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
       if (e != cudaSuccess) return e;
     }
     attr = true;
   }
-  return launch_pdl_cluster(few ? combine_nvfp4_kernel<kCombineBatch> : combine_nvfp4_kernel<1>,
-                            dim3(T * C), dim3(kRowThreads), smem, s, C, y, ss_y, ld_ss, row_of, idx, w,
+  auto kern = few ? (y_bf16 ? combine_nvfp4_kernel<kCombineBatch, false> : combine_nvfp4_kernel<kCombineBatch, true>)
+                  : (y_bf16 ? combine_nvfp4_kernel<1, false> : combine_nvfp4_kernel<1, true>);
+  return launch_pdl_cluster(kern, dim3(T * C), dim3(kRowThreads), smem, s, C, y, ss_y, ld_ss, row_of, idx, w,
                             g_expert, L, k, eps, codes, scales, s_row, C);
 }
 
@@ -1653,13 +1765,13 @@ cudaError_t launch_nvfp4_block_scales(const uint8_t* src, long long rows, int K,
                     block_rows, dst);
 }
 
-cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, float* out,
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int rows, int N, void* out,
                                  long long ldo, float* ss, int ld_ss, int group, cudaStream_t s,
-                                 const int* splits_dev) {
+                                 const int* splits_dev, bool out_bf16) {
   if (rows == 0) return cudaSuccess;
   dim3 grid(rows, (N + group - 1) / group);
   return launch_pdl(splitk_reduce_kernel, dim3(grid), dim3(group), 0, s, partial, splits, rows, N,
-                    out, ldo, ss, ld_ss, splits_dev);
+                    out, ldo, ss, ld_ss, splits_dev, out_bf16 ? 1 : 0);
 }
 
 cudaError_t launch_swiglu_reduce_nvfp4(const float* partial, const int* splits_dev, int rows, int N,
@@ -1669,6 +1781,16 @@ cudaError_t launch_swiglu_reduce_nvfp4(const float* partial, const int* splits_d
   dim3 grid(max_tiles, (N / 16 + 255) / 256);
   return launch_pdl(swiglu_reduce_nvfp4_kernel, grid, dim3(256), 0, s, partial, splits_dev, rows, N,
                     tiles, n_tiles, codes, scales);
+}
+
+cudaError_t launch_validate_routing(int32_t* idx, int T, int k, int E, const int32_t* counts, int32_t* offsets,
+                                    int32_t* row_of, const int32_t* tok_of, const Tile* tiles, int32_t* n_tiles,
+                                    int max_tiles, int32_t* tile_base, const Tile* tiles2, int32_t* n_tiles2,
+                                    int max_tiles2, unsigned* err, bool sanitize, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  return launch_pdl(validate_routing_kernel, dim3(1), dim3(kValidateThreads), 0, s, idx, T, k, E, counts,
+                    offsets, row_of, tok_of, tiles, n_tiles, max_tiles, tile_base, tiles2, n_tiles2,
+                    max_tiles2, err, sanitize ? 1 : 0);
 }
 
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s) {

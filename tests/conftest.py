@@ -17,3 +17,13 @@ def build_library():
     """Compile the CUDA library in-tree (no-op when up to date)."""
     import __graft_entry__
     __graft_entry__.build()
+
+
+def build_checked_library() -> str:
+    """Compile the bounds-checked variant of the library (liblatent_moe_checked.so)."""
+    import importlib.util
+    path = os.path.join(ROOT, "latent_mixture_experts_router_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_lmoe_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build(checked=True)

@@ -70,7 +70,7 @@ def views(blk, cfg) -> dict:
         "p": get("p", T * L, torch.float32).view(T, L),
         "xe": get("xe", R * L, bf).view(R, L) if cfg.weight_dtype != "nvfp4" else None,
         "h": get("h", R * I, bf).view(R, I) if cfg.weight_dtype != "nvfp4" else None,
-        "y": get("y", R * L, torch.float32).view(R, L),
+        "y": get("y", R * L, bf if cfg.weight_dtype == "nvfp4" else torch.float32).view(R, L),
         "c": get("c", T * L, bf).view(T, L) if cfg.weight_dtype != "nvfp4" else None,
         "u": get("u", T * D, torch.float32).view(T, D),
     }

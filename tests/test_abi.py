@@ -126,3 +126,44 @@ def test_no_alloc_rejects_misaligned_arrays_without_launching(lm, which):
 def test_no_alloc_rejects_sizes_without_launching(lm, T, k, E, status):
     fake = 1 << 20
     assert _noalloc_fn(lm)(fake, T, k, E, fake, fake, fake, None) == status
+
+
+@pytest.mark.parametrize("layout,status", [(0, -2), (1, -4)])
+def test_nvfp4_scale_layout_is_checked_without_launching(lm, layout, status):
+    # row-major scales (the zero value of the field) are refused before any launch; with the
+    # block layout declared the call gets as far as the (too small) workspace check
+    lib = lm.load()
+    from latent_mixture_experts_router_gb300._lib import lmoe_nvfp4_weight
+    c = lm.Config(8, 256, 256, 8, 256, 2, weight_dtype="nvfp4").c()
+    fake = 1 << 20   # never dereferenced
+    ws = [lmoe_nvfp4_weight(fake, fake, fake, layout) for _ in range(5)]
+    p = [ctypes.addressof(w) for w in ws]
+    st = lib.latent_moe_forward(ctypes.byref(c), fake, fake, p[0], fake, p[1], p[2], p[3], fake, p[4], fake,
+                                fake, 2, fake + 4096, fake, 16, None)
+    assert st == status
+
+
+@pytest.mark.parametrize("shape", [(128, 8192, 4096, 256, 4096, 8, "bf16"), (4096, 8192, 4096, 256, 4096, 8, "nvfp4"),
+                                   (37, 512, 256, 8, 256, 2, "f32")])
+def test_workspace_guard_bands_lie_between_sub_buffers(lm, shape):
+    # every band is LMOE_GUARD_BYTES long, inside the workspace, and overlaps none of the
+    # public sub-buffers (sized here from the shape)
+    T, D, L, E, I, k, wd = shape
+    c = lm.Config(T, D, L, E, I, k, act_dtype="f32" if wd == "f32" else "bf16", weight_dtype=wd)
+    lay = lm.lmoe_get_workspace_layout(c)
+    g = lm.lmoe_workspace_guards(c)
+    g_io = lm.lmoe_workspace_guards(c, host_io=True)
+    assert len(g) >= 25 and g_io[:len(g)] == g and len(g_io) == len(g) + 2
+    assert all(b % 256 == 0 and b + lm.GUARD_BYTES <= lay["total"] for b in g)
+    assert max(g_io) + lm.GUARD_BYTES <= lm.lmoe_workspace_size_host_io(c)
+    R = T * k
+    fp4 = wd == "nvfp4"
+    sizes = {"xa": T * lay["xa_cols"] * 2, "logits": T * ((E + 31) // 32 * 32) * 4, "topk_idx": R * 4,
+             "topk_w": R * 4, "counts": E * 4, "offsets": (E + 1) * 4, "row_of": R * 4, "tok_of": R * 4,
+             "p": T * L * 4, "y": R * L * (2 if fp4 else 4), "u": T * D * 4,
+             "xe": R * L // 2 if fp4 else R * L * 2, "h": R * I // 2 if fp4 else R * I * 2,
+             "c": T * L // 2 if fp4 else T * L * 2}
+    for name, n in sizes.items():
+        o = lay[name]
+        for b in g:
+            assert b + lm.GUARD_BYTES <= o or b >= o + n, (name, o, n, b)

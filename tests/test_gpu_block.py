@@ -90,6 +90,10 @@ SHAPES = [  # (T, D, L, E, I, k): ragged T, N tails of the 256-wide tiles, k = 1
     (600, 512, 256, 4, 384, 2),     # 256-row tiles, dense and grouped, ragged last tiles
     (2100, 512, 256, 8, 256, 2),    # router in 256-row tiles split along K, ragged last tile
     (2100, 512, 256, 64, 256, 8),   # 16800 pairs: the chunked permutation
+    (12, 256, 128, 1024, 128, 16),  # the header's limits: E = 1024, k = 16 (fused top-k/permutation)
+    (40, 256, 128, 1024, 128, 16),  # E = 1024, k = 16 through the separate top-k and permutation
+    (1100, 256, 128, 1024, 128, 16),  # E = 1024, k = 16, 17600 pairs: the chunked permutation
+    (50, 256, 128, 16, 128, 16),    # k = E = 16
 ]
 
 
@@ -288,3 +292,32 @@ def test_wait_budget_runs_out_and_reports(cuda):
     out, idx, _, _ = run(inp, blk=blk)
     P, x, tr, ref = _oracle(inp)
     assert compare_block(out.cpu().numpy(), idx.cpu().numpy(), x, P, w.k, TOL_BF16, tr=tr, ref=ref).ok
+
+
+@pytest.mark.parametrize("T,k,weights", [(8, 2, "bf16"), (300, 4, "bf16"), (8, 2, "nvfp4"), (300, 4, "nvfp4")])
+def test_nan_token_routes_to_valid_experts(cuda, T, k, weights):
+    # A NaN in one token's input makes all of its router logits NaN.  The top-k orders NaN as
+    # -inf, so the token still gets k distinct valid experts (the lowest ids), the call reports
+    # no error, and the other tokens keep their routing and outputs (bitwise with BF16
+    # weights; with NVFP4 the grouped GEMMs may pick another split count, so they are graded
+    # against the oracle instead).  T = 8 takes the fused top-k + permutation kernel, T = 300
+    # the separate ones.
+    w = workloads.Workload(f"nan_{T}_{weights}", T=T, D=256, L=256, E=16, I=256, k=k, weights=weights, seed=2)
+    inp = workloads.make_inputs(w, cuda)
+    out0, idx0, blk, _ = run(inp)
+    out0, idx0 = out0.clone(), idx0.clone()
+    x = inp.x.clone()
+    x[3, 5] = float("nan")
+    out1, idx1, _, _ = run(inp, blk=blk, x=x)        # run() asserts the device status is OK
+    assert idx1[3].cpu().tolist() == list(range(k))
+    keep = torch.ones(T, dtype=torch.bool, device=cuda)
+    keep[3] = False
+    assert torch.equal(idx1[keep], idx0[keep])
+    assert bool(torch.isfinite(out1[keep]).all())
+    if weights == "bf16":
+        assert torch.equal(out1[keep], out0[keep])
+    else:
+        P, xs, tr, ref = _oracle(inp)
+        kk = keep.cpu().numpy()
+        rep = compare_block(out1.cpu().numpy()[kk], idx1.cpu().numpy()[kk], xs[kk], P, k, 6e-2)
+        assert rep.ok, str(rep)
