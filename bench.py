@@ -184,7 +184,10 @@ def measured_traffic(stage: str, w: workloads.Workload, units: int):
     if not os.path.exists(path):
         return None
     regime = "decode" if w.T <= 512 else "prefill"
-    rec = json.load(open(path)).get(f"{stage}/{w.weights}/{regime}")
+    table = json.load(open(path))
+    # a capture of this very workload (full size, one pass of the DRAM counters) first, else
+    # one of the same regime scaled by the units
+    rec = table.get(f"{stage}/{w.name}") or table.get(f"{stage}/{w.weights}/{regime}")
     if rec is None:
         return None
     src = os.path.join(ROOT, rec["kernel_source"])

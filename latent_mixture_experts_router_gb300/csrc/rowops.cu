@@ -830,6 +830,8 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
   for (int j = threadIdx.x >> 5; j < k; j += kRowThreads / 32) {   // a warp per slot
     const int lane = threadIdx.x & 31;
     const int row = row_of[t * k + j];
+    // (no L2 prefetch of the slot's fp32 row here, unlike the NVFP4 combine: with ~1200
+    // resident CTAs the prefetched rows exceed L2, measured 381 -> 410 us at T = 16384)
     const float ss = warp_sum_partials(ss_y + static_cast<long long>(row) * ld_ss, ld_ss, lane);
     if (lane == 0) {
       s_coef[j] = w[t * k + j] * rsqrtf(ss / static_cast<float>(L) + eps);
@@ -1115,9 +1117,13 @@ __global__ void __launch_bounds__(kRowThreads) combine_nvfp4_kernel(
   __shared__ QDest s_d;
   load_recip(recip);
   const long long t = sl.t;
+  constexpr uint32_t kYBytes = YF32 ? 4u : 2u;
   for (int j = threadIdx.x >> 5; j < k; j += kRowThreads / 32) {   // a warp per slot
     const int lane = threadIdx.x & 31;
     const int row = row_of[t * k + j];
+    if (lane == 0)   // the slot's row slice streams into L2 while the norms are computed
+      prefetch_l2_bulk(static_cast<const char*>(y) + (static_cast<long long>(row) * L + sl.i0) * kYBytes,
+                       static_cast<uint32_t>(sl.i1 - sl.i0) * kYBytes);
     const float ss = warp_sum_partials(ss_y + static_cast<long long>(row) * ld_ss, ld_ss, lane);
     if (lane == 0) {
       s_coef[j] = w[t * k + j] * rsqrtf(ss / static_cast<float>(L) + eps);
@@ -1359,8 +1365,14 @@ __global__ void __launch_bounds__(TPB) combine_nvfp4_q_kernel(
   const RowSlice sl = row_slice(L, C);
   const long long t = sl.t;
   const int lane = threadIdx.x & 31;
+  constexpr uint32_t kYBytes = YF32 ? 4u : 2u;
   for (int j = threadIdx.x >> 5; j < k; j += TPB / 32) {   // a warp per slot
     const int row = row_of[t * k + j];
+    // the slot's row slice starts streaming into L2 now; the weighted sum then reads it from
+    // there (measured without: long-scoreboard stalls bound this kernel at 0.48 of HBM)
+    if (lane == 0)
+      prefetch_l2_bulk(static_cast<const char*>(y) + (static_cast<long long>(row) * L + sl.i0) * kYBytes,
+                       static_cast<uint32_t>(sl.i1 - sl.i0) * kYBytes);
     const float ss = warp_sum_partials(ss_y + static_cast<long long>(row) * ld_ss, ld_ss, lane);
     if (lane == 0) {
       s_coef[j] = w[t * k + j] * rsqrtf(ss / static_cast<float>(L) + eps);
