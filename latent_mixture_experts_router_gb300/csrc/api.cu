@@ -399,7 +399,8 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                                            n_tiles, m_tiles, static_cast<uint8_t*>(out), out_scales, s));
     else
       LMOE_CUDA(launch_splitk_reduce(partial, splits, static_cast<int>(a_rows), N, out, ldo, ss, ld_ss, 128, s,
-                                     adaptive ? splits_dev : nullptr, epi == kFp4EpiBf16Ss));
+                                     adaptive ? splits_dev : nullptr,
+                                     epi == kFp4EpiBf16Ss || epi == kFp4EpiBf16SsWide));
   }
   return LMOE_OK;
 }
@@ -703,10 +704,15 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                       grouped_splits(I, Ld / 256), partial, splits_dev);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_DOWN);
-    // S8 grouped down: y rounded to bf16, with per-row partial sums of squares of those values
-    st = run_gemm_fp4(kFp4EpiBf16Ss, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
+    // S8 grouped down: y rounded to bf16, with per-row partial sums of squares of those values;
+    // at many rows per expert (no split possible) on 128 x 256 tiles, which read each expert's
+    // h tile once per 256 output columns
+    const int down_splits = grouped_splits(Ld, I / 256);
+    const Fp4EpiKind down_epi = down_splits <= 1 && R / E >= kBM / 2 && Ld % 256 == 0 ? kFp4EpiBf16SsWide
+                                                                                      : kFp4EpiBf16Ss;
+    st = run_gemm_fp4(down_epi, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
                       L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
-                      nullptr, err, budget, s, R / E, grouped_splits(Ld, I / 256), partial, splits_dev + 1);
+                      nullptr, err, budget, s, R / E, down_splits, partial, splits_dev + 1);
     if (st != LMOE_OK) return st;
     LMOE_MARK(LMOE_STAGE_COMBINE);
     // S9 combine, c quantised per token

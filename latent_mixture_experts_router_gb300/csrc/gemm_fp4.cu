@@ -33,7 +33,8 @@
 // accumulator buffers, so the next tile's MMAs overlap this tile's epilogue.  kFp4EpiBf16Ss —
 // the same with the values rounded to bf16 and the sums of squares taken of the rounded values
 // (the expert down projection: each tile's partial sum of squares of the bf16 values it holds).
-// kFp4EpiF32SsWide — the fp32 epilogue on 128 x 256 tiles for dense GEMMs of many rows: a stage
+// kFp4EpiF32SsWide / kFp4EpiBf16SsWide — those epilogues on 128 x 256 tiles for GEMMs of many
+// rows (the dense pooler/unpooler, the grouped down projection at prefill): a stage
 // loads the two 128-row halves of the tile's weights (as gate/up loads its two weights), so
 // the A tile is read once per 256 output columns (the operand intake of an SM, ~97 GB/s
 // measured, bounds these GEMMs); one accumulator buffer of 256 columns.
@@ -91,7 +92,7 @@ template <int BN, int EPI>
 struct Fp4Cfg {
   // kDual: two B boxes per stage into two accumulators of BN columns — gate and up tiles of the
   // same columns (SwiGLU), or the two BN-row halves of one 2*BN-wide output tile (kWide)
-  static constexpr bool kWide = (EPI == kFp4EpiF32SsWide);
+  static constexpr bool kWide = (EPI == kFp4EpiF32SsWide) || (EPI == kFp4EpiBf16SsWide);
   static constexpr bool kDual = (EPI == kFp4EpiSwiGLUQuant) || kWide;
   static constexpr int kTileN = kWide ? 2 * BN : BN;   // output columns of one tile
   static constexpr int kNB = kDual ? 2 : 1;
@@ -379,8 +380,10 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
         // warp half h takes accumulator columns [h BN, (h+1) BN) = output columns n0 + h BN ..:
         // all of them are read into registers and the single accumulator buffer is handed back
         // to the MMA issuer before the scaling and the stores
-        const float alpha = rs * args.tensor_scale[0];
+        const float alpha = rs * args.tensor_scale[args.tiles ? expert : 0];
         const bool split = walk.splits > 1;
+        // bf16 output (unsplit): rounded values, and the sum of squares of the rounded values
+        const bool bf = EPI == kFp4EpiBf16SsWide && !split;
         constexpr int kCh = BN / 32;
         uint32_t v[kCh][32];
 #pragma unroll
@@ -395,18 +398,39 @@ __global__ void __launch_bounds__(Fp4Cfg<BN, EPI>::kThreads, 1)
                             : static_cast<float*>(args.out) + grow * args.ldo;
         float ss = 0.f;
         if (row_ok && cbase + BN <= args.N) {
+          if (bf) {
+            __nv_bfloat16* brow = static_cast<__nv_bfloat16*>(args.out) + grow * args.ldo + cbase;
 #pragma unroll
-          for (int ch = 0; ch < kCh; ++ch) {
-            float4* o = reinterpret_cast<float4*>(orow + cbase + 32 * ch);
+            for (int ch = 0; ch < kCh; ++ch) {
+              uint4* o = reinterpret_cast<uint4*>(brow + 32 * ch);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 f = make_float4(__uint_as_float(v[ch][4 * i]) * alpha, __uint_as_float(v[ch][4 * i + 1]) * alpha,
-                                           __uint_as_float(v[ch][4 * i + 2]) * alpha, __uint_as_float(v[ch][4 * i + 3]) * alpha);
-              ss = fmaf(f.x, f.x, ss);
-              ss = fmaf(f.y, f.y, ss);
-              ss = fmaf(f.z, f.z, ss);
-              ss = fmaf(f.w, f.w, ss);
-              o[i] = f;
+              for (int i = 0; i < 4; ++i) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                  const float a = bf16_round(__uint_as_float(v[ch][8 * i + 2 * h]) * alpha);
+                  const float b = bf16_round(__uint_as_float(v[ch][8 * i + 2 * h + 1]) * alpha);
+                  ss = fmaf(a, a, ss);
+                  ss = fmaf(b, b, ss);
+                  w4[h] = pack_bf16x2(a, b);
+                }
+                o[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int ch = 0; ch < kCh; ++ch) {
+              float4* o = reinterpret_cast<float4*>(orow + cbase + 32 * ch);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 f = make_float4(__uint_as_float(v[ch][4 * i]) * alpha, __uint_as_float(v[ch][4 * i + 1]) * alpha,
+                                             __uint_as_float(v[ch][4 * i + 2]) * alpha, __uint_as_float(v[ch][4 * i + 3]) * alpha);
+                ss = fmaf(f.x, f.x, ss);
+                ss = fmaf(f.y, f.y, ss);
+                ss = fmaf(f.z, f.z, ss);
+                ss = fmaf(f.w, f.w, ss);
+                o[i] = f;
+              }
             }
           }
           if (!split) args.ss[grow * args.ld_ss + cbase / BN] = ss;   // one sum per 128 columns
@@ -575,6 +599,7 @@ cudaError_t launch_gemm_fp4(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Ar
     case kFp4EpiSwiGLUQuant: return launch_fp4_one<kBNFp4, kFp4EpiSwiGLUQuant>(maps, a, m_tiles, s);
     case kFp4EpiBf16Ss: return launch_fp4_one<kBNFp4, kFp4EpiBf16Ss>(maps, a, m_tiles, s);
     case kFp4EpiF32SsWide: return launch_fp4_one<kBNFp4, kFp4EpiF32SsWide>(maps, a, m_tiles, s);
+    case kFp4EpiBf16SsWide: return launch_fp4_one<kBNFp4, kFp4EpiBf16SsWide>(maps, a, m_tiles, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -43,6 +43,8 @@ enum Fp4EpiKind : int {
                             // rounded values (the expert down projection's y)
   kFp4EpiF32SsWide = 3,     // as kFp4EpiF32Ss, with 128 x 256 output tiles (dense GEMMs of many
                             // rows: the two 128-row halves of the tile's weights per stage)
+  kFp4EpiBf16SsWide = 4,    // as kFp4EpiBf16Ss, with 128 x 256 output tiles (the grouped down
+                            // projection at many rows per expert)
 };
 
 // One M tile of a grouped GEMM: rows [row0, row0 + nrows) of A, all of expert `expert`.
