@@ -345,9 +345,11 @@ def topk_margins(blk, cfg, w, bias=None):
     return rec
 
 
-def block_roofline(w, costs, used, ms_step, pk, pk_kind, sustained):
+def block_roofline(w, costs, used, ms_step, pk, pk_kind, sustained, clk=None):
     """The whole step against the block's own bound (SURVEY-style algorithmic bytes: unique
-    weights touched + x read + out written; FLOPs of every contraction)."""
+    weights touched + x read + out written; FLOPs of every contraction).  A tensor-bound step
+    also reports its fraction of the burst peak and of the burst peak scaled to the median SM
+    clock of the timed region (the peak was measured at the maximum clock)."""
     T, D, L, E, I = w.T, w.D, w.L, w.E, w.I
     wb = 0.5625 if w.weights == "nvfp4" else 2
     xb = 4 if w.act == "f32" else 2
@@ -358,10 +360,17 @@ def block_roofline(w, costs, used, ms_step, pk, pk_kind, sustained):
     t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tf * 1e12)
     t = ms_step * 1e-3
     if t_tc > t_hbm:
-        return {"bound": "tensor", "frac": round(t_tc / t, 4), "achieved_tflops": round(flops / t / 1e12, 1),
-                "peak_tflops": round(tf, 1), "algorithmic_flop": int(flops),
-                "peak_source": f"{pk_kind} bf16_tflops{'_sustained' if sustained else ''}"
-                               + (" x 6" if w.weights == "nvfp4" else "")}
+        rec = {"bound": "tensor", "frac": round(t_tc / t, 4), "achieved_tflops": round(flops / t / 1e12, 1),
+               "peak_tflops": round(tf, 1), "algorithmic_flop": int(flops),
+               "peak_source": f"{pk_kind} bf16_tflops{'_sustained' if sustained else ''}"
+                              + (" x 6" if w.weights == "nvfp4" else "")}
+        burst = pk["bf16_tflops"] * (FP4_OVER_BF16 if w.weights == "nvfp4" else 1)
+        rec["frac_of_burst"] = round(flops / t / 1e12 / burst, 4)
+        mhz, mx = (clk or {}).get("sm_mhz"), (clk or {}).get("sm_max_mhz") or pk.get("sm_max_mhz")
+        if mhz and mx:
+            rec["frac_of_burst_at_median_clock"] = round(flops / t / 1e12 / (burst * mhz / mx), 4)
+            rec["median_sm_mhz"] = mhz
+        return rec
     return {"bound": "hbm", "frac": round(t_hbm / t, 4), "achieved_gbs": round(nbytes / t / 1e9, 1),
             "peak_gbs": hbm, "algorithmic_bytes": int(nbytes), "peak_source": f"{pk_kind} hbm_gbs"}
 
@@ -496,7 +505,7 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
                    "l2": "inputs larger than L2: each step streams "
                          f"{sum(b for b, _ in costs.values()) / 1e9:.2f} GB (129 MB L2)"},
         "tflops": round(total_flops / (ms_step * 1e-3) / 1e12, 2),
-        "block_roofline": block_roofline(w, costs, used, ms_step, pk, pk_kind, capped),
+        "block_roofline": block_roofline(w, costs, used, ms_step, pk, pk_kind, capped, clk),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "stage_ms_note": f"separate pass of {n_bd} steps, an event at every stage boundary",
         # a kernel that ran under the power cap is held against the sustained tensor peak (the
@@ -576,6 +585,50 @@ def run_ours(args, ws, rank, local):
     return line
 
 
+# ------------------------------------------------------------------ timeline
+def run_timeline(args):
+    """Device start and end of every kernel of one block call, from the CUDA activity records of
+    torch.profiler (CUPTI): unlike a serialising profiler it keeps the overlap of programmatically
+    dependent launches.  Prints one JSON line: the kernels of the last of `steps` profiled calls,
+    in start order, with start/end in microseconds from the call's first kernel start."""
+    import latent_mixture_experts_router_gb300 as lm
+    from torch.profiler import ProfilerActivity, profile
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    w = pick_workload(args)
+    inp = workloads.make_inputs(w, dev)
+    blk = lm.LatentMoEBlock(inp.W_router, inp.W_pool, inp.g_pool, inp.W_gate, inp.W_up, inp.W_down,
+                            inp.g_expert, inp.W_unpool, inp.g_pre, inp.g_post, w.k, w.eps, weight_dtype=w.weights)
+    out = torch.empty(w.T, w.D, dtype=torch.float32, device=dev)
+    ex = {}
+    if inp.router_bias is not None:
+        ex["router_bias"] = inp.router_bias
+    if inp.forced_idx is not None:
+        ex["forced_idx"] = inp.forced_idx
+    for _ in range(args.warmup):
+        blk.forward(inp.x, out=out, **ex)
+    torch.cuda.synchronize()
+    n_per_call = None
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        for _ in range(args.steps):
+            n0 = lm.lmoe_kernel_launches()
+            blk.forward(inp.x, out=out, **ex)
+            n_per_call = lm.lmoe_kernel_launches() - n0
+        torch.cuda.synchronize()
+    kern = [e for e in prof.events() if getattr(e, "device_type", None) is not None
+            and str(e.device_type).endswith("CUDA") and e.device_time_total > 0 and not e.name.startswith("Memset")]
+    kern.sort(key=lambda e: e.time_range.start)
+    last = kern[-n_per_call:]
+    t0 = last[0].time_range.start
+    rows = [{"kernel": e.name.split("(")[0][:60], "start_us": round(e.time_range.start - t0, 2),
+             "end_us": round(e.time_range.end - t0, 2), "dur_us": round(e.time_range.end - e.time_range.start, 2)}
+            for e in last]
+    span = max(r["end_us"] for r in rows)
+    return {"timeline": rows, "call_span_us": round(span, 2), "kernels": n_per_call, "workload": w.name,
+            "note": "CUPTI activity records of the last of the profiled calls (torch.profiler); times in us from "
+                    "the call's first kernel start"}
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, ws, rank):
     if rank != 0:
@@ -611,8 +664,15 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=None,
                     help="oracle sample size in tokens (default: ~10-30 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--timeline", action="store_true",
+                    help="print the device timeline of one call of --workload (no benchmark line)")
     args = ap.parse_args()
     ws, rank, local = dist_init()
+    if args.timeline:
+        args.steps = 3 if args.steps is None else args.steps
+        args.warmup = 5 if args.warmup is None else args.warmup
+        print(json.dumps(run_timeline(args)), flush=True)
+        return
     if args.impl == "reference" and args.cpu_tokens is None:   # bounded host memory
         args.cpu_tokens = {"tiny_fp32": 64}.get(args.workload, 4)
     if args.impl == "reference":
