@@ -585,50 +585,6 @@ def run_ours(args, ws, rank, local):
     return line
 
 
-# ------------------------------------------------------------------ timeline
-def run_timeline(args):
-    """Device start and end of every kernel of one block call, from the CUDA activity records of
-    torch.profiler (CUPTI): unlike a serialising profiler it keeps the overlap of programmatically
-    dependent launches.  Prints one JSON line: the kernels of the last of `steps` profiled calls,
-    in start order, with start/end in microseconds from the call's first kernel start."""
-    import latent_mixture_experts_router_gb300 as lm
-    from torch.profiler import ProfilerActivity, profile
-    dev = torch.device("cuda:0")
-    torch.cuda.set_device(dev)
-    w = pick_workload(args)
-    inp = workloads.make_inputs(w, dev)
-    blk = lm.LatentMoEBlock(inp.W_router, inp.W_pool, inp.g_pool, inp.W_gate, inp.W_up, inp.W_down,
-                            inp.g_expert, inp.W_unpool, inp.g_pre, inp.g_post, w.k, w.eps, weight_dtype=w.weights)
-    out = torch.empty(w.T, w.D, dtype=torch.float32, device=dev)
-    ex = {}
-    if inp.router_bias is not None:
-        ex["router_bias"] = inp.router_bias
-    if inp.forced_idx is not None:
-        ex["forced_idx"] = inp.forced_idx
-    for _ in range(args.warmup):
-        blk.forward(inp.x, out=out, **ex)
-    torch.cuda.synchronize()
-    n_per_call = None
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        for _ in range(args.steps):
-            n0 = lm.lmoe_kernel_launches()
-            blk.forward(inp.x, out=out, **ex)
-            n_per_call = lm.lmoe_kernel_launches() - n0
-        torch.cuda.synchronize()
-    kern = [e for e in prof.events() if getattr(e, "device_type", None) is not None
-            and str(e.device_type).endswith("CUDA") and e.device_time_total > 0 and not e.name.startswith("Memset")]
-    kern.sort(key=lambda e: e.time_range.start)
-    last = kern[-n_per_call:]
-    t0 = last[0].time_range.start
-    rows = [{"kernel": e.name.split("(")[0][:60], "start_us": round(e.time_range.start - t0, 2),
-             "end_us": round(e.time_range.end - t0, 2), "dur_us": round(e.time_range.end - e.time_range.start, 2)}
-            for e in last]
-    span = max(r["end_us"] for r in rows)
-    return {"timeline": rows, "call_span_us": round(span, 2), "kernels": n_per_call, "workload": w.name,
-            "note": "CUPTI activity records of the last of the profiled calls (torch.profiler); times in us from "
-                    "the call's first kernel start"}
-
-
 # ------------------------------------------------------------------ reference arm
 def run_reference(args, ws, rank):
     if rank != 0:
@@ -664,15 +620,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=None,
                     help="oracle sample size in tokens (default: ~10-30 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--timeline", action="store_true",
-                    help="print the device timeline of one call of --workload (no benchmark line)")
     args = ap.parse_args()
     ws, rank, local = dist_init()
-    if args.timeline:
-        args.steps = 3 if args.steps is None else args.steps
-        args.warmup = 5 if args.warmup is None else args.warmup
-        print(json.dumps(run_timeline(args)), flush=True)
-        return
     if args.impl == "reference" and args.cpu_tokens is None:   # bounded host memory
         args.cpu_tokens = {"tiny_fp32": 64}.get(args.workload, 4)
     if args.impl == "reference":
