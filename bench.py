@@ -375,6 +375,16 @@ def block_roofline(w, costs, used, ms_step, pk, pk_kind, sustained, clk=None):
             "peak_gbs": hbm, "algorithmic_bytes": int(nbytes), "peak_source": f"{pk_kind} hbm_gbs"}
 
 
+def workload_config(w: workloads.Workload, counts: np.ndarray, ws: int) -> dict:
+    """The `config` object of a line: the workload and what one step streams (both arms)."""
+    costs, used = stage_costs(w, counts)
+    return {"workload": w.name, "T_per_gpu": w.T, "d_model": w.D, "d_latent": w.L, "n_experts": w.E,
+            "d_ff": w.I, "top_k": w.k, "routing": w.routing, "weights": w.weights,
+            "experts_touched": used, "parallelism": f"replicas x{ws} (token-independent, no exchange)",
+            "l2": "inputs larger than L2: each step streams "
+                  f"{sum(b for b, _ in costs.values()) / 1e9:.2f} GB (129 MB L2)"}
+
+
 def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: float):
     """One workload: stage pass, timed pass, dominant-kernel pass, end-to-end pass; the record
     (rank 0) or None."""
@@ -499,11 +509,7 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
         "value": round(ws * T * args.steps / (ms_max * 1e-3), 1), "unit": "tokens/s",
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "dtype": "nvfp4" if w.weights == "nvfp4" else "bf16",
-        "config": {"workload": w.name, "T_per_gpu": T, "d_model": w.D, "d_latent": w.L, "n_experts": w.E,
-                   "d_ff": w.I, "top_k": w.k, "routing": w.routing, "weights": w.weights,
-                   "experts_touched": used, "parallelism": f"replicas x{ws} (token-independent, no exchange)",
-                   "l2": "inputs larger than L2: each step streams "
-                         f"{sum(b for b, _ in costs.values()) / 1e9:.2f} GB (129 MB L2)"},
+        "config": workload_config(w, counts, ws),
         "tflops": round(total_flops / (ms_step * 1e-3) / 1e12, 2),
         "block_roofline": block_roofline(w, costs, used, ms_step, pk, pk_kind, capped, clk),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
@@ -586,6 +592,22 @@ def run_ours(args, ws, rank, local):
 
 
 # ------------------------------------------------------------------ reference arm
+def host_routing_counts(w: workloads.Workload) -> np.ndarray:
+    """Rows per expert of the workload's routing, from the oracle's router on the host (the
+    reference arm's config, which names the same workload as the GPU arm's)."""
+    import oracle
+    if w.routing == "hot4":
+        sel = workloads.forced_routing(w).numpy()
+    else:
+        g = workloads.gammas(w)
+        xn = oracle.rms_norm(workloads.x_tensor(w).double().numpy(), g["g_pre"].double().numpy(), w.eps)
+        lg = xn @ workloads.dense_weight(w, "W_router").double().numpy().T
+        if w.routing == "zipf":
+            lg = lg + workloads.zipf_bias(w).double().numpy()
+        sel = oracle.top_k(lg, w.k)
+    return np.bincount(np.asarray(sel).reshape(-1), minlength=w.E)
+
+
 def run_reference(args, ws, rank):
     if rank != 0:
         return None
@@ -594,13 +616,14 @@ def run_reference(args, ws, rank):
     times = time_oracle(w, n_tok, repeats=args.warmup + args.steps)[args.warmup:]
     dt = sum(times)
     v = round(n_tok * args.steps / dt, 3)
-    sample = (f"each step: the first {n_tok} tokens of {w.name} through the fp64 oracle (numpy BLAS "
-              f"on the host cores); weights of the routed experts generated on the host and widened "
-              f"to fp64 before timing")
+    sample = (f"each step: the first {n_tok} of the workload's {w.T} tokens ({w.name}) through the fp64 "
+              f"oracle (numpy BLAS on the host cores); weights of the routed experts generated on the host "
+              f"and widened to fp64 before timing; tokens/s of that sample")
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name, "T": w.T, "sample_tokens": n_tok},
+            "data": "synthetic (seeded counter-based generator; random-init weights of the Muse layer shapes)",
+            "config": workload_config(w, host_routing_counts(w), ws),
             "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
