@@ -708,8 +708,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     // at many rows per expert (no split possible) on 128 x 256 tiles, which read each expert's
     // h tile once per 256 output columns
     const int down_splits = grouped_splits(Ld, I / 256);
-    const Fp4EpiKind down_epi = down_splits <= 1 && R / E >= kBM / 2 && Ld % 256 == 0 ? kFp4EpiBf16SsWide
-                                                                                      : kFp4EpiBf16Ss;
+    const Fp4EpiKind down_epi = down_splits <= 1 && Ld % 256 == 0 ? kFp4EpiBf16SsWide : kFp4EpiBf16Ss;
     st = run_gemm_fp4(down_epi, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
                       L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
                       nullptr, err, budget, s, R / E, down_splits, partial, splits_dev + 1);
