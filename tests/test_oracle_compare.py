@@ -1,6 +1,6 @@
 """Pins for the parity comparator (oracle/compare.py): classify_topk and compare_block.
 
-Every GPU parity verdict goes through these two functions, so they are fed hand-built cases
+Every GPU parity decision goes through these two functions, so they are fed hand-built cases
 whose right answer follows from the grading rules alone (LMSYS Muse Spark Open post, "MoE
 with pooler, unpooler and per-expert normalization": the router's top-k over the full-width
 logits; the near-tie band of 1e-3 on the k-th/(k+1)-th margin and the 2e-2 / 6e-2 x RMS output
