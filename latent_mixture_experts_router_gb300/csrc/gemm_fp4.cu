@@ -33,11 +33,13 @@
 // accumulator buffers, so the next tile's MMAs overlap this tile's epilogue.  kFp4EpiBf16Ss —
 // the same with the values rounded to bf16 and the sums of squares taken of the rounded values
 // (the expert down projection: each tile's partial sum of squares of the bf16 values it holds).
-// kFp4EpiF32SsWide / kFp4EpiBf16SsWide — those epilogues on 128 x 256 tiles for GEMMs of many
-// rows (the dense pooler/unpooler, the grouped down projection at prefill): a stage
+// kFp4EpiF32SsWide / kFp4EpiBf16SsWide — those epilogues on 128 x 256 tiles (the dense
+// pooler/unpooler at many rows, the grouped down projection wherever it runs unsplit): a stage
 // loads the two 128-row halves of the tile's weights (as gate/up loads its two weights), so
-// the A tile is read once per 256 output columns (the operand intake of an SM, ~97 GB/s
-// measured, bounds these GEMMs); one accumulator buffer of 256 columns.
+// the A tile, its scales and the per-stage barrier and scale-copy work come once per 256
+// output columns (at prefill the operand intake of an SM, ~97 GB/s measured, bounds these
+// GEMMs; at decode the per-stage overheads of a 16 KB weight stage); one accumulator buffer
+// of 256 columns.
 // kFp4EpiSwiGLUQuant — gate and up tiles of the same columns, h = silu(alpha_g acc_g) *
 // (alpha_u acc_u) requantised to NVFP4 with scale 1 (block scales only, through the
 // reciprocal table) for the down projection; one accumulator buffer (two would leave no

@@ -44,7 +44,7 @@ enum Fp4EpiKind : int {
   kFp4EpiF32SsWide = 3,     // as kFp4EpiF32Ss, with 128 x 256 output tiles (dense GEMMs of many
                             // rows: the two 128-row halves of the tile's weights per stage)
   kFp4EpiBf16SsWide = 4,    // as kFp4EpiBf16Ss, with 128 x 256 output tiles (the grouped down
-                            // projection at many rows per expert)
+                            // projection wherever it runs unsplit)
 };
 
 // One M tile of a grouped GEMM: rows [row0, row0 + nrows) of A, all of expert `expert`.
