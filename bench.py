@@ -345,15 +345,21 @@ def topk_margins(blk, cfg, w, bias=None):
     return rec
 
 
+def block_bytes(w, used: int) -> float:
+    """Algorithmic bytes of one step: the weights of the `used` experts and the dense weights
+    (NVFP4: 0.5 + 1/16 bytes per weight), the router, x read and out (fp32) written."""
+    T, D, L, E, I = w.T, w.D, w.L, w.E, w.I
+    wb = 0.5625 if w.weights == "nvfp4" else 2
+    xb = 4 if w.act == "f32" else 2
+    return used * 3 * L * I * wb + 2 * D * L * wb + E * D * 2 + T * D * xb + T * D * 4
+
+
 def block_roofline(w, costs, used, ms_step, pk, pk_kind, sustained, clk=None):
     """The whole step against the block's own bound (SURVEY-style algorithmic bytes: unique
     weights touched + x read + out written; FLOPs of every contraction).  A tensor-bound step
     also reports its fraction of the burst peak and of the burst peak scaled to the median SM
     clock of the timed region (the peak was measured at the maximum clock)."""
-    T, D, L, E, I = w.T, w.D, w.L, w.E, w.I
-    wb = 0.5625 if w.weights == "nvfp4" else 2
-    xb = 4 if w.act == "f32" else 2
-    nbytes = used * 3 * L * I * wb + 2 * D * L * wb + E * D * 2 + T * D * xb + T * D * 4
+    nbytes = block_bytes(w, used)
     flops = sum(f for _, f in costs.values())
     hbm = pk["hbm_gbs"]
     tf = pk["bf16_tflops_sustained" if sustained else "bf16_tflops"] * (FP4_OVER_BF16 if w.weights == "nvfp4" else 1)
@@ -399,6 +405,8 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
         ex["router_bias"] = inp.router_bias
     if inp.forced_idx is not None:
         ex["forced_idx"] = inp.forced_idx
+    if getattr(args, "single_token_kernel", False):
+        ex["single_token_kernel"] = True
     stream = torch.cuda.current_stream(dev)
 
     def step(evs=None):
@@ -450,21 +458,39 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
 
     # ---- the dominant kernel, timed live in a second pass of K steps right after: events on
     #      the launching stream around that kernel only.  An event between two kernels turns off
-    #      their launch overlap, which is why the headline pass above records none.
-    evs = [[torch.cuda.Event(enable_timing=True) if j in (di, di + 1) else None
-            for j in range(lm.NUM_STAGE_EVENTS)] for _ in range(args.steps)]
+    #      their launch overlap, which is why the headline pass above records none.  A step that
+    #      ran as one kernel (one token with NVFP4 weights: the single-token kernel, which stage
+    #      events turn back into the kernel chain) is timed by events around each call.
+    single = launches == args.steps
+    rcosts = dict(costs)
+    if single:
+        dom = "single_token_kernel"
+        rcosts[dom] = (block_bytes(w, used), sum(f for _, f in costs.values()))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    else:
+        evs = [[torch.cuda.Event(enable_timing=True) if j in (di, di + 1) else None
+                for j in range(lm.NUM_STAGE_EVENTS)] for _ in range(args.steps)]
     barrier(ws)
     torch.cuda.synchronize()
     k_start = torch.cuda.Event(enable_timing=True)
     k_end = torch.cuda.Event(enable_timing=True)
     k_start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        if single:
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        else:
+            step(evs[i])
     k_end.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     clk = clocks.stop() if clocks else None
-    dom_ms = statistics.mean(e[di].elapsed_time(e[di + 1]) for e in evs)
+    if single:
+        dom_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    else:
+        dom_ms = statistics.mean(e[di].elapsed_time(e[di + 1]) for e in evs)
     ms_kpass = k_start.elapsed_time(k_end) / args.steps
 
     # ---- end to end through the host-I/O entry point: pinned x in, pinned out back
@@ -513,14 +539,19 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
         "tflops": round(total_flops / (ms_step * 1e-3) / 1e12, 2),
         "block_roofline": block_roofline(w, costs, used, ms_step, pk, pk_kind, capped, clk),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-        "stage_ms_note": f"separate pass of {n_bd} steps, an event at every stage boundary",
+        "stage_ms_note": f"separate pass of {n_bd} steps, an event at every stage boundary"
+                         + (" (the stage kernels: events at the stage boundaries select the kernel chain, "
+                            "the timed steps ran as the single-token kernel)" if single else ""),
         # a kernel that ran under the power cap is held against the sustained tensor peak (the
         # measured one of a seconds-long GEMM loop under the same cap), else the burst peak
-        "roofline": {**roofline(dom, dom_ms, costs, pk, pk_kind, sustained=capped, fp4=w.weights == "nvfp4"),
+        "roofline": {**roofline(dom, dom_ms, rcosts, pk, pk_kind, sustained=capped, fp4=w.weights == "nvfp4"),
                      "traffic": measured_traffic(dom, w, used),
-                     "timing": f"CUDA events on the launching stream around the kernel, {args.steps} steps "
-                               "timed right after the headline pass (that pass records no events: an "
-                               "event between two kernels turns off their launch overlap)",
+                     "timing": (f"CUDA events on the launching stream around each call (the single-token "
+                                f"kernel and the memset of its status words), {args.steps} steps timed right "
+                                "after the headline pass" if single else
+                                f"CUDA events on the launching stream around the kernel, {args.steps} steps "
+                                "timed right after the headline pass (that pass records no events: an "
+                                "event between two kernels turns off their launch overlap)"),
                      "step_ms_with_kernel_events": round(ms_kpass, 4)},
         "routing": margins,
         "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
@@ -643,6 +674,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=None,
                     help="oracle sample size in tokens (default: ~10-30 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single-token-kernel", action="store_true",
+                    help="NVFP4 at T = 1: run the block as one cooperative kernel (lmoe_ex.single_token_kernel)")
     args = ap.parse_args()
     ws, rank, local = dist_init()
     if args.impl == "reference" and args.cpu_tokens is None:   # bounded host memory

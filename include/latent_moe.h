@@ -140,7 +140,20 @@ enum {
  *                    recorded on the stream at the stage boundaries above (timing only);
  *                    a NULL entry is skipped.  Kernels of one call are launched with
  *                    programmatic dependent launch, so a kernel's set-up overlaps the end of
- *                    the previous one; an event between two kernels serialises them fully. */
+ *                    the previous one; an event between two kernels serialises them fully.
+ *  single_token_kernel  nonzero, with NVFP4 weights and T = 1 (one decode token): run the whole
+ *                    block as one cooperative kernel of one CTA per SM, which streams the
+ *                    weights into shared memory by bulk copies and dots them on the CUDA cores
+ *                    (four weight phases behind bounded grid barriers), when the shapes allow
+ *                    it (D and I multiples of 256 up to 8192, L up to 4096, E <= 1024, and the
+ *                    shared memory it needs) and no stage event is set; otherwise, and by
+ *                    default, the stage kernels run (on a GB300 at the Muse shapes the kernel
+ *                    chain is the faster of the two).  Same arithmetic as the chain up to the
+ *                    order of fp32 sums; the workspace then holds xa, the logits, the routing
+ *                    tables, p, y and u as after the chain, but not the quantised operands
+ *                    (xq, xe, h, c and their scales) nor the partial sums of squares.  A grid
+ *                    barrier or stage wait past wait_budget_cycles sets bit 0x40 of the error
+ *                    word (LMOE_ERR_TIMEOUT). */
 typedef struct {
   const float* router_bias;
   const int32_t* forced_idx;
@@ -151,6 +164,7 @@ typedef struct {
   cudaEvent_t* stage_events;
   const float* next_norm_gamma;
   void* next_norm_out;
+  int single_token_kernel;
 } lmoe_ex;
 
 /* Bytes of device workspace a call with this config needs (host out-parameter). */
@@ -209,7 +223,7 @@ lmoe_status latent_moe_forward_host_io_ex(const lmoe_config* cfg, const void* x_
                                           cudaStream_t stream, const lmoe_ex* ex);
 
 /* Reads (synchronising `stream`) and clears the device error word of `workspace`.
- * Returns LMOE_OK, LMOE_ERR_TIMEOUT (a device wait gave up: bits 0x1, 0x2, 0x4, 0x10) or
+ * Returns LMOE_OK, LMOE_ERR_TIMEOUT (a device wait gave up: bits 0x1, 0x2, 0x4, 0x10, 0x40) or
  * LMOE_ERR_ARG (a forced expert id out of range or repeated: bit 0x8; routing structures
  * that failed lmoe_validate_routing: bit 0x20); *detail (host, may be NULL) receives the raw
  * word. */

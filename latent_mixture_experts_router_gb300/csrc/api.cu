@@ -50,6 +50,7 @@ struct Layout {
   long long splits_dev; // [2] split counts the grouped NVFP4 GEMMs chose (gate/up, down)
   long long tiles2, n_tiles2;  // table of 256-row tiles (BF16 grouped GEMMs of many rows)
   long long perm_hist, perm_base;  // [chunks][E] each: the chunked permutation of many pairs
+  long long mk_scratch;  // single-token NVFP4 kernel: logit halves and sums of squares (or -1)
   // fp32-weight mode: bf16 copies of the weights
   long long w_router, w_pool, w_gate, w_up, w_down, w_unpool;
   long long x_stage, out_stage, host_io_total;
@@ -230,6 +231,13 @@ void make_layout(const lmoe_config* c, Layout* L) {
     L->splits_dev = take(2 * 4);
     P.grouped_splits = c->weight_dtype == LMOE_NVFP4 ? L->splits_dev : -1;
   }
+  // one token with NVFP4 weights runs as one cooperative kernel (decode_mk.cu) where it fits
+  L->mk_scratch = fp4 && T == 1 && decode_megakernel_fits(static_cast<int>(D), static_cast<int>(Ld),
+                                                          static_cast<int>(I), static_cast<int>(E),
+                                                          static_cast<int>(k))
+                      ? take(decode_megakernel_scratch_floats(static_cast<int>(D), static_cast<int>(Ld),
+                                                              static_cast<int>(E), static_cast<int>(k)) * 4)
+                      : -1;
   P.total = static_cast<long long>(off);
   L->x_stage = take(T * D * (c->act_dtype == LMOE_F32 ? 4 : 2));
   L->out_stage = take(T * D * (c->out_dtype == LMOE_F32 ? 4 : 2));
@@ -519,6 +527,72 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   };
 #define LMOE_MARK(i) \
   if (!mark(i)) return LMOE_ERR_CUDA;
+
+  // One token with NVFP4 weights, when the caller asks for it: the whole block as one
+  // cooperative kernel that streams the weights through shared memory (decode_mk.cu), unless
+  // stages are timed
+  const bool mk = fp4 && L.mk_scratch >= 0 && ev == nullptr && ex != nullptr && ex->single_token_kernel != 0;
+  if (mk) {
+    // the error word, the near-tie counter and the barrier's arrival count start at zero
+    LMOE_CUDA(cudaMemsetAsync(err, 0, 12, s));
+    DecodeMkArgs d{};
+    d.x = x;
+    d.x_f32 = x_f32;
+    d.W_router = static_cast<const __nv_bfloat16*>(W_router);
+    d.router_bias = ex ? ex->router_bias : nullptr;
+    d.forced = ex ? ex->forced_idx : nullptr;
+    d.g_pre = g_pre;
+    d.g_pool = g_pool;
+    d.g_expert = g_expert;
+    d.g_post = g_post;
+    for (int i = 0; i < 5; ++i)
+      d.w[i] = DecodeMkWeight{static_cast<const uint8_t*>(q4[i]->data), static_cast<const uint8_t*>(q4[i]->scales),
+                              q4[i]->tensor_scale};
+    d.D = D;
+    d.L = Ld;
+    d.E = E;
+    d.I = I;
+    d.k = k;
+    d.eps = eps;
+    d.out = out;
+    d.out_f32 = cfg->out_dtype == LMOE_F32;
+    d.g_next = ex ? ex->next_norm_gamma : nullptr;
+    d.next_out = ex ? ex->next_norm_out : nullptr;
+    d.xa = xa;
+    d.logits = logits;
+    d.topk_idx = tk_idx;
+    d.topk_w = tk_w;
+    d.idx_copy = ex ? ex->topk_idx_out : nullptr;
+    d.w_copy = ex ? ex->topk_w_out : nullptr;
+    d.near_tie = near_tie;
+    d.counts = counts;
+    d.offsets = offsets;
+    d.row_of = row_of;
+    d.tok_of = tok_of;
+    d.tiles = tiles;
+    d.n_tiles = n_tiles;
+    d.tile_base = static_cast<int32_t*>(at(L.tile_base));
+    d.tiles2 = static_cast<Tile*>(at(L.tiles2));
+    d.n_tiles2 = static_cast<int32_t*>(at(L.n_tiles2));
+    d.p = p;
+    d.h_codes = static_cast<uint8_t*>(at(L.pub.h));
+    d.h_scales = static_cast<uint8_t*>(at(L.pub.h_scale));
+    d.y = static_cast<__nv_bfloat16*>(at(L.pub.y));
+    d.u = u;
+    d.ss_part = static_cast<float*>(at(L.mk_scratch));
+    d.router_part = d.ss_part + 1LL * k * (Ld / 16) + D / 4;
+    d.bar = err + 2;
+    d.err = err;
+    d.budget = budget;
+    LMOE_CUDA(launch_decode_megakernel(d, s));
+#if LMOE_BOUNDS_CHECKS
+    LMOE_CUDA(launch_validate_routing(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, L.max_tiles,
+                                      d.tile_base, d.tiles2, d.n_tiles2, L.max_tiles2, err, false, s));
+#endif
+    if (ex && ex->near_tie_count_out)
+      LMOE_CUDA(cudaMemcpyAsync(ex->near_tie_count_out, near_tie, 4, cudaMemcpyDeviceToDevice, s));
+    return LMOE_OK;
+  }
 
   LMOE_MARK(LMOE_STAGE_PRENORM);
   // the error word and near-tie counter start at zero on every call: the pre-norm kernel
@@ -876,7 +950,8 @@ lmoe_status lmoe_check_status(const lmoe_config* cfg, void* workspace, cudaStrea
   if (cudaStreamSynchronize(stream) != cudaSuccess) return LMOE_ERR_CUDA;
   if (cudaMemsetAsync(err, 0, 4, stream) != cudaSuccess) return LMOE_ERR_CUDA;
   if (detail) *detail = word;
-  if (word & (kErrWaitProducer | kErrWaitMma | kErrWaitEpilogue | kErrDrain)) return LMOE_ERR_TIMEOUT;
+  if (word & (kErrWaitProducer | kErrWaitMma | kErrWaitEpilogue | kErrDrain | kErrGridBarrier))
+    return LMOE_ERR_TIMEOUT;
   if (word & (kErrBadIndex | kErrBounds)) return LMOE_ERR_ARG;
   return LMOE_OK;
 }

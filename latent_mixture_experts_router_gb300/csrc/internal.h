@@ -28,6 +28,7 @@ enum : uint32_t {
   kErrBadIndex = 1u << 3,
   kErrDrain = 1u << 4,
   kErrBounds = 1u << 5,   // routing structures failed validation (launch_validate_routing)
+  kErrGridBarrier = 1u << 6,   // a grid barrier of the single-token kernel gave up waiting
 };
 
 enum EpiKind : int {
@@ -248,6 +249,52 @@ cudaError_t launch_postnorm_residual(const void* x, bool x_f32, float* u,
                                      const float* upart = nullptr, int usplits = 1,
                                      const float* g_next = nullptr, void* next_out = nullptr);
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s);
+
+// ---- the single-token NVFP4 block as one cooperative kernel (decode_mk.cu)
+constexpr int kDecodeMkMaxSmem = 225 * 1024;   // dynamic; the static part stays under 2 KB
+struct DecodeMkWeight {
+  const uint8_t* codes;        // [rows, K/2] E2M1 pairs
+  const uint8_t* scales;       // E4M3 block scales, block layout of 128-row blocks
+  const float* tensor_scale;   // [1] or [E]
+};
+struct DecodeMkArgs {
+  const void* x;               // [D] bf16 or fp32 (x_f32)
+  int x_f32;
+  const __nv_bfloat16* W_router;   // [E, D]
+  const float* router_bias;    // [E] or nullptr
+  const int32_t* forced;       // [k] or nullptr
+  const float *g_pre, *g_pool, *g_expert, *g_post;
+  DecodeMkWeight w[5];         // pooler, gate, up, down, unpooler
+  int D, L, E, I, k;
+  float eps;
+  void* out;                   // [D] bf16 or fp32 (out_f32)
+  int out_f32;
+  const float* g_next;         // [D] or nullptr: also next_out = RMSNorm(out as stored) * g_next
+  void* next_out;
+  // workspace (the block's layout at T = 1)
+  __nv_bfloat16* xa;           // [2D] xn as bf16 hi | lo
+  float* logits;               // [E]
+  int32_t *topk_idx, *idx_copy, *near_tie, *counts, *offsets, *row_of, *tok_of, *n_tiles, *tile_base, *n_tiles2;
+  float *topk_w, *w_copy;
+  Tile *tiles, *tiles2;
+  float* p;                    // [L]
+  uint8_t* h_codes;            // [k][I/2] by slot
+  uint8_t* h_scales;           // [k][I/16] E4M3 codes by slot
+  __nv_bfloat16* y;            // [k][L], slot j at row row_of[j]
+  float* u;                    // [D]
+  float* ss_part;              // [k L/16 + D/4] sums of squares of 16 values of y, of 4 of u
+  float* router_part;          // [rp][E] the logits over the rp parts of each router row
+  unsigned* bar;               // grid barrier arrivals, zero at the launch
+  unsigned* err;
+  long long budget;
+};
+// Shapes the kernel takes: D, L, I multiples of 256 up to 8192, E <= 1024, k <= 16, and the
+// shared memory it needs within kDecodeMkMaxSmem.
+bool decode_megakernel_fits(int D, int L, int I, int E, int k);
+size_t decode_megakernel_smem(int D, int L, int I, int E, int k);
+long long decode_megakernel_scratch_floats(int D, int L, int E, int k);
+// One launch of one CTA per SM; the caller zeroes *bar (and the status words) before it.
+cudaError_t launch_decode_megakernel(const DecodeMkArgs& d, cudaStream_t s);
 // Checks the routing structures one call left in its workspace: ids in [0, E); offsets start
 // at 0, never decrease, end at R = T k and agree with counts; every pair's row lies in its
 // expert's range and every row is the row of exactly one pair (row_of / tok_of: the scatter
