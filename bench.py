@@ -405,8 +405,8 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
         ex["router_bias"] = inp.router_bias
     if inp.forced_idx is not None:
         ex["forced_idx"] = inp.forced_idx
-    if getattr(args, "single_token_kernel", False):
-        ex["single_token_kernel"] = True
+    if getattr(args, "single_token_path", 0):
+        ex["single_token_path"] = args.single_token_path
     stream = torch.cuda.current_stream(dev)
 
     def step(evs=None):
@@ -540,8 +540,10 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
         "block_roofline": block_roofline(w, costs, used, ms_step, pk, pk_kind, capped, clk),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "stage_ms_note": f"separate pass of {n_bd} steps, an event at every stage boundary"
-                         + (" (the stage kernels: events at the stage boundaries select the kernel chain, "
-                            "the timed steps ran as the single-token kernel)" if single else ""),
+                         + (" (the stage kernels: events at the stage boundaries select the kernel chain; "
+                            "the timed steps ran the single-token path "
+                            f"{getattr(args, 'single_token_path', 0)} of lmoe_ex.single_token_path)"
+                            if T == 1 and w.weights == "nvfp4" and getattr(args, "single_token_path", 0) != 2 else ""),
         # a kernel that ran under the power cap is held against the sustained tensor peak (the
         # measured one of a seconds-long GEMM loop under the same cap), else the burst peak
         "roofline": {**roofline(dom, dom_ms, rcosts, pk, pk_kind, sustained=capped, fp4=w.weights == "nvfp4"),
@@ -674,8 +676,9 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=None,
                     help="oracle sample size in tokens (default: ~10-30 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--single-token-kernel", action="store_true",
-                    help="NVFP4 at T = 1: run the block as one cooperative kernel (lmoe_ex.single_token_kernel)")
+    ap.add_argument("--single-token-path", type=int, default=0, choices=[0, 1, 2],
+                    help="NVFP4 at T = 1: 0 pre/post kernels around the expert GEMMs (default), 1 the whole "
+                         "block as one kernel, 2 the stage kernels (lmoe_ex.single_token_path)")
     args = ap.parse_args()
     ws, rank, local = dist_init()
     if args.impl == "reference" and args.cpu_tokens is None:   # bounded host memory

@@ -141,19 +141,33 @@ enum {
  *                    a NULL entry is skipped.  Kernels of one call are launched with
  *                    programmatic dependent launch, so a kernel's set-up overlaps the end of
  *                    the previous one; an event between two kernels serialises them fully.
- *  single_token_kernel  nonzero, with NVFP4 weights and T = 1 (one decode token): run the whole
- *                    block as one cooperative kernel of one CTA per SM, which streams the
- *                    weights into shared memory by bulk copies and dots them on the CUDA cores
- *                    (four weight phases behind bounded grid barriers), when the shapes allow
- *                    it (D and I multiples of 256 up to 8192, L up to 4096, E <= 1024, and the
- *                    shared memory it needs) and no stage event is set; otherwise, and by
- *                    default, the stage kernels run (on a GB300 at the Muse shapes the kernel
- *                    chain is the faster of the two).  Same arithmetic as the chain up to the
- *                    order of fp32 sums; the workspace then holds xa, the logits, the routing
- *                    tables, p, y and u as after the chain, but not the quantised operands
- *                    (xq, xe, h, c and their scales) nor the partial sums of squares.  A grid
- *                    barrier or stage wait past wait_budget_cycles sets bit 0x40 of the error
- *                    word (LMOE_ERR_TIMEOUT). */
+ *  single_token_path  with NVFP4 weights and T = 1 (one decode token), which kernels run
+ *                    (ignored otherwise, and when a stage event is set; a value outside the
+ *                    three below: LMOE_ERR_ARG):
+ *                    LMOE_SINGLE_TOKEN_DEFAULT (0): two cooperative kernels of one CTA per SM
+ *                      around the tensor-core grouped gate/up and down GEMMs: before them the
+ *                      pre-norm, router, pooler, top-k, routing tables and pool norm (writing
+ *                      the gate/up GEMM's NVFP4 input rows), after them the per-expert norms,
+ *                      combine, unpooler and post-norm; each streams its weights into shared
+ *                      memory by bulk copies and dots them on the CUDA cores, the row steps
+ *                      redundant in every CTA;
+ *                    LMOE_SINGLE_TOKEN_KERNEL (1): the whole block as one such kernel, the
+ *                      expert weights on the CUDA cores too (four weight phases behind grid
+ *                      barriers);
+ *                    LMOE_SINGLE_TOKEN_CHAIN (2): the stage kernels, as at T > 1.
+ *                    On a GB300 at the Muse shapes the default is the fastest of the three.
+ *                    The cooperative kernels take D and I multiples of 256 up to 8192, L up to
+ *                    4096 and E <= 1024 (else the stage kernels run), with the same arithmetic
+ *                    as the chain up to the order of fp32 sums; after them the workspace holds
+ *                    xa, the logits, the routing tables, p, y and u as after the chain, but not
+ *                    every quantised operand nor every partial sum of squares.  A grid barrier
+ *                    or stage wait past wait_budget_cycles sets bit 0x40 of the error word
+ *                    (LMOE_ERR_TIMEOUT). */
+enum {
+  LMOE_SINGLE_TOKEN_DEFAULT = 0,
+  LMOE_SINGLE_TOKEN_KERNEL = 1,
+  LMOE_SINGLE_TOKEN_CHAIN = 2
+};
 typedef struct {
   const float* router_bias;
   const int32_t* forced_idx;
@@ -164,7 +178,7 @@ typedef struct {
   cudaEvent_t* stage_events;
   const float* next_norm_gamma;
   void* next_norm_out;
-  int single_token_kernel;
+  int single_token_path;
 } lmoe_ex;
 
 /* Bytes of device workspace a call with this config needs (host out-parameter). */

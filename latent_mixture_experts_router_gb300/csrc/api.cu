@@ -450,6 +450,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   if (st != LMOE_OK) return st;
   if (top_k != cfg->top_k) return LMOE_ERR_ARG;
   if (ex != nullptr && (ex->next_norm_gamma == nullptr) != (ex->next_norm_out == nullptr)) return LMOE_ERR_ARG;
+  if (ex != nullptr && (ex->single_token_path < LMOE_SINGLE_TOKEN_DEFAULT || ex->single_token_path > LMOE_SINGLE_TOKEN_CHAIN))
+    return LMOE_ERR_ARG;
   if (ex != nullptr && ex->next_norm_out != nullptr &&
       (!aligned16(ex->next_norm_out) || !aligned16(ex->next_norm_gamma)))
     return LMOE_ERR_ALIGN;
@@ -528,14 +530,19 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
 #define LMOE_MARK(i) \
   if (!mark(i)) return LMOE_ERR_CUDA;
 
-  // One token with NVFP4 weights, when the caller asks for it: the whole block as one
-  // cooperative kernel that streams the weights through shared memory (decode_mk.cu), unless
-  // stages are timed
-  const bool mk = fp4 && L.mk_scratch >= 0 && ev == nullptr && ex != nullptr && ex->single_token_kernel != 0;
-  if (mk) {
+  // One token with NVFP4 weights (not when stages are timed): by default the steps around the
+  // expert GEMMs run as two cooperative kernels (decode_mk.cu) — pre-norm, router, pooler, top-k
+  // and pool norm before, combine, unpooler and post-norm after — with the tensor-core grouped
+  // gate/up and down GEMMs between (measured the fastest at the Muse shapes); or the whole
+  // block as one such kernel, or the stage kernels, when the caller asks for them.
+  const int stp = ex ? ex->single_token_path : LMOE_SINGLE_TOKEN_DEFAULT;
+  const bool mk_ok = fp4 && L.mk_scratch >= 0 && ev == nullptr;
+  const bool mk = mk_ok && stp == LMOE_SINGLE_TOKEN_KERNEL;
+  const bool hybrid = mk_ok && stp == LMOE_SINGLE_TOKEN_DEFAULT;
+  DecodeMkArgs d{};
+  if (mk || hybrid) {
     // the error word, the near-tie counter and the barrier's arrival count start at zero
     LMOE_CUDA(cudaMemsetAsync(err, 0, 12, s));
-    DecodeMkArgs d{};
     d.x = x;
     d.x_f32 = x_f32;
     d.W_router = static_cast<const __nv_bfloat16*>(W_router);
@@ -584,7 +591,15 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     d.bar = err + 2;
     d.err = err;
     d.budget = budget;
+    d.mode = mk ? kDecodeMkFull : kDecodeMkPre;
+    d.xe_codes = static_cast<uint8_t*>(at(L.pub.xe));
+    d.xe_scales = static_cast<uint8_t*>(at(L.pub.xe_scale));
+    d.xe_rowscale = static_cast<float*>(at(L.pub.xe_rowscale));
+    d.ss_y = static_cast<const float*>(at(L.pub.ss_y));
+    d.ld_ss_y = L.ld_ss_y;
     LMOE_CUDA(launch_decode_megakernel(d, s));
+  }
+  if (mk) {
 #if LMOE_BOUNDS_CHECKS
     LMOE_CUDA(launch_validate_routing(tk_idx, T, k, E, counts, offsets, row_of, tok_of, tiles, n_tiles, L.max_tiles,
                                       d.tile_base, d.tiles2, d.n_tiles2, L.max_tiles2, err, false, s));
@@ -626,7 +641,9 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
 
   // S1 pre-norm (NVFP4: xn is also quantised per token for the pooler)
   uint8_t* wsb = reinterpret_cast<uint8_t*>(ws);
-  if (fp4)
+  if (hybrid) {
+    // S1-S6 ran in the pre kernel
+  } else if (fp4)
     LMOE_CUDA(launch_prenorm_nvfp4(x, x_f32, g_pre, T, D, eps, xa, xa_cols, wsb + L.pub.xq,
                                    wsb + L.pub.xq_scale, reinterpret_cast<float*>(wsb + L.pub.xq_rowscale),
                                    status2, s));
@@ -677,7 +694,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   bool staged = false;
   for (int i = LMOE_STAGE_PRENORM; ev != nullptr && i <= LMOE_STAGE_POOLNORM; ++i)
     staged = staged || ev[i] != nullptr;
-  SideStream* side = staged ? nullptr : side_stream();
+  SideStream* side = staged || hybrid ? nullptr : side_stream();
   std::unique_lock<std::mutex> side_lock;
   struct Join {  // the caller's stream waits for the side stream on every way out
     cudaStream_t s;
@@ -709,7 +726,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   const bool fused_route = route_small_fits(T, k, E) && (ev == nullptr || ev[LMOE_STAGE_PERMUTE] == nullptr);
   const int rsplits = fused_route && dsp.router > 1 && 1LL * T * dsp.router * E <= 65536 ? dsp.router : 1;
   const int router_mh = dsp.router_mh;
-  st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
+  if (!hybrid) st = run_gemm(kEpiF32, xa, T, xa_cols, xa_cols, wr, E, f32w ? 3LL * D : D, nullptr, E,
                 xa_cols / kBK, nullptr, nullptr, cdiv(T, kBM * router_mh), logits, L.ld_logits, nullptr, 0,
                 err, budget, s, T, dsp.router, partial, router_mh, rsplits == 1);
   if (st != LMOE_OK) return st;
@@ -720,7 +737,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   int32_t* tile_base = static_cast<int32_t*>(at(L.tile_base));
   Tile* tiles2 = static_cast<Tile*>(at(L.tiles2));
   int32_t* n_tiles2 = static_cast<int32_t*>(at(L.n_tiles2));
-  if (fused_route) {
+  if (hybrid) {
+  } else if (fused_route) {
     LMOE_CUDA(launch_route_small(logits, L.ld_logits, partial, rsplits, bias, forced, T, E, k, tk_idx, tk_w,
                                  near_tie,
                                  ex ? ex->topk_idx_out : nullptr, ex ? ex->topk_w_out : nullptr, err,
@@ -746,7 +764,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   if (side != nullptr) {
     if (!joiner.join()) return LMOE_ERR_CUDA;
     side_lock.unlock();
-  } else {
+  } else if (!hybrid) {
     LMOE_MARK(LMOE_STAGE_POOLER);
     st = pooler(s);
     if (st != LMOE_OK) return st;
@@ -754,7 +772,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   if (fp4) {
     LMOE_MARK(LMOE_STAGE_POOLNORM);
     // S6 pool norm, quantised per token, copied to the k expert rows
-    LMOE_CUDA(launch_poolnorm_scatter_nvfp4(p, ss_p, L.ld_ss_p, g_pool, row_of, tk_idx, offsets,
+    if (!hybrid)
+      LMOE_CUDA(launch_poolnorm_scatter_nvfp4(p, ss_p, L.ld_ss_p, g_pool, row_of, tk_idx, offsets,
                                             tile_base, T, Ld, k, eps, wsb + L.pub.xe,
                                             wsb + L.pub.xe_scale, xe_s, s));
     LMOE_MARK(LMOE_STAGE_GATE_UP);
@@ -787,6 +806,12 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
                       L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
                       nullptr, err, budget, s, R / E, down_splits, partial, splits_dev + 1);
     if (st != LMOE_OK) return st;
+    if (hybrid) {   // S9-S11 in the post kernel
+      LMOE_CUDA(cudaMemsetAsync(d.bar, 0, 4, s));
+      d.mode = kDecodeMkPost;
+      LMOE_CUDA(launch_decode_megakernel(d, s));
+      return LMOE_OK;
+    }
     LMOE_MARK(LMOE_STAGE_COMBINE);
     // S9 combine, c quantised per token
     LMOE_CUDA(launch_combine_nvfp4(y, true, ss_y, L.ld_ss_y, row_of, tk_idx, tk_w, g_expert, T, Ld, k, eps,

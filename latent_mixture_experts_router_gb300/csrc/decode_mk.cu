@@ -210,8 +210,11 @@ LMOE_DEV void put_block(uint4* act, float* asc, int np, int b, uint2 q, float sc
 }
 
 // Q of a row held in shared memory (fp32 v[K]) with the row scale of the rule, stored as the
-// dot products read it; returns s.  Consumers only.
-LMOE_DEV float quantize_row_smem(const float* v, int K, const float* recip, float* red, uint4* act, float* asc) {
+// dot products read it; returns s.  With codes_out, the packed codes also go to codes_out
+// [K/2] and the scale codes to the block-layout row (M tile blk_out, its row 0) of scales_out.
+// Consumers only.
+LMOE_DEV float quantize_row_smem(const float* v, int K, const float* recip, float* red, uint4* act, float* asc,
+                                 uint8_t* codes_out = nullptr, uint8_t* scales_out = nullptr, int blk_out = 0) {
   const float4* v4 = reinterpret_cast<const float4*>(v);
   float amax = 0.f;
   for (int i = threadIdx.x; i < K / 4; i += kMkConsumers) {
@@ -233,6 +236,10 @@ LMOE_DEV float quantize_row_smem(const float* v, int K, const float* recip, floa
     uint2 q;
     const uint32_t sc = nvfp4_quant16(blk, six_s, inv_s, recip, q);
     put_block(act, asc, K / 32, b, q, e4m3x2_to_f2(sc).x);
+    if (codes_out != nullptr) {
+      *reinterpret_cast<uint2*>(codes_out + b * 8) = q;
+      scales_out[blocked_sf_offset(blk_out, 0, b, K)] = static_cast<uint8_t>(sc);
+    }
   }
   csync();
   return s;
@@ -508,6 +515,7 @@ __host__ __device__ inline size_t mk_smem_bytes(int D, int L, int I, int E, int 
   return mk_fixed_bytes(D, L, I, E, k) + static_cast<size_t>(kMkSlots) * kMkStageBytes;
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeMkArgs a) {
   extern __shared__ __align__(1024) uint8_t mk_smem[];
   const int D = a.D, L = a.L, I = a.I, E = a.E, k = a.k;
@@ -566,7 +574,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
       int qbase_p = 0;
       // the pre-norm's loads of x and g_pre come back first: the weight stream starts after
       bool ok = mk_wait(&inputs_ready, 0, budget, &s_dead, a.err);
-      for (int ph = 0; ph < 4; ++ph) {
+      const int ph0 = MODE == kDecodeMkPost ? 3 : 0, ph1 = MODE == kDecodeMkPre ? 0 : 3;
+      for (int ph = ph0; ph <= ph1; ++ph) {
         if (ph == 1 && ok) ok = mk_wait(&route_ready, 0, budget, &s_dead, a.err);   // expert rows need the top-k
         const PhaseShare& S = P.ph[ph];
         const int nr_rt = ph == 0 ? P.r1 - P.r0 : 0, rb = S.K / 2;
@@ -675,6 +684,15 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
     return true;
   };
 
+  if constexpr (MODE == kDecodeMkPost) {   // the routing of the pre kernel, from the workspace
+    if (tid == 0) mbar_arrive(&inputs_ready);
+    if (tid < k) {
+      s_idx[tid] = a.topk_idx[tid];
+      s_w[tid] = a.topk_w[tid];
+      s_row[tid] = a.row_of[tid];
+    }
+    csync();
+  } else {
   // ---- P1: pre-norm (fp32 xn in `row`; this CTA's slice of xa as bf16 hi/lo), Q(xn)
   {
     float v[kRowChunks][8], g[kRowChunks][8];
@@ -837,6 +855,16 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
     }
   }
   csync();
+  if constexpr (MODE == kDecodeMkPre) {
+    // Q(h0) as the gate/up GEMM's A row of slot j = this CTA (CTAs 0 .. k-1): its row of the
+    // expert-ordered rows, whose M tile is that row (one row per expert at one token)
+    const int j = cta;
+    const int r = j < k ? s_row[j] : 0;
+    const float s = quantize_row_smem(row, L, recip, red, act, asc, j < k ? a.xe_codes + static_cast<long long>(r) * (L / 2) : nullptr,
+                                      a.xe_scales, r);
+    if (j < k && tid == 0) a.xe_rowscale[r] = s;
+    return;
+  }
   const float s_h0 = quantize_row_smem(row, L, recip, red, act, asc);
 
   // ---- P4: gate and up rows of the k experts; a unit is 16 rows of h (its 16 gate and 16 up
@@ -939,11 +967,21 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
         });
   }
   if (!grid_barrier(a, 2, &s_dead, &s_flag)) return;
+  }   // the pre and expert phases
 
   // ---- P6: per-expert norms (the units' sums of squares, staged in shared memory and summed
   // by one warp per slot), the weighted sum in slot order, Q(c)
+  if constexpr (MODE == kDecodeMkPost) {   // the down GEMM's partial sums of squares of each y row
+    for (int j = warp; j < k; j += kMkCWarps) {
+      float sy = 0.f;
+      for (int i = lane; i < a.ld_ss_y; i += 32) sy += __ldcg(a.ss_y + static_cast<long long>(s_row[j]) * a.ld_ss_y + i);
+      sy = warp_sum(sy);
+      if (lane == 0) s_coef[j] = s_w[j] * rsqrtf(sy / static_cast<float>(L) + a.eps);
+    }
+    csync();
+  }
   {
-    const int nl = L / 16, n4 = k * nl / 4;
+    const int nl = L / 16, n4 = MODE == kDecodeMkPost ? 0 : k * nl / 4;
     for (int q0 = 0; q0 < n4; q0 += 4 * kMkConsumers) {
       float4 v[4];
 #pragma unroll
@@ -958,7 +996,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
       }
     }
     csync();
-    for (int j = warp; j < k; j += kMkCWarps) {
+    for (int j = warp; j < k && MODE != kDecodeMkPost; j += kMkCWarps) {
       float sy = 0.f;
       for (int i = lane; i < nl; i += 32) sy += row[j * nl + i];
       sy = warp_sum(sy);
@@ -1034,7 +1072,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
           ss_u[u] = sq;
         });
   }
-  if (!grid_barrier(a, 3, &s_dead, &s_flag)) return;
+  if (!grid_barrier(a, MODE == kDecodeMkPost ? 0 : 3, &s_dead, &s_flag)) return;
 
   // ---- P8: post-norm + residual; CTA c writes its slice of the output row (and of the next
   // layer's pre-norm of it, whose row sum every CTA takes over the whole row)
@@ -1080,8 +1118,6 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
   }
 }
 
-bool g_mk_attr_set = false;
-
 }  // namespace
 
 size_t decode_megakernel_smem(int D, int L, int I, int E, int k) { return mk_smem_bytes(D, L, I, E, k); }
@@ -1097,13 +1133,14 @@ long long decode_megakernel_scratch_floats(int D, int L, int E, int k) {
   return static_cast<long long>(k) * (L / 16) + D / 4 + static_cast<long long>(router_parts(D)) * E;
 }
 
-cudaError_t launch_decode_megakernel(const DecodeMkArgs& d, cudaStream_t s) {
-  if (!decode_megakernel_fits(d.D, d.L, d.I, d.E, d.k)) return cudaErrorInvalidValue;
-  if (!g_mk_attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(decode_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeMkMaxSmem);
+template <int MODE>
+cudaError_t launch_mode(const DecodeMkArgs& d, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(decode_megakernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kDecodeMkMaxSmem);
     if (e != cudaSuccess) return e;
-    g_mk_attr_set = true;
+    attr = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(sm_count()));   // one CTA per SM
@@ -1116,7 +1153,16 @@ cudaError_t launch_decode_megakernel(const DecodeMkArgs& d, cudaStream_t s) {
   cfg.attrs = attrs;
   cfg.numAttrs = 1;
   count_launch();
-  return cudaLaunchKernelEx(&cfg, decode_megakernel, d);
+  return cudaLaunchKernelEx(&cfg, decode_megakernel<MODE>, d);
+}
+
+cudaError_t launch_decode_megakernel(const DecodeMkArgs& d, cudaStream_t s) {
+  if (!decode_megakernel_fits(d.D, d.L, d.I, d.E, d.k)) return cudaErrorInvalidValue;
+  switch (d.mode) {
+    case kDecodeMkPre: return launch_mode<kDecodeMkPre>(d, s);
+    case kDecodeMkPost: return launch_mode<kDecodeMkPost>(d, s);
+    default: return launch_mode<kDecodeMkFull>(d, s);
+  }
 }
 
 }  // namespace lmoe

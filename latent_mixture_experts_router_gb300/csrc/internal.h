@@ -287,7 +287,18 @@ struct DecodeMkArgs {
   unsigned* bar;               // grid barrier arrivals, zero at the launch
   unsigned* err;
   long long budget;
+  // kDecodeMkFull: the whole block.  kDecodeMkPre: pre-norm, router, pooler, top-k and pool
+  // norm, ending with Q(h0) written as the grouped gate/up GEMM's A rows (xe codes, block-layout
+  // scales, row scales) for the k routed rows.  kDecodeMkPost: from the down GEMM's bf16 y and
+  // its partial sums of squares ss_y (ld_ss_y per row): combine, unpooler, post-norm.
+  int mode;
+  uint8_t* xe_codes;
+  uint8_t* xe_scales;
+  float* xe_rowscale;
+  const float* ss_y;
+  int ld_ss_y;
 };
+enum : int { kDecodeMkFull = 0, kDecodeMkPre = 1, kDecodeMkPost = 2 };
 // Shapes the kernel takes: D, L, I multiples of 256 up to 8192, E <= 1024, k <= 16, and the
 // shared memory it needs within kDecodeMkMaxSmem.
 bool decode_megakernel_fits(int D, int L, int I, int E, int k);

@@ -1,11 +1,12 @@
-"""GPU parity of the single-token NVFP4 kernel (one cooperative launch for the whole block,
-lmoe_ex.single_token_kernel).
+"""GPU parity of the single-token NVFP4 paths (lmoe_ex.single_token_path): the default —
+cooperative pre and post kernels around the tensor-core expert GEMMs (0) — and the whole block
+as one cooperative kernel (1).
 
 * Against the fp64 oracle, under the NVFP4 rules (top-k exact with near ties counted, output
   within 6e-2 x RMS, near-boundary roundings accepted only as a legitimate alternative), over
   every lane layout of the dot products (64-code chunks per lane 1 to 4: D, L, I from 256 to
   8192), fp32 and bf16 inputs and outputs, zipf router bias, forced routing, E = 1024, k = 16.
-* Against the kernel chain on the same call (the default path): the same experts and
+* Against the kernel chain on the same call (SINGLE_TOKEN_CHAIN = 2): the same experts and
   routing tables bit for bit, and p, y, u and the output within the fp32 reordering of the
   same products (both compute every block's products exactly; the sums differ in order).
 * One launch of the library per call; a grid barrier whose wait budget runs out ends the call
@@ -57,15 +58,18 @@ def _launches(lm, fn):
     return lm.lmoe_kernel_launches() - n0
 
 
+@pytest.mark.parametrize("path", [0, 1])
 @pytest.mark.parametrize("D,L,E,I,k,act,routing", SHAPES)
-def test_single_token_parity_with_oracle(cuda, D, L, E, I, k, act, routing):
+def test_single_token_parity_with_oracle(cuda, D, L, E, I, k, act, routing, path):
     import latent_mixture_experts_router_gb300 as lm
     w = _workload(D, L, E, I, k, act, routing)
     inp = workloads.make_inputs(w, cuda)
     blk = make_block(inp)
-    n = _launches(lm, lambda: run(inp, blk=blk, single_token_kernel=True))
-    assert n == 1, f"{n} launches: the single-token kernel did not run"
-    out, idx, _, _ = run(inp, blk=blk, single_token_kernel=True)
+    n = _launches(lm, lambda: run(inp, blk=blk, single_token_path=path))
+    chain = _launches(lm, lambda: run(inp, blk=blk, single_token_path=2))
+    # the whole block as one launch; the default: the pre and post kernels and the expert GEMMs
+    assert (n == 1) if path == 1 else (1 < n < chain), (n, chain)
+    out, idx, _, _ = run(inp, blk=blk, single_token_path=path)
     P = oracle.params_from_inputs(inp)
     x = inp.x.double().cpu().numpy()
     forced = None if inp.forced_idx is None else inp.forced_idx.cpu().numpy()
@@ -82,16 +86,17 @@ def _rel(a, b):
 
 @pytest.mark.parametrize("D,L,E,I,k,act,routing", [SHAPES[0], SHAPES[3], SHAPES[5], SHAPES[6]])
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
-def test_single_token_matches_kernel_chain(cuda, D, L, E, I, k, act, routing, out_dtype):
+@pytest.mark.parametrize("path", [0, 1])
+def test_single_token_matches_kernel_chain(cuda, D, L, E, I, k, act, routing, out_dtype, path):
     import latent_mixture_experts_router_gb300 as lm
     w = _workload(D, L, E, I, k, act, routing, seed=2)
     inp = workloads.make_inputs(w, cuda)
     blk = make_block(inp)
-    assert _launches(lm, lambda: run(inp, blk=blk, out_dtype=out_dtype)) > 1
-    out_c, idx_c, _, cfg = run(inp, blk=blk, out_dtype=out_dtype)
+    assert _launches(lm, lambda: run(inp, blk=blk, out_dtype=out_dtype, single_token_path=2)) > 2
+    out_c, idx_c, _, cfg = run(inp, blk=blk, out_dtype=out_dtype, single_token_path=2)
     out_c = out_c.clone()
     vc = views(blk, cfg)
-    out_m, idx_m, _, _ = run(inp, blk=blk, out_dtype=out_dtype, single_token_kernel=True)
+    out_m, idx_m, _, _ = run(inp, blk=blk, out_dtype=out_dtype, single_token_path=path)
     vm = views(blk, cfg)
     assert torch.equal(idx_m, idx_c)
     for name in ("topk_idx", "counts", "offsets", "row_of", "tok_of", "n_tiles"):
@@ -112,33 +117,35 @@ def test_single_token_matches_kernel_chain(cuda, D, L, E, I, k, act, routing, ou
     assert _rel(out_m.double().cpu().numpy(), out_c.double().cpu().numpy()) < 2e-2
 
 
-def test_grid_barrier_timeout_is_reported_and_context_survives(cuda):
+@pytest.mark.parametrize("path", [0, 1])
+def test_grid_barrier_timeout_is_reported_and_context_survives(cuda, path):
     import latent_mixture_experts_router_gb300 as lm
     w = _workload(2048, 1024, 16, 512, 4, "bf16", "uniform", seed=3)
     inp = workloads.make_inputs(w, cuda)
     blk = make_block(inp)
-    ref, _, _, cfg = run(inp, blk=blk, single_token_kernel=True)
+    ref, _, _, cfg = run(inp, blk=blk, single_token_path=path)
     ref = ref.clone()
     # a budget of one cycle: the waits give up (the first grid barrier at the latest)
-    blk.forward(inp.x, wait_budget_cycles=1, single_token_kernel=True)
+    blk.forward(inp.x, wait_budget_cycles=1, single_token_path=path)
     st, word = lm.lmoe_check_status(cfg, blk._ws)
     assert st == -6 and word & 0x40, (st, hex(word))
-    out, _, _, _ = run(inp, blk=blk, single_token_kernel=True)
+    out, _, _, _ = run(inp, blk=blk, single_token_path=path)
     assert torch.equal(out, ref)
 
 
+@pytest.mark.parametrize("path", [0, 1])
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
-def test_single_token_next_layer_pre_norm(cuda, out_dtype):
+def test_single_token_next_layer_pre_norm(cuda, out_dtype, path):
     w = _workload(4096, 1024, 8, 512, 2, "bf16", "uniform", seed=4)
     inp = workloads.make_inputs(w, cuda)
     blk = make_block(inp)
-    base, _, _, _ = run(inp, blk=blk, out_dtype=out_dtype, single_token_kernel=True)
+    base, _, _, _ = run(inp, blk=blk, out_dtype=out_dtype, single_token_path=path)
     base = base.clone()
     g_next = (1.0 + 0.1 * torch.randn(w.D, generator=torch.Generator().manual_seed(5), dtype=torch.float64)
               ).to(torch.float32).to(cuda)
     nxt = torch.empty(1, w.D, dtype=base.dtype, device=cuda)
     out, _, _, _ = run(inp, blk=blk, out_dtype=out_dtype, next_norm_gamma=g_next, next_norm_out=nxt,
-                       single_token_kernel=True)
+                       single_token_path=path)
     assert torch.equal(out, base)
     ref = oracle.rms_norm(out.double().cpu().numpy(), g_next.double().cpu().numpy(), w.eps)
     err = np.abs(nxt.double().cpu().numpy() - ref).max() / np.sqrt(np.mean(ref ** 2))
@@ -151,8 +158,8 @@ def test_stage_events_take_the_chain_and_16_byte_codes_the_kernel(cuda):
     inp = workloads.make_inputs(w, cuda)
     blk = make_block(inp)
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(lm.NUM_STAGE_EVENTS)]
-    assert _launches(lm, lambda: run(inp, blk=blk, stage_events=evs, single_token_kernel=True)) > 1
-    ref, idx_ref, _, _ = run(inp, blk=blk, single_token_kernel=True)
+    assert _launches(lm, lambda: run(inp, blk=blk, stage_events=evs, single_token_path=1)) > 1
+    ref, idx_ref, _, _ = run(inp, blk=blk, single_token_path=1)
     ref = ref.clone()
     # codes at 16 (not 32) bytes past an allocation: the bulk copies need 16
     codes, scales, s, layout = blk.W["W_pool"]
@@ -161,6 +168,17 @@ def test_stage_events_take_the_chain_and_16_byte_codes_the_kernel(cuda):
     shifted.copy_(codes)
     assert shifted.data_ptr() % 32 == 16
     blk.W["W_pool"] = (shifted, scales, s, layout)
-    assert _launches(lm, lambda: run(inp, blk=blk, single_token_kernel=True)) == 1
-    out, idx, _, _ = run(inp, blk=blk, single_token_kernel=True)
+    assert _launches(lm, lambda: run(inp, blk=blk, single_token_path=1)) == 1
+    out, idx, _, _ = run(inp, blk=blk, single_token_path=1)
     assert torch.equal(out, ref) and torch.equal(idx, idx_ref)
+
+
+def test_single_token_path_out_of_range_is_refused(cuda):
+    import latent_mixture_experts_router_gb300 as lm
+    w = _workload(256, 256, 4, 256, 2, "bf16", "uniform")
+    inp = workloads.make_inputs(w, cuda)
+    blk = make_block(inp)
+    with pytest.raises(lm.LmoeError):
+        blk.forward(inp.x, single_token_path=3)
+    with pytest.raises(lm.LmoeError):
+        blk.forward(inp.x, single_token_path=-1)

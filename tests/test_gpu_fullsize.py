@@ -165,17 +165,18 @@ def test_full_size_bf16(cuda, name):
     del out, idx, blk, inp
 
 
-@pytest.mark.parametrize("name,T,single", [("prefill_nvfp4", None, False), ("decode_nvfp4_hot", 1, False),
-                                           ("decode_nvfp4_hot", 1, True), ("decode_nvfp4_hot", 8, False),
-                                           ("decode_nvfp4_hot", 32, False), ("decode_nvfp4_hot", 128, False),
-                                           ("decode_nvfp4_hot", 512, False)])
-def test_full_size_nvfp4(cuda, name, T, single):
-    # single: T = 1 through the single-token kernel (lmoe_ex.single_token_kernel)
+@pytest.mark.parametrize("name,T,path", [("prefill_nvfp4", None, 0), ("decode_nvfp4_hot", 1, 0),
+                                         ("decode_nvfp4_hot", 1, 1), ("decode_nvfp4_hot", 1, 2),
+                                         ("decode_nvfp4_hot", 8, 0), ("decode_nvfp4_hot", 32, 0),
+                                         ("decode_nvfp4_hot", 128, 0), ("decode_nvfp4_hot", 512, 0)])
+def test_full_size_nvfp4(cuda, name, T, path):
+    # path (lmoe_ex.single_token_path, T = 1 only): 0 pre/post kernels around the expert GEMMs
+    # (the default), 1 one kernel, 2 the stage kernels
     w = workloads.WORKLOADS[name]
     if T is not None:
         w = w.with_tokens(T)
     inp = workloads.make_inputs(w, cuda)
-    out, idx, blk, cfg = run(inp, single_token_kernel=True) if single else run(inp)
+    out, idx, blk, cfg = run(inp, single_token_path=path)
     forced = None if inp.forced_idx is None else inp.forced_idx.cpu().numpy()
     n = _grade(w.name, w, inp, out, idx, blk, cfg, forced=forced)
     assert n >= min(w.T, N_SAMPLE)
