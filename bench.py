@@ -262,17 +262,20 @@ def oracle_resident(w: workloads.Workload, n_tokens: int, inp=None):
 
 
 def time_oracle(w: workloads.Workload, n_tokens: int, inp=None, min_seconds: float = 0.0,
-                repeats: int = 1):
+                repeats: int = 1, keep: bool = False):
     """Per-call seconds of the fp64 oracle on the first n_tokens of w; repeats the call
-    at least ``repeats`` times and until ``min_seconds`` of oracle time have passed."""
+    at least ``repeats`` times and until ``min_seconds`` of oracle time have passed.  With keep,
+    also (P, x, forced, out, trace) of the last call."""
     import oracle
     P, x, forced = oracle_resident(w, n_tokens, inp=inp)
     times = []
+    ref = tr = None
     while len(times) < repeats or sum(times) < min_seconds:
+        tr = oracle.Trace() if keep else None
         t0 = time.perf_counter()
-        oracle.forward_batched(x, P, w.k, forced_idx=forced)
+        ref = oracle.forward_batched(x, P, w.k, forced_idx=forced, trace=tr)
         times.append(time.perf_counter() - t0)
-    return times
+    return (times, (P, x, forced, ref, tr)) if keep else times
 
 
 def pick_workload(args) -> workloads.Workload:
@@ -519,6 +522,17 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
     torch.cuda.synchronize()
     barrier(ws)
     ms_io = allreduce_max(e0.elapsed_time(e1), ws)
+    # the parity sample: one more step on the timed path, the output and top-k of its first
+    # tokens kept for the oracle (rank 0, with the CPU baseline)
+    par = None
+    if rank == 0 and not args.no_cpu_baseline:
+        step()
+        torch.cuda.synchronize()
+        n_par = max(1, min(cpu_tokens, T))
+        lay_p = lm.lmoe_get_workspace_layout(cfg)
+        par = (out[:n_par].double().cpu().numpy(),
+               blk._ws[lay_p["topk_idx"]:lay_p["topk_idx"] + 4 * n_par * w.k].view(torch.int32)
+               .view(n_par, w.k).cpu().numpy())
     e2e = {"value": round(ws * T * args.steps / (ms_io * 1e-3), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": int(x_host.numel() * x_host.element_size()),
            "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()),
@@ -559,8 +573,21 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
         "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
     }
     if not args.no_cpu_baseline:
+        from oracle.compare import TOL_BF16, TOL_NVFP4, compare_block
         n_tok = max(1, min(cpu_tokens, w.T))
-        times = time_oracle(w, n_tok, inp=inp, min_seconds=cpu_seconds)
+        times, (P_o, x_o, forced_o, ref_o, tr_o) = time_oracle(w, n_tok, inp=inp, min_seconds=cpu_seconds, keep=True)
+        tol = TOL_NVFP4 if w.weights == "nvfp4" else TOL_BF16
+        pr = compare_block(par[0], par[1], x_o, P_o, w.k, tol, tr=tr_o, ref=ref_o, forced_idx=forced_o)
+        rec["parity"] = {
+            "tokens": pr.tokens, "topk_exact": pr.idx_exact, "near_tie": pr.near_tie_tokens,
+            "order_swaps": pr.order_swaps, "quant_boundary": pr.quant_boundary_tokens,
+            "bad_topk": len(pr.bad_idx_tokens), "max_abs_err": float(f"{pr.max_abs_err:.4e}"),
+            "ref_rms": float(f"{pr.ref_rms:.4e}"),
+            "max_abs_err_over_rms": float(f"{pr.max_abs_err / max(pr.ref_rms, 1e-30):.4e}"), "tolerance": tol,
+            "ok": bool(pr.ok),
+            "source": f"the first {pr.tokens} tokens of the timed workload: the output and top-k of one more "
+                      "step on the timed path against the fp64 oracle, under the rules of oracle/compare.py "
+                      "(near ties and in-band order swaps re-graded; NVFP4 rounding-boundary alternatives)"}
         t = sum(times)
         rec["cpu_baseline"] = {"value": round(n_tok * len(times) / t, 3), "unit": "tokens/s",
                                "cores": os.cpu_count(), "kind": "oracle",
@@ -619,7 +646,8 @@ def run_ours(args, ws, rank, local):
         line["workloads"] = {r["config"]["workload"]: r for r in recs[1:]}
         line["workloads_note"] = ("the block's other workloads, measured after the headline one in the "
                                   "same run and the same way (each record: K device-timed steps, "
-                                  "dominant kernel, end-to-end host-I/O figure, clocks, oracle baseline)")
+                                  "dominant kernel, end-to-end host-I/O figure, clocks, oracle baseline, parity "
+                                  "of the first tokens against the oracle)")
     line["bench_wall_s"] = round(time.perf_counter() - t0, 1)
     return line
 
