@@ -162,7 +162,8 @@ void make_layout(const lmoe_config* c, Layout* L) {
   L->ld_ss_u = cdiv(D, bn_ss);
   L->max_tiles = cdiv(R, kBM) + static_cast<int>(E < R ? E : R);
   L->max_tiles2 = cdiv(R, 2 * kBM) + static_cast<int>(E < R ? E : R);
-  P.err = take(kAlign);  // error word; the near-tie counter shares this line
+  P.err = take(kAlign);  // error word; the near-tie counter and the single-token kernels' grid
+                         // barrier counters (words 2 and 3) share this line
   L->near_tie = P.err + 4;
   P.xa = take(T * P.xa_cols * 2);
   P.logits = take(T * L->ld_logits * 4);
@@ -358,7 +359,7 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                          const int* n_tiles, int m_tiles, void* out, long long ldo,
                          uint8_t* out_scales, float* ss, int ld_ss, const float* row_scale,
                          const float* ts, const float* ts2, unsigned* err, long long budget,
-                         cudaStream_t s, long long rows_per_b, int splits = 1,
+                         cudaStream_t s, long long rows_per_b, int tile_rows, int splits = 1,
                          float* partial = nullptr, int* splits_dev = nullptr,
                          bool reduce = true) {
   CUtensorMap maps[6];
@@ -400,7 +401,7 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
   a.adaptive_splits = adaptive ? 1 : 0;
   a.splits_out = tiles != nullptr ? splits_dev : nullptr;
   if (adaptive && (partial == nullptr || splits_dev == nullptr)) return LMOE_ERR_WORKSPACE;
-  LMOE_CUDA(launch_gemm_fp4(epi, maps, a, m_tiles, s));
+  LMOE_CUDA(launch_gemm_fp4(epi, maps, a, m_tiles, tile_rows, s));
   if (splits > 1 && reduce) {   // else the consumer sums the partials
     if (epi == kFp4EpiSwiGLUQuant)
       LMOE_CUDA(launch_swiglu_reduce_nvfp4(partial, splits_dev, static_cast<int>(a_rows), N, tiles,
@@ -410,6 +411,71 @@ lmoe_status run_gemm_fp4(Fp4EpiKind epi, Fp4Operand A, long long a_rows, int K, 
                                      adaptive ? splits_dev : nullptr,
                                      epi == kFp4EpiBf16Ss || epi == kFp4EpiBf16SsWide));
   }
+  return LMOE_OK;
+}
+
+// The grouped gate/up and down GEMMs of a few tokens (every M tile at most 32 rows) as one
+// launch: xe (R rows, K = Ld) times the gate and up weights into h (codes and block-layout
+// scales, the down GEMM's A), then h (K = I) times the down weights into bf16 y with its sums
+// of squares per 128 columns.  Both unsplit; the split counts left for inspection are 1.
+lmoe_status run_gemm_fp4_pair(Fp4Operand xe, const float* xe_s, Fp4Operand gate, Fp4Operand up, Fp4Operand down,
+                              const float* ts_g, const float* ts_u, const float* ts_d, long long R, int Ld, int I,
+                              long long E, Tile* tiles, const int* n_tiles, int m_tiles, uint8_t* h, uint8_t* h_scales,
+                              void* y, float* ss_y, int ld_ss_y, int* splits_dev, unsigned* err,
+                              long long budget, cudaStream_t s) {
+  CUtensorMap maps[5];
+  const unsigned long long k1 = Ld / 2, k2 = I / 2;
+  if (!encode_u8_2d(&maps[0], xe.codes, k1, R, k1, 128, 32, true) ||
+      !encode_u8_2d(&maps[1], gate.codes, k1, E * I, k1, 128, kBNFp4, true) ||
+      !encode_u8_2d(&maps[2], up.codes, k1, E * I, k1, 128, kBNFp4, true) ||
+      !encode_u8_2d(&maps[3], h, k2, R, k2, 128, 32, true) ||
+      !encode_u8_2d(&maps[4], down.codes, k2, E * Ld, k2, 128, kBNFp4, true))
+    return LMOE_ERR_CUDA;
+  Fp4PairArgs a{};
+  Fp4Args& g = a.gu;
+  g.M = static_cast<int>(R);
+  g.N = I;
+  g.num_kb = Ld / 256;
+  g.tiles = tiles;
+  g.n_tiles = n_tiles;
+  g.out = h;
+  g.ldo = I;
+  g.out_scales = h_scales;
+  g.row_scale = xe_s;
+  g.tensor_scale = ts_g;
+  g.tensor_scale2 = ts_u;
+  g.a_scales = xe.scales;
+  g.b_scales = gate.scales;
+  g.b2_scales = up.scales;
+  g.err = err;
+  g.budget = budget;
+  g.b_stream_once = 1;
+  g.k_splits = 1;
+  g.splits_out = splits_dev;
+  g.max_tiles = m_tiles;
+  g.n_groups = static_cast<int>(E);
+  Fp4Args& d = a.dn;
+  d.M = static_cast<int>(R);
+  d.N = Ld;
+  d.num_kb = I / 256;
+  d.tiles = tiles;
+  d.n_tiles = n_tiles;
+  d.out = y;
+  d.ldo = Ld;
+  d.ss = ss_y;
+  d.ld_ss = ld_ss_y;
+  d.tensor_scale = ts_d;
+  d.a_scales = h_scales;
+  d.b_scales = down.scales;
+  d.err = err;
+  d.budget = budget;
+  d.b_stream_once = 1;
+  d.k_splits = 1;
+  d.splits_out = splits_dev != nullptr ? splits_dev + 1 : nullptr;
+  d.max_tiles = m_tiles;
+  d.n_groups = static_cast<int>(E);
+  a.tiles = tiles;
+  LMOE_CUDA(launch_gemm_fp4_pair(maps, a, m_tiles, s));
   return LMOE_OK;
 }
 
@@ -541,8 +607,9 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   const bool hybrid = mk_ok && stp == LMOE_SINGLE_TOKEN_DEFAULT;
   DecodeMkArgs d{};
   if (mk || hybrid) {
-    // the error word, the near-tie counter and the barrier's arrival count start at zero
-    LMOE_CUDA(cudaMemsetAsync(err, 0, 12, s));
+    // the error word, the near-tie counter and the arrival counts of the grid barriers (the
+    // whole-block or pre kernel's; the post kernel's) start at zero
+    LMOE_CUDA(cudaMemsetAsync(err, 0, 16, s));
     d.x = x;
     d.x_f32 = x_f32;
     d.W_router = static_cast<const __nv_bfloat16*>(W_router);
@@ -683,7 +750,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     if (fp4)
       return run_gemm_fp4(fp4_dense_epi(dsp.pooler, Ld), xq, T, D, op(q4[0]), Ld, nullptr, Ld, nullptr, nullptr, m_tiles_T,
                           p, Ld, nullptr, ss_p, L.ld_ss_p, xq_s, q4[0]->tensor_scale, nullptr, err, budget,
-                          ps, T, dsp.pooler, partial_pool);
+                          ps, T, T, dsp.pooler, partial_pool);
     const int pool_k = f32w ? 3 * D : D;
     return run_gemm(kEpiF32Ss, xa, T, pool_k, xa_cols, wp, Ld, pool_k, nullptr, Ld, pool_k / kBK,
                     nullptr, nullptr, cdiv(T, kBM * pool_mh), p, Ld, ss_p, L.ld_ss_p, err, budget, ps, T,
@@ -791,23 +858,32 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
       return grouped_split_possible(lo_tiles, L.max_tiles, cdiv(N, kBNFp4), num_kb, grid, gs) ? gs : 1;
     };
     const Fp4Operand up = op(q4[2]);
-    st = run_gemm_fp4(kFp4EpiSwiGLUQuant, xeq, R, Ld, op(q4[1]), 1LL * E * I, &up, I, tiles, n_tiles,
-                      L.max_tiles, wsb + L.pub.h, I, wsb + L.pub.h_scale, nullptr, 0, xe_s,
-                      q4[1]->tensor_scale, q4[2]->tensor_scale, err, budget, s, R / E,
-                      grouped_splits(I, Ld / 256), partial, splits_dev);
-    if (st != LMOE_OK) return st;
-    LMOE_MARK(LMOE_STAGE_DOWN);
-    // S8 grouped down: y rounded to bf16, with per-row partial sums of squares of those values;
-    // unsplit on 128 x 256 tiles, which read each expert's h tile (and pay each stage's A box,
-    // scale copies and barriers) once per 256 output columns: measured faster at every T
-    const int down_splits = grouped_splits(Ld, I / 256);
-    const Fp4EpiKind down_epi = down_splits <= 1 && Ld % 256 == 0 ? kFp4EpiBf16SsWide : kFp4EpiBf16Ss;
-    st = run_gemm_fp4(down_epi, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
-                      L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
-                      nullptr, err, budget, s, R / E, down_splits, partial, splits_dev + 1);
-    if (st != LMOE_OK) return st;
-    if (hybrid) {   // S9-S11 in the post kernel
-      LMOE_CUDA(cudaMemsetAsync(d.bar, 0, 4, s));
+    // a few tokens (M tiles of at most 32 rows) and gate/up tiles for at least every SM: S7 and
+    // S8 as one launch, whose down tiles fill the SMs that finish their gate/up tiles first
+    if (T <= 32 && Ld % 256 == 0 && ev == nullptr && 1LL * lo_tiles * cdiv(I, kBNFp4) >= sm_count()) {
+      st = run_gemm_fp4_pair(xeq, xe_s, op(q4[1]), up, op(q4[3]), q4[1]->tensor_scale, q4[2]->tensor_scale,
+                             q4[3]->tensor_scale, R, Ld, I, E, tiles, n_tiles, L.max_tiles, wsb + L.pub.h,
+                             wsb + L.pub.h_scale, y, ss_y, L.ld_ss_y, splits_dev, err, budget, s);
+      if (st != LMOE_OK) return st;
+    } else {
+      st = run_gemm_fp4(kFp4EpiSwiGLUQuant, xeq, R, Ld, op(q4[1]), 1LL * E * I, &up, I, tiles, n_tiles,
+                        L.max_tiles, wsb + L.pub.h, I, wsb + L.pub.h_scale, nullptr, 0, xe_s,
+                        q4[1]->tensor_scale, q4[2]->tensor_scale, err, budget, s, R / E, T,
+                        grouped_splits(I, Ld / 256), partial, splits_dev);
+      if (st != LMOE_OK) return st;
+      LMOE_MARK(LMOE_STAGE_DOWN);
+      // S8 grouped down: y rounded to bf16, with per-row partial sums of squares of those values;
+      // unsplit on 128 x 256 tiles, which read each expert's h tile (and pay each stage's A box,
+      // scale copies and barriers) once per 256 output columns: measured faster at every T
+      const int down_splits = grouped_splits(Ld, I / 256);
+      const Fp4EpiKind down_epi = down_splits <= 1 && Ld % 256 == 0 ? kFp4EpiBf16SsWide : kFp4EpiBf16Ss;
+      st = run_gemm_fp4(down_epi, hq, R, I, op(q4[3]), 1LL * E * Ld, nullptr, Ld, tiles, n_tiles,
+                        L.max_tiles, y, Ld, nullptr, ss_y, L.ld_ss_y, nullptr, q4[3]->tensor_scale,
+                        nullptr, err, budget, s, R / E, T, down_splits, partial, splits_dev + 1);
+      if (st != LMOE_OK) return st;
+    }
+    if (hybrid) {   // S9-S11 in the post kernel, with a barrier counter of its own
+      d.bar = err + 3;
       d.mode = kDecodeMkPost;
       LMOE_CUDA(launch_decode_megakernel(d, s));
       return LMOE_OK;
@@ -819,8 +895,8 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     LMOE_MARK(LMOE_STAGE_UNPOOLER);
     // S10 unpooler u = s_c * s_W * (Q(c) . W_unpool^T)
     st = run_gemm_fp4(fp4_dense_epi(dsp.unpool, D), cq, T, Ld, op(q4[4]), D, nullptr, D, nullptr, nullptr, m_tiles_T, u,
-                      D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s, T, dsp.unpool,
-                      partial, nullptr, false);
+                      D, nullptr, ss_u, L.ld_ss_u, c_s, q4[4]->tensor_scale, nullptr, err, budget, s, T, T,
+                      dsp.unpool, partial, nullptr, false);
     if (st != LMOE_OK) return st;
   } else {
   LMOE_MARK(LMOE_STAGE_POOLNORM);

@@ -685,7 +685,10 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
   };
 
   if constexpr (MODE == kDecodeMkPost) {   // the routing of the pre kernel, from the workspace
+    // launched while the down GEMM drains: the producer streams the unpooler's weights at once,
+    // the consumers read nothing an earlier kernel wrote before that GEMM has completed
     if (tid == 0) mbar_arrive(&inputs_ready);
+    griddep_wait();
     if (tid < k) {
       s_idx[tid] = a.topk_idx[tid];
       s_w[tid] = a.topk_w[tid];
@@ -1147,11 +1150,15 @@ cudaError_t launch_mode(const DecodeMkArgs& d, cudaStream_t s) {
   cfg.blockDim = dim3(kMkThreads);
   cfg.dynamicSmemBytes = decode_megakernel_smem(d.D, d.L, d.I, d.E, d.k);
   cfg.stream = s;
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeCooperative;   // every CTA resident at once: the grid
   attrs[0].val.cooperative = 1;                     // barriers wait on one another
+  // the post kernel follows the down GEMM with programmatic dependent launch (it waits for
+  // that GEMM before reading its outputs); the others follow a memset of their counters
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = MODE == kDecodeMkPost ? 2 : 1;
   count_launch();
   return cudaLaunchKernelEx(&cfg, decode_megakernel<MODE>, d);
 }

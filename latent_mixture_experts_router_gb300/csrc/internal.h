@@ -50,7 +50,10 @@ enum Fp4EpiKind : int {
 
 // One M tile of a grouped GEMM: rows [row0, row0 + nrows) of A, all of expert `expert`.
 struct Tile {
-  int expert, row0, nrows, pad;
+  int expert, row0, nrows;
+  // written as 0 with the tile; the expert-pair GEMM counts in it the gate/up epilogue warps
+  // done with the tile's h rows (gemm_fp4.cu)
+  int ready;
 };
 
 struct GemmArgs {
@@ -108,10 +111,21 @@ struct Fp4Args {
   int n_groups;              // grouped: experts (B holds n_groups * N rows)
 };
 
+// The grouped gate/up (kFp4EpiSwiGLUQuant) and down (kFp4EpiBf16SsWide) GEMMs of a few tokens
+// as one persistent launch, both unsplit, every M tile of at most 32 rows; gu.out / gu.out_scales
+// (h) are dn's A operand.  tiles: the table of gu and dn, writable (Tile::ready).  maps = {A of
+// gu (box of 32 rows), gate codes, up codes, A of dn (h, box of 32 rows), down codes}.
+struct Fp4PairArgs {
+  Fp4Args gu, dn;
+  Tile* tiles;
+};
+cudaError_t launch_gemm_fp4_pair(const CUtensorMap* maps, const Fp4PairArgs& a, int m_tiles, cudaStream_t s);
+
 // NVFP4 GEMM; maps = {A codes with boxes of 32, 64, 96, 128 rows, B codes, B2 codes}; scales
-// come from the Fp4Args pointers (block layout; B in blocks of the tile's N rows).
+// come from the Fp4Args pointers (block layout; B in blocks of the tile's N rows).  tile_rows
+// bounds the rows of every M tile (at most 32: the variant with a 32-row A area per stage).
 cudaError_t launch_gemm_fp4(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Args& a, int m_tiles,
-                            cudaStream_t s);
+                            int tile_rows, cudaStream_t s);
 
 // NVFP4 row kernels (rowops.cu)
 cudaError_t launch_prenorm_nvfp4(const void* x, bool x_f32, const float* g_pre, int T, int D,

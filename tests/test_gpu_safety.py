@@ -99,7 +99,7 @@ def test_validate_routing_accepts_real_routing_and_flags_corruption(lm, T, E, k,
     saved = ws.clone()
     row_of = lambda: _i32(ws, lay["row_of"], R)   # noqa: E731
     offsets = lambda: _i32(ws, lay["offsets"], E + 1)   # noqa: E731
-    tiles = lambda: _i32(ws, lay["tiles"], 4 * 64)   # noqa: E731  (expert, row0, nrows, pad)
+    tiles = lambda: _i32(ws, lay["tiles"], 4 * 64)   # noqa: E731  (expert, row0, nrows, ready)
     n_tiles = lambda: _i32(ws, lay["n_tiles"], 1)   # noqa: E731
 
     def dup_row():
