@@ -437,8 +437,15 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
     stage_ms = {name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in bd)
                 for i, name in enumerate(lm.STAGES)}
     costs, used = stage_costs(w, counts)
+    # the expert pair (lmoe_expert_pair): gate/up and down in one kernel, which the gate_up stage
+    # spans (the down stage is empty); its bytes are both GEMMs'
+    pair = lm.lmoe_expert_pair(cfg)
+    if pair:
+        costs["expert_pair"] = tuple(a + b for a, b in zip(costs["gate_up"], costs["down"]))
+        stage_ms["expert_pair"] = stage_ms["gate_up"] + stage_ms["down"]
+        del costs["gate_up"], costs["down"]
     dom = max((s for s in costs if s in stage_ms), key=lambda s: stage_ms[s])
-    di = lm.STAGES.index(dom)
+    di = lm.STAGES.index("gate_up" if dom == "expert_pair" else dom)
 
     # ---- timed region (device): K whole steps, nothing recorded between the kernels
     clocks = ClockSampler(local) if rank == 0 else None
@@ -464,7 +471,8 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
     #      their launch overlap, which is why the headline pass above records none.  A step that
     #      ran as one kernel (one token with NVFP4 weights: the single-token kernel, which stage
     #      events turn back into the kernel chain) is timed by events around each call.
-    single = launches == args.steps
+    single = (T == 1 and w.weights == "nvfp4" and getattr(args, "single_token_path", 0) == 1
+              and launches == 2 * args.steps)
     rcosts = dict(costs)
     if single:
         dom = "single_token_kernel"
@@ -554,6 +562,8 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
         "block_roofline": block_roofline(w, costs, used, ms_step, pk, pk_kind, capped, clk),
         "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "stage_ms_note": f"separate pass of {n_bd} steps, an event at every stage boundary"
+                         + ("; gate/up and down ran as one kernel (the expert pair), which the gate_up stage "
+                            "spans (down empty); expert_pair = their sum" if pair else "")
                          + (" (the stage kernels: events at the stage boundaries select the kernel chain; "
                             "the timed steps ran the single-token path "
                             f"{getattr(args, 'single_token_path', 0)} of lmoe_ex.single_token_path)"
@@ -563,8 +573,8 @@ def measure(args, ws, rank, local, w, blk, inp, cpu_tokens: int, cpu_seconds: fl
         "roofline": {**roofline(dom, dom_ms, rcosts, pk, pk_kind, sustained=capped, fp4=w.weights == "nvfp4"),
                      "traffic": measured_traffic(dom, w, used),
                      "timing": (f"CUDA events on the launching stream around each call (the single-token "
-                                f"kernel and the memset of its status words), {args.steps} steps timed right "
-                                "after the headline pass" if single else
+                                f"kernel and the kernel that clears its status words), {args.steps} steps timed "
+                                "right after the headline pass" if single else
                                 f"CUDA events on the launching stream around the kernel, {args.steps} steps "
                                 "timed right after the headline pass (that pass records no events: an "
                                 "event between two kernels turns off their launch overlap)"),

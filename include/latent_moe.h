@@ -162,7 +162,10 @@ enum {
  *                    xa, the logits, the routing tables, p, y and u as after the chain, but not
  *                    every quantised operand nor every partial sum of squares.  A grid barrier
  *                    or stage wait past wait_budget_cycles sets bit 0x40 of the error word
- *                    (LMOE_ERR_TIMEOUT). */
+ *                    (LMOE_ERR_TIMEOUT).
+ *  separate_expert_gemms  nonzero: the grouped gate/up and down GEMMs run as two launches
+ *                    even where lmoe_expert_pair() says they run as one (for inspection:
+ *                    both compute the same values bit for bit). */
 enum {
   LMOE_SINGLE_TOKEN_DEFAULT = 0,
   LMOE_SINGLE_TOKEN_KERNEL = 1,
@@ -179,7 +182,18 @@ typedef struct {
   const float* next_norm_gamma;
   void* next_norm_out;
   int single_token_path;
+  int separate_expert_gemms;
 } lmoe_ex;
+
+/* Whether a call with this config runs the grouped gate/up (S7) and down (S8) GEMMs as one
+ * persistent launch, the expert pair (host arithmetic only; *used = 1 or 0): NVFP4 weights,
+ * T <= 32 (every expert's rows fit one 32-row tile), d_latent a multiple of 256, and at
+ * least 152 gate/up tiles of 128 columns (top_k * d_ff / 128, or more rows' worth).  The
+ * down tiles of an expert start once all of its gate/up tiles have stored h (a count per
+ * tile in the workspace, waited on with wait_budget_cycles; past it: LMOE_ERR_TIMEOUT), so
+ * the SMs that finish their gate/up tiles first take the down tiles.  With stage events the
+ * gate_up stage then spans both GEMMs and the down stage is empty.                      */
+lmoe_status lmoe_expert_pair(const lmoe_config* cfg, int* used);
 
 /* Bytes of device workspace a call with this config needs (host out-parameter). */
 lmoe_status lmoe_workspace_size(const lmoe_config* cfg, size_t* bytes);

@@ -21,7 +21,7 @@ import torch
 from ._lib import (Config, LmoeError, lmoe_workspace_size, lmoe_workspace_size_host_io,  # noqa: F401
                    lmoe_get_workspace_layout, latent_moe_forward, latent_moe_forward_ex,
                    latent_moe_forward_host_io, latent_moe_forward_host_io_ex, lmoe_check_status,
-                   lmoe_wait_selftest, load,
+                   lmoe_wait_selftest, lmoe_expert_pair, load,
                    LIB_PATH, STAGES, NUM_STAGE_EVENTS, lmoe_kernel_launches, SINGLE_TOKEN_DEFAULT,
                    SINGLE_TOKEN_KERNEL, SINGLE_TOKEN_CHAIN,
                    lmoe_quantize_nvfp4, lmoe_nvfp4_block_scales, SCALES_ROW_MAJOR, SCALES_BLOCKED,

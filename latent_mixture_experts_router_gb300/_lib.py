@@ -49,7 +49,8 @@ class lmoe_ex(ctypes.Structure):
                 ("topk_idx_out", ctypes.c_void_p), ("topk_w_out", ctypes.c_void_p),
                 ("near_tie_count_out", ctypes.c_void_p), ("wait_budget_cycles", ctypes.c_longlong),
                 ("stage_events", ctypes.c_void_p), ("next_norm_gamma", ctypes.c_void_p),
-                ("next_norm_out", ctypes.c_void_p), ("single_token_path", ctypes.c_int)]
+                ("next_norm_out", ctypes.c_void_p), ("single_token_path", ctypes.c_int),
+                ("separate_expert_gemms", ctypes.c_int)]
 
 SINGLE_TOKEN_DEFAULT, SINGLE_TOKEN_KERNEL, SINGLE_TOKEN_CHAIN = 0, 1, 2   # lmoe_ex.single_token_path
 
@@ -102,6 +103,8 @@ def _lib():
         L.lmoe_check_status.restype = ctypes.c_int
         L.lmoe_wait_selftest.argtypes = [ctypes.POINTER(lmoe_config), _P, ctypes.c_longlong, _P]
         L.lmoe_wait_selftest.restype = ctypes.c_int
+        L.lmoe_expert_pair.argtypes = [ctypes.POINTER(lmoe_config), ctypes.POINTER(ctypes.c_int)]
+        L.lmoe_expert_pair.restype = ctypes.c_int
         L.lmoe_kernel_launches.restype = ctypes.c_ulonglong
         L.lmoe_kernel_launches.argtypes = []
         _lib_handle = L
@@ -180,6 +183,14 @@ def lmoe_workspace_size_host_io(cfg: Config) -> int:
     return n.value
 
 
+def lmoe_expert_pair(cfg: Config) -> bool:
+    """Whether a call with ``cfg`` runs the grouped gate/up and down GEMMs as one launch."""
+    used = ctypes.c_int()
+    c = cfg.c()
+    _check(_lib().lmoe_expert_pair(ctypes.byref(c), ctypes.byref(used)), "lmoe_expert_pair")
+    return bool(used.value)
+
+
 def lmoe_get_workspace_layout(cfg: Config) -> dict:
     lay = lmoe_workspace_layout()
     c = cfg.c()
@@ -212,11 +223,12 @@ def latent_moe_forward_ex(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down
                           g_pre, g_post, top_k, out, workspace, stream=None, router_bias=None,
                           forced_idx=None, topk_idx_out=None, topk_w_out=None, near_tie_count_out=None,
                           wait_budget_cycles=0, stage_events=None, next_norm_gamma=None, next_norm_out=None,
-                          single_token_path=0):
+                          single_token_path=0, separate_expert_gemms=False):
     """``stage_events``: a list of NUM_STAGE_EVENTS torch.cuda.Event(enable_timing=True) or None,
     recorded by the library at the stage boundaries (for per-stage timing; None entries are
     skipped).  ``single_token_path``: with NVFP4 weights and one token, which kernels run
-    (SINGLE_TOKEN_DEFAULT, SINGLE_TOKEN_KERNEL or SINGLE_TOKEN_CHAIN; lmoe_ex.single_token_path)."""
+    (SINGLE_TOKEN_DEFAULT, SINGLE_TOKEN_KERNEL or SINGLE_TOKEN_CHAIN; lmoe_ex.single_token_path).
+    ``separate_expert_gemms``: gate/up and down as two launches where lmoe_expert_pair() says one."""
     keep = []
     args = _fwd_args(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool, g_pre,
                      g_post, top_k, out, workspace, stream, keep)
@@ -232,7 +244,8 @@ def latent_moe_forward_ex(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down
     ex = lmoe_ex(_ptr(router_bias), _ptr(forced_idx), _ptr(topk_idx_out), _ptr(topk_w_out),
                  _ptr(near_tie_count_out), int(wait_budget_cycles),
                  ctypes.cast(evs, ctypes.c_void_p) if evs is not None else None,
-                 _ptr(next_norm_gamma), _ptr(next_norm_out), int(single_token_path))
+                 _ptr(next_norm_gamma), _ptr(next_norm_out), int(single_token_path),
+                 1 if separate_expert_gemms else 0)
     _check(_lib().latent_moe_forward_ex(*args, ctypes.byref(ex)), "latent_moe_forward_ex")
 
 
@@ -252,7 +265,7 @@ def latent_moe_forward_host_io_ex(cfg, x_host, W_router, W_pool, g_pool, W_gate,
     args = _fwd_args(cfg, x_host, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool,
                      g_pre, g_post, top_k, out_host, workspace, stream, keep)
     ex = lmoe_ex(_ptr(router_bias), _ptr(forced_idx), None, None, None, 0, None, None, None,
-                 int(single_token_path))
+                 int(single_token_path), 0)
     _check(_lib().latent_moe_forward_host_io_ex(*args, ctypes.byref(ex)), "latent_moe_forward_host_io_ex")
 
 

@@ -73,6 +73,17 @@ int grouped_max_splits(const lmoe_config* c) {
 // SMs of a GB300 work, at least `min_kb` K blocks each, at most 32.  A fixed SM count keeps
 // the workspace layout independent of the device a call runs on.
 constexpr int kSplitSms = 152;
+
+// The expert pair (lmoe_expert_pair): NVFP4, T <= 32, L a multiple of 256 and gate/up tiles
+// for every SM of a GB300 (a token's k experts are distinct, so there are at least
+// max(k, T k / 128) M tiles of I / 128 tiles each).
+bool expert_pair_rule(const lmoe_config* c) {
+  if (c->weight_dtype != LMOE_NVFP4 || c->T < 1 || c->T > 32 || c->d_latent % 256 != 0) return false;
+  const long long R = 1LL * c->T * c->top_k;
+  const long long lo_tiles = std::max<long long>(c->top_k, (R + kBM - 1) / kBM);
+  return lo_tiles * ((c->d_ff + kBNFp4 - 1) / kBNFp4) >= kSplitSms;
+}
+
 // The pooler runs beside the router (side stream): at small T its split count is sized for
 // about two thirds of the SMs, so that the router's CTAs find SMs of their own.
 constexpr int kPoolerSms = 100;
@@ -609,7 +620,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   if (mk || hybrid) {
     // the error word, the near-tie counter and the arrival counts of the grid barriers (the
     // whole-block or pre kernel's; the post kernel's) start at zero
-    LMOE_CUDA(cudaMemsetAsync(err, 0, 16, s));
+    LMOE_CUDA(launch_decode_clear(err, 4, s));
     d.x = x;
     d.x_f32 = x_f32;
     d.W_router = static_cast<const __nv_bfloat16*>(W_router);
@@ -860,11 +871,12 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     const Fp4Operand up = op(q4[2]);
     // a few tokens (M tiles of at most 32 rows) and gate/up tiles for at least every SM: S7 and
     // S8 as one launch, whose down tiles fill the SMs that finish their gate/up tiles first
-    if (T <= 32 && Ld % 256 == 0 && ev == nullptr && 1LL * lo_tiles * cdiv(I, kBNFp4) >= sm_count()) {
+    if (expert_pair_rule(cfg) && !(ex && ex->separate_expert_gemms)) {
       st = run_gemm_fp4_pair(xeq, xe_s, op(q4[1]), up, op(q4[3]), q4[1]->tensor_scale, q4[2]->tensor_scale,
                              q4[3]->tensor_scale, R, Ld, I, E, tiles, n_tiles, L.max_tiles, wsb + L.pub.h,
                              wsb + L.pub.h_scale, y, ss_y, L.ld_ss_y, splits_dev, err, budget, s);
       if (st != LMOE_OK) return st;
+      LMOE_MARK(LMOE_STAGE_DOWN);   // the down stage of a recorded call is empty
     } else {
       st = run_gemm_fp4(kFp4EpiSwiGLUQuant, xeq, R, Ld, op(q4[1]), 1LL * E * I, &up, I, tiles, n_tiles,
                         L.max_tiles, wsb + L.pub.h, I, wsb + L.pub.h_scale, nullptr, 0, xe_s,
@@ -950,6 +962,14 @@ lmoe_status lmoe_workspace_size(const lmoe_config* cfg, size_t* bytes) {
   Layout L;
   make_layout(cfg, &L);
   *bytes = static_cast<size_t>(L.pub.total);
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_expert_pair(const lmoe_config* cfg, int* used) {
+  const lmoe_status st = check_config(cfg);
+  if (st != LMOE_OK) return st;
+  if (used == nullptr) return LMOE_ERR_ARG;
+  *used = expert_pair_rule(cfg) ? 1 : 0;
   return LMOE_OK;
 }
 

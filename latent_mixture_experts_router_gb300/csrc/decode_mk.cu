@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
   float* vals = recip + 256;
   float* part_all = vals + (E + 3) / 4 * 4;                         // [kMkUnitSlots][32]
   int* ucnt = reinterpret_cast<int*>(part_all + kMkUnitSlots * 32); // [kMkUnitSlots]
-  __shared__ __align__(8) uint64_t full[kMkSlots], empty[kMkSlots], route_ready, inputs_ready;
+  __shared__ __align__(8) uint64_t full[kMkSlots], empty[kMkSlots], route_ready;
   __shared__ float red[33];
   __shared__ int s_flag, s_idx[16], s_row[16], s_nt;
   __shared__ volatile int s_dead;
@@ -547,7 +547,6 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
       mbar_init(&empty[s], 1);
     }
     mbar_init(&route_ready, 1);
-    mbar_init(&inputs_ready, 1);
     fence_mbar_init();
     // the gammas read later by every CTA into L2 now, a 1 KB piece per CTA, before the
     // weight stream fills the memory queues
@@ -572,8 +571,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
     if (lane < kLanes) {
       const uint64_t pol = policy_evict_first();
       int qbase_p = 0;
-      // the pre-norm's loads of x and g_pre come back first: the weight stream starts after
-      bool ok = mk_wait(&inputs_ready, 0, budget, &s_dead, a.err);
+      // the weights depend on no earlier kernel: the stream starts at once, while the
+      // consumers wait for the previous kernel (programmatic dependent launch)
+      bool ok = true;
       const int ph0 = MODE == kDecodeMkPost ? 3 : 0, ph1 = MODE == kDecodeMkPre ? 0 : 3;
       for (int ph = ph0; ph <= ph1; ++ph) {
         if (ph == 1 && ok) ok = mk_wait(&route_ready, 0, budget, &s_dead, a.err);   // expert rows need the top-k
@@ -687,7 +687,6 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
   if constexpr (MODE == kDecodeMkPost) {   // the routing of the pre kernel, from the workspace
     // launched while the down GEMM drains: the producer streams the unpooler's weights at once,
     // the consumers read nothing an earlier kernel wrote before that GEMM has completed
-    if (tid == 0) mbar_arrive(&inputs_ready);
     griddep_wait();
     if (tid < k) {
       s_idx[tid] = a.topk_idx[tid];
@@ -696,7 +695,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
     }
     csync();
   } else {
-  // ---- P1: pre-norm (fp32 xn in `row`; this CTA's slice of xa as bf16 hi/lo), Q(xn)
+  // ---- P1: pre-norm (fp32 xn in `row`; this CTA's slice of xa as bf16 hi/lo), Q(xn); x is
+  // read once the previous kernel of the stream has completed
+  griddep_wait();
   {
     float v[kRowChunks][8], g[kRowChunks][8];
     float ss = 0.f;
@@ -711,7 +712,6 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
       }
     }
     const float rs = rsqrtf(creduce(ss, red, false) / static_cast<float>(D) + a.eps);
-    if (tid == 0) mbar_arrive(&inputs_ready);   // every consumer's loads have returned
 #pragma unroll
     for (int c = 0; c < kRowChunks; ++c) {
       const int i = (tid + kMkConsumers * c) * 8;
@@ -834,6 +834,12 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
       *a.n_tiles2 = k;
       if (s_nt) atomicAdd(a.near_tie, 1);
     }
+  }
+  if constexpr (MODE == kDecodeMkPre) {
+    // the gate/up GEMM may be launched now: its CTAs take the SMs as these exit (its set-up
+    // reads the tables above as a hint; what it computes it reads after this kernel completes)
+    if (cta == 0) __threadfence();
+    griddep_launch_dependents();
   }
 #pragma unroll
   for (int c = 0; c < kRowChunks; ++c) {
@@ -1076,6 +1082,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
         });
   }
   if (!grid_barrier(a, MODE == kDecodeMkPost ? 0 : 3, &s_dead, &s_flag)) return;
+  griddep_launch_dependents();   // the next kernel may be launched during the post-norm
 
   // ---- P8: post-norm + residual; CTA c writes its slice of the output row (and of the next
   // layer's pre-norm of it, whose row sum every CTA takes over the whole row)
@@ -1136,6 +1143,15 @@ long long decode_megakernel_scratch_floats(int D, int L, int E, int k) {
   return static_cast<long long>(k) * (L / 16) + D / 4 + static_cast<long long>(router_parts(D)) * E;
 }
 
+// The words a single-token call starts from zero (error word, near-tie count, the grid barrier
+// counts), cleared once the previous kernel of the stream has completed.  It lets the kernel
+// after it launch at once, which then waits for it.
+__global__ void decode_clear_kernel(unsigned* w, int n) {
+  griddep_launch_dependents();
+  griddep_wait();
+  if (static_cast<int>(threadIdx.x) < n) w[threadIdx.x] = 0u;
+}
+
 template <int MODE>
 cudaError_t launch_mode(const DecodeMkArgs& d, cudaStream_t s) {
   static bool attr = false;
@@ -1153,14 +1169,19 @@ cudaError_t launch_mode(const DecodeMkArgs& d, cudaStream_t s) {
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeCooperative;   // every CTA resident at once: the grid
   attrs[0].val.cooperative = 1;                     // barriers wait on one another
-  // the post kernel follows the down GEMM with programmatic dependent launch (it waits for
-  // that GEMM before reading its outputs); the others follow a memset of their counters
+  // programmatic dependent launch: the kernel's set-up and weight stream run while the previous
+  // kernel finishes; its consumers wait for that kernel before reading what it wrote
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = MODE == kDecodeMkPost ? 2 : 1;
+  cfg.numAttrs = 2;
   count_launch();
   return cudaLaunchKernelEx(&cfg, decode_megakernel<MODE>, d);
+}
+
+cudaError_t launch_decode_clear(unsigned* words, int n, cudaStream_t s) {
+  if (n < 0 || n > 32) return cudaErrorInvalidValue;
+  return launch_pdl(decode_clear_kernel, dim3(1), dim3(32), 0, s, words, n);
 }
 
 cudaError_t launch_decode_megakernel(const DecodeMkArgs& d, cudaStream_t s) {

@@ -319,6 +319,8 @@ bool decode_megakernel_fits(int D, int L, int I, int E, int k);
 size_t decode_megakernel_smem(int D, int L, int I, int E, int k);
 long long decode_megakernel_scratch_floats(int D, int L, int E, int k);
 // One launch of one CTA per SM; the caller zeroes *bar (and the status words) before it.
+// Zeroes words[0, n) (n <= 32) after the previous kernel of the stream (decode_mk.cu).
+cudaError_t launch_decode_clear(unsigned* words, int n, cudaStream_t s);
 cudaError_t launch_decode_megakernel(const DecodeMkArgs& d, cudaStream_t s);
 // Checks the routing structures one call left in its workspace: ids in [0, E); offsets start
 // at 0, never decrease, end at R = T k and agree with counts; every pair's row lies in its

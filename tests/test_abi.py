@@ -54,6 +54,21 @@ def test_workspace_sizes_and_layout(lm):
     assert lm.lmoe_get_workspace_layout(c32)["xa_cols"] == 3 * 512
 
 
+def test_expert_pair_rule(lm):
+    # host arithmetic: NVFP4, T <= 32 and at least 152 gate/up tiles of 128 columns among
+    # max(top_k, T top_k / 128) M tiles (NVFP4 configs have d_latent % 256 == 0)
+    muse = dict(d_model=8192, d_latent=4096, n_experts=256, d_ff=4096, top_k=8, weight_dtype="nvfp4")
+    for T in (1, 8, 32):
+        assert lm.lmoe_expert_pair(lm.Config(T, **muse))
+    assert not lm.lmoe_expert_pair(lm.Config(33, **muse))                         # more rows
+    assert not lm.lmoe_expert_pair(lm.Config(8, **dict(muse, weight_dtype="bf16")))
+    assert not lm.lmoe_expert_pair(lm.Config(1, **dict(muse, d_ff=2304)))         # 8 x 18 = 144
+    assert not lm.lmoe_expert_pair(lm.Config(1, **dict(muse, top_k=4, d_ff=4608)))   # 4 x 36
+    assert lm.lmoe_expert_pair(lm.Config(1, **dict(muse, top_k=4, d_ff=4864)))   # 4 x 38 = 152
+    assert lm.lmoe_expert_pair(lm.Config(3, **dict(muse, top_k=16, d_ff=1280)))   # 16 x 10
+    assert not lm.lmoe_expert_pair(lm.Config(2, **dict(muse, top_k=2, d_ff=8192)))   # 2 x 64
+
+
 @pytest.mark.parametrize("kw,status", [
     (dict(top_k=0), -1), (dict(top_k=17), -1), (dict(n_experts=4, top_k=5), -1),
     (dict(d_model=200), -2), (dict(d_latent=96), -2), (dict(n_experts=2048), -2),

@@ -9,8 +9,10 @@ as one cooperative kernel (1).
 * Against the kernel chain on the same call (SINGLE_TOKEN_CHAIN = 2): the same experts and
   routing tables bit for bit, and p, y, u and the output within the fp32 reordering of the
   same products (both compute every block's products exactly; the sums differ in order).
-* One launch of the library per call; a grid barrier whose wait budget runs out ends the call
-  with LMOE_ERR_TIMEOUT (bit 0x40) and leaves the context usable; stage events select the chain.
+* Two launches of the library per call for the whole-block path (the kernel that clears the
+  call's counters, then the block kernel); a grid barrier whose wait budget runs out ends the
+  call with LMOE_ERR_TIMEOUT (bit 0x40) and leaves the context usable; stage events select the
+  chain.
 * The next layer's pre-norm from the same row."""
 import numpy as np
 import pytest
@@ -67,8 +69,9 @@ def test_single_token_parity_with_oracle(cuda, D, L, E, I, k, act, routing, path
     blk = make_block(inp)
     n = _launches(lm, lambda: run(inp, blk=blk, single_token_path=path))
     chain = _launches(lm, lambda: run(inp, blk=blk, single_token_path=2))
-    # the whole block as one launch; the default: the pre and post kernels and the expert GEMMs
-    assert (n == 1) if path == 1 else (1 < n < chain), (n, chain)
+    # the whole block as one kernel after the clear kernel; the default: the pre and post kernels
+    # and the expert GEMMs
+    assert (n == 2) if path == 1 else (2 < n < chain), (n, chain)
     out, idx, _, _ = run(inp, blk=blk, single_token_path=path)
     P = oracle.params_from_inputs(inp)
     x = inp.x.double().cpu().numpy()
@@ -168,7 +171,7 @@ def test_stage_events_take_the_chain_and_16_byte_codes_the_kernel(cuda):
     shifted.copy_(codes)
     assert shifted.data_ptr() % 32 == 16
     blk.W["W_pool"] = (shifted, scales, s, layout)
-    assert _launches(lm, lambda: run(inp, blk=blk, single_token_path=1)) == 1
+    assert _launches(lm, lambda: run(inp, blk=blk, single_token_path=1)) == 2
     out, idx, _, _ = run(inp, blk=blk, single_token_path=1)
     assert torch.equal(out, ref) and torch.equal(idx, idx_ref)
 

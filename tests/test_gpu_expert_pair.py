@@ -4,9 +4,9 @@ tile at most 32 rows, gate/up tiles for every SM) as one persistent launch.
 * Against the fp64 oracle under the NVFP4 rules, at T = 1 (the single-token path around it),
   ragged T = 3, T = 8 and T = 32 (hot experts; every token on the same k experts: M tiles of
   exactly 32 rows), bf16 and fp32 activations and outputs.
-* Against the two separate GEMM launches on the same call (a call that records stage events
-  runs them): the same h codes, y and output bit for bit (the pair computes every tile with
-  the same MMAs in the same K order and the same epilogues).
+* Against the two separate GEMM launches on the same inputs (lmoe_ex.separate_expert_gemms):
+  the same h codes, y and output bit for bit (the pair computes every tile with the same MMAs
+  in the same K order and the same epilogues).  lmoe_expert_pair says which calls take it.
 * The ready counts left in the tile table: every live M tile counted by all 8 epilogue warps of
   each of its I / 128 gate/up tiles (zero where the separate GEMMs ran).
 * Waits that run out end the call with LMOE_ERR_TIMEOUT and leave the context usable."""
@@ -52,10 +52,6 @@ def _inputs(T, D, L, E, I, k, act, routing, device, seed=7):
     return w, inp
 
 
-def _stage_events(lm):
-    return [torch.cuda.Event(enable_timing=True) for _ in range(lm.NUM_STAGE_EVENTS)]
-
-
 def _h_codes(lm, blk, cfg, R, I):
     lay = lm.lmoe_get_workspace_layout(cfg)
     return blk._ws[lay["h"]:lay["h"] + R * I // 2].view(R, I // 2).cpu().numpy().copy()
@@ -81,8 +77,6 @@ def test_expert_pair_matches_separate_gemms(cuda, T, D, L, E, I, k, act, routing
     import latent_mixture_experts_router_gb300 as lm
     w, inp = _inputs(T, D, L, E, I, k, act, routing, cuda, seed=11)
     blk = make_block(inp)
-    # at T = 1 both runs take the stage kernels (stage events select them), so that the only
-    # difference is the pair against the two GEMMs
     path = {"single_token_path": lm.SINGLE_TOKEN_CHAIN} if T == 1 else {}
 
     def tile_table(cfg, vw):
@@ -90,7 +84,8 @@ def test_expert_pair_matches_separate_gemms(cuda, T, D, L, E, I, k, act, routing
         o = lm.lmoe_get_workspace_layout(cfg)["tiles"]
         return blk._ws[o:o + 16 * n_tiles].view(torch.int32).view(n_tiles, 4).cpu().numpy()
 
-    out_s, idx_s, _, cfg = run(inp, blk=blk, out_dtype=out_dtype, stage_events=_stage_events(lm), **path)
+    out_s, idx_s, _, cfg = run(inp, blk=blk, out_dtype=out_dtype, separate_expert_gemms=True, **path)
+    assert lm.lmoe_expert_pair(cfg)
     out_s = out_s.clone()
     vs = views(blk, cfg)
     R = T * k
@@ -124,3 +119,23 @@ def test_expert_pair_timeout_is_reported_and_context_survives(cuda, T):
     assert st == -6, (st, hex(word))
     out, _, _, _ = run(inp, blk=blk, **path)
     assert torch.equal(out, ref)
+
+
+def test_expert_pair_with_stage_events(cuda):
+    # stage events keep the pair: the gate_up stage spans both GEMMs, the down stage is empty,
+    # and the output is the one without events
+    import latent_mixture_experts_router_gb300 as lm
+    w, inp = _inputs(8, 1024, 512, 64, 2560, 8, "bf16", "hot4", cuda, seed=17)
+    blk = make_block(inp)
+    ref, _, _, cfg = run(inp, blk=blk)
+    ref = ref.clone()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(lm.NUM_STAGE_EVENTS)]
+    out, _, _, _ = run(inp, blk=blk, stage_events=evs)
+    assert torch.equal(out, ref)
+    g, d = lm.STAGES.index("gate_up"), lm.STAGES.index("down")
+    assert evs[g].elapsed_time(evs[g + 1]) > 0
+    assert evs[d].elapsed_time(evs[d + 1]) < 0.1 * evs[g].elapsed_time(evs[g + 1])
+    n_tiles = int(views(blk, cfg)["n_tiles"][0])
+    o = lm.lmoe_get_workspace_layout(cfg)["tiles"]
+    tiles = blk._ws[o:o + 16 * n_tiles].view(torch.int32).view(n_tiles, 4).cpu().numpy()
+    assert (tiles[:, 3] == 8 * (2560 // 128)).all()
