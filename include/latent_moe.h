@@ -144,7 +144,7 @@ enum {
  *  single_token_path  with NVFP4 weights and T = 1 (one decode token), which kernels run
  *                    (ignored otherwise, and when a stage event is set; a value outside the
  *                    three below: LMOE_ERR_ARG):
- *                    LMOE_SINGLE_TOKEN_DEFAULT (0): two cooperative kernels of one CTA per SM
+ *                    LMOE_SINGLE_TOKEN_DEFAULT (0): two persistent kernels of one CTA per SM
  *                      around the tensor-core grouped gate/up and down GEMMs: before them the
  *                      pre-norm, router, pooler, top-k, routing tables and pool norm (writing
  *                      the gate/up GEMM's NVFP4 input rows), after them the per-expert norms,
@@ -156,13 +156,21 @@ enum {
  *                      barriers);
  *                    LMOE_SINGLE_TOKEN_CHAIN (2): the stage kernels, as at T > 1.
  *                    On a GB300 at the Muse shapes the default is the fastest of the three.
- *                    The cooperative kernels take D and I multiples of 256 up to 8192, L up to
+ *                    The persistent kernels take D and I multiples of 256 up to 8192, L up to
  *                    4096 and E <= 1024 (else the stage kernels run), with the same arithmetic
  *                    as the chain up to the order of fp32 sums; after them the workspace holds
  *                    xa, the logits, the routing tables, p, y and u as after the chain, but not
  *                    every quantised operand nor every partial sum of squares.  A grid barrier
  *                    or stage wait past wait_budget_cycles sets bit 0x40 of the error word
  *                    (LMOE_ERR_TIMEOUT).
+ *  cooperative_launch  nonzero: those persistent kernels are launched cooperatively, so the
+ *                    driver starts one only once every CTA can be resident; needed where other
+ *                    work may hold SMs meanwhile (another stream or process; two such calls at
+ *                    once on two streams).  0 (default): launched as ordinary grids of one CTA
+ *                    per SM with programmatic dependent launch, so each starts on the SMs the
+ *                    previous kernel leaves while it drains (measured 7.6 us faster per call at
+ *                    the Muse shapes); their grid barriers assume the call has the SMs to itself,
+ *                    and give up after wait_budget_cycles (LMOE_ERR_TIMEOUT) otherwise.
  *  separate_expert_gemms  nonzero: the grouped gate/up and down GEMMs run as two launches
  *                    even where lmoe_expert_pair() says they run as one (for inspection:
  *                    both compute the same values bit for bit). */
@@ -183,6 +191,7 @@ typedef struct {
   void* next_norm_out;
   int single_token_path;
   int separate_expert_gemms;
+  int cooperative_launch;
 } lmoe_ex;
 
 /* Whether a call with this config runs the grouped gate/up (S7) and down (S8) GEMMs as one

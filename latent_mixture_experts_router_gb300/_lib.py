@@ -50,7 +50,7 @@ class lmoe_ex(ctypes.Structure):
                 ("near_tie_count_out", ctypes.c_void_p), ("wait_budget_cycles", ctypes.c_longlong),
                 ("stage_events", ctypes.c_void_p), ("next_norm_gamma", ctypes.c_void_p),
                 ("next_norm_out", ctypes.c_void_p), ("single_token_path", ctypes.c_int),
-                ("separate_expert_gemms", ctypes.c_int)]
+                ("separate_expert_gemms", ctypes.c_int), ("cooperative_launch", ctypes.c_int)]
 
 SINGLE_TOKEN_DEFAULT, SINGLE_TOKEN_KERNEL, SINGLE_TOKEN_CHAIN = 0, 1, 2   # lmoe_ex.single_token_path
 
@@ -223,12 +223,13 @@ def latent_moe_forward_ex(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down
                           g_pre, g_post, top_k, out, workspace, stream=None, router_bias=None,
                           forced_idx=None, topk_idx_out=None, topk_w_out=None, near_tie_count_out=None,
                           wait_budget_cycles=0, stage_events=None, next_norm_gamma=None, next_norm_out=None,
-                          single_token_path=0, separate_expert_gemms=False):
+                          single_token_path=0, separate_expert_gemms=False, cooperative_launch=False):
     """``stage_events``: a list of NUM_STAGE_EVENTS torch.cuda.Event(enable_timing=True) or None,
     recorded by the library at the stage boundaries (for per-stage timing; None entries are
     skipped).  ``single_token_path``: with NVFP4 weights and one token, which kernels run
     (SINGLE_TOKEN_DEFAULT, SINGLE_TOKEN_KERNEL or SINGLE_TOKEN_CHAIN; lmoe_ex.single_token_path).
-    ``separate_expert_gemms``: gate/up and down as two launches where lmoe_expert_pair() says one."""
+    ``separate_expert_gemms``: gate/up and down as two launches where lmoe_expert_pair() says one.
+    ``cooperative_launch``: the single-token persistent kernels launched cooperatively."""
     keep = []
     args = _fwd_args(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool, g_pre,
                      g_post, top_k, out, workspace, stream, keep)
@@ -245,7 +246,7 @@ def latent_moe_forward_ex(cfg, x, W_router, W_pool, g_pool, W_gate, W_up, W_down
                  _ptr(near_tie_count_out), int(wait_budget_cycles),
                  ctypes.cast(evs, ctypes.c_void_p) if evs is not None else None,
                  _ptr(next_norm_gamma), _ptr(next_norm_out), int(single_token_path),
-                 1 if separate_expert_gemms else 0)
+                 1 if separate_expert_gemms else 0, 1 if cooperative_launch else 0)
     _check(_lib().latent_moe_forward_ex(*args, ctypes.byref(ex)), "latent_moe_forward_ex")
 
 
@@ -265,7 +266,7 @@ def latent_moe_forward_host_io_ex(cfg, x_host, W_router, W_pool, g_pool, W_gate,
     args = _fwd_args(cfg, x_host, W_router, W_pool, g_pool, W_gate, W_up, W_down, g_expert, W_unpool,
                      g_pre, g_post, top_k, out_host, workspace, stream, keep)
     ex = lmoe_ex(_ptr(router_bias), _ptr(forced_idx), None, None, None, 0, None, None, None,
-                 int(single_token_path), 0)
+                 int(single_token_path), 0, 0)
     _check(_lib().latent_moe_forward_host_io_ex(*args, ctypes.byref(ex)), "latent_moe_forward_host_io_ex")
 
 

@@ -670,6 +670,7 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
     d.err = err;
     d.budget = budget;
     d.mode = mk ? kDecodeMkFull : kDecodeMkPre;
+    d.cooperative = ex && ex->cooperative_launch ? 1 : 0;
     d.xe_codes = static_cast<uint8_t*>(at(L.pub.xe));
     d.xe_scales = static_cast<uint8_t*>(at(L.pub.xe_scale));
     d.xe_rowscale = static_cast<float*>(at(L.pub.xe_rowscale));

@@ -1,5 +1,5 @@
 // decode_mk.cu — the whole latent-MoE block for one token with NVFP4 weights, as one
-// cooperative persistent kernel.
+// persistent kernel of one CTA per SM (or its parts before and after the expert GEMMs).
 //
 // At one token every contraction of the block is a matrix-vector product: each weight is used
 // once, so the block is bound by streaming its packed weights (Muse Spark Open shape: router
@@ -16,9 +16,10 @@
 // run redundantly in every CTA (a row of at most 8192 values) in one fixed order, so all CTAs
 // hold bit-identical copies without a barrier for them.
 //
-// Roles: warp 15 lane 0 streams the CTA's weight rows of all four phases, in order, as bulk
-// copies into a ring of 8 KB shared-memory stages (an mbarrier per stage, full and empty); it
-// runs ahead across the grid barriers, waiting only for the top-k before the expert rows.
+// Roles: lanes 0-3 of warp 15 stream the CTA's weight rows of all four phases, in order, as
+// bulk copies into a ring of 30 shared-memory stages of 4 KB (an mbarrier per stage, full and
+// empty); they run ahead across the grid barriers, waiting only for the top-k before the
+// expert rows.
 // Warps 0-14 take the row steps (a named barrier of their own) and the stages, stage q by warp
 // q mod 15; a unit of rows that spans several stages (16 rows of h, of y) is finished by the
 // warp that completes it.
@@ -37,6 +38,12 @@
 // kErrGridBarrier, and the CTA's other waits give up at once, so the call ends with
 // LMOE_ERR_TIMEOUT instead of waiting forever; the producer lets its copies in flight land
 // before it leaves.
+//
+// Launch: programmatic dependent launch, so the CTAs start on the SMs the previous kernel
+// leaves and stream their weights while the consumers wait for that kernel (griddepcontrol);
+// an ordinary grid of one CTA per SM, every CTA resident at once on a GPU the call has to
+// itself, or, on request, a cooperative launch, which the driver starts only once all of them
+// can be resident (measured 7.6 us slower per call: the grid cannot start on part of the SMs).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -1167,8 +1174,11 @@ cudaError_t launch_mode(const DecodeMkArgs& d, cudaStream_t s) {
   cfg.dynamicSmemBytes = decode_megakernel_smem(d.D, d.L, d.I, d.E, d.k);
   cfg.stream = s;
   cudaLaunchAttribute attrs[2];
-  attrs[0].id = cudaLaunchAttributeCooperative;   // every CTA resident at once: the grid
-  attrs[0].val.cooperative = 1;                     // barriers wait on one another
+  // cooperative: the driver starts the grid once every CTA can be resident (the grid barriers
+  // wait on one another); else an ordinary grid of one CTA per SM, whose CTAs take the SMs the
+  // previous kernel leaves (every CTA fits at once on an otherwise idle GPU)
+  attrs[0].id = cudaLaunchAttributeCooperative;
+  attrs[0].val.cooperative = d.cooperative ? 1 : 0;
   // programmatic dependent launch: the kernel's set-up and weight stream run while the previous
   // kernel finishes; its consumers wait for that kernel before reading what it wrote
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

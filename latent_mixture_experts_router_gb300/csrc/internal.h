@@ -306,6 +306,7 @@ struct DecodeMkArgs {
   // scales, row scales) for the k routed rows.  kDecodeMkPost: from the down GEMM's bf16 y and
   // its partial sums of squares ss_y (ld_ss_y per row): combine, unpooler, post-norm.
   int mode;
+  int cooperative;             // launched cooperatively (else an ordinary grid of one CTA per SM)
   uint8_t* xe_codes;
   uint8_t* xe_scales;
   float* xe_rowscale;

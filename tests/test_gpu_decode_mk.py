@@ -13,7 +13,8 @@ as one cooperative kernel (1).
   call's counters, then the block kernel); a grid barrier whose wait budget runs out ends the
   call with LMOE_ERR_TIMEOUT (bit 0x40) and leaves the context usable; stage events select the
   chain.
-* The next layer's pre-norm from the same row."""
+* The next layer's pre-norm from the same row; a cooperative launch (lmoe_ex.cooperative_launch)
+  gives the same call bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -185,3 +186,15 @@ def test_single_token_path_out_of_range_is_refused(cuda):
         blk.forward(inp.x, single_token_path=3)
     with pytest.raises(lm.LmoeError):
         blk.forward(inp.x, single_token_path=-1)
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_cooperative_launch_gives_the_same_call(cuda, path):
+    # lmoe_ex.cooperative_launch: the same kernels launched cooperatively, bit for bit the same
+    w = _workload(4096, 2048, 16, 1024, 8, "bf16", "uniform", seed=6)
+    inp = workloads.make_inputs(w, cuda)
+    blk = make_block(inp)
+    a, ia, _, _ = run(inp, blk=blk, single_token_path=path)
+    a = a.clone()
+    b, ib, _, _ = run(inp, blk=blk, single_token_path=path, cooperative_launch=True)
+    assert torch.equal(a, b) and torch.equal(ia, ib)
