@@ -506,6 +506,19 @@ LMOE_DEV void l2_prefetch_share(const void* p, uint32_t bytes) {
     prefetch_l2_bulk(static_cast<const uint8_t*>(p) + off, min(1024u, bytes - off));
 }
 
+// The scale blocks of rows [r0, r1) of a weight with K columns (block layout: 128 rows,
+// K/64 pieces of 512 bytes) into L2.  The dot products read a stage's scales from global
+// memory one stage ahead; from HBM each such read would stall its stage.  (A call repeated on
+// one layer finds them in L2 already — they are read with the default policy, the codes
+// evict-first — and runs no faster with this; in a model the other layers evict them.)
+LMOE_DEV void l2_prefetch_scales(const uint8_t* scales, int r0, int r1, int K) {
+  if (r1 <= r0) return;
+  const uint32_t blk = static_cast<uint32_t>(K / 64) * 512u;
+  for (int b = r0 >> 7; b <= (r1 - 1) >> 7; ++b)
+    for (uint32_t off = 0; off < blk; off += 4096u)
+      prefetch_l2_bulk(scales + static_cast<long long>(b) * blk + off, min(4096u, blk - off));
+}
+
 // ---- shared memory: [ring of stages][region A][recip][vals][unit sums][unit counters]; region
 // A holds act, asc and row (phases P1-P4, P6-P8) or, in P5, every slot's Q(h) (hact, hsc)
 __host__ __device__ inline size_t mk_region_a_bytes(int D, int L, int I, int k) {
@@ -566,6 +579,16 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const DecodeM
   for (int i = tid; i < kMkUnitSlots; i += kMkThreads) ucnt[i] = 0;
   __syncthreads();   // the only CTA-wide barrier: the producer takes no part in the others
   const Phases P = phases_of(a);
+  if (tid == 32) {   // the scales of this CTA's pooler and unpooler rows into L2 at once
+    if (MODE != kDecodeMkPost) {
+      const PhaseShare& S = P.ph[0];
+      l2_prefetch_scales(a.w[0].scales, S.u0 * S.nr, S.u1 * S.nr, S.K);
+    }
+    if (MODE != kDecodeMkPre) {
+      const PhaseShare& S = P.ph[3];
+      l2_prefetch_scales(a.w[4].scales, S.u0 * 4, S.u1 * 4, S.K);
+    }
+  }
 
   if (warp == kMkProducerWarp) {
     // ---- producer: lanes 0-3 of warp 15 issue the CTA's stages of all four phases, four
