@@ -39,6 +39,7 @@ SHAPES = [
     (8, 1024, 512, 64, 2560, 8, "bf16", "hot4"),
     (32, 1024, 512, 32, 2560, 8, "bf16", "hot4"),
     (32, 512, 1024, 24, 2560, 8, "bf16", "same"),
+    (2, 256, 512, 1024, 1280, 16, "bf16", "uniform"),   # the header's limits: E = 1024, k = 16
 ]
 
 
