@@ -145,7 +145,9 @@ enum {
  *                    (ignored otherwise, and when a stage event is set; a value outside the
  *                    three below: LMOE_ERR_ARG):
  *                    LMOE_SINGLE_TOKEN_DEFAULT (0): two persistent kernels of one CTA per SM
- *                      around the tensor-core grouped gate/up and down GEMMs: before them the
+ *                      around the tensor-core grouped gate/up and down GEMMs (as one launch
+ *                      where lmoe_expert_pair() says so), after a one-warp kernel that zeroes
+ *                      the call's status and barrier words: before them the
  *                      pre-norm, router, pooler, top-k, routing tables and pool norm (writing
  *                      the gate/up GEMM's NVFP4 input rows), after them the per-expert norms,
  *                      combine, unpooler and post-norm; each streams its weights into shared
