@@ -1173,6 +1173,12 @@ long long decode_megakernel_scratch_floats(int D, int L, int E, int k) {
   return static_cast<long long>(k) * (L / 16) + D / 4 + static_cast<long long>(router_parts(D)) * E;
 }
 
+// Internal linkage for the launch helpers below: a template's function-local static (the
+// shared-memory attribute flag) would otherwise be one weak symbol shared by every copy of
+// this library in a process (the release and the bounds-checked builds), and the second copy
+// would skip setting the attribute on its own kernel.
+namespace {
+
 // The words a single-token call starts from zero (error word, near-tie count, the grid barrier
 // counts), cleared once the previous kernel of the stream has completed.  It lets the kernel
 // after it launch at once, which then waits for it.
@@ -1211,6 +1217,8 @@ cudaError_t launch_mode(const DecodeMkArgs& d, cudaStream_t s) {
   count_launch();
   return cudaLaunchKernelEx(&cfg, decode_megakernel<MODE>, d);
 }
+
+}  // namespace
 
 cudaError_t launch_decode_clear(unsigned* words, int n, cudaStream_t s) {
   if (n < 0 || n > 32) return cudaErrorInvalidValue;

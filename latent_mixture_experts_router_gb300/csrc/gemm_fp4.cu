@@ -932,8 +932,6 @@ cudaError_t launch_fp4_one(const CUtensorMap* maps, const Fp4Args& a, int m_tile
                     maps[4], maps[5], a);
 }
 
-}  // namespace
-
 template <int AROWS>
 cudaError_t launch_fp4_rows(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Args& a, int m_tiles,
                             cudaStream_t s) {
@@ -946,6 +944,8 @@ cudaError_t launch_fp4_rows(Fp4EpiKind epi, const CUtensorMap* maps, const Fp4Ar
   }
   return cudaErrorInvalidValue;
 }
+
+}  // namespace
 
 cudaError_t launch_gemm_fp4_pair(const CUtensorMap* maps, const Fp4PairArgs& a, int m_tiles, cudaStream_t s) {
   using C = Fp4Cfg<kBNFp4, kFp4EpiSwiGLUQuant, 32>;

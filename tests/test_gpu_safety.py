@@ -2,8 +2,9 @@
 
 * Guard bands: every workspace sub-buffer is followed by LMOE_GUARD_BYTES that no call may
   touch.  The workspace is filled with a canary byte, a full-size call of each weight dtype
-  runs, and every band must still hold the canary; the same call on a zeroed workspace must
-  give bitwise the same output (nothing depends on the workspace's initial contents).
+  (and the NVFP4 decode at T = 1 and 8) runs, and every band must still hold the canary; the
+  same call on a zeroed workspace must give bitwise the same output (nothing depends on the
+  workspace's initial contents).
 * Routing validation: lmoe_validate_routing accepts the routing a real call leaves behind and
   flags (error bit 0x20, LMOE_ERR_ARG) each kind of corruption written into it on purpose:
   a pair's row outside the table, two pairs sharing a row, broken offsets, a tile too tall or
@@ -44,9 +45,12 @@ def _bands_intact(lm, cfg, ws, host_io=False):
     return bad.numel() == 0, (idx[bad[:8, 0]].tolist() if bad.numel() else [])
 
 
-@pytest.mark.parametrize("name", ["decode_bf16", "prefill_nvfp4", "tiny_fp32"])
-def test_guard_bands_intact_and_initial_contents_irrelevant(lm, name):
-    w = workloads.WORKLOADS[name]
+@pytest.mark.parametrize("name,T", [("decode_bf16", None), ("prefill_nvfp4", None), ("tiny_fp32", None),
+                                    ("decode_nvfp4_hot", 1), ("decode_nvfp4_hot", 8)])
+def test_guard_bands_intact_and_initial_contents_irrelevant(lm, name, T):
+    # NVFP4 decode at T = 1 (the clear, pre, expert-pair and post kernels) and T = 8 (the chain
+    # with the expert pair): their counters start from whatever the workspace holds
+    w = workloads.WORKLOADS[name] if T is None else workloads.WORKLOADS[name].with_tokens(T)
     dev = torch.device("cuda:0")
     inp = workloads.make_inputs(w, dev)
     blk = make_block(inp)
@@ -136,9 +140,14 @@ def test_validate_routing_accepts_real_routing_and_flags_corruption(lm, T, E, k,
         assert lm.lmoe_check_status(cfg, ws) == (0, 0), what
 
 
-@pytest.mark.parametrize("weights,routing,T", [("bf16", "uniform", 300), ("bf16", "zipf", 600), ("nvfp4", "hot4", 40),
-                                               ("nvfp4", "uniform", 2100), ("f32", "uniform", 64)])
-def test_bounds_checked_build_matches_release(lm, weights, routing, T):
+PAIR_SHAPE = dict(D=512, L=512, E=16, I=2560, k=8)   # the expert pair applies (8 x 20 gate/up tiles)
+
+
+@pytest.mark.parametrize("weights,routing,T,shape", [("bf16", "uniform", 300, None), ("bf16", "zipf", 600, None),
+                                                     ("nvfp4", "hot4", 40, None), ("nvfp4", "uniform", 2100, None),
+                                                     ("f32", "uniform", 64, None), ("nvfp4", "hot4", 8, PAIR_SHAPE),
+                                                     ("nvfp4", "uniform", 1, PAIR_SHAPE)])
+def test_bounds_checked_build_matches_release(lm, weights, routing, T, shape):
     from conftest import build_checked_library
     from latent_mixture_experts_router_gb300 import _lib
     path = build_checked_library()
@@ -149,8 +158,8 @@ def test_bounds_checked_build_matches_release(lm, weights, routing, T):
                                       ctypes.POINTER(ctypes.c_uint32)]
     chk.lmoe_check_status.restype = ctypes.c_int
     act = "f32" if weights == "f32" else "bf16"
-    w = workloads.Workload(f"chk_{weights}_{T}", T=T, D=512, L=256, E=16, I=256, k=4, act=act, weights=weights,
-                           routing=routing, seed=T % 5)
+    dims = shape or dict(D=512, L=256, E=16, I=256, k=4)
+    w = workloads.Workload(f"chk_{weights}_{T}", T=T, act=act, weights=weights, routing=routing, seed=T % 5, **dims)
     inp = workloads.make_inputs(w, torch.device("cuda:0"))
     ref, idx_ref, blk, cfg = run(inp)
     W = blk.W
