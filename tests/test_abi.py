@@ -182,3 +182,17 @@ def test_workspace_guard_bands_lie_between_sub_buffers(lm, shape):
         o = lay[name]
         for b in g:
             assert b + lm.GUARD_BYTES <= o or b >= o + n, (name, o, n, b)
+
+
+def test_no_process_wide_unique_symbols(lm):
+    # A function-local static of a template with external linkage becomes a GNU unique symbol,
+    # shared by every copy of the library in a process (the release and the bounds-checked
+    # builds): one copy's "attribute already set" flag would then stand for the other's kernels.
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", lm.LIB_PATH], capture_output=True, text=True).stdout
+    unique = [ln for ln in out.splitlines() if len(ln.split()) >= 3 and ln.split()[1] == "u"]
+    assert unique == [], unique[:5]
