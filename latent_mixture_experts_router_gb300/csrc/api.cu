@@ -243,7 +243,7 @@ void make_layout(const lmoe_config* c, Layout* L) {
     L->splits_dev = take(2 * 4);
     P.grouped_splits = c->weight_dtype == LMOE_NVFP4 ? L->splits_dev : -1;
   }
-  // one token with NVFP4 weights runs as one cooperative kernel (decode_mk.cu) where it fits
+  // one token with NVFP4 weights runs through the persistent kernels of decode_mk.cu where they fit
   L->mk_scratch = fp4 && T == 1 && decode_megakernel_fits(static_cast<int>(D), static_cast<int>(Ld),
                                                           static_cast<int>(I), static_cast<int>(E),
                                                           static_cast<int>(k))
@@ -608,10 +608,11 @@ lmoe_status forward_impl(const lmoe_config* cfg, const void* x, const void* W_ro
   if (!mark(i)) return LMOE_ERR_CUDA;
 
   // One token with NVFP4 weights (not when stages are timed): by default the steps around the
-  // expert GEMMs run as two cooperative kernels (decode_mk.cu) — pre-norm, router, pooler, top-k
-  // and pool norm before, combine, unpooler and post-norm after — with the tensor-core grouped
-  // gate/up and down GEMMs between (measured the fastest at the Muse shapes); or the whole
-  // block as one such kernel, or the stage kernels, when the caller asks for them.
+  // expert GEMMs run as two persistent kernels of one CTA per SM (decode_mk.cu) — pre-norm,
+  // router, pooler, top-k and pool norm before, combine, unpooler and post-norm after — with the
+  // tensor-core grouped gate/up and down GEMMs between (the expert pair where it applies;
+  // measured the fastest at the Muse shapes); or the whole block as one such kernel, or the
+  // stage kernels, when the caller asks for them.
   const int stp = ex ? ex->single_token_path : LMOE_SINGLE_TOKEN_DEFAULT;
   const bool mk_ok = fp4 && L.mk_scratch >= 0 && ev == nullptr;
   const bool mk = mk_ok && stp == LMOE_SINGLE_TOKEN_KERNEL;

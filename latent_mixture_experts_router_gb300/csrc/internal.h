@@ -264,7 +264,7 @@ cudaError_t launch_postnorm_residual(const void* x, bool x_f32, float* u,
                                      const float* g_next = nullptr, void* next_out = nullptr);
 cudaError_t launch_wait_selftest(long long budget, unsigned* err, cudaStream_t s);
 
-// ---- the single-token NVFP4 block as one cooperative kernel (decode_mk.cu)
+// ---- the single-token NVFP4 block as persistent kernels of one CTA per SM (decode_mk.cu)
 constexpr int kDecodeMkMaxSmem = 225 * 1024;   // dynamic; the static part stays under 2 KB
 struct DecodeMkWeight {
   const uint8_t* codes;        // [rows, K/2] E2M1 pairs
