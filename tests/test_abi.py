@@ -196,3 +196,35 @@ def test_no_process_wide_unique_symbols(lm):
     out = subprocess.run([nm, "-D", "--defined-only", lm.LIB_PATH], capture_output=True, text=True).stdout
     unique = [ln for ln in out.splitlines() if len(ln.split()) >= 3 and ln.split()[1] == "u"]
     assert unique == [], unique[:5]
+
+
+def test_binding_structs_match_the_header(lm, tmp_path):
+    # every struct the binding passes through the C ABI has the header's size and field offsets
+    # (compiled with the host compiler against include/latent_moe.h)
+    import shutil
+    import subprocess
+    from latent_mixture_experts_router_gb300 import _lib
+    cc = shutil.which("gcc") or shutil.which("cc")
+    cuda_inc = "/usr/local/cuda/include"
+    if cc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime.h")):
+        pytest.skip("no host compiler or CUDA headers")
+    structs = {"lmoe_config": _lib.lmoe_config, "lmoe_nvfp4_weight": _lib.lmoe_nvfp4_weight,
+               "lmoe_ex": _lib.lmoe_ex, "lmoe_workspace_layout": _lib.lmoe_workspace_layout}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "latent_moe.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'  printf("{name} size %zu\\n", sizeof({name}));')
+        for f, _ in cls._fields_:
+            lines.append(f'  printf("{name} {f} %zu\\n", offsetof({name}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "abi.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "abi"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o", str(exe)], check=True)
+    got = {}
+    for ln in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        name, field, val = ln.split()
+        got[(name, field)] = int(val)
+    for name, cls in structs.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for f, _ in cls._fields_:
+            assert got[(name, f)] == getattr(cls, f).offset, (name, f)
